@@ -1,0 +1,196 @@
+"""Radix tree of token prefixes whose node values are KV-pool slot indices (oracle copy).
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+Source: "[SGLang] RadixAttention: Radix Tree 기반 프리픽스 캐싱의 핵심"
+(blog.secrett2633.cloud/opensource/sglang/radix-cache), sections
+  * "Radix Tree 구조도"             -- keys are token sequences, values are KV indices;
+  * "핵심 자료구조: TreeNode"        -- children keyed by first token, parent, key, value,
+                                      lock_ref, last_access_time;
+  * "프리픽스 매칭: match_prefix"    -- longest-prefix walk, split on a partial match;
+  * "노드 분할: _split_node"         -- upper part inherits lock_ref;
+  * "삽입: _insert_helper"           -- walk, split, append the remainder as a leaf,
+                                      return the already-cached length;
+  * "Eviction 전략"                  -- heap of evictable leaves, parents re-queued;
+  * "참조 카운트: lock_ref"          -- lock the whole path up to the root.
+
+Readings where the page leaves a step open (each is also listed in the design notes):
+  * page size 1: a node's child key is the first token of the child's key;
+  * time is a logical clock that advances once per public operation (match_prefix,
+    insert); every timestamp written inside one operation is that tick;
+  * the insert walk's elided "split on partial match" splits exactly like match does and
+    then continues from the upper half; only the node the walk starts from and the nodes
+    it creates get the new timestamp (the printed loop touches no other node);
+  * LRU priority is last_access_time, ties broken by node id (creation order);
+  * the root is created with lock_ref = 1 (as in the page's diagram) and is never
+    evicted or counted in the evictable / protected sizes.
+"""
+
+from __future__ import annotations
+
+import heapq
+
+
+class TreeNode:
+    def __init__(self, node_id: int, now: int):
+        self.id = node_id
+        self.children: dict[int, "TreeNode"] = {}
+        self.parent: TreeNode | None = None
+        self.key: list[int] = []
+        self.value: list[int] = []
+        self.lock_ref = 0
+        self.last_access_time = now
+
+
+def _key_match(a, b) -> int:
+    """Number of equal leading tokens of a and b."""
+    n = 0
+    for x, y in zip(a, b):
+        if x != y:
+            break
+        n += 1
+    return n
+
+
+class RadixCache:
+    def __init__(self):
+        self._next_id = 0
+        self.clock = 0
+        self.root = self._new_node()
+        self.root.lock_ref = 1
+        self.evictable_size_ = 0
+        self.protected_size_ = 0
+
+    def _new_node(self) -> TreeNode:
+        n = TreeNode(self._next_id, self.clock)
+        self._next_id += 1
+        return n
+
+    # ---- match -------------------------------------------------------------------
+    def match_prefix(self, key):
+        """Longest cached prefix of ``key``: (concatenated slot values, last node)."""
+        self.clock += 1
+        key = list(key)
+        node = self.root
+        node.last_access_time = self.clock
+        values = []
+        while key and key[0] in node.children:
+            child = node.children[key[0]]
+            child.last_access_time = self.clock
+            n = _key_match(child.key, key)
+            if n < len(child.key):
+                upper = self._split_node(child.key, child, n)
+                values.extend(upper.value)
+                node = upper
+                break
+            values.extend(child.value)
+            node = child
+            key = key[n:]
+        return values, node
+
+    def _split_node(self, key, child: TreeNode, split_len: int) -> TreeNode:
+        upper = self._new_node()
+        upper.children = {key[split_len]: child}
+        upper.parent = child.parent
+        upper.lock_ref = child.lock_ref
+        upper.key = child.key[:split_len]
+        upper.value = child.value[:split_len]
+        child.parent = upper
+        child.key = child.key[split_len:]
+        child.value = child.value[split_len:]
+        upper.parent.children[key[0]] = upper
+        return upper
+
+    # ---- insert ------------------------------------------------------------------
+    def insert(self, key, value) -> int:
+        """Insert ``key`` -> ``value``; returns how many leading tokens were already cached
+        (the caller frees those entries of ``value``, they duplicate cached slots)."""
+        assert len(key) == len(value)
+        self.clock += 1
+        key, value = list(key), list(value)
+        node = self.root
+        node.last_access_time = self.clock
+        total = 0
+        while key and key[0] in node.children:
+            node = node.children[key[0]]
+            n = _key_match(node.key, key)
+            total += n
+            key, value = key[n:], value[n:]
+            if n < len(node.key):
+                node = self._split_node(node.key, node, n)
+        if key:
+            leaf = self._new_node()
+            leaf.parent = node
+            leaf.key = key
+            leaf.value = value
+            node.children[key[0]] = leaf
+            self.evictable_size_ += len(key)
+        return total
+
+    # ---- eviction ----------------------------------------------------------------
+    def _all_nodes(self):
+        out, stack = [], [self.root]
+        while stack:
+            n = stack.pop()
+            out.append(n)
+            stack.extend(n.children.values())
+        return out
+
+    def evict(self, num_tokens: int):
+        """Free at least ``num_tokens`` slots from unlocked leaves, least recently used
+        first; returns the freed slot values in the order they were freed."""
+        heap = [(n.last_access_time, n.id, n) for n in self._all_nodes()
+                if n is not self.root and not n.children and n.lock_ref == 0]
+        heapq.heapify(heap)
+        freed, evicted = [], 0
+        while evicted < num_tokens and heap:
+            _, _, x = heapq.heappop(heap)
+            freed.extend(x.value)
+            evicted += len(x.value)
+            parent = x.parent
+            del parent.children[x.key[0]]
+            self.evictable_size_ -= len(x.key)
+            if not parent.children and parent.lock_ref == 0:
+                heapq.heappush(heap, (parent.last_access_time, parent.id, parent))
+        return freed
+
+    # ---- locking -----------------------------------------------------------------
+    def inc_lock_ref(self, node: TreeNode) -> int:
+        delta = 0
+        while node is not self.root:
+            if node.lock_ref == 0:
+                self.evictable_size_ -= len(node.key)
+                self.protected_size_ += len(node.key)
+                delta -= len(node.key)
+            node.lock_ref += 1
+            node = node.parent
+        return delta
+
+    def dec_lock_ref(self, node: TreeNode) -> int:
+        delta = 0
+        while node is not self.root:
+            if node.lock_ref == 1:
+                self.evictable_size_ += len(node.key)
+                self.protected_size_ -= len(node.key)
+                delta += len(node.key)
+            node.lock_ref -= 1
+            node = node.parent
+        return delta
+
+    # ---- inspection --------------------------------------------------------------
+    def total_size(self) -> int:
+        return sum(len(n.key) for n in self._all_nodes() if n is not self.root)
+
+    def node_by_id(self, node_id: int):
+        for n in self._all_nodes():
+            if n.id == node_id:
+                return n
+        return None
+
+    def dump(self):
+        """Canonical description: sorted (id, parent id, key, value, lock_ref, time)."""
+        rows = []
+        for n in self._all_nodes():
+            rows.append((n.id, -1 if n.parent is None else n.parent.id, tuple(n.key),
+                         tuple(n.value), n.lock_ref, n.last_access_time))
+        return sorted(rows)

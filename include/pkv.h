@@ -1,0 +1,270 @@
+/*
+ * pkv.h -- C ABI of the prefix-shared, token-indexed KV attention library (libpkv.so).
+ *
+ * One KV pool indexed per token: K_pool[num_slots][num_kv_heads][head_dim] and the same for
+ * V.  A host-side radix tree of token prefixes maps each cached token to its pool slot, so
+ * requests that share a prefix share its slots.  Sources for what each call computes:
+ *
+ *   [RC]  "[SGLang] RadixAttention: Radix Tree 기반 프리픽스 캐싱의 핵심"
+ *         (blog.secrett2633.cloud/opensource/sglang/radix-cache) -- sections
+ *         "Radix Tree 구조도", "핵심 자료구조: TreeNode", "프리픽스 매칭", "노드 분할",
+ *         "삽입", "Eviction 전략", "참조 카운트: lock_ref".
+ *   [SG]  "Efficiently Programming Large Language Models using SGLang" (summary,
+ *         0h-n0.github.io/posts/paper-2312-07910) -- §RadixAttention (match length,
+ *         "only the remainder is prefilled"), §LRU Evictionポリシー.
+ *   [PR]  "SGLang: Treating LLM Interactions as Programs for High-Throughput Inference"
+ *         (codethepapers.com) -- §Key Algorithmic Steps (prefix reuse, forked branches
+ *         sharing the prefix cache), §Why this matters in production.
+ *   [RT]  "SGLang后端运行时优化细节" (highthink.cn) -- §显存分级管理机制, the fp8_e4m3 KV
+ *         cache dtype.
+ *
+ * Conventions for every function below
+ *   - Returns PKV_OK (0) or a negative PKV_E_* code; pkv_strerror() names it.
+ *   - "device" pointers are CUDA device memory owned by the caller; "host" pointers are
+ *     ordinary host memory owned by the caller.  The library allocates no device memory and
+ *     never synchronises a stream, except pkv_get_device_error(), which synchronises.
+ *   - Device calls are asynchronous on the given stream (a cudaStream_t passed as void*;
+ *     NULL is the legacy default stream).  Argument errors are reported before anything is
+ *     enqueued; launch errors come back as PKV_E_CUDA.
+ *   - bf16 is IEEE bfloat16 (raw 16-bit patterns); e4m3 is OCP FP8 E4M3 (bias 7, max 448).
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------------------------ */
+/* status                                                                                */
+
+#define PKV_OK             0
+#define PKV_E_INVALID     -1  /* null pointer, negative size, inconsistent arguments      */
+#define PKV_E_UNSUPPORTED -2  /* head_dim / group size / dtype combination not built       */
+#define PKV_E_WORKSPACE   -3  /* workspace or plan buffer too small                        */
+#define PKV_E_CUDA        -4  /* a CUDA runtime call or kernel launch failed               */
+#define PKV_E_NOSPACE     -5  /* allocator: fewer free slots than requested                */
+#define PKV_E_NOTFOUND    -6  /* tree: unknown node id                                     */
+#define PKV_E_DEVICE      -7  /* a kernel recorded an error in the workspace error word    */
+#define PKV_E_PLAN        -8  /* plan blob does not match the call                         */
+
+/* values a kernel may leave in the workspace error word (first error wins) */
+#define PKV_DERR_SLOT_RANGE 0x100  /* a slot read from a table was outside [0, num_slots)     */
+#define PKV_DERR_TIMEOUT    0x200  /* a bounded wait inside a kernel gave up (low byte: which) */
+#define PKV_DERR_POSITION   0x400  /* a work item addressed positions outside its row         */
+
+const char *pkv_strerror(int code);
+int pkv_version(void);  /* major*10000 + minor*100 + patch */
+
+/* ------------------------------------------------------------------------------------ */
+/* the KV pool                                                                          */
+
+typedef enum { PKV_BF16 = 0, PKV_FP8_E4M3 = 1 } pkv_dtype;
+
+typedef struct pkv_pool {
+    void   *k;             /* device, [num_slots][num_kv_heads][head_dim] elements        */
+    void   *v;             /* device, same layout; bf16 (2 B) or e4m3 (1 B) elements      */
+    int64_t num_slots;     /* num_slots * num_kv_heads must be < 2^31                     */
+    int32_t num_kv_heads;
+    int32_t head_dim;      /* 64 or 128                                                   */
+    int32_t dtype;         /* pkv_dtype                                                   */
+    float   k_scale;       /* fp8 only: stored code = e4m3(x / k_scale), value = code*k_scale */
+    float   v_scale;
+} pkv_pool;
+
+/* ------------------------------------------------------------------------------------ */
+/* kv_store: write the K/V rows of newly computed tokens into their pool slots.          */
+/*                                                                                      */
+/* Pool values are per-token KV indices held by the radix tree ([RC] "Radix Tree 구조도",  */
+/* TreeNode.value); tokens not yet cached get fresh slots (out_cache_loc) from the       */
+/* allocator and their K/V are written there before attention reads them ([PR] "compute  */
+/* missing KV tensors -> insert node").                                                  */
+/*   k_new, v_new   device, bf16 [n][num_kv_heads][head_dim], row-major                   */
+/*   out_cache_loc  device, int32 [n]; slot of token i; entries must be distinct and in   */
+/*                  [0, num_slots) (a duplicate makes the result of that slot undefined)  */
+/*   workspace      device error word (4 bytes, 4-aligned) or NULL; a slot outside         */
+/*                  [0, num_slots) is never written and sets PKV_DERR_SLOT_RANGE there     */
+/* bf16 pool: bit-exact copy.  fp8 pool: e4m3_rn_satfinite(float(x) / scale) per element  */
+/* (IEEE fp32 division).  n == 0 is a no-op.                                              */
+int pkv_kv_store(const pkv_pool *pool, const void *k_new, const void *v_new,
+                 const int32_t *out_cache_loc, int64_t n, void *workspace, void *stream);
+
+/* ------------------------------------------------------------------------------------ */
+/* batch tables consumed by the attention calls (all device memory)                     */
+
+typedef struct pkv_batch {
+    const int32_t *req_to_token;      /* [num_rows][stride]: slot of each context position */
+    int64_t        stride;            /* >= longest context                                 */
+    int32_t        num_rows;
+    const int32_t *req_pool_indices;  /* [batch]: row of request r in req_to_token          */
+    const int32_t *seq_lens;          /* [batch]: context length of r, new tokens included  */
+    int32_t        batch;
+} pkv_batch;
+
+/* A shared-prefix cascade, in host memory.  Span s is a run of positions
+ * [span_start[s], span_start[s] + span_len[s]) whose slots are identical in the rows of all
+ * its member requests grp_req[grp_indptr[s] .. grp_indptr[s+1]) (a radix-tree node, or a
+ * chain of nodes, on the path of >= 2 requests of the batch: [RC] "Radix Tree 구조도" -- the
+ * two branches under [1,2,3] share its KV).  span_req[s] is one member whose row is read.
+ * For every request the spans it belongs to must tile [0, t) for some t, in order; the
+ * attention kernels read each span once per group and merge partial softmax states.
+ * pkv_tree_cascade() produces this description from the tree.                             */
+typedef struct pkv_cascade {
+    int32_t        num_spans;
+    const int32_t *span_req;
+    const int32_t *span_start;
+    const int32_t *span_len;
+    const int32_t *grp_indptr;        /* [num_spans + 1] */
+    const int32_t *grp_req;           /* batch indices   */
+} pkv_cascade;
+
+/* Planner knobs (NULL = defaults). */
+typedef struct pkv_plan_opts {
+    int32_t chunk_keys;    /* decode: keys per unshared work item (0 = default 256)         */
+    int32_t span_chunk;    /* decode: keys per shared-span work item (0 = default 4096)     */
+    int32_t num_sms;       /* SMs of the target GPU for load balancing (0 = 152)             */
+    int32_t dynamic_tail;  /* decode: last item of each request reads its end from seq_lens  */
+                           /* on the device, so the plan stays valid while tails grow by     */
+                           /* whole decode steps inside the same chunk                        */
+} pkv_plan_opts;
+
+/* Host description of a plan; pass it, with a device copy of the plan blob, to the device
+ * call.  Filled by pkv_plan_decode / pkv_plan_extend. */
+typedef struct pkv_plan_info {
+    int32_t op;                /* 1 = decode, 2 = extend                                   */
+    int32_t batch;
+    int32_t num_q_heads, num_kv_heads, head_dim;
+    int32_t num_items;         /* attention work items                                      */
+    int32_t num_span_items;    /* of which read a shared span (cascade)                     */
+    int32_t num_records;       /* partial (m, l, acc) records written for merging            */
+    int32_t num_merge;         /* requests (decode) or query tokens (extend) to merge        */
+    int32_t total_q;           /* query tokens in the call                                  */
+    size_t  plan_bytes;        /* size of the plan blob                                     */
+    size_t  workspace_bytes;   /* device workspace the call needs (>= 256)                  */
+    int64_t offsets[8];        /* byte offsets of the blob's sections (internal)            */
+} pkv_plan_info;
+
+/* Decode plan: one query token per request, at position seq_lens[r] - 1, attending to the
+ * whole context [0, seq_lens[r]) including its own just-stored token.  Work is split over
+ * (request or shared span) x KV head x key chunk (split-KV); partial states are merged.
+ *   seq_lens  host int32 [batch], each >= 1
+ *   cascade   host, may be NULL (every request reads its whole row)
+ *   plan      host buffer of plan_cap bytes, or NULL to only size the plan in *info        */
+int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t num_q_heads,
+                    int32_t num_kv_heads, int32_t head_dim, const pkv_cascade *cascade,
+                    const pkv_plan_opts *opts, void *plan, size_t plan_cap,
+                    pkv_plan_info *info);
+
+/* Extend plan: request r queries its extend_lens[r] new tokens at positions
+ * seq_lens[r] - extend_lens[r] + i; query token i attends causally to positions
+ * [0, seq_lens[r] - extend_lens[r] + i] -- the matched prefix plus its own suffix ([SG]
+ * §RadixAttention: only the unmatched remainder is prefilled).
+ *   seq_lens, extend_lens  host int32 [batch], 1 <= extend_lens[r] <= seq_lens[r]
+ *   qo_indptr              host int32 [batch + 1]: query tokens of r are rows
+ *                          qo_indptr[r] .. qo_indptr[r+1]-1 of q and o
+ *   cascade                host, may be NULL                                            */
+int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int32_t *extend_lens,
+                    const int32_t *qo_indptr, int32_t num_q_heads, int32_t num_kv_heads,
+                    int32_t head_dim, const pkv_cascade *cascade, const pkv_plan_opts *opts,
+                    void *plan, size_t plan_cap, pkv_plan_info *info);
+
+/* Attention over the pool, read through req_to_token (see the two plan calls for the
+ * positions each query sees).  Head h uses KV head h / (num_q_heads / num_kv_heads).
+ *   q          device, bf16 [total_q][num_q_heads][head_dim]
+ *   o          device, bf16 [total_q][num_q_heads][head_dim], fully overwritten
+ *   sm_scale   logit scale, usually 1/sqrt(head_dim)
+ *   info       host, from the matching pkv_plan_* call
+ *   plan_dev   device copy of the plan blob (info->plan_bytes bytes, 16-byte aligned)
+ *   workspace  device, >= info->workspace_bytes, 256-byte aligned; its first 4 bytes are
+ *              the error word (zero it once; kernels only ever set it)
+ * Accumulation is fp32; softmax probabilities enter the P*V product as bf16.  For an fp8
+ * pool the codes are converted exactly to bf16 and the scales are applied in fp32.     */
+int pkv_attn_decode(const pkv_pool *pool, const pkv_batch *batch, const void *q, void *o,
+                    float sm_scale, const pkv_plan_info *info, const void *plan_dev,
+                    void *workspace, size_t ws_bytes, void *stream);
+
+int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, const void *q, void *o,
+                    float sm_scale, const pkv_plan_info *info, const void *plan_dev,
+                    void *workspace, size_t ws_bytes, void *stream);
+
+/* Synchronises `stream`, reads the error word of `workspace` (PKV_OK when zero, else
+ * PKV_E_DEVICE with the raw word in *raw when raw != NULL). */
+int pkv_get_device_error(void *workspace, void *stream, int32_t *raw);
+
+/* ------------------------------------------------------------------------------------ */
+/* host radix tree ([RC]): token ids -> pool slots, with LRU eviction and lock_ref       */
+/*                                                                                      */
+/* Page size 1: children are keyed by the first token of their key.  Time is a logical   */
+/* clock that advances once per match_prefix / insert; LRU ties break by node id.        */
+/* Node ids are assigned in creation order (root = 0) and stay valid until the node is    */
+/* evicted.                                                                              */
+
+typedef struct pkv_tree pkv_tree;
+
+pkv_tree *pkv_tree_new(void);
+void pkv_tree_free(pkv_tree *t);
+
+/* Longest cached prefix of key[0..n) ([RC] "프리픽스 매칭"): writes its slots to values
+ * (up to values_cap of them), the matched length to *matched and the last node on the
+ * matched path to *last_node (0 = root when nothing matched).  A match that ends inside a
+ * node splits that node first ([RC] "노드 분할"), so *last_node ends exactly at the match. */
+int pkv_tree_match_prefix(pkv_tree *t, const int32_t *key, int64_t n, int32_t *values,
+                          int64_t values_cap, int64_t *matched, int64_t *last_node);
+
+/* Insert key -> value (n tokens each) ([RC] "삽입").  *prefix_len receives how many
+ * leading tokens were already cached; value[0 .. *prefix_len) duplicate cached slots and
+ * are the caller's to free. */
+int pkv_tree_insert(pkv_tree *t, const int32_t *key, const int32_t *value, int64_t n,
+                    int64_t *prefix_len);
+
+/* Evict unlocked leaves, least recently used first, until at least num_tokens slots are
+ * freed or nothing is evictable ([RC] "Eviction 전략").  A parent that becomes an unlocked
+ * leaf joins the candidates.  Freed slots go to freed[0 .. *num_freed) in eviction order
+ * (PKV_E_WORKSPACE if freed_cap is too small; nothing is evicted then). */
+int pkv_tree_evict(pkv_tree *t, int64_t num_tokens, int32_t *freed, int64_t freed_cap,
+                   int64_t *num_freed);
+
+/* lock_ref on the path node..root ([RC] "참조 카운트: lock_ref"); locked nodes are never
+ * evicted.  *delta (may be NULL) gets the change of the evictable size. */
+int pkv_tree_inc_lock_ref(pkv_tree *t, int64_t node, int64_t *delta);
+int pkv_tree_dec_lock_ref(pkv_tree *t, int64_t node, int64_t *delta);
+
+int pkv_tree_sizes(pkv_tree *t, int64_t *evictable, int64_t *protected_size,
+                   int64_t *total, int64_t *num_nodes);
+
+/* Canonical dump for tests: per live node in id order, 6 + 2*len int64 entries
+ * (id, parent id, lock_ref, last_access_time, len, num_children, key[len], value[len]).
+ * *used gets the entries needed; PKV_E_WORKSPACE when cap is smaller (nothing written). */
+int pkv_tree_dump(pkv_tree *t, int64_t *out, int64_t cap, int64_t *used);
+
+/* Shared-prefix cascade of a batch.  last_nodes[r] is request r's last matched node
+ * (from match_prefix; its path from the root is the request's cached prefix).  Every node
+ * on the paths of >= min_group requests becomes part of a span; consecutive nodes with the
+ * same member set are fused into one span.  Output arrays are host buffers sized
+ * cap_spans (span_*; grp_indptr needs cap_spans + 1) and cap_members (grp_req).       */
+int pkv_tree_cascade(pkv_tree *t, const int64_t *last_nodes, int32_t batch, int32_t min_group,
+                     int32_t *span_req, int32_t *span_start, int32_t *span_len,
+                     int32_t *grp_indptr, int32_t *grp_req, int32_t cap_spans,
+                     int32_t cap_members, int32_t *num_spans, int32_t *num_members);
+
+/* ------------------------------------------------------------------------------------ */
+/* token-slot allocator: owns the free slot indices ([RC] "Eviction 전략":                */
+/* token_to_kv_pool_allocator.free(x.value)).  FIFO: alloc pops from the front, free     */
+/* appends at the back.                                                                  */
+
+typedef struct pkv_allocator pkv_allocator;
+
+pkv_allocator *pkv_allocator_new(const int32_t *free_slots, int64_t n);  /* host, copied */
+void pkv_allocator_free_all(pkv_allocator *a);
+int pkv_allocator_alloc(pkv_allocator *a, int64_t n, int32_t *out);      /* PKV_E_NOSPACE */
+int pkv_allocator_release(pkv_allocator *a, const int32_t *slots, int64_t n);
+int64_t pkv_allocator_available(const pkv_allocator *a);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

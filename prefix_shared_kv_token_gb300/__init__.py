@@ -1,0 +1,307 @@
+"""Prefix-shared, token-indexed KV attention for GB300 (sm_103a).
+
+Thin Python binding of ``libpkv.so`` (C ABI in ``include/pkv.h``): every call below only
+marshals arguments -- torch tensors supply device memory and streams, numpy arrays host
+memory -- and forwards to the library.  Names follow the C entry points without the
+``pkv_`` prefix:
+
+    kv_store      scatter new K/V rows into pool slots (bf16 copy or fp8 quantisation)
+    plan_decode   host work decomposition of a decode call (split-KV, shared-prefix cascade)
+    plan_extend   host work decomposition of an extend call
+    attn_decode   one query token per request over its whole context (tcgen05-free, mma.sync)
+    attn_extend   causal extend of the uncached suffix (tcgen05 / TMEM / TMA gather4)
+    RadixTree     host radix tree: match_prefix (with split), insert, LRU evict, lock_ref,
+                  cascade extraction
+    Allocator     token-slot free list
+
+There is no CPU or eager fallback: importing the package loads the library or raises.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+from dataclasses import dataclass
+
+import numpy as np
+
+from ._lib import (PKV_BF16, PKV_FP8_E4M3, PkvBatch, PkvCascade, PkvError, PkvPlanInfo, PkvPlanOpts, PkvPool,
+                   check, lib)
+
+__all__ = ["Pool", "Batch", "Plan", "Cascade", "kv_store", "plan_decode", "plan_extend", "attn_decode",
+           "attn_extend", "get_device_error", "RadixTree", "Allocator", "PkvError", "version"]
+
+
+def version() -> int:
+    return lib.pkv_version()
+
+
+def _ptr(t) -> int:
+    """Device pointer of a torch tensor or host pointer of a numpy array (None -> NULL)."""
+    if t is None:
+        return None
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+# ----------------------------------------------------------------------------------------
+# pool, batch, plan
+
+
+@dataclass
+class Pool:
+    """Device KV pool: k, v are torch tensors [num_slots, num_kv_heads, head_dim] of bfloat16
+    (dtype 'bf16') or uint8 holding e4m3 codes (dtype 'fp8_e4m3')."""
+    k: object
+    v: object
+    dtype: str = "bf16"
+    k_scale: float = 1.0
+    v_scale: float = 1.0
+
+    @classmethod
+    def allocate(cls, num_slots, num_kv_heads, head_dim, dtype="bf16", k_scale=1.0, v_scale=1.0, device="cuda"):
+        import torch
+        tdt = torch.bfloat16 if dtype == "bf16" else torch.uint8
+        k = torch.zeros((num_slots, num_kv_heads, head_dim), dtype=tdt, device=device)
+        v = torch.zeros_like(k)
+        return cls(k, v, dtype, float(k_scale), float(v_scale))
+
+    @property
+    def num_slots(self):
+        return self.k.shape[0]
+
+    def c(self) -> PkvPool:
+        return PkvPool(_ptr(self.k), _ptr(self.v), self.k.shape[0], self.k.shape[1], self.k.shape[2],
+                       PKV_BF16 if self.dtype == "bf16" else PKV_FP8_E4M3, self.k_scale, self.v_scale)
+
+
+@dataclass
+class Batch:
+    """Device batch tables: req_to_token [rows, stride] int32, req_pool_indices [B] int32,
+    seq_lens [B] int32 (torch tensors on the GPU)."""
+    req_to_token: object
+    req_pool_indices: object
+    seq_lens: object
+
+    def c(self) -> PkvBatch:
+        rt = self.req_to_token
+        return PkvBatch(_ptr(rt), rt.shape[1], rt.shape[0], _ptr(self.req_pool_indices), _ptr(self.seq_lens),
+                        self.req_pool_indices.shape[0])
+
+
+@dataclass
+class Cascade:
+    """Host description of the shared spans of a batch (see pkv_cascade in pkv.h)."""
+    span_req: np.ndarray
+    span_start: np.ndarray
+    span_len: np.ndarray
+    grp_indptr: np.ndarray
+    grp_req: np.ndarray
+
+    @property
+    def num_spans(self):
+        return int(self.span_req.shape[0])
+
+    def c(self) -> PkvCascade:
+        return PkvCascade(self.num_spans, _ptr(self.span_req), _ptr(self.span_start), _ptr(self.span_len),
+                          _ptr(self.grp_indptr), _ptr(self.grp_req))
+
+
+@dataclass
+class Plan:
+    info: PkvPlanInfo
+    blob: np.ndarray  # uint8 host copy of the plan
+
+
+def _opts(opts):
+    if opts is None:
+        return None
+    o = PkvPlanOpts(0, 0, 0, 0)
+    for k, v in opts.items():
+        setattr(o, k, int(v))
+    return C.byref(o)
+
+
+def _cascade_ref(cascade):
+    if cascade is None:
+        return None, None
+    c = cascade.c()
+    return C.byref(c), c
+
+
+def plan_decode(seq_lens, num_q_heads, num_kv_heads, head_dim, cascade=None, opts=None) -> Plan:
+    seq = _i32(seq_lens)
+    info = PkvPlanInfo()
+    cref, _keep = _cascade_ref(cascade)
+    o = _opts(opts)
+    args = (len(seq), _ptr(seq), num_q_heads, num_kv_heads, head_dim, cref, o)
+    check("pkv_plan_decode", lib.pkv_plan_decode(*args, None, 0, C.byref(info)))
+    blob = np.zeros(info.plan_bytes, dtype=np.uint8)
+    check("pkv_plan_decode", lib.pkv_plan_decode(*args, _ptr(blob), blob.nbytes, C.byref(info)))
+    return Plan(info, blob)
+
+
+def plan_extend(seq_lens, extend_lens, qo_indptr, num_q_heads, num_kv_heads, head_dim, cascade=None,
+                opts=None) -> Plan:
+    seq, ext, qo = _i32(seq_lens), _i32(extend_lens), _i32(qo_indptr)
+    info = PkvPlanInfo()
+    cref, _keep = _cascade_ref(cascade)
+    o = _opts(opts)
+    args = (len(seq), _ptr(seq), _ptr(ext), _ptr(qo), num_q_heads, num_kv_heads, head_dim, cref, o)
+    check("pkv_plan_extend", lib.pkv_plan_extend(*args, None, 0, C.byref(info)))
+    blob = np.zeros(info.plan_bytes, dtype=np.uint8)
+    check("pkv_plan_extend", lib.pkv_plan_extend(*args, _ptr(blob), blob.nbytes, C.byref(info)))
+    return Plan(info, blob)
+
+
+# ----------------------------------------------------------------------------------------
+# device calls
+
+
+def kv_store(pool: Pool, k_new, v_new, out_cache_loc, workspace=None, stream=None) -> None:
+    p = pool.c()
+    check("pkv_kv_store", lib.pkv_kv_store(C.byref(p), _ptr(k_new), _ptr(v_new), _ptr(out_cache_loc),
+                                           int(out_cache_loc.shape[0]), _ptr(workspace), _stream(stream)))
+
+
+def attn_decode(pool: Pool, batch: Batch, q, o, sm_scale, plan: Plan, plan_dev, workspace, stream=None) -> None:
+    p, b = pool.c(), batch.c()
+    check("pkv_attn_decode", lib.pkv_attn_decode(C.byref(p), C.byref(b), _ptr(q), _ptr(o), float(sm_scale),
+                                                 C.byref(plan.info), _ptr(plan_dev), _ptr(workspace),
+                                                 workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def attn_extend(pool: Pool, batch: Batch, q, o, sm_scale, plan: Plan, plan_dev, workspace, stream=None) -> None:
+    p, b = pool.c(), batch.c()
+    check("pkv_attn_extend", lib.pkv_attn_extend(C.byref(p), C.byref(b), _ptr(q), _ptr(o), float(sm_scale),
+                                                 C.byref(plan.info), _ptr(plan_dev), _ptr(workspace),
+                                                 workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def get_device_error(workspace, stream=None) -> int:
+    """Synchronises the stream and returns the raw error word (0 = no error)."""
+    raw = C.c_int32(0)
+    rc = lib.pkv_get_device_error(_ptr(workspace), _stream(stream), C.byref(raw))
+    if rc not in (0, -7):
+        check("pkv_get_device_error", rc)
+    return raw.value
+
+
+# ----------------------------------------------------------------------------------------
+# host radix tree and allocator
+
+
+class RadixTree:
+    def __init__(self):
+        self._h = lib.pkv_tree_new()
+        if not self._h:
+            raise MemoryError("pkv_tree_new")
+
+    def __del__(self):
+        if getattr(self, "_h", None):
+            lib.pkv_tree_free(self._h)
+            self._h = None
+
+    def match_prefix(self, key):
+        key = _i32(key)
+        out = np.zeros(len(key), dtype=np.int32)
+        matched, last = C.c_int64(0), C.c_int64(0)
+        check("pkv_tree_match_prefix", lib.pkv_tree_match_prefix(self._h, _ptr(key), len(key), _ptr(out), len(out),
+                                                                 C.byref(matched), C.byref(last)))
+        return out[:matched.value], last.value
+
+    def insert(self, key, value) -> int:
+        key, value = _i32(key), _i32(value)
+        assert len(key) == len(value)
+        n = C.c_int64(0)
+        check("pkv_tree_insert", lib.pkv_tree_insert(self._h, _ptr(key), _ptr(value), len(key), C.byref(n)))
+        return n.value
+
+    def sizes(self):
+        e, p, t, n = C.c_int64(0), C.c_int64(0), C.c_int64(0), C.c_int64(0)
+        check("pkv_tree_sizes", lib.pkv_tree_sizes(self._h, C.byref(e), C.byref(p), C.byref(t), C.byref(n)))
+        return {"evictable": e.value, "protected": p.value, "total": t.value, "nodes": n.value}
+
+    def evict(self, num_tokens: int) -> np.ndarray:
+        cap = self.sizes()["evictable"]
+        out = np.zeros(max(cap, 1), dtype=np.int32)
+        n = C.c_int64(0)
+        check("pkv_tree_evict", lib.pkv_tree_evict(self._h, int(num_tokens), _ptr(out), len(out), C.byref(n)))
+        return out[:n.value].copy()
+
+    def inc_lock_ref(self, node: int) -> int:
+        d = C.c_int64(0)
+        check("pkv_tree_inc_lock_ref", lib.pkv_tree_inc_lock_ref(self._h, int(node), C.byref(d)))
+        return d.value
+
+    def dec_lock_ref(self, node: int) -> int:
+        d = C.c_int64(0)
+        check("pkv_tree_dec_lock_ref", lib.pkv_tree_dec_lock_ref(self._h, int(node), C.byref(d)))
+        return d.value
+
+    def dump(self):
+        """[(id, parent, lock_ref, time, key tuple, value tuple, num_children)] in id order."""
+        used = C.c_int64(0)
+        check("pkv_tree_dump", lib.pkv_tree_dump(self._h, None, 0, C.byref(used)))
+        buf = np.zeros(max(used.value, 1), dtype=np.int64)
+        check("pkv_tree_dump", lib.pkv_tree_dump(self._h, _ptr(buf), len(buf), C.byref(used)))
+        rows, i = [], 0
+        while i < used.value:
+            nid, par, lock, t, n, nch = (int(x) for x in buf[i:i + 6])
+            key = tuple(int(x) for x in buf[i + 6:i + 6 + n])
+            val = tuple(int(x) for x in buf[i + 6 + n:i + 6 + 2 * n])
+            rows.append((nid, par, lock, t, key, val, nch))
+            i += 6 + 2 * n
+        return rows
+
+    def cascade(self, last_nodes, min_group: int = 2) -> Cascade:
+        last = np.ascontiguousarray(np.asarray(last_nodes, dtype=np.int64))
+        ns, nm = C.c_int32(0), C.c_int32(0)
+        check("pkv_tree_cascade", lib.pkv_tree_cascade(self._h, _ptr(last), len(last), min_group, None, None, None,
+                                                       None, None, 0, 0, C.byref(ns), C.byref(nm)))
+        s, m = ns.value, nm.value
+        sr, ss, sl = (np.zeros(s, np.int32) for _ in range(3))
+        ip, gr = np.zeros(s + 1, np.int32), np.zeros(max(m, 1), np.int32)
+        check("pkv_tree_cascade", lib.pkv_tree_cascade(self._h, _ptr(last), len(last), min_group, _ptr(sr), _ptr(ss),
+                                                       _ptr(sl), _ptr(ip), _ptr(gr), s, m, C.byref(ns),
+                                                       C.byref(nm)))
+        return Cascade(sr, ss, sl, ip, gr[:m])
+
+
+class Allocator:
+    """FIFO free list of pool slots."""
+
+    def __init__(self, free_slots):
+        fs = _i32(free_slots)
+        self._h = lib.pkv_allocator_new(_ptr(fs), len(fs))
+        if not self._h:
+            raise MemoryError("pkv_allocator_new")
+
+    def __del__(self):
+        if getattr(self, "_h", None):
+            lib.pkv_allocator_free_all(self._h)
+            self._h = None
+
+    def alloc(self, n: int) -> np.ndarray:
+        out = np.zeros(max(n, 1), dtype=np.int32)
+        check("pkv_allocator_alloc", lib.pkv_allocator_alloc(self._h, int(n), _ptr(out)))
+        return out[:n]
+
+    def release(self, slots) -> None:
+        s = _i32(slots)
+        check("pkv_allocator_release", lib.pkv_allocator_release(self._h, _ptr(s), len(s)))
+
+    @property
+    def available(self) -> int:
+        return int(lib.pkv_allocator_available(self._h))

@@ -1,0 +1,83 @@
+// Status strings, version, the device error word, device properties and the tensor-map
+// encoder shared by the launchers.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/pkv.h"
+#include "launch.h"
+
+namespace pkv {
+
+int num_sms() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType dtype, cuuint32_t rank, void *base,
+                      const cuuint64_t *dims, const cuuint64_t *strides_bytes, const cuuint32_t *box,
+                      CUtensorMapSwizzle swizzle) {
+    EncodeTiledFn fn = get_encode_fn();
+    if (!fn) return CUDA_ERROR_NOT_FOUND;
+    cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
+    return fn(map, dtype, rank, base, dims, strides_bytes, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace pkv
+
+extern "C" {
+
+const char *pkv_strerror(int code) {
+    switch (code) {
+        case PKV_OK: return "ok";
+        case PKV_E_INVALID: return "invalid argument";
+        case PKV_E_UNSUPPORTED: return "unsupported shape or dtype";
+        case PKV_E_WORKSPACE: return "workspace or buffer too small";
+        case PKV_E_CUDA: return "CUDA error";
+        case PKV_E_NOSPACE: return "no free KV slots";
+        case PKV_E_NOTFOUND: return "unknown tree node";
+        case PKV_E_DEVICE: return "device-side check failed";
+        case PKV_E_PLAN: return "plan does not match the call";
+        default: return "unknown error";
+    }
+}
+
+int pkv_version(void) { return 100; }
+
+int pkv_get_device_error(void *workspace, void *stream, int32_t *raw) {
+    if (!workspace) return PKV_E_INVALID;
+    int32_t w = 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&w, workspace, sizeof(w), cudaMemcpyDeviceToHost, s) != cudaSuccess) return PKV_E_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_E_CUDA;
+    if (raw) *raw = w;
+    return w == 0 ? PKV_OK : PKV_E_DEVICE;
+}
+
+}  // extern "C"

@@ -1,0 +1,31 @@
+// Host-side helpers shared by the C-ABI entry points: argument validation, device
+// properties, tensor-map encoding through the driver entry point.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+int num_sms();  // SMs of the current device (cached per device)
+
+inline int validate_pool(const pkv_pool *p) {
+    if (!p || !p->k || !p->v) return PKV_E_INVALID;
+    if (p->num_slots <= 0 || p->num_kv_heads <= 0) return PKV_E_INVALID;
+    if (p->head_dim != 64 && p->head_dim != 128) return PKV_E_UNSUPPORTED;
+    if (p->dtype != PKV_BF16 && p->dtype != PKV_FP8_E4M3) return PKV_E_UNSUPPORTED;
+    if (p->num_slots * (int64_t)p->num_kv_heads >= ((int64_t)1 << 31)) return PKV_E_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(p->k) | reinterpret_cast<uintptr_t>(p->v)) & 127) return PKV_E_INVALID;
+    if (p->dtype == PKV_FP8_E4M3 && !(p->k_scale > 0.f && p->v_scale > 0.f)) return PKV_E_INVALID;
+    return PKV_OK;
+}
+
+// cuTensorMapEncodeTiled, resolved once through cudaGetDriverEntryPoint (no -lcuda needed).
+CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType dtype, cuuint32_t rank, void *base,
+                      const cuuint64_t *dims, const cuuint64_t *strides_bytes, const cuuint32_t *box,
+                      CUtensorMapSwizzle swizzle);
+
+}  // namespace pkv

@@ -1,0 +1,318 @@
+// Host planner: turns one attention call (batch tables + optional shared-prefix cascade)
+// into a flat list of work items for the kernels, the partial-state records they write and
+// the merges that combine those records.
+//
+// Decode ([SG] summary §RadixAttention: each running request decodes over its whole cached
+// context): work = (shared span or unshared tail) x KV head x key chunk.  A span item reads
+// the span's slots once for all member requests of the span (a radix-tree node on several
+// paths: "Radix Tree 구조도" -- the two branches under [1,2,3] share its KV); a tail item reads
+// one request's remaining positions.  Every (request, span chunk) and (request, tail chunk)
+// owns one partial record (m, l, acc) unless the request has a single item, which then
+// writes its output directly.  Items are ordered longest first so the hardware block
+// scheduler packs them like LPT.
+//
+// Extend (only the uncached remainder is prefilled, [SG] §RadixAttention): work = tile of
+// up to 128/G query tokens x KV head over keys [k0, k1), causal within the request.  With a
+// cascade, span items cover the contiguous query tokens of the span's members against the
+// span (no mask needed: every query comes after the span) and the per-request items cover
+// the rest of the context causally; one record per (query token, part), merged per token.
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <numeric>
+#include <vector>
+
+#include "../../include/pkv.h"
+
+namespace {
+
+struct DecodeItem { int32_t g, mode, nreq, row_off, src, k0, k1, pad; };
+struct ExtendItem { int32_t g, src, tok0, ntok, qpos0, k0, k1, rec; };
+struct MergeItem { int32_t out_row, rec0, nrec, rec_stride; };
+static_assert(sizeof(DecodeItem) == 32 && sizeof(ExtendItem) == 32 && sizeof(MergeItem) == 16, "layout");
+
+constexpr size_t kHeader = 256;
+size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+
+int check_heads(int32_t hq, int32_t hkv, int32_t d) {
+    if (hq <= 0 || hkv <= 0 || hq % hkv) return PKV_E_INVALID;
+    int32_t G = hq / hkv;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return PKV_E_UNSUPPORTED;
+    if (d != 64 && d != 128) return PKV_E_UNSUPPORTED;
+    return PKV_OK;
+}
+
+// Per-request ordered span lists from the cascade; fills tail_start.  Validates that the
+// spans of every member tile [0, tail_start) in order and stay inside the context.
+int spans_per_request(const pkv_cascade *c, int32_t batch, const int32_t *seq_lens,
+                      std::vector<std::vector<int32_t>> *per_req, std::vector<int32_t> *tail_start) {
+    per_req->assign((size_t)batch, {});
+    tail_start->assign((size_t)batch, 0);
+    if (!c || c->num_spans == 0) return PKV_OK;
+    if (c->num_spans < 0 || !c->span_req || !c->span_start || !c->span_len || !c->grp_indptr || !c->grp_req)
+        return PKV_E_INVALID;
+    if (c->grp_indptr[0] != 0) return PKV_E_INVALID;
+    for (int32_t s = 0; s < c->num_spans; ++s) {
+        if (c->span_len[s] <= 0 || c->span_start[s] < 0) return PKV_E_INVALID;
+        if (c->grp_indptr[s + 1] < c->grp_indptr[s]) return PKV_E_INVALID;
+        if (c->span_req[s] < 0 || c->span_req[s] >= batch) return PKV_E_INVALID;
+        bool src_is_member = false;
+        for (int32_t i = c->grp_indptr[s]; i < c->grp_indptr[s + 1]; ++i) {
+            int32_t r = c->grp_req[i];
+            if (r < 0 || r >= batch) return PKV_E_INVALID;
+            (*per_req)[r].push_back(s);
+            src_is_member |= (r == c->span_req[s]);
+        }
+        if (!src_is_member) return PKV_E_INVALID;
+    }
+    for (int32_t r = 0; r < batch; ++r) {
+        auto &v = (*per_req)[r];
+        std::sort(v.begin(), v.end(), [&](int32_t a, int32_t b) { return c->span_start[a] < c->span_start[b]; });
+        int32_t pos = 0;
+        for (int32_t s : v) {
+            if (c->span_start[s] != pos) return PKV_E_INVALID;
+            pos += c->span_len[s];
+        }
+        if (pos > seq_lens[r]) return PKV_E_INVALID;
+        (*tail_start)[r] = pos;
+    }
+    return PKV_OK;
+}
+
+template <class T>
+void put(std::vector<uint8_t> &blob, size_t off, const std::vector<T> &v) {
+    if (!v.empty()) std::memcpy(blob.data() + off, v.data(), v.size() * sizeof(T));
+}
+
+int emit(const std::vector<uint8_t> &blob, void *plan, size_t plan_cap, pkv_plan_info *info) {
+    info->plan_bytes = blob.size();
+    if (!plan) return PKV_OK;
+    if (plan_cap < blob.size()) return PKV_E_WORKSPACE;
+    std::memcpy(plan, blob.data(), blob.size());
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_dim, const pkv_cascade *cascade,
+                               const pkv_plan_opts *opts, void *plan, size_t plan_cap,
+                               pkv_plan_info *info) {
+    if (!info || batch < 0 || (batch > 0 && !seq_lens)) return PKV_E_INVALID;
+    int rc = check_heads(num_q_heads, num_kv_heads, head_dim);
+    if (rc) return rc;
+    for (int32_t r = 0; r < batch; ++r)
+        if (seq_lens[r] < 1) return PKV_E_INVALID;
+    const int32_t G = num_q_heads / num_kv_heads;
+    const int32_t chunk = (opts && opts->chunk_keys > 0) ? opts->chunk_keys : 256;
+    const int32_t span_chunk = (opts && opts->span_chunk > 0) ? opts->span_chunk : 4096;
+    const bool dyn_tail = opts && opts->dynamic_tail;
+    const int32_t rows_per_cta = 4 * (16 / G);  // requests per span item: 4 warps x 16 rows
+
+    std::vector<std::vector<int32_t>> spans_of;
+    std::vector<int32_t> tail_start;
+    rc = spans_per_request(cascade, batch, seq_lens, &spans_of, &tail_start);
+    if (rc) return rc;
+
+    // records per request: its span chunks (in path order), then its tail chunks
+    auto nchunks = [](int32_t len, int32_t c) { return len <= 0 ? 0 : (len + c - 1) / c; };
+    std::vector<int32_t> nrec(batch, 0), rec_base(batch, 0);
+    for (int32_t r = 0; r < batch; ++r) {
+        int32_t n = 0;
+        for (int32_t s : spans_of[r]) n += nchunks(cascade->span_len[s], span_chunk);
+        n += nchunks(seq_lens[r] - tail_start[r], chunk);
+        nrec[r] = n;
+    }
+    int32_t num_records = 0;
+    for (int32_t r = 0; r < batch; ++r) {
+        if (nrec[r] >= 2) {
+            rec_base[r] = num_records;
+            num_records += nrec[r];
+        } else {
+            rec_base[r] = -1;  // single item: direct output
+        }
+    }
+    // per-request running index into its own records
+    std::vector<int32_t> next_rec(batch, 0);
+
+    std::vector<DecodeItem> items;
+    std::vector<int32_t> row_req, row_rec;
+    std::vector<MergeItem> merges;
+    int32_t num_span_items = 0;
+
+    if (cascade) {
+        for (int32_t s = 0; s < cascade->num_spans; ++s) {
+            const int32_t st = cascade->span_start[s], len = cascade->span_len[s];
+            const int32_t m0 = cascade->grp_indptr[s], m1 = cascade->grp_indptr[s + 1];
+            for (int32_t c0 = 0; c0 < len; c0 += span_chunk) {
+                const int32_t c1 = std::min(len, c0 + span_chunk);
+                for (int32_t a = m0; a < m1; a += rows_per_cta) {
+                    const int32_t b = std::min(m1, a + rows_per_cta);
+                    const int32_t off = (int32_t)row_req.size();
+                    for (int32_t i = a; i < b; ++i) {
+                        const int32_t r = cascade->grp_req[i];
+                        row_req.push_back(r);
+                        row_rec.push_back(rec_base[r] < 0 ? -1 : rec_base[r] + next_rec[r]);
+                        next_rec[r] += 1;
+                    }
+                    for (int32_t g = 0; g < num_kv_heads; ++g) {
+                        items.push_back({g, 0, b - a, off, cascade->span_req[s], st + c0, st + c1, 0});
+                        ++num_span_items;
+                    }
+                }
+            }
+        }
+    }
+    for (int32_t r = 0; r < batch; ++r) {
+        const int32_t t0 = tail_start[r], L = seq_lens[r];
+        for (int32_t k0 = t0; k0 < L; k0 += chunk) {
+            const int32_t k1 = std::min(L, k0 + chunk);
+            const int32_t off = (int32_t)row_req.size();
+            row_req.push_back(r);
+            row_rec.push_back(rec_base[r] < 0 ? -1 : rec_base[r] + next_rec[r]);
+            next_rec[r] += 1;
+            const bool last = k1 == L;
+            for (int32_t g = 0; g < num_kv_heads; ++g)
+                items.push_back({g, 1, 1, off, r, k0, (last && dyn_tail) ? -1 : k1, 0});
+        }
+    }
+    for (int32_t r = 0; r < batch; ++r)
+        if (rec_base[r] >= 0) merges.push_back({r, rec_base[r], nrec[r], 1});
+
+    // longest first; span items weigh more (several requests' rows per key)
+    std::stable_sort(items.begin(), items.end(), [&](const DecodeItem &x, const DecodeItem &y) {
+        auto cost = [&](const DecodeItem &it) {
+            int64_t k1 = it.k1 < 0 ? seq_lens[it.src] : it.k1;
+            int64_t keys = k1 - it.k0;
+            return it.mode == 0 ? keys * 4 + keys * it.nreq / 4 : keys * 4;
+        };
+        return cost(x) > cost(y);
+    });
+
+    std::memset(info, 0, sizeof(*info));
+    info->op = 1;
+    info->batch = batch;
+    info->num_q_heads = num_q_heads;
+    info->num_kv_heads = num_kv_heads;
+    info->head_dim = head_dim;
+    info->num_items = (int32_t)items.size();
+    info->num_span_items = num_span_items;
+    info->num_records = num_records;
+    info->num_merge = (int32_t)merges.size();
+    info->total_q = batch;
+    size_t off = 0;
+    info->offsets[0] = (int64_t)off; off = align16(off + items.size() * sizeof(DecodeItem));
+    info->offsets[1] = (int64_t)off; off = align16(off + row_req.size() * sizeof(int32_t));
+    info->offsets[2] = (int64_t)off; off = align16(off + row_rec.size() * sizeof(int32_t));
+    info->offsets[3] = (int64_t)off; off = align16(off + merges.size() * sizeof(MergeItem));
+    std::vector<uint8_t> blob(std::max<size_t>(off, 16), 0);
+    put(blob, (size_t)info->offsets[0], items);
+    put(blob, (size_t)info->offsets[1], row_req);
+    put(blob, (size_t)info->offsets[2], row_rec);
+    put(blob, (size_t)info->offsets[3], merges);
+    info->workspace_bytes = kHeader + (size_t)num_records * num_q_heads * head_dim * 4 +
+                            (size_t)num_records * num_q_heads * 2 * 4;
+    return emit(blob, plan, plan_cap, info);
+}
+
+extern "C" int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int32_t *extend_lens,
+                               const int32_t *qo_indptr, int32_t num_q_heads, int32_t num_kv_heads,
+                               int32_t head_dim, const pkv_cascade *cascade, const pkv_plan_opts *opts,
+                               void *plan, size_t plan_cap, pkv_plan_info *info) {
+    (void)opts;
+    if (!info || batch < 0 || (batch > 0 && (!seq_lens || !extend_lens || !qo_indptr))) return PKV_E_INVALID;
+    int rc = check_heads(num_q_heads, num_kv_heads, head_dim);
+    if (rc) return rc;
+    if (qo_indptr[0] != 0) return PKV_E_INVALID;
+    for (int32_t r = 0; r < batch; ++r) {
+        if (extend_lens[r] < 1 || extend_lens[r] > seq_lens[r]) return PKV_E_INVALID;
+        if (qo_indptr[r + 1] - qo_indptr[r] != extend_lens[r]) return PKV_E_INVALID;
+    }
+    const int32_t G = num_q_heads / num_kv_heads;
+    const int32_t TQ = 128 / G;
+    const int32_t total_q = qo_indptr[batch];
+
+    std::vector<std::vector<int32_t>> spans_of;
+    std::vector<int32_t> tail_start;
+    rc = spans_per_request(cascade, batch, seq_lens, &spans_of, &tail_start);
+    if (rc) return rc;
+    // a span must lie inside the cached prefix of each member (queries come after it)
+    for (int32_t r = 0; r < batch; ++r)
+        if (tail_start[r] > seq_lens[r] - extend_lens[r]) return PKV_E_INVALID;
+
+    // parts per token of request r: one per span plus the causal remainder
+    int32_t kmax = 1;
+    for (int32_t r = 0; r < batch; ++r) kmax = std::max<int32_t>(kmax, (int32_t)spans_of[r].size() + 1);
+    const bool cascaded = kmax > 1;
+
+    std::vector<ExtendItem> items;
+    std::vector<MergeItem> merges;
+    int32_t num_span_items = 0;
+    if (cascaded) {
+        // part index of span s for its members = position of s in their span list
+        for (int32_t s = 0; s < cascade->num_spans; ++s) {
+            const int32_t m0 = cascade->grp_indptr[s], m1 = cascade->grp_indptr[s + 1];
+            // contiguous runs of consecutive batch indices among the members
+            std::vector<int32_t> mem(cascade->grp_req + m0, cascade->grp_req + m1);
+            std::sort(mem.begin(), mem.end());
+            for (size_t i = 0; i < mem.size();) {
+                size_t j = i + 1;
+                int32_t part = (int32_t)(std::find(spans_of[mem[i]].begin(), spans_of[mem[i]].end(), s) -
+                                         spans_of[mem[i]].begin());
+                while (j < mem.size() && mem[j] == mem[j - 1] + 1 &&
+                       (int32_t)(std::find(spans_of[mem[j]].begin(), spans_of[mem[j]].end(), s) -
+                                 spans_of[mem[j]].begin()) == part)
+                    ++j;
+                const int32_t t0 = qo_indptr[mem[i]], t1 = qo_indptr[mem[j - 1] + 1];
+                for (int32_t a = t0; a < t1; a += TQ) {
+                    const int32_t n = std::min(TQ, t1 - a);
+                    for (int32_t g = 0; g < num_kv_heads; ++g) {
+                        items.push_back({g, cascade->span_req[s], a, n, 1 << 30, cascade->span_start[s],
+                                         cascade->span_start[s] + cascade->span_len[s], part * total_q + a});
+                        ++num_span_items;
+                    }
+                }
+                i = j;
+            }
+        }
+    }
+    for (int32_t r = 0; r < batch; ++r) {
+        const int32_t e = extend_lens[r], p = seq_lens[r] - e;
+        const int32_t part = (int32_t)spans_of[r].size();
+        for (int32_t i0 = 0; i0 < e; i0 += TQ) {
+            const int32_t n = std::min(TQ, e - i0);
+            const int32_t tok0 = qo_indptr[r] + i0;
+            for (int32_t g = 0; g < num_kv_heads; ++g)
+                items.push_back({g, r, tok0, n, p + i0, tail_start[r], p + i0 + n,
+                                 cascaded ? part * total_q + tok0 : -1});
+        }
+        if (cascaded)
+            for (int32_t t = qo_indptr[r]; t < qo_indptr[r + 1]; ++t)
+                merges.push_back({t, t, part + 1, total_q});
+    }
+    std::stable_sort(items.begin(), items.end(), [](const ExtendItem &x, const ExtendItem &y) {
+        return (int64_t)(x.k1 - x.k0) * x.ntok > (int64_t)(y.k1 - y.k0) * y.ntok;
+    });
+
+    std::memset(info, 0, sizeof(*info));
+    info->op = 2;
+    info->batch = batch;
+    info->num_q_heads = num_q_heads;
+    info->num_kv_heads = num_kv_heads;
+    info->head_dim = head_dim;
+    info->num_items = (int32_t)items.size();
+    info->num_span_items = num_span_items;
+    info->num_records = cascaded ? kmax * total_q : 0;
+    info->num_merge = (int32_t)merges.size();
+    info->total_q = total_q;
+    size_t off = 0;
+    info->offsets[0] = (int64_t)off; off = align16(off + items.size() * sizeof(ExtendItem));
+    info->offsets[3] = (int64_t)off; off = align16(off + merges.size() * sizeof(MergeItem));
+    std::vector<uint8_t> blob(std::max<size_t>(off, 16), 0);
+    put(blob, (size_t)info->offsets[0], items);
+    put(blob, (size_t)info->offsets[3], merges);
+    info->workspace_bytes = kHeader + (size_t)info->num_records * num_q_heads * head_dim * 4 +
+                            (size_t)info->num_records * num_q_heads * 2 * 4;
+    return emit(blob, plan, plan_cap, info);
+}

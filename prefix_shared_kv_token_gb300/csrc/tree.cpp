@@ -1,0 +1,414 @@
+// Host radix tree of token prefixes (values = KV-pool slots) and the token-slot allocator.
+//
+// Semantics follow "[SGLang] RadixAttention: Radix Tree 기반 프리픽스 캐싱의 핵심"
+// (blog.secrett2633.cloud/opensource/sglang/radix-cache):
+//   TreeNode            -- children keyed by the first token, parent, key, value, lock_ref,
+//                          last_access_time ("핵심 자료구조: TreeNode");
+//   match_prefix        -- longest-prefix walk, a partial match splits the child
+//                          ("프리픽스 매칭: match_prefix", "노드 분할: _split_node");
+//   insert              -- walk, split on a partial match, append the remainder as a leaf,
+//                          return the already-cached length ("삽입: _insert_helper");
+//   evict               -- heap of unlocked leaves by last access, parents re-queued once
+//                          they become unlocked leaves ("Eviction 전략");
+//   inc/dec_lock_ref    -- lock the path up to the root ("참조 카운트: lock_ref").
+// Readings where the page leaves a step open: page size 1; a logical clock that ticks once
+// per match_prefix / insert; the insert walk only stamps the node it starts from and the
+// nodes it creates; LRU ties break by node id; the root starts with lock_ref 1.
+//
+// The cascade extraction (pkv_tree_cascade) turns the nodes shared by several requests of a
+// batch into spans for the attention kernels: the tree already knows which prefix KV is
+// shared ("Radix Tree 구조도": both branches under [1,2,3] share its KV).
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <deque>
+#include <new>
+#include <queue>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/pkv.h"
+
+namespace {
+
+struct Node {
+    int64_t id = 0;
+    int64_t parent = -1;
+    std::unordered_map<int32_t, int64_t> children;
+    std::vector<int32_t> key;
+    std::vector<int32_t> value;
+    int64_t lock_ref = 0;
+    int64_t last_access_time = 0;
+    bool alive = true;
+};
+
+}  // namespace
+
+struct pkv_tree {
+    std::vector<Node> nodes;  // indexed by id; evicted nodes stay as tombstones
+    int64_t clock = 0;
+    int64_t evictable = 0;
+    int64_t protected_ = 0;
+    int64_t live = 0;
+
+    pkv_tree() {
+        Node root;
+        root.id = 0;
+        root.lock_ref = 1;
+        nodes.push_back(std::move(root));
+        live = 1;
+    }
+
+    int64_t new_node() {
+        Node n;
+        n.id = (int64_t)nodes.size();
+        n.last_access_time = clock;
+        nodes.push_back(std::move(n));
+        ++live;
+        return nodes.back().id;
+    }
+
+    static int64_t key_match(const int32_t *a, int64_t na, const int32_t *b, int64_t nb) {
+        int64_t n = std::min(na, nb), i = 0;
+        while (i < n && a[i] == b[i]) ++i;
+        return i;
+    }
+
+    // Split `child` after split_len tokens; returns the new upper node.
+    int64_t split(int64_t child, int64_t split_len) {
+        int64_t up = new_node();  // may reallocate `nodes`: index by id only
+        Node &c = nodes[child];
+        Node &u = nodes[up];
+        u.parent = c.parent;
+        u.lock_ref = c.lock_ref;
+        u.key.assign(c.key.begin(), c.key.begin() + split_len);
+        u.value.assign(c.value.begin(), c.value.begin() + split_len);
+        c.key.erase(c.key.begin(), c.key.begin() + split_len);
+        c.value.erase(c.value.begin(), c.value.begin() + split_len);
+        c.parent = up;
+        u.children[c.key[0]] = child;
+        nodes[u.parent].children[u.key[0]] = up;
+        return up;
+    }
+
+    int64_t match(const int32_t *key, int64_t n, std::vector<int32_t> *values) {
+        ++clock;
+        int64_t node = 0;
+        nodes[0].last_access_time = clock;
+        int64_t pos = 0;
+        while (pos < n) {
+            auto it = nodes[node].children.find(key[pos]);
+            if (it == nodes[node].children.end()) break;
+            int64_t child = it->second;
+            nodes[child].last_access_time = clock;
+            int64_t m = key_match(nodes[child].key.data(), (int64_t)nodes[child].key.size(),
+                                  key + pos, n - pos);
+            if (m < (int64_t)nodes[child].key.size()) {
+                int64_t up = split(child, m);
+                values->insert(values->end(), nodes[up].value.begin(), nodes[up].value.end());
+                node = up;
+                break;
+            }
+            values->insert(values->end(), nodes[child].value.begin(), nodes[child].value.end());
+            node = child;
+            pos += m;
+        }
+        return node;
+    }
+
+    int64_t insert(const int32_t *key, const int32_t *value, int64_t n) {
+        ++clock;
+        int64_t node = 0;
+        nodes[0].last_access_time = clock;
+        int64_t pos = 0, total = 0;
+        while (pos < n) {
+            auto it = nodes[node].children.find(key[pos]);
+            if (it == nodes[node].children.end()) break;
+            node = it->second;
+            int64_t m = key_match(nodes[node].key.data(), (int64_t)nodes[node].key.size(),
+                                  key + pos, n - pos);
+            total += m;
+            pos += m;
+            if (m < (int64_t)nodes[node].key.size()) node = split(node, m);
+        }
+        if (pos < n) {
+            int64_t leaf = new_node();
+            Node &l = nodes[leaf];
+            l.parent = node;
+            l.key.assign(key + pos, key + n);
+            l.value.assign(value + pos, value + n);
+            nodes[node].children[key[pos]] = leaf;
+            evictable += n - pos;
+        }
+        return total;
+    }
+
+    bool evictable_leaf(const Node &x) const {
+        return x.alive && x.id != 0 && x.children.empty() && x.lock_ref == 0;
+    }
+
+    void evict(int64_t num_tokens, std::vector<int32_t> *freed) {
+        using Item = std::pair<std::pair<int64_t, int64_t>, int64_t>;  // ((time, id), id)
+        std::priority_queue<Item, std::vector<Item>, std::greater<Item>> heap;
+        for (const Node &x : nodes)
+            if (evictable_leaf(x)) heap.push({{x.last_access_time, x.id}, x.id});
+        int64_t evicted = 0;
+        while (evicted < num_tokens && !heap.empty()) {
+            int64_t id = heap.top().second;
+            heap.pop();
+            Node &x = nodes[id];
+            freed->insert(freed->end(), x.value.begin(), x.value.end());
+            evicted += (int64_t)x.value.size();
+            Node &p = nodes[x.parent];
+            p.children.erase(x.key[0]);
+            evictable -= (int64_t)x.key.size();
+            x.alive = false;
+            x.children.clear();
+            std::vector<int32_t>().swap(x.key);
+            std::vector<int32_t>().swap(x.value);
+            --live;
+            if (p.children.empty() && p.lock_ref == 0)
+                heap.push({{p.last_access_time, p.id}, p.id});
+        }
+    }
+
+    int64_t inc_lock(int64_t node) {
+        int64_t delta = 0;
+        while (node != 0) {
+            Node &x = nodes[node];
+            if (x.lock_ref == 0) {
+                evictable -= (int64_t)x.key.size();
+                protected_ += (int64_t)x.key.size();
+                delta -= (int64_t)x.key.size();
+            }
+            x.lock_ref += 1;
+            node = x.parent;
+        }
+        return delta;
+    }
+
+    int64_t dec_lock(int64_t node) {
+        int64_t delta = 0;
+        while (node != 0) {
+            Node &x = nodes[node];
+            if (x.lock_ref == 1) {
+                evictable += (int64_t)x.key.size();
+                protected_ -= (int64_t)x.key.size();
+                delta += (int64_t)x.key.size();
+            }
+            x.lock_ref -= 1;
+            node = x.parent;
+        }
+        return delta;
+    }
+
+    int64_t max_leaf_len() const {
+        int64_t m = 0;
+        for (const Node &x : nodes)
+            if (evictable_leaf(x)) m = std::max<int64_t>(m, (int64_t)x.key.size());
+        return m;
+    }
+
+    bool valid(int64_t id) const { return id >= 0 && id < (int64_t)nodes.size() && nodes[id].alive; }
+};
+
+struct pkv_allocator {
+    std::deque<int32_t> free_list;
+};
+
+extern "C" {
+
+pkv_tree *pkv_tree_new(void) { return new (std::nothrow) pkv_tree(); }
+
+void pkv_tree_free(pkv_tree *t) { delete t; }
+
+int pkv_tree_match_prefix(pkv_tree *t, const int32_t *key, int64_t n, int32_t *values,
+                          int64_t values_cap, int64_t *matched, int64_t *last_node) {
+    if (!t || n < 0 || (n > 0 && !key) || !matched || !last_node) return PKV_E_INVALID;
+    std::vector<int32_t> v;
+    v.reserve((size_t)n);
+    int64_t node = t->match(key, n, &v);
+    *matched = (int64_t)v.size();
+    *last_node = node;
+    if (values) {
+        int64_t m = std::min<int64_t>((int64_t)v.size(), values_cap);
+        if (m > 0) std::memcpy(values, v.data(), sizeof(int32_t) * (size_t)m);
+    }
+    return PKV_OK;
+}
+
+int pkv_tree_insert(pkv_tree *t, const int32_t *key, const int32_t *value, int64_t n,
+                    int64_t *prefix_len) {
+    if (!t || n < 0 || (n > 0 && (!key || !value))) return PKV_E_INVALID;
+    int64_t total = t->insert(key, value, n);
+    if (prefix_len) *prefix_len = total;
+    return PKV_OK;
+}
+
+int pkv_tree_evict(pkv_tree *t, int64_t num_tokens, int32_t *freed, int64_t freed_cap,
+                   int64_t *num_freed) {
+    if (!t || num_tokens < 0 || !num_freed) return PKV_E_INVALID;
+    // every freed slot belongs to an unlocked node, so the evictable size bounds the output;
+    // refuse up front rather than evict into a buffer that cannot hold the result
+    if (freed_cap < std::min<int64_t>(t->evictable, num_tokens + t->max_leaf_len()))
+        return PKV_E_WORKSPACE;
+    std::vector<int32_t> f;
+    t->evict(num_tokens, &f);
+    if ((int64_t)f.size() > freed_cap) return PKV_E_WORKSPACE;  // unreachable by the check
+    if (!f.empty()) {
+        if (!freed) return PKV_E_INVALID;
+        std::memcpy(freed, f.data(), sizeof(int32_t) * f.size());
+    }
+    *num_freed = (int64_t)f.size();
+    return PKV_OK;
+}
+
+int pkv_tree_inc_lock_ref(pkv_tree *t, int64_t node, int64_t *delta) {
+    if (!t) return PKV_E_INVALID;
+    if (!t->valid(node)) return PKV_E_NOTFOUND;
+    int64_t d = t->inc_lock(node);
+    if (delta) *delta = d;
+    return PKV_OK;
+}
+
+int pkv_tree_dec_lock_ref(pkv_tree *t, int64_t node, int64_t *delta) {
+    if (!t) return PKV_E_INVALID;
+    if (!t->valid(node)) return PKV_E_NOTFOUND;
+    // refuse to unlock below zero: the walk would corrupt the size bookkeeping
+    for (int64_t x = node; x != 0; x = t->nodes[x].parent)
+        if (t->nodes[x].lock_ref <= 0) return PKV_E_INVALID;
+    int64_t d = t->dec_lock(node);
+    if (delta) *delta = d;
+    return PKV_OK;
+}
+
+int pkv_tree_sizes(pkv_tree *t, int64_t *evictable, int64_t *protected_size, int64_t *total,
+                   int64_t *num_nodes) {
+    if (!t) return PKV_E_INVALID;
+    if (evictable) *evictable = t->evictable;
+    if (protected_size) *protected_size = t->protected_;
+    if (total) {
+        int64_t s = 0;
+        for (const Node &x : t->nodes)
+            if (x.alive && x.id != 0) s += (int64_t)x.key.size();
+        *total = s;
+    }
+    if (num_nodes) *num_nodes = t->live;
+    return PKV_OK;
+}
+
+int pkv_tree_dump(pkv_tree *t, int64_t *out, int64_t cap, int64_t *used) {
+    if (!t || !used) return PKV_E_INVALID;
+    int64_t need = 0;
+    for (const Node &x : t->nodes)
+        if (x.alive) need += 6 + 2 * (int64_t)x.key.size();
+    *used = need;
+    if (!out || cap < need) return out ? PKV_E_WORKSPACE : PKV_OK;
+    int64_t k = 0;
+    for (const Node &x : t->nodes) {
+        if (!x.alive) continue;
+        out[k++] = x.id;
+        out[k++] = x.parent;
+        out[k++] = x.lock_ref;
+        out[k++] = x.last_access_time;
+        out[k++] = (int64_t)x.key.size();
+        out[k++] = (int64_t)x.children.size();
+        for (int32_t v : x.key) out[k++] = v;
+        for (int32_t v : x.value) out[k++] = v;
+    }
+    return PKV_OK;
+}
+
+int pkv_tree_cascade(pkv_tree *t, const int64_t *last_nodes, int32_t batch, int32_t min_group,
+                     int32_t *span_req, int32_t *span_start, int32_t *span_len,
+                     int32_t *grp_indptr, int32_t *grp_req, int32_t cap_spans,
+                     int32_t cap_members, int32_t *num_spans, int32_t *num_members) {
+    if (!t || batch < 0 || (batch > 0 && !last_nodes) || !num_spans || !num_members)
+        return PKV_E_INVALID;
+    if (min_group < 2) min_group = 2;
+    // paths root -> last node (root excluded), and the members of every node
+    std::vector<std::vector<int64_t>> paths((size_t)batch);
+    std::unordered_map<int64_t, std::vector<int32_t>> members;
+    for (int32_t r = 0; r < batch; ++r) {
+        int64_t x = last_nodes[r];
+        if (!t->valid(x)) return PKV_E_NOTFOUND;
+        for (; x != 0; x = t->nodes[x].parent) paths[r].push_back(x);
+        std::reverse(paths[r].begin(), paths[r].end());
+        for (int64_t n : paths[r]) members[n].push_back(r);
+    }
+    struct Span { int32_t req, start, len; int64_t head; };
+    std::vector<Span> spans;
+    std::unordered_map<int64_t, int32_t> span_of_head;  // first node of a span -> span index
+    std::vector<int32_t> member_flat, indptr{0};
+    for (int32_t r = 0; r < batch; ++r) {
+        int64_t pos = 0;
+        int64_t cur_head = -1;
+        for (size_t i = 0; i < paths[r].size(); ++i) {
+            int64_t n = paths[r][i];
+            const auto &mem = members[n];
+            int64_t len = (int64_t)t->nodes[n].key.size();
+            if ((int32_t)mem.size() < min_group) break;  // shared nodes form a prefix
+            bool fuse = cur_head >= 0 && members[cur_head].size() == mem.size();
+            if (!fuse) {
+                cur_head = n;
+                auto it = span_of_head.find(n);
+                if (it == span_of_head.end()) {
+                    span_of_head[n] = (int32_t)spans.size();
+                    spans.push_back({mem[0], (int32_t)pos, (int32_t)len, n});
+                    member_flat.insert(member_flat.end(), mem.begin(), mem.end());
+                    indptr.push_back((int32_t)member_flat.size());
+                }
+            } else if (members[cur_head][0] == r) {
+                // first member extends the fused span (every member walks the same chain)
+                spans[span_of_head[cur_head]].len += (int32_t)len;
+            }
+            pos += len;
+        }
+    }
+    *num_spans = (int32_t)spans.size();
+    *num_members = (int32_t)member_flat.size();
+    if ((int32_t)spans.size() > cap_spans || (int32_t)member_flat.size() > cap_members)
+        return (cap_spans == 0 && cap_members == 0) ? PKV_OK : PKV_E_WORKSPACE;
+    if (!spans.empty() && (!span_req || !span_start || !span_len || !grp_indptr || !grp_req))
+        return PKV_E_INVALID;
+    for (size_t s = 0; s < spans.size(); ++s) {
+        span_req[s] = spans[s].req;
+        span_start[s] = spans[s].start;
+        span_len[s] = spans[s].len;
+    }
+    if (grp_indptr)
+        for (size_t s = 0; s <= spans.size(); ++s) grp_indptr[s] = indptr[s];
+    if (!member_flat.empty()) std::memcpy(grp_req, member_flat.data(), sizeof(int32_t) * member_flat.size());
+    return PKV_OK;
+}
+
+pkv_allocator *pkv_allocator_new(const int32_t *free_slots, int64_t n) {
+    if (n < 0 || (n > 0 && !free_slots)) return nullptr;
+    auto *a = new (std::nothrow) pkv_allocator();
+    if (!a) return nullptr;
+    a->free_list.assign(free_slots, free_slots + n);
+    return a;
+}
+
+void pkv_allocator_free_all(pkv_allocator *a) { delete a; }
+
+int pkv_allocator_alloc(pkv_allocator *a, int64_t n, int32_t *out) {
+    if (!a || n < 0 || (n > 0 && !out)) return PKV_E_INVALID;
+    if ((int64_t)a->free_list.size() < n) return PKV_E_NOSPACE;
+    for (int64_t i = 0; i < n; ++i) {
+        out[i] = a->free_list.front();
+        a->free_list.pop_front();
+    }
+    return PKV_OK;
+}
+
+int pkv_allocator_release(pkv_allocator *a, const int32_t *slots, int64_t n) {
+    if (!a || n < 0 || (n > 0 && !slots)) return PKV_E_INVALID;
+    a->free_list.insert(a->free_list.end(), slots, slots + n);
+    return PKV_OK;
+}
+
+int64_t pkv_allocator_available(const pkv_allocator *a) { return a ? (int64_t)a->free_list.size() : 0; }
+
+}  // extern "C"

@@ -1,0 +1,210 @@
+"""Host side of one serving step: prefix-cache population, batch tables, cascade, plans and
+device buffers for the kv_store + attention calls.
+
+A *workload* (see ``workloads/``) describes token segments with their K/V rows and a batch
+of requests whose contexts are paths of segments; the last ``n_new`` tokens of each context
+are new in the step.  :class:`PrefixCache` owns the device pool, the radix tree and the
+slot allocator; :meth:`PrefixCache.populate` caches every request's already-cached part the
+way a server would have after earlier steps (match, allocate the unmatched rest, store its
+K/V, insert), and :meth:`PrefixCache.prepare` builds one attention call (extend or decode):
+match the cached part (it must hit completely), lock the path, allocate slots for the new
+tokens (``out_cache_loc``), write ``req_to_token`` rows, extract the shared-prefix cascade
+from the tree and plan the kernels.  Everything runs through ``libpkv`` (tree, allocator,
+planner, kernels); this module only moves arrays around.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+from . import Allocator, Batch, Pool, RadixTree, attn_decode, attn_extend, kv_store, plan_decode, plan_extend
+
+
+def _ctx_tokens(w, req):
+    return np.concatenate([w.segments[s].tokens for s in req.path])
+
+
+def _ctx_kv(w, req, lo, hi):
+    """bf16 bits of context rows [lo, hi) of K and V, as [n, Hkv, d] uint16 arrays."""
+    ks, vs, pos = [], [], 0
+    for s in req.path:
+        seg = w.segments[s]
+        n = len(seg.tokens)
+        a, b = max(lo, pos), min(hi, pos + n)
+        if a < b:
+            ks.append(seg.k[a - pos:b - pos])
+            vs.append(seg.v[a - pos:b - pos])
+        pos += n
+    if not ks:
+        shape = (0, w.num_kv_heads, w.head_dim)
+        return np.zeros(shape, np.uint16), np.zeros(shape, np.uint16)
+    return np.concatenate(ks), np.concatenate(vs)
+
+
+def _bf16_dev(bits: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+@dataclass
+class Call:
+    """One attention call of a step with all its device inputs."""
+    kind: str
+    pool: Pool
+    batch: Batch
+    plan: object
+    plan_dev: torch.Tensor
+    workspace: torch.Tensor
+    q: torch.Tensor
+    o: torch.Tensor
+    out_cache_loc: torch.Tensor
+    k_new: torch.Tensor
+    v_new: torch.Tensor
+    sm_scale: float
+    last_nodes: list
+    host: dict = field(default_factory=dict)
+    cascade: object = None
+
+    @property
+    def num_queries(self) -> int:
+        return int(self.q.shape[0])
+
+    def store(self, stream=None):
+        kv_store(self.pool, self.k_new, self.v_new, self.out_cache_loc, self.workspace, stream)
+
+    def attend(self, stream=None):
+        f = attn_extend if self.kind == "extend" else attn_decode
+        f(self.pool, self.batch, self.q, self.o, self.sm_scale, self.plan, self.plan_dev, self.workspace, stream)
+
+    def run(self, stream=None):
+        self.store(stream)
+        self.attend(stream)
+
+    # ---- end-to-end variant: inputs from pinned host buffers, output back to the host
+    def pin_host(self):
+        h = self.host
+        for name in ("q", "k_new", "v_new", "out_cache_loc"):
+            t = getattr(self, name)
+            h[name] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+        for name in ("req_to_token", "req_pool_indices", "seq_lens"):
+            t = getattr(self.batch, name)
+            h[name] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+        h["plan"] = torch.from_numpy(self.plan.blob).pin_memory()
+        h["o"] = torch.empty(self.o.shape, dtype=self.o.dtype, pin_memory=True)
+
+    def h2d_bytes(self) -> int:
+        return sum(v.numel() * v.element_size() for k, v in self.host.items() if k != "o")
+
+    def d2h_bytes(self) -> int:
+        return self.o.numel() * self.o.element_size()
+
+    def run_e2e(self, stream=None):
+        h = self.host
+        for name in ("q", "k_new", "v_new", "out_cache_loc"):
+            getattr(self, name).copy_(h[name], non_blocking=True)
+        for name in ("req_to_token", "req_pool_indices", "seq_lens"):
+            getattr(self.batch, name).copy_(h[name], non_blocking=True)
+        self.plan_dev.copy_(h["plan"], non_blocking=True)
+        self.run(stream)
+        h["o"].copy_(self.o, non_blocking=True)
+
+
+class PrefixCache:
+    """Device pool + host radix tree + slot allocator for one workload's shapes."""
+
+    def __init__(self, w, device="cuda"):
+        self.w = w
+        self.device = device
+        self.pool = Pool.allocate(w.num_slots, w.num_kv_heads, w.head_dim, w.dtype, w.k_scale, w.v_scale, device)
+        self.tree = RadixTree()
+        self.alloc = Allocator(w.slot_perm)
+        self.err = torch.zeros(64, dtype=torch.int32, device=device)
+
+    # ---- cache population (setup, not part of a step)
+    def populate(self, max_batch_tokens=1 << 18):
+        w = self.w
+        ks, vs, locs, pending = [], [], [], 0
+        for r in w.requests:
+            toks = _ctx_tokens(w, r)
+            c = len(toks) - r.n_new
+            vals, _ = self.tree.match_prefix(toks[:c])
+            m = len(vals)
+            if m == c:
+                continue
+            new = self.alloc.alloc(c - m)
+            kb, vb = _ctx_kv(w, r, m, c)
+            ks.append(kb)
+            vs.append(vb)
+            locs.append(new)
+            pending += c - m
+            pre = self.tree.insert(toks[:c], np.concatenate([vals, new]))
+            assert pre == m, (pre, m)
+            if pending >= max_batch_tokens:
+                self._store(ks, vs, locs)
+                ks, vs, locs, pending = [], [], [], 0
+        if ks:
+            self._store(ks, vs, locs)
+        torch.cuda.synchronize()
+
+    def _store(self, ks, vs, locs):
+        k = _bf16_dev(np.concatenate(ks), self.device)
+        v = _bf16_dev(np.concatenate(vs), self.device)
+        loc = torch.from_numpy(np.concatenate(locs).astype(np.int32)).to(self.device)
+        kv_store(self.pool, k, v, loc, self.err)
+
+    # ---- one attention call of a step
+    def prepare(self, kind, cascade=True, opts=None, min_group=2) -> Call:
+        w = self.w
+        reqs = [r for r in w.requests if r.kind == kind]
+        rows, last_nodes, seq, ext, new_all, kn, vn, qs = [], [], [], [], [], [], [], []
+        for r in reqs:
+            toks = _ctx_tokens(w, r)
+            L, c = len(toks), len(toks) - r.n_new
+            vals, last = self.tree.match_prefix(toks[:c])
+            if len(vals) != c:
+                raise RuntimeError(f"request {r.rid}: cached part not fully in the tree ({len(vals)} of {c})")
+            self.tree.inc_lock_ref(last)
+            new = self.alloc.alloc(r.n_new)
+            rows.append(np.concatenate([vals, new]).astype(np.int32))
+            last_nodes.append(last)
+            seq.append(L)
+            ext.append(r.n_new)
+            new_all.append(new)
+            kb, vb = _ctx_kv(w, r, c, L)
+            kn.append(kb)
+            vn.append(vb)
+            qs.append(r.q)
+        B = len(reqs)
+        stride = max(16, ((max(seq) if seq else 1) + 15) // 16 * 16)
+        rt = np.zeros((max(B, 1), stride), dtype=np.int32)
+        for i, row in enumerate(rows):
+            rt[i, :len(row)] = row
+        seq = np.asarray(seq, dtype=np.int32)
+        ext = np.asarray(ext, dtype=np.int32)
+        casc = self.tree.cascade(last_nodes, min_group) if (cascade and B > 1) else None
+        if casc is not None and casc.num_spans == 0:
+            casc = None
+        hq, hkv, d = w.num_q_heads, w.num_kv_heads, w.head_dim
+        if kind == "extend":
+            qo = np.concatenate([[0], np.cumsum(ext)]).astype(np.int32)
+            plan = plan_extend(seq, ext, qo, hq, hkv, d, casc, opts)
+        else:
+            plan = plan_decode(seq, hq, hkv, d, casc, opts)
+        dev = self.device
+        batch = Batch(torch.from_numpy(rt).to(dev), torch.arange(B, dtype=torch.int32, device=dev),
+                      torch.from_numpy(seq).to(dev))
+        plan_dev = torch.from_numpy(plan.blob).to(dev)
+        ws = torch.zeros((plan.info.workspace_bytes + 3) // 4, dtype=torch.int32, device=dev)
+        q = _bf16_dev(np.concatenate(qs), dev)
+        o = torch.empty_like(q)
+        loc = torch.from_numpy(np.concatenate(new_all).astype(np.int32)).to(dev)
+        k_new = _bf16_dev(np.concatenate(kn), dev)
+        v_new = _bf16_dev(np.concatenate(vn), dev)
+        return Call(kind, self.pool, batch, plan, plan_dev, ws, q, o, loc, k_new, v_new, w.sm_scale, last_nodes,
+                    cascade=casc)
+
+    def release(self, call: Call):
+        for n in call.last_nodes:
+            self.tree.dec_lock_ref(n)

@@ -11,3 +11,10 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: takes more than a few seconds on CPU")
+
+
+def pytest_sessionstart(session):
+    # The product tests load the in-tree library; (re)build it when sources changed.  nvcc
+    # cross-compiles for sm_103a without a GPU, so this also works on CPU-only hosts.
+    from prefix_shared_kv_token_gb300.build import build
+    build()

@@ -1,0 +1,245 @@
+"""GPU parity: the CUDA path (through the C ABI) against the oracle on the same seeded inputs.
+
+Bars: kv_store and every index table bit-exact; attention max-abs error <= 1e-2 for a bf16
+pool and <= 5e-2 for an fp8 pool, against the float64 oracle (contiguous recompute, which
+never looks at slots or tables).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import step as ostep
+from oracle.fp8 import quantize_to_pool
+from oracle.kv_store import kv_store_bf16, kv_store_fp8
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 1e-2, "fp8_e4m3": 5e-2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _pkv():
+    import prefix_shared_kv_token_gb300 as pkv
+    from prefix_shared_kv_token_gb300.runtime import PrefixCache
+    return pkv, PrefixCache
+
+
+def _f64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def _bits(t):
+    return t.cpu().view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.cpu().numpy()
+
+
+def run_step(w, cascade=True, opts=None, kinds=("extend", "decode")):
+    pkv, PrefixCache = _pkv()
+    pc = PrefixCache(w)
+    pc.populate()
+    calls = {}
+    for kind in kinds:
+        if any(r.kind == kind for r in w.requests):
+            calls[kind] = pc.prepare(kind, cascade=cascade, opts=opts)
+    for c in calls.values():
+        c.run()
+    torch.cuda.synchronize()
+    for c in calls.values():
+        assert pkv.get_device_error(c.workspace) == 0
+    assert pkv.get_device_error(pc.err) == 0
+    return pc, calls
+
+
+def check_outputs(w, calls, tol=None):
+    tol = tol or TOL[w.dtype]
+    for kind, c in calls.items():
+        want = ostep.expected_outputs(w, kind)
+        got = _f64(c.o)
+        assert got.shape == want.shape
+        assert np.all(np.isfinite(got))
+        err = np.max(np.abs(got - want))
+        assert err <= tol, (kind, err)
+
+
+def check_pool(w, pc):
+    """Every cached and new token's pool row equals the oracle's store of its K/V."""
+    rows_k, rows_v, slots = [], [], []
+    for r in w.requests:
+        toks = W.context_tokens(w, r)
+        vals, _ = pc.tree.match_prefix(toks[:len(toks) - r.n_new])
+        kb, vb = W.context_kv_bits(w, r)
+        slots.append(vals)
+        rows_k.append(kb[:len(vals)])
+        rows_v.append(vb[:len(vals)])
+    slots = np.concatenate(slots)
+    kb, vb = np.concatenate(rows_k), np.concatenate(rows_v)
+    idx = torch.from_numpy(slots.astype(np.int64)).to(pc.pool.k.device)
+    gk, gv = _bits(pc.pool.k[idx]), _bits(pc.pool.v[idx])
+    if w.dtype == "bf16":
+        assert np.array_equal(gk, kb) and np.array_equal(gv, vb)
+    else:
+        assert np.array_equal(gk, quantize_to_pool(W.bf16_bits_to_f64(kb), w.k_scale))
+        assert np.array_equal(gv, quantize_to_pool(W.bf16_bits_to_f64(vb), w.v_scale))
+
+
+# ------------------------------------------------------------------------------ kv_store
+
+@pytest.mark.parametrize("n,hkv,d", [(1, 8, 128), (7, 2, 64), (333, 8, 128), (4096, 8, 128)])
+@pytest.mark.parametrize("dtype,scale", [("bf16", 1.0), ("fp8_e4m3", 1.0), ("fp8_e4m3", 0.0125), ("fp8_e4m3", 3.7)])
+def test_kv_store_bit_exact(n, hkv, d, dtype, scale):
+    pkv, _ = _pkv()
+    S = 5000
+    rng = np.random.default_rng(n + hkv)
+    x = rng.standard_normal((2, n, hkv, d)).astype(np.float32) * np.float32(scale * 40)
+    x[:, :, 0, :4] = [500.0, -1e4, 3e-3 * scale, -2e-4 * scale]       # saturation and subnormal cases
+    bits = W.generate.to_bf16_bits(x)
+    loc = rng.permutation(S)[:n].astype(np.int32)
+    pool = pkv.Pool.allocate(S, hkv, d, dtype, scale, scale)
+    init = rng.integers(0, 255, size=pool.k.numel() * pool.k.element_size(), dtype=np.uint8)
+    pool.k.view(torch.uint8).view(-1).copy_(torch.from_numpy(init))
+    pool.v.view(torch.uint8).view(-1).copy_(torch.from_numpy(init[::-1].copy()))
+    k0, v0 = _bits(pool.k), _bits(pool.v)
+    dev = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).cuda()
+    err = torch.zeros(4, dtype=torch.int32, device="cuda")
+    pkv.kv_store(pool, dev(bits[0]), dev(bits[1]), torch.from_numpy(loc).cuda(), err)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error(err) == 0
+    if dtype == "bf16":
+        want_k, want_v = kv_store_bf16(k0, bits[0], loc), kv_store_bf16(v0, bits[1], loc)
+    else:
+        want_k, want_v = kv_store_fp8(k0, bits[0], loc, scale), kv_store_fp8(v0, bits[1], loc, scale)
+    assert np.array_equal(_bits(pool.k), want_k)
+    assert np.array_equal(_bits(pool.v), want_v)
+
+
+def test_kv_store_out_of_range_slot_is_reported_not_written():
+    pkv, _ = _pkv()
+    pool = pkv.Pool.allocate(64, 2, 64)
+    k = torch.ones((3, 2, 64), dtype=torch.bfloat16, device="cuda")
+    loc = torch.tensor([5, 64, 7], dtype=torch.int32, device="cuda")   # 64 == num_slots
+    err = torch.zeros(4, dtype=torch.int32, device="cuda")
+    pkv.kv_store(pool, k, k, loc, err)
+    assert pkv.get_device_error(err) == 0x100
+    assert pool.k[5].float().sum().item() == 128 and pool.k[7].float().sum().item() == 128
+    assert pool.k.float().sum().item() == 256
+
+
+def test_kv_store_empty_is_noop():
+    pkv, _ = _pkv()
+    pool = pkv.Pool.allocate(8, 1, 64)
+    e = torch.empty((0, 1, 64), dtype=torch.bfloat16, device="cuda")
+    pkv.kv_store(pool, e, e, torch.empty(0, dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------------------ decode
+
+def test_tiny_decode_full():
+    w = W.config(1)
+    pc, calls = run_step(w)
+    check_outputs(w, calls)
+    check_pool(w, pc)
+
+
+@pytest.mark.parametrize("cascade", [True, False])
+@pytest.mark.parametrize("hq,hkv,d", [(32, 8, 128), (8, 8, 64), (16, 8, 128), (64, 8, 64)])
+def test_decode_small(cascade, hq, hkv, d):
+    w = W.batched_decode(seed=31, n_req=21, prefix=200, lo=1, hi=300, hq=hq, hkv=hkv, d=d, num_slots=20000)
+    pc, calls = run_step(w, cascade=cascade)
+    check_outputs(w, calls)
+    if cascade:
+        assert calls["decode"].plan.info.num_span_items > 0
+
+
+@pytest.mark.parametrize("cascade", [True, False])
+def test_decode_fp8_small(cascade):
+    w = W.batched_decode(seed=32, n_req=9, prefix=150, lo=20, hi=200, num_slots=8000, dtype="fp8_e4m3")
+    pc, calls = run_step(w, cascade=cascade)
+    check_outputs(w, calls)
+    check_pool(w, pc)
+
+
+@pytest.mark.parametrize("chunk", [64, 100, 4096])
+def test_decode_chunking(chunk):
+    w = W.batched_decode(seed=33, n_req=6, prefix=64, lo=100, hi=700, hq=8, hkv=2, d=64, num_slots=6000)
+    _, calls = run_step(w, opts={"chunk_keys": chunk, "span_chunk": chunk})
+    check_outputs(w, calls)
+
+
+def test_multiturn_small():
+    w = W.multiturn_decode(seed=34, n_conv=3, turns=3, user=(20, 90), reply=(5, 60), num_slots=20000)
+    pc, calls = run_step(w)
+    check_outputs(w, calls)
+    check_pool(w, pc)
+
+
+def test_decode_context_of_one_token():
+    b = W.generate._Builder(35, 8, 2, 64, 64)
+    leaves = [b.segment(-1, 1) for _ in range(3)]      # contexts of a single (query) token
+    for leaf in leaves:
+        b.request(leaf, "decode", 1)
+    w = b.finish("single", 35, 64)
+    _, calls = run_step(w)
+    got = _f64(calls["decode"].o)
+    want = ostep.expected_outputs(w, "decode")
+    assert np.max(np.abs(got - want)) <= 1e-2     # one key: the output is its value (bf16-rounded)
+
+
+# ------------------------------------------------------------------------------ extend
+
+@pytest.mark.parametrize("cascade", [True, False])
+@pytest.mark.parametrize("hq,hkv,d", [(32, 8, 128), (8, 2, 64), (16, 16, 128), (64, 8, 128)])
+def test_extend_small(cascade, hq, hkv, d):
+    w = W.fewshot_extend(seed=41, n_req=3, prefix=300, suffix=70, hq=hq, hkv=hkv, d=d, num_slots=4000)
+    pc, calls = run_step(w, cascade=cascade)
+    check_outputs(w, calls)
+    check_pool(w, pc)
+
+
+@pytest.mark.parametrize("prefix,suffix", [(1, 1), (127, 129), (256, 33), (5, 300)])
+def test_extend_ragged(prefix, suffix):
+    w = W.fewshot_extend(seed=42 + prefix, n_req=2, prefix=prefix, suffix=suffix, num_slots=4000)
+    _, calls = run_step(w)
+    check_outputs(w, calls)
+
+
+def test_extend_without_prefix():
+    b = W.generate._Builder(43, 32, 8, 128, 2000)
+    leaves = [b.segment(-1, n) for n in (1, 77, 160)]
+    for leaf, n in zip(leaves, (1, 77, 160)):
+        b.request(leaf, "extend", n)
+    w = b.finish("noprefix", 43, 2000)
+    _, calls = run_step(w)
+    check_outputs(w, calls)
+
+
+@pytest.mark.parametrize("cascade", [True, False])
+def test_extend_fp8_small(cascade):
+    w = W.fewshot_extend(seed=44, n_req=3, prefix=200, suffix=90, num_slots=4000, dtype="fp8_e4m3")
+    pc, calls = run_step(w, cascade=cascade)
+    check_outputs(w, calls)
+    check_pool(w, pc)
+
+
+def test_tot_mixed_small():
+    w = W.tot_mixed(seed=45, root_len=300, depth=2, branch=3, seg=40, n_new_branches=2, num_slots=8000)
+    pc, calls = run_step(w)
+    assert set(calls) == {"extend", "decode"}
+    check_outputs(w, calls)
+    check_pool(w, pc)
+
+
+def test_shared_equals_duplicated_prefix():
+    """Same K/V reached through one shared span or through per-request copies (no
+    sharing): the kernels give identical results either way within fp32 noise."""
+    w = W.fewshot_extend(seed=46, n_req=4, prefix=180, suffix=40, hq=8, hkv=2, d=64, num_slots=4000)
+    _, shared = run_step(w, cascade=True)
+    _, plain = run_step(w, cascade=False)
+    a, b = _f64(shared["extend"].o), _f64(plain["extend"].o)
+    assert np.max(np.abs(a - b)) <= 2 * 2.0 ** -8

@@ -1,0 +1,132 @@
+"""Planner checks on the host: every (request, query head, key position) is covered by
+exactly one work item, records and merges are consistent, and malformed inputs are
+rejected.  Also checks that libpkv exports every entry point include/pkv.h declares."""
+
+import os
+import re
+
+import numpy as np
+import pytest
+
+import prefix_shared_kv_token_gb300 as pkv
+from prefix_shared_kv_token_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+DEC = np.dtype([("g", "<i4"), ("mode", "<i4"), ("nreq", "<i4"), ("row_off", "<i4"), ("src", "<i4"),
+                ("k0", "<i4"), ("k1", "<i4"), ("pad", "<i4")])
+EXT = np.dtype([("g", "<i4"), ("src", "<i4"), ("tok0", "<i4"), ("ntok", "<i4"), ("qpos0", "<i4"),
+                ("k0", "<i4"), ("k1", "<i4"), ("rec", "<i4")])
+MRG = np.dtype([("out_row", "<i4"), ("rec0", "<i4"), ("nrec", "<i4"), ("stride", "<i4")])
+
+
+def test_header_symbols_exported():
+    hdr = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    declared = set(re.findall(r"\b(pkv_[a-z_0-9]+)\s*\(", hdr))
+    assert len(declared) >= 20
+    for name in sorted(declared):
+        assert hasattr(_lib.lib, name), name
+    assert set(_lib.SIGNATURES) == declared
+
+
+def _sections(plan, dtype, n, off):
+    b = plan.blob
+    return np.frombuffer(b[off:off + n * dtype.itemsize].tobytes(), dtype=dtype)
+
+
+def _decode_cover(plan, seq, hkv, cascade_spans=None):
+    info = plan.info
+    items = _sections(plan, DEC, info.num_items, info.offsets[0])
+    nrows = (info.offsets[2] - info.offsets[1]) // 4
+    row_req = np.frombuffer(plan.blob[info.offsets[1]:info.offsets[1] + 4 * nrows].tobytes(), np.int32)
+    row_rec = np.frombuffer(plan.blob[info.offsets[2]:info.offsets[2] + 4 * nrows].tobytes(), np.int32)
+    merges = _sections(plan, MRG, info.num_merge, info.offsets[3])
+    B = len(seq)
+    cover = [np.zeros((hkv, seq[r]), np.int32) for r in range(B)]
+    recs_seen = {}
+    for it in items:
+        for i in range(it["nreq"]):
+            r = row_req[it["row_off"] + i]
+            k1 = it["k1"] if it["k1"] >= 0 else seq[r]
+            cover[r][it["g"], it["k0"]:k1] += 1
+            recs_seen.setdefault(r, set()).add(row_rec[it["row_off"] + i])
+    for r in range(B):
+        assert np.all(cover[r] == 1), r
+    merged = {int(m["out_row"]): m for m in merges}
+    for r in range(B):
+        rec = recs_seen[r]
+        if r in merged:
+            m = merged[r]
+            assert rec == set(range(m["rec0"], m["rec0"] + m["nrec"]))
+        else:
+            assert rec == {-1}
+    return items
+
+
+@pytest.mark.parametrize("chunk", [0, 64, 1000])
+def test_decode_plan_covers_every_key_once(chunk):
+    rng = np.random.default_rng(0)
+    seq = rng.integers(1, 900, size=37).astype(np.int32)
+    plan = pkv.plan_decode(seq, 32, 8, 128, None, {"chunk_keys": chunk} if chunk else None)
+    _decode_cover(plan, seq, 8)
+
+
+def test_decode_plan_with_cascade():
+    # requests 0..5 share positions [0, 100); requests 0..2 also share [100, 130)
+    seq = np.array([300, 150, 131, 120, 101, 400], np.int32)
+    casc = pkv.Cascade(span_req=np.array([0, 1], np.int32), span_start=np.array([0, 100], np.int32),
+                       span_len=np.array([100, 30], np.int32), grp_indptr=np.array([0, 6, 9], np.int32),
+                       grp_req=np.array([0, 1, 2, 3, 4, 5, 0, 1, 2], np.int32))
+    plan = pkv.plan_decode(seq, 8, 2, 64, casc)
+    items = _decode_cover(plan, seq, 2)
+    assert plan.info.num_span_items == 4
+    assert sum(1 for it in items if it["mode"] == 0) == 4
+
+
+def test_decode_plan_rejects_bad_cascade():
+    seq = np.array([50, 50], np.int32)
+    bad = pkv.Cascade(span_req=np.array([0], np.int32), span_start=np.array([5], np.int32),
+                      span_len=np.array([10], np.int32), grp_indptr=np.array([0, 2], np.int32),
+                      grp_req=np.array([0, 1], np.int32))
+    with pytest.raises(pkv.PkvError):
+        pkv.plan_decode(seq, 8, 2, 64, bad)   # a span must start where the previous ended (0)
+    with pytest.raises(pkv.PkvError):
+        pkv.plan_decode(np.array([0], np.int32), 8, 2, 64)  # empty context
+    with pytest.raises(pkv.PkvError):
+        pkv.plan_decode(seq, 12, 8, 64)      # G not in {1, 2, 4, 8}
+    with pytest.raises(pkv.PkvError):
+        pkv.plan_decode(seq, 8, 2, 96)       # head_dim
+
+
+@pytest.mark.parametrize("cascade", [False, True])
+def test_extend_plan_covers_causal_triangle(cascade):
+    ext = np.array([70, 33, 1, 129], np.int32)
+    pre = np.array([300, 300, 300, 0], np.int32) if not cascade else np.array([300, 300, 300, 0], np.int32)
+    seq = pre + ext
+    qo = np.concatenate([[0], np.cumsum(ext)]).astype(np.int32)
+    casc = None
+    if cascade:
+        casc = pkv.Cascade(span_req=np.array([1], np.int32), span_start=np.array([0], np.int32),
+                           span_len=np.array([250], np.int32), grp_indptr=np.array([0, 3], np.int32),
+                           grp_req=np.array([0, 1, 2], np.int32))
+    plan = pkv.plan_extend(seq, ext, qo, 32, 8, 128, casc)
+    info = plan.info
+    items = _sections(plan, EXT, info.num_items, info.offsets[0])
+    T = int(qo[-1])
+    req_of_tok = np.repeat(np.arange(4), ext)
+    pos_of_tok = np.concatenate([np.arange(pre[r], seq[r]) for r in range(4)])
+    cover = np.zeros((T, 8, int(seq.max())), np.int32)
+    for it in items:
+        for t in range(it["ntok"]):
+            tok = it["tok0"] + t
+            lim = min(it["k1"] - 1, it["qpos0"] + t)
+            cover[tok, it["g"], it["k0"]:lim + 1] += 1
+            if casc is None:
+                assert it["rec"] == -1
+    for tok in range(T):
+        want = np.zeros(cover.shape[2], np.int32)
+        want[:pos_of_tok[tok] + 1] = 1
+        assert np.array_equal(cover[tok, 0], want), tok
+        assert np.all(cover[tok] == cover[tok, 0])
+    if cascade:
+        assert info.num_merge == T and info.num_span_items > 0

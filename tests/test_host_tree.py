@@ -1,0 +1,128 @@
+"""The C++ radix tree and allocator (libpkv) against the oracle's tree, bit for bit: same
+node ids, keys, values, lock_refs and timestamps after random operation sequences, the
+pages' worked example, and eviction order."""
+
+import random
+
+import numpy as np
+import pytest
+
+from oracle.radix_tree import RadixCache
+from prefix_shared_kv_token_gb300 import Allocator, RadixTree
+
+
+def _oracle_dump(t: RadixCache):
+    rows = []
+    for n in t._all_nodes():
+        rows.append((n.id, -1 if n.parent is None else n.parent.id, n.lock_ref, n.last_access_time,
+                     tuple(n.key), tuple(n.value), len(n.children)))
+    return sorted(rows)
+
+
+def test_worked_example_cpp():
+    t = RadixTree()
+    assert t.insert([1, 2, 3, 4, 5], [0, 1, 2, 3, 4]) == 0
+    assert t.insert([1, 2, 3, 13, 14], [90, 91, 92, 5, 6]) == 3
+    assert t.insert([8, 9, 10, 11, 12], [7, 8, 9, 10, 11]) == 0
+    vals, last = t.match_prefix([1, 2, 3, 4, 5, 6])
+    assert vals.tolist() == [0, 1, 2, 3, 4]
+    nodes = {r[0]: r for r in t.dump()}
+    assert nodes[last][4] == (4, 5)
+    shared = [r for r in nodes.values() if r[4] == (1, 2, 3)]
+    assert len(shared) == 1 and shared[0][6] == 2
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_ops_bit_exact(seed):
+    rng = random.Random(seed)
+    a, b = RadixCache(), RadixTree()
+    locked = []
+    nxt = 0
+    for _ in range(400):
+        op = rng.random()
+        key = [rng.randint(0, 5) for _ in range(rng.randint(0, 12))]
+        if op < 0.35:
+            v = list(range(nxt, nxt + len(key)))
+            nxt += len(key)
+            assert a.insert(key, v) == b.insert(key, v)
+        elif op < 0.6:
+            va, na = a.match_prefix(key)
+            vb, nb = b.match_prefix(key)
+            assert va == vb.tolist() and na.id == nb
+            if va and rng.random() < 0.4:
+                assert a.inc_lock_ref(na) == b.inc_lock_ref(nb)
+                locked.append((na, nb))
+        elif op < 0.72 and locked:
+            na, nb = locked.pop(rng.randrange(len(locked)))
+            assert a.dec_lock_ref(na) == b.dec_lock_ref(nb)
+        else:
+            n = rng.randint(1, 10)
+            assert a.evict(n) == b.evict(n).tolist()
+        s = b.sizes()
+        assert (s["evictable"], s["protected"]) == (a.evictable_size_, a.protected_size_)
+        assert s["total"] == a.total_size()
+    assert _oracle_dump(a) == sorted(b.dump())
+
+
+def test_long_sequences_and_splits():
+    rng = np.random.default_rng(3)
+    a, b = RadixCache(), RadixTree()
+    base = rng.integers(0, 50, size=600).tolist()
+    for i in range(30):
+        cut = int(rng.integers(0, 600))
+        key = base[:cut] + rng.integers(0, 50, size=int(rng.integers(1, 200))).tolist()
+        v = list(range(10000 * i, 10000 * i + len(key)))
+        assert a.insert(key, v) == b.insert(key, v)
+        q = base[:int(rng.integers(0, 700))]
+        va, na = a.match_prefix(q)
+        vb, nb = b.match_prefix(q)
+        assert va == vb.tolist() and na.id == nb
+    assert _oracle_dump(a) == sorted(b.dump())
+
+
+def test_lock_errors():
+    t = RadixTree()
+    t.insert([1, 2], [0, 1])
+    _, n = t.match_prefix([1, 2])
+    with pytest.raises(Exception):
+        t.dec_lock_ref(n)           # nothing locked
+    with pytest.raises(Exception):
+        t.inc_lock_ref(12345)       # unknown node
+
+
+def test_allocator_fifo():
+    a = Allocator([5, 3, 9, 1])
+    assert a.alloc(2).tolist() == [5, 3]
+    a.release([7])
+    assert a.available == 3
+    assert a.alloc(3).tolist() == [9, 1, 7]
+    with pytest.raises(Exception):
+        a.alloc(1)
+
+
+def test_cascade_spans_tile_shared_prefixes():
+    t = RadixTree()
+    # root segment A (10), children B (5) and C (7); B has children D (3), E (4)
+    A = list(range(100, 110))
+    B, C = [1, 2, 3, 4, 5], [6, 7, 8, 9, 10, 11, 12]
+    D, E = [20, 21, 22], [30, 31, 32, 33]
+    paths = [A + B + D, A + B + E, A + C, A + B + D[:1]]
+    slot = 0
+    last = []
+    for p in paths:
+        vals, _ = t.match_prefix(p)
+        new = list(range(slot, slot + len(p) - len(vals)))
+        slot += len(new)
+        t.insert(p, list(vals) + new)
+    for p in paths:
+        vals, node = t.match_prefix(p)
+        assert len(vals) == len(p)
+        last.append(node)
+    c = t.cascade(last)
+    spans = [(int(c.span_start[s]), int(c.span_len[s]),
+              sorted(c.grp_req[c.grp_indptr[s]:c.grp_indptr[s + 1]].tolist())) for s in range(c.num_spans)]
+    # A shared by all 4; B by requests 0, 1, 3; D[:1] by requests 0 and 3
+    assert (0, 10, [0, 1, 2, 3]) in spans
+    assert (10, 5, [0, 1, 3]) in spans
+    assert (15, 1, [0, 3]) in spans
+    assert len(spans) == 3

@@ -1,0 +1,401 @@
+"""Benchmark of the prefix-shared KV attention hot path on one GB300 (or N replicas).
+
+One *step* is the whole hot path over one batch of the chosen synthetic workload:
+kv_store of the step's new tokens, then the attention call(s) (extend and/or decode,
+with the shared-prefix cascade), then the partial-state merge.  Inputs are resident in HBM
+when the timed region starts; the L2 is flushed (512 MiB write) between timed steps, outside
+the per-step CUDA events.  ``e2e`` repeats the measurement through the same C-ABI calls with
+the step's inputs copied from pinned host memory and the output copied back inside the
+timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl ours|reference]
+
+--impl reference times the oracle (plain float64 CPU code) on the host cores on bounded
+samples of the same workload.  Under torchrun each rank runs an independent replica (the
+path shards by request group with no exchange); rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention tokens/s (extend+decode) and achieved HBM GB/s vs roofline, 1 GB300"
+DEFAULT_CONFIG = 2
+
+
+# ----------------------------------------------------------------------------------------
+# helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def kernel_hash(kind):
+    src = {"extend": "attn_extend.cu", "decode": "attn_decode.cu", "store": "kv_store.cu"}[kind]
+    h = hashlib.sha256()
+    for f in (src, "common.cuh"):
+        with open(os.path.join(ROOT, "prefix_shared_kv_token_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kind, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current source."""
+    path = os.path.join(ROOT, "profiles", f"{kind}_{workload}.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("source_hash") == kernel_hash(kind):
+            return float(d["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def workload_facts(w):
+    """Algorithmic work of one step: query tokens, unmasked-pair FLOPs, unique KV bytes."""
+    hq, hkv, d = w.num_q_heads, w.num_kv_heads, w.head_dim
+    elem = 1 if w.dtype == "fp8_e4m3" else 2
+    facts = {}
+    for kind in ("extend", "decode"):
+        reqs = [r for r in w.requests if r.kind == kind]
+        if not reqs:
+            continue
+        pairs = 0
+        segs = set()
+        for r in reqs:
+            L = w.context_len(r)
+            if kind == "extend":
+                p = L - r.n_new
+                pairs += sum(p + i + 1 for i in range(r.n_new))
+            else:
+                pairs += L
+            segs.update(r.path)
+        unique_tokens = sum(len(w.segments[s].tokens) for s in segs)
+        nq = sum(r.n_new if kind == "extend" else 1 for r in reqs)
+        facts[kind] = {
+            "queries": nq,
+            "flops": 4.0 * d * hq * pairs,
+            "kv_bytes": float(unique_tokens * hkv * d * elem * 2),
+            "qo_bytes": float(nq * hq * d * 2 * 2),
+            "new_tokens": sum(r.n_new for r in reqs),
+        }
+    return facts
+
+
+# ----------------------------------------------------------------------------------------
+# our arm
+
+
+def run_ours(args, rank, world):
+    import torch
+    import workloads as W
+    from prefix_shared_kv_token_gb300.runtime import PrefixCache
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = W.config(args.config)
+    facts = workload_facts(w)
+    pc = PrefixCache(w, device=str(dev))
+    pc.populate()
+    calls = [pc.prepare(kind, cascade=not args.no_cascade) for kind in ("extend", "decode")
+             if any(r.kind == kind for r in w.requests)]
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        for c in calls:
+            c.store()
+        for c in calls:
+            c.attend()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    import prefix_shared_kv_token_gb300 as pkv
+    for c in calls:
+        if pkv.get_device_error(c.workspace) != 0:
+            raise RuntimeError("device error word set during warm-up")
+
+    # timed region: per-step events (store, attention per call) on the launching stream
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 + 2 * len(calls))] for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        t0 = time.perf_counter()
+        for k in range(K):
+            flush.zero_()
+            e = ev[k]
+            e[0].record(stream)
+            for c in calls:
+                c.store()
+            e[1].record(stream)
+            for i, c in enumerate(calls):
+                e[2 + 2 * i].record(stream)
+                c.attend()
+                e[3 + 2 * i].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        if world > 1:
+            torch.distributed.barrier()
+        # end-to-end: same calls, inputs from pinned host memory, output back to the host
+        for c in calls:
+            c.pin_host()
+        e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for c in calls:
+            c.run_e2e()
+        torch.cuda.synchronize()
+        for k in range(K):
+            flush.zero_()
+            e2e_ev[k][0].record(stream)
+            for c in calls:
+                c.run_e2e()
+            e2e_ev[k][1].record(stream)
+        torch.cuda.synchronize()
+    step_ms = [ev[k][0].elapsed_time(ev[k][-1]) for k in range(K)]
+    store_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    attn_ms = {c.kind: [ev[k][2 + 2 * i].elapsed_time(ev[k][3 + 2 * i]) for k in range(K)]
+               for i, c in enumerate(calls)}
+    e2e_ms = [a.elapsed_time(b) for a, b in e2e_ev]
+    for c in calls:
+        if pkv.get_device_error(c.workspace) != 0:
+            raise RuntimeError("device error word set during the timed steps")
+
+    tokens_per_step = sum(c.num_queries for c in calls)
+    t_total = sum(step_ms) / 1e3
+    t_e2e = sum(e2e_ms) / 1e3
+    if world > 1:
+        tt = torch.tensor([t_total, t_e2e], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t_total, t_e2e = float(tt[0]), float(tt[1])
+    value = world * K * tokens_per_step / t_total
+    e2e_value = world * K * tokens_per_step / t_e2e
+
+    # roofline of the dominant kernel
+    pk = peaks()
+    dominant = max(attn_ms, key=lambda k: float(np.mean(attn_ms[k])))
+    dur = float(np.mean(attn_ms[dominant])) / 1e3
+    fx = facts[dominant]
+    if dominant == "extend":
+        achieved = fx["flops"] / dur / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved / pk["bf16_tflops"], 4), "kernel": "extend_kernel",
+                "algorithmic_per_launch": fx["flops"]}
+    else:
+        achieved = (fx["kv_bytes"] + fx["qo_bytes"]) / dur / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / pk["hbm_gbs"], 4), "kernel": "decode_kernel+merge_kernel",
+                "algorithmic_per_launch": fx["kv_bytes"] + fx["qo_bytes"]}
+    traffic = profiled_traffic(dominant, w.name)
+    roof["traffic"] = traffic
+    roof["peak_source"] = pk["source"] + " (burst)"
+
+    launches_per_step = sum(1 + 1 + (1 if c.plan.info.num_merge > 0 else 0) for c in calls)
+    h2d = sum(c.h2d_bytes() for c in calls)
+    d2h = sum(c.d2h_bytes() for c in calls)
+    cfg = {"workload": w.name, "config_id": args.config, "requests": len(w.requests),
+           "heads_q_kv": f"{w.num_q_heads}/{w.num_kv_heads}", "head_dim": w.head_dim, "pool_dtype": w.dtype,
+           "pool_slots": w.num_slots, "cascade": not args.no_cascade,
+           "l2": "flushed between timed steps (512 MiB write outside the step events)",
+           "tokens_per_step": tokens_per_step}
+    for kind, fx_ in facts.items():
+        cfg[f"{kind}_queries"] = fx_["queries"]
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(t_total * 1e3 / K, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "bf16 (fp8_e4m3 pool)",
+        "data": "synthetic", "config": cfg,
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(t_e2e * 1e3 / K, 4)},
+        "roofline": roof,
+        "gpu_launches": K * launches_per_step,
+        "kernel_ms": {"kv_store": round(float(np.mean(store_ms)), 4),
+                      **{f"attn_{k}": round(float(np.mean(v)), 4) for k, v in attn_ms.items()}},
+        "wall_s": round(wall, 4),
+        "clocks": clocks.summary(),
+    }
+    return out, w
+
+
+# ----------------------------------------------------------------------------------------
+# the oracle on the host cores
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+        return int(n)
+    except Exception:
+        return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+def oracle_sample(w, budget_s, start=0):
+    """Run the oracle over requests (round robin from `start`) until `budget_s` of CPU work;
+    returns (query tokens, seconds, requests used)."""
+    from oracle import step as ostep
+    t0 = time.perf_counter()
+    toks, used, i = 0, 0, start
+    n = len(w.requests)
+    while used < n:
+        r = w.requests[i % n]
+        ostep.request_output(w, r)
+        toks += r.n_new if r.kind == "extend" else 1
+        used += 1
+        i += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    return toks, time.perf_counter() - t0, used
+
+
+def cpu_baseline(w, budget_s=12.0):
+    toks, secs, used = oracle_sample(w, budget_s)
+    return {"value": round(toks / secs, 2), "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+            "sample": f"{used} of {len(w.requests)} requests ({toks} query tokens) of {w.name}, float64 numpy, "
+                      f"{secs:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    import workloads as W
+    w = W.config(args.config)
+    per_step = 2.0
+    for k in range(args.warmup):
+        oracle_sample(w, 0.2, start=k)
+    toks_total, secs_total, used_total = 0, 0.0, 0
+    for k in range(args.steps):
+        toks, secs, used = oracle_sample(w, per_step, start=k * 7)
+        toks_total += toks
+        secs_total += secs
+        used_total += used
+    value = toks_total / secs_total
+    cb = {"value": round(value, 2), "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+          "sample": f"{args.steps} steps x ~{per_step:.0f} s, {used_total} requests ({toks_total} query tokens) "
+                    f"of {w.name}, float64 numpy"}
+    return {"metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(secs_total * 1e3 / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "config_id": args.config, "requests": len(w.requests)},
+            "impl": "reference", "cpu_baseline": cb,
+            "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ----------------------------------------------------------------------------------------
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cascade", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)))
+        return
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    out, w = run_ours(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(w)
+        print(json.dumps(out))
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -16,5 +16,9 @@ def pytest_configure(config):
 def pytest_sessionstart(session):
     # The product tests load the in-tree library; (re)build it when sources changed.  nvcc
     # cross-compiles for sm_103a without a GPU, so this also works on CPU-only hosts.
-    from prefix_shared_kv_token_gb300.build import build
-    build()
+    import importlib.util
+    path = os.path.join(ROOT, "prefix_shared_kv_token_gb300", "build.py")
+    spec = importlib.util.spec_from_file_location("_pkv_build", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()

@@ -66,7 +66,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except Exception:
@@ -159,6 +159,16 @@ def workload_facts(w):
     return facts
 
 
+def load_workload(args):
+    """The configuration's workload; --pool-slots only shrinks the pool (same tokens/values
+    up to the slot permutation), for profiler captures that must stay a few GB."""
+    import workloads as W
+    if not args.pool_slots:
+        return W.config(args.config)
+    gen = {1: W.tiny_decode, 2: W.fewshot_extend, 3: W.batched_decode, 4: W.multiturn_decode, 5: W.tot_mixed}
+    return gen[args.config](seed=args.config, num_slots=args.pool_slots)
+
+
 # ----------------------------------------------------------------------------------------
 # our arm
 
@@ -170,7 +180,7 @@ def run_ours(args, rank, world):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    w = W.config(args.config)
+    w = load_workload(args)
     facts = workload_facts(w)
     pc = PrefixCache(w, device=str(dev))
     pc.populate()
@@ -334,8 +344,7 @@ def cpu_baseline(w, budget_s=12.0):
 
 
 def run_reference(args, rank, world):
-    import workloads as W
-    w = W.config(args.config)
+    w = load_workload(args)
     per_step = 2.0
     for k in range(args.warmup):
         oracle_sample(w, 0.2, start=k)
@@ -363,12 +372,13 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cascade", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pool-slots", type=int, default=0)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

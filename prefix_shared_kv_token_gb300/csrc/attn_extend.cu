@@ -12,11 +12,13 @@
 //   * 128 rows = 128/G query tokens x the G heads that share KV head g, so every K/V row
 //     gathered from the pool feeds G query heads.  Q comes in with two 3-D TMA tile loads
 //     (box 64 x G x 128/G, 128-byte swizzle).
-//   * K and V tiles of 128 keys are gathered straight from the token-indexed pool by TMA
-//     tile::gather4 (4 arbitrary rows of the [slots * Hkv, d] view per instruction, one lane
-//     per 4 keys), landing in the 128-byte-swizzled K-major layout tcgen05 reads.  Keys past
-//     the end of the item read slot 0's row and are masked to p = 0, so the pool must hold
-//     finite values in slot 0 (pools start zeroed).
+//   * K and V tiles of 128 keys are gathered straight from the token-indexed pool by three
+//     loader warps with 16-byte cp.async (LSU path; lanes of a warp cover whole 256-byte
+//     rows), landing in the 128-byte-swizzled K-major layout tcgen05 reads; each loader
+//     waits for its own copies and issues fence.proxy.async before arriving on the tile's
+//     mbarrier.  Keys past the end of the item are zero-filled.  (TMA tile::gather4 of
+//     128-byte rows was measured first: it delivered ~8 B/clk/SM, far below what the tensor
+//     core consumes, so the gather runs on the LSU.)
 //   * warp 0 issues tcgen05.mma (one thread): S = Q K^T into tensor memory (two S buffers),
 //     then O += P V with P taken from tensor memory (the A operand) and V from shared memory
 //     as an MN-major operand.  tcgen05.commit signals mbarriers.
@@ -24,8 +26,8 @@
 //     tcgen05.ld S, causal mask, exp2, write P (bf16) back over S with tcgen05.st.  O is
 //     rescaled in tensor memory only when the running max grows by more than 2^8 (the
 //     stale max keeps every p <= 256, exact in fp32 and bf16), so rescales are rare.
-//   * fp8 pools: gather4 brings raw e4m3 rows into a staging ring; warps 2-3 convert them
-//     exactly to bf16 in the swizzled operand layout (generic-proxy writes, then
+//   * fp8 pools: the loaders read e4m3 rows into registers, convert them exactly to bf16
+//     and store them into the same swizzled operand layout (generic-proxy writes, then
 //     fence.proxy.async before the MMA reads them).
 //   * Every wait is bounded (2 s); on expiry the kernel records PKV_DERR_TIMEOUT, lets the
 //     other roles time out too, drains in-flight work and frees tensor memory.
@@ -44,6 +46,8 @@ constexpr float kLog2eX = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct ExtendParams {
+    const uint8_t *k_pool;
+    const uint8_t *v_pool;
     const int32_t *req_to_token;
     int64_t rt_stride;
     int32_t rt_rows;
@@ -61,15 +65,14 @@ struct ExtendParams {
 
 template <int D, bool FP8>
 struct ExtendCfg {
-    static constexpr int kStages = FP8 ? 2 : 3;
+    static constexpr int kStages = 3;
     static constexpr int kBlk = kBN * 128;              // one 64-column block of a K/V tile
     static constexpr int kTile = kBN * D * 2;           // bf16 K (or V) tile
     static constexpr int kQBytes = kBM * D * 2;
-    static constexpr int kRawTile = FP8 ? kBN * D : 0;  // e4m3 staging tile
     static constexpr int kQOff = 0;
     static constexpr int kStageOff = kQBytes;
-    static constexpr int kRawOff = kStageOff + kStages * 2 * kTile;
-    static constexpr int kBarOff = kRawOff + kStages * 2 * kRawTile;
+    static constexpr int kSlotOff = kStageOff + kStages * 2 * kTile;  // [2][kBN] int32
+    static constexpr int kBarOff = kSlotOff + 2 * kBN * 4;
     static constexpr int kBarBytes = 256;
     static constexpr int kSmem = kBarOff + kBarBytes + 1024;  // + alignment slack
     static constexpr uint32_t kTmemCols = 512;
@@ -80,7 +83,6 @@ struct ExtendCfg {
 struct Bars {
     uint64_t q;
     uint64_t kfull[3], vfull[3], kvempty[3];
-    uint64_t rawk[3], rawv[3], rawempty[3];
     uint64_t sfull[2], pfull[2];
     uint64_t odone, ofinal, drain;
     uint32_t tmem_base;
@@ -105,8 +107,7 @@ PKV_DEV bool wait_or_abort(uint64_t *bar, uint32_t parity, Bars *b, int32_t *err
 
 template <int D, int G, bool FP8>
 __global__ void __launch_bounds__(256, 1)
-    extend_kernel(const ExtendParams p, const __grid_constant__ CUtensorMap qmap,
-                  const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
+    extend_kernel(const ExtendParams p, const __grid_constant__ CUtensorMap qmap) {
     using C = ExtendCfg<D, FP8>;
     constexpr int ST = C::kStages;
     constexpr int NBLK = D / 64;
@@ -136,12 +137,9 @@ __global__ void __launch_bounds__(256, 1)
     if (threadIdx.x == 0) {
         mbar_init(&bars->q, 1);
         for (int s = 0; s < ST; ++s) {
-            mbar_init(&bars->kfull[s], FP8 ? 64 : 1);
-            mbar_init(&bars->vfull[s], FP8 ? 64 : 1);
+            mbar_init(&bars->kfull[s], 96);  // every loader thread arrives
+            mbar_init(&bars->vfull[s], 96);
             mbar_init(&bars->kvempty[s], 1);
-            mbar_init(&bars->rawk[s], 1);
-            mbar_init(&bars->rawv[s], 1);
-            mbar_init(&bars->rawempty[s], 64);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bars->sfull[b], 1);
@@ -207,119 +205,129 @@ __global__ void __launch_bounds__(256, 1)
             wait_or_abort(&bars->drain, 0, bars, nullptr, 0);
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ================= TMA producer (all 32 lanes; lane l gathers keys 4l .. 4l+3) =====
-        constexpr uint32_t kRowBytes = FP8 ? D : 2 * D;
-        constexpr uint32_t kTileTx = kBN * kRowBytes;
-        if (lane == 0) {
+    } else if (warp < 4) {
+        // ================= loaders (warps 1-3, 96 threads) =================
+        // Q arrives with one TMA tile load per 64-column block.  K/V: every 16-byte chunk of
+        // the tile's key rows is gathered with cp.async (bf16 pool) or loaded, converted
+        // e4m3 -> bf16 exactly and stored (fp8 pool), straight into the 128-byte-swizzled
+        // K-major layout; lanes of a warp cover contiguous 256-byte rows.  The slot numbers
+        // of the next tile are staged in shared memory while the current tile is issued.
+        constexpr int NP = 96;
+        const int pt = threadIdx.x - 32;  // 0..95
+        int32_t *sl = reinterpret_cast<int32_t *>(smem + C::kSlotOff);  // [2][kBN]
+        if (pt == 0) {
             prefetch_tmap(&qmap);
-            prefetch_tmap(&kmap);
-            prefetch_tmap(&vmap);
             mbar_arrive_expect_tx(&bars->q, kBM * D * 2);
 #pragma unroll
             for (int b = 0; b < NBLK; ++b)
                 tma_load_3d(sbase + C::kQOff + b * (kBM * 128), &qmap, b * 64, g * G, it.tok0, &bars->q);
         }
-        int issued = 0;
-        for (int j = 0; j < ntiles; ++j) {
-            const int s = j % ST;
-            if (j >= ST) {
-                uint64_t *free_bar = FP8 ? &bars->rawempty[s] : &bars->kvempty[s];
-                if (!wait_or_abort(free_bar, ((j / ST) - 1) & 1, bars, p.err, 5)) break;
-            }
-            int32_t rows[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int kp = k0 + j * kBN + 4 * lane + i;
-                int32_t r = g;  // keys past k1: slot 0's row; masked to p = 0 by the softmax
+        auto load_slots = [&](int j, int buf) {
+            for (int k = pt; k < kBN; k += NP) {
+                const int kp = k0 + j * kBN + k;
+                int32_t slot = -1;
                 if (kp < k1) {
-                    const int32_t slot = __ldg(rt + kp);
-                    if (slot >= 0 && (int64_t)slot < p.num_slots)
-                        r = slot * p.hkv + g;
-                    else
+                    slot = __ldg(rt + kp);
+                    if (slot < 0 || (int64_t)slot >= p.num_slots) {
                         set_error(p.err, DERR_SLOT_RANGE);
-                }
-                rows[i] = r;
-            }
-            uint64_t *kb = FP8 ? &bars->rawk[s] : &bars->kfull[s];
-            uint64_t *vb = FP8 ? &bars->rawv[s] : &bars->vfull[s];
-            if (lane == 0) {
-                mbar_arrive_expect_tx(kb, kTileTx);
-                mbar_arrive_expect_tx(vb, kTileTx);
-            }
-            __syncwarp();
-            if constexpr (!FP8) {
-                const uint32_t k_s = sbase + C::kStageOff + (s * 2) * C::kTile;
-                const uint32_t v_s = k_s + C::kTile;
-#pragma unroll
-                for (int b = 0; b < NBLK; ++b) {
-                    const uint32_t dk = k_s + b * C::kBlk + (4 * lane) * 128;
-                    tma_gather4(dk, &kmap, b * 64, rows[0], rows[1], rows[2], rows[3], kb);
-                }
-#pragma unroll
-                for (int b = 0; b < NBLK; ++b) {
-                    const uint32_t dv = v_s + b * C::kBlk + (4 * lane) * 128;
-                    tma_gather4(dv, &vmap, b * 64, rows[0], rows[1], rows[2], rows[3], vb);
-                }
-            } else {
-                const uint32_t rk = sbase + C::kRawOff + (s * 2) * C::kRawTile;
-                const uint32_t rv = rk + C::kRawTile;
-                tma_gather4(rk + (4 * lane) * D, &kmap, 0, rows[0], rows[1], rows[2], rows[3], kb);
-                tma_gather4(rv + (4 * lane) * D, &vmap, 0, rows[0], rows[1], rows[2], rows[3], vb);
-            }
-            issued = j + 1;
-        }
-        // After an abort, copies may still be in flight: let the last stages land (bounded)
-        // before the CTA exits.  On the normal path the consumers already waited for them.
-        if (*reinterpret_cast<volatile int32_t *>(&bars->abort_flag)) {
-            for (int j = issued > ST ? issued - ST : 0; j < issued; ++j) {
-                const int s = j % ST;
-                uint64_t *kb = FP8 ? &bars->rawk[s] : &bars->kfull[s];
-                uint64_t *vb = FP8 ? &bars->rawv[s] : &bars->vfull[s];
-                mbar_wait(kb, (j / ST) & 1);
-                mbar_wait(vb, (j / ST) & 1);
-            }
-        }
-    } else if (warp < 4) {
-        // ================= fp8 converters (warps 2-3) =================
-        if constexpr (FP8) {
-            const int ct = threadIdx.x - 64;  // 0..63
-            constexpr int kChunks = kBN * D / 16;  // 16 codes per chunk
-            for (int j = 0; j < ntiles; ++j) {
-                const int s = j % ST;
-                if (j >= ST && !wait_or_abort(&bars->kvempty[s], ((j / ST) - 1) & 1, bars, p.err, 6)) break;
-                bool ok = true;
-                for (int tensor = 0; tensor < 2 && ok; ++tensor) {
-                    uint64_t *rb = tensor ? &bars->rawv[s] : &bars->rawk[s];
-                    if (!wait_or_abort(rb, (j / ST) & 1, bars, p.err, 7)) { ok = false; break; }
-                    const uint8_t *raw = smem + C::kRawOff + (s * 2 + tensor) * C::kRawTile;
-                    uint8_t *dst = smem + C::kStageOff + (s * 2 + tensor) * C::kTile;
-                    for (int ci = ct; ci < kChunks; ci += 64) {
-                        const int key = ci / (D / 16), c = ci % (D / 16);
-                        const uint4 x = *reinterpret_cast<const uint4 *>(raw + key * D + c * 16);
-                        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-                        uint32_t y[8];
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            y[2 * k] = e4m3x2_to_bf16x2((uint16_t)(w[k] & 0xFFFFu));
-                            y[2 * k + 1] = e4m3x2_to_bf16x2((uint16_t)(w[k] >> 16));
-                        }
-                        // bf16 chunks 2c and 2c+1 of this key row, 128-byte swizzle
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int cc = 2 * c + h;
-                            const uint32_t off = (cc >> 3) * C::kBlk + key * 128 + (((cc & 7) ^ (key & 7)) << 4);
-                            *reinterpret_cast<uint4 *>(dst + off) =
-                                make_uint4(y[4 * h], y[4 * h + 1], y[4 * h + 2], y[4 * h + 3]);
-                        }
+                        slot = -1;
                     }
-                    fence_proxy_async_smem();
-                    mbar_arrive(tensor ? &bars->vfull[s] : &bars->kfull[s]);
                 }
-                if (!ok) break;
-                mbar_arrive(&bars->rawempty[s]);
+                sl[buf * kBN + k] = slot;  // -1: zero-filled row (past k1 or invalid)
             }
+        };
+        load_slots(0, 0);
+        named_bar_sync(1, NP);
+        bool ok = true;
+        // bf16: tile j is signalled ST-1 iterations after it was issued, before the stage
+        // wait of the current iteration (so the MMA never waits on a tile the loaders hold)
+        const int niter = FP8 ? ntiles : ntiles + ST - 1;
+        for (int j = 0; j < niter; ++j) {
+            if constexpr (!FP8) {
+                const int jj = j - (ST - 1);
+                if (jj >= 0) {
+                    cp_async_wait<2 * ST - 3>();
+                    fence_proxy_async_smem();
+                    mbar_arrive(&bars->kfull[jj % ST]);
+                    cp_async_wait<2 * ST - 4>();
+                    fence_proxy_async_smem();
+                    mbar_arrive(&bars->vfull[jj % ST]);
+                }
+            }
+            if (j < ntiles) {
+                const int s = j % ST;
+                if (j >= ST && !wait_or_abort(&bars->kvempty[s], ((j / ST) - 1) & 1, bars, p.err, 5)) {
+                    ok = false;
+                    break;
+                }
+                const int32_t *ts = sl + (j & 1) * kBN;
+                uint8_t *kdst = smem + C::kStageOff + (s * 2) * C::kTile;
+                if constexpr (!FP8) {
+                    constexpr int CPR = D / 8;  // 16-byte chunks per row
+#pragma unroll
+                    for (int tensor = 0; tensor < 2; ++tensor) {
+                        const uint8_t *pool = tensor ? p.v_pool : p.k_pool;
+                        const uint32_t dst = smem_u32(kdst) + tensor * C::kTile;
+                        for (int ci = pt; ci < kBN * CPR; ci += NP) {
+                            const int key = ci / CPR, c = ci % CPR;
+                            const int32_t slot = ts[key];
+                            const uint32_t off = (c >> 3) * C::kBlk + key * 128 + (((c & 7) ^ (key & 7)) << 4);
+                            const int64_t src = ((int64_t)(slot < 0 ? 0 : slot) * p.hkv + g) * (D * 2) + c * 16;
+                            cp_async_16(dst + off, pool + src, slot < 0 ? 0u : 16u);
+                        }
+                        cp_async_commit();
+                    }
+                } else {
+                    constexpr int CPR = D / 16;  // 16-code chunks per row
+                    constexpr int PER = (kBN * CPR + NP - 1) / NP;
+#pragma unroll
+                    for (int tensor = 0; tensor < 2; ++tensor) {
+                        const uint8_t *pool = tensor ? p.v_pool : p.k_pool;
+                        uint8_t *dst = kdst + tensor * C::kTile;
+                        uint4 x[PER];
+#pragma unroll
+                        for (int i = 0; i < PER; ++i) {  // all loads in flight first
+                            const int ci = pt + i * NP;
+                            x[i] = make_uint4(0u, 0u, 0u, 0u);
+                            if (ci < kBN * CPR) {
+                                const int32_t slot = ts[ci / CPR];
+                                if (slot >= 0)
+                                    x[i] = __ldg(reinterpret_cast<const uint4 *>(
+                                        pool + ((int64_t)slot * p.hkv + g) * D + (ci % CPR) * 16));
+                            }
+                        }
+#pragma unroll
+                        for (int i = 0; i < PER; ++i) {
+                            const int ci = pt + i * NP;
+                            if (ci >= kBN * CPR) continue;
+                            const int key = ci / CPR, c = ci % CPR;
+                            const uint32_t w[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
+                            uint32_t y[8];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                y[2 * k] = e4m3x2_to_bf16x2((uint16_t)(w[k] & 0xFFFFu));
+                                y[2 * k + 1] = e4m3x2_to_bf16x2((uint16_t)(w[k] >> 16));
+                            }
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {  // bf16 chunks 2c and 2c+1
+                                const int cc = 2 * c + h;
+                                const uint32_t off = (cc >> 3) * C::kBlk + key * 128 + (((cc & 7) ^ (key & 7)) << 4);
+                                *reinterpret_cast<uint4 *>(dst + off) =
+                                    make_uint4(y[4 * h], y[4 * h + 1], y[4 * h + 2], y[4 * h + 3]);
+                            }
+                        }
+                        fence_proxy_async_smem();
+                        mbar_arrive(tensor ? &bars->vfull[s] : &bars->kfull[s]);
+                    }
+                }
+                if (j + 1 < ntiles) load_slots(j + 1, (j + 1) & 1);
+            } else if constexpr (!FP8) {
+                cp_async_commit();  // keep two groups per iteration for the wait counts
+                cp_async_commit();
+            }
+            named_bar_sync(1, NP);
         }
+        if (!ok) cp_async_wait<0>();  // abort: let this thread's copies land before exit
     } else {
         // ================= softmax + epilogue (warps 4-7, one query row per thread) ========
         const int r = threadIdx.x - 128;                   // row = TMEM lane
@@ -434,29 +442,27 @@ __global__ void __launch_bounds__(256, 1)
 }
 
 template <int D, int G, bool FP8>
-static int launch_extend(const ExtendParams &p, const CUtensorMap &qm, const CUtensorMap &km, const CUtensorMap &vm,
-                         int nitems, cudaStream_t s) {
+static int launch_extend(const ExtendParams &p, const CUtensorMap &qm, int nitems, cudaStream_t s) {
     constexpr int smem = ExtendCfg<D, FP8>::kSmem;
     static_assert(smem <= 232448, "shared memory budget");
     auto kern = extend_kernel<D, G, FP8>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return PKV_E_CUDA;
-    kern<<<nitems, 256, smem, s>>>(p, qm, km, vm);
+    kern<<<nitems, 256, smem, s>>>(p, qm);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_E_CUDA;
 }
 
 template <int D>
-static int dispatch_extend(int G, bool fp8, const ExtendParams &p, const CUtensorMap &qm, const CUtensorMap &km,
-                           const CUtensorMap &vm, int n, cudaStream_t s) {
+static int dispatch_extend(int G, bool fp8, const ExtendParams &p, const CUtensorMap &qm, int n, cudaStream_t s) {
     switch (G * 2 + (fp8 ? 1 : 0)) {
-        case 2: return launch_extend<D, 1, false>(p, qm, km, vm, n, s);
-        case 3: return launch_extend<D, 1, true>(p, qm, km, vm, n, s);
-        case 4: return launch_extend<D, 2, false>(p, qm, km, vm, n, s);
-        case 5: return launch_extend<D, 2, true>(p, qm, km, vm, n, s);
-        case 8: return launch_extend<D, 4, false>(p, qm, km, vm, n, s);
-        case 9: return launch_extend<D, 4, true>(p, qm, km, vm, n, s);
-        case 16: return launch_extend<D, 8, false>(p, qm, km, vm, n, s);
-        case 17: return launch_extend<D, 8, true>(p, qm, km, vm, n, s);
+        case 2: return launch_extend<D, 1, false>(p, qm, n, s);
+        case 3: return launch_extend<D, 1, true>(p, qm, n, s);
+        case 4: return launch_extend<D, 2, false>(p, qm, n, s);
+        case 5: return launch_extend<D, 2, true>(p, qm, n, s);
+        case 8: return launch_extend<D, 4, false>(p, qm, n, s);
+        case 9: return launch_extend<D, 4, true>(p, qm, n, s);
+        case 16: return launch_extend<D, 8, false>(p, qm, n, s);
+        case 17: return launch_extend<D, 8, true>(p, qm, n, s);
         default: return PKV_E_UNSUPPORTED;
     }
 }
@@ -477,10 +483,9 @@ extern "C" int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, con
     if (info->num_items == 0) return PKV_OK;
     const int D = info->head_dim, hq = info->num_q_heads, hkv = info->num_kv_heads, G = hq / hkv;
     const bool fp8 = pool->dtype == PKV_FP8_E4M3;
-    const int64_t rows = pool->num_slots * hkv;
 
-    // tensor maps: Q as [T][Hq][D] (box 64 x G x 128/G), K/V pools as [slots * Hkv][D] rows
-    CUtensorMap qm, km, vm;
+    // Q as a [T][Hq][D] tensor, box 64 x G x 128/G: one load fills 128 rows (token, head)
+    CUtensorMap qm;
     {
         cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)hq, (cuuint64_t)std::max(info->total_q, 1)};
         cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)hq * D * 2};
@@ -489,28 +494,11 @@ extern "C" int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, con
                          CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
             return PKV_E_CUDA;
     }
-    for (int t = 0; t < 2; ++t) {
-        void *base = t ? pool->v : pool->k;
-        CUtensorMap *m = t ? &vm : &km;
-        CUresult cr;
-        if (!fp8) {
-            cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-            cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-            cuuint32_t box[2] = {64, 1};
-            cr = encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box,
-                              CU_TENSOR_MAP_SWIZZLE_128B);
-        } else {
-            cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-            cuuint64_t strides[1] = {(cuuint64_t)D};
-            cuuint32_t box[2] = {(cuuint32_t)D, 1};
-            cr = encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box,
-                              CU_TENSOR_MAP_SWIZZLE_NONE);
-        }
-        if (cr != CUDA_SUCCESS) return PKV_E_CUDA;
-    }
 
     const uint8_t *plan = static_cast<const uint8_t *>(plan_dev);
     ExtendParams p;
+    p.k_pool = static_cast<const uint8_t *>(pool->k);
+    p.v_pool = static_cast<const uint8_t *>(pool->v);
     p.req_to_token = batch->req_to_token;
     p.rt_stride = batch->stride;
     p.rt_rows = batch->num_rows;
@@ -527,8 +515,8 @@ extern "C" int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, con
     p.rec_acc = reinterpret_cast<float *>(ws + kWorkspaceHeader);
     p.rec_ml = p.rec_acc + (size_t)info->num_records * hq * D;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    rc = D == 128 ? dispatch_extend<128>(G, fp8, p, qm, km, vm, info->num_items, s)
-                  : dispatch_extend<64>(G, fp8, p, qm, km, vm, info->num_items, s);
+    rc = D == 128 ? dispatch_extend<128>(G, fp8, p, qm, info->num_items, s)
+                  : dispatch_extend<64>(G, fp8, p, qm, info->num_items, s);
     if (rc) return rc;
     return launch_merge(info, plan_dev, p.rec_acc, p.rec_ml, p.o, s);
 }

@@ -36,6 +36,11 @@ PKV_DEV uint64_t global_timer_ns() {
 
 PKV_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// Named barrier `id` (1..15) among `count` threads (a multiple of 32).
+PKV_DEV void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ---------------------------------------------------------------------------------------
 // mbarrier
 PKV_DEV void mbar_init(uint64_t *bar, uint32_t count) {

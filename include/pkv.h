@@ -194,6 +194,25 @@ int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, const void *q,
  * PKV_E_DEVICE with the raw word in *raw when raw != NULL). */
 int pkv_get_device_error(void *workspace, void *stream, int32_t *raw);
 
+/* pkv_attn_decode for callers that cannot allocate device memory (no counterpart in the
+ * pages: it exists for embedding).  Some callers have no workspace to pass at call time --
+ * a serving loop that froze its device-memory budget after start-up, or a host program
+ * without a device allocator of its own.  This call runs the same kernels as
+ * pkv_attn_decode with its scratch (error word + partial-state records) in one fixed
+ * device array of PKV_NOALLOC_WORKSPACE_BYTES that every GPU loading the library holds until
+ * exit; the caller still passes every input and output.
+ *   - plans needing more than PKV_NOALLOC_WORKSPACE_BYTES of workspace: PKV_E_WORKSPACE,
+ *     nothing launched;
+ *   - the first call on a device looks up the array's address on that device (with it
+ *     current) and caches it: make that first call before any stream capture;
+ *   - every call clears the error word on `stream` first; all calls share the array, so
+ *     calls that overlap on the GPU race on it;
+ *   - allocates nothing (no cudaMalloc / cudaFree / allocating library routine).       */
+#define PKV_NOALLOC_WORKSPACE_BYTES (32u << 20)
+int pkv_attn_decode_noalloc(const pkv_pool *pool, const pkv_batch *batch, const void *q, void *o,
+                            float sm_scale, const pkv_plan_info *info, const void *plan_dev,
+                            void *stream);
+
 /* ------------------------------------------------------------------------------------ */
 /* host radix tree ([RC]): token ids -> pool slots, with LRU eviction and lock_ref       */
 /*                                                                                      */

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OUT = os.path.join(HERE, "libpkv.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 
-SOURCES = ["api.cpp", "tree.cpp", "plan.cpp", "kv_store.cu", "attn_decode.cu", "attn_extend.cu"]
+SOURCES = ["api.cpp", "tree.cpp", "plan.cpp", "kv_store.cu", "attn_decode.cu", "attn_extend.cu", "decode_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -60,85 +60,69 @@ constexpr int kBK = 64;       // keys per tile
 constexpr int kStages = 3;
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D>
-struct TileGeom {
-    static constexpr int kBlk = kBK * 128;          // bytes of one 64-element column block
-    static constexpr int kTileBytes = kBK * D * 2;  // bf16 tile
-    // byte offset of element (key, d) in a bf16 tile (d multiple of 2)
-    static PKV_DEV uint32_t off(int key, int d) {
-        const int blk = d >> 6, chunk = (d >> 3) & 7;
-        return blk * kBlk + key * 128 + ((chunk ^ (key & 7)) << 4) + (d & 7) * 2;
-    }
-    // byte offset of 16-byte chunk c (of D/8) of a key row
-    static PKV_DEV uint32_t chunk_off(int key, int c) {
-        return (c >> 3) * kBlk + key * 128 + (((c & 7) ^ (key & 7)) << 4);
-    }
+// Shared-memory geometry.  Compute tiles hold bf16 rows of 64 keys at a padded stride so that
+// the mma.sync fragment loads (8 bytes per lane, K) and ldmatrix.trans (16-byte rows, V) are
+// bank-conflict free: K rows at 2D + 32 bytes, V rows at 2D + 16 bytes.  A bf16 pool is
+// gathered straight into these tiles; an fp8 pool lands as raw rows of D codes and is
+// converted into a separate pair of compute tiles.
+template <int D, bool FP8>
+struct DLayout {
+    static constexpr int kRow = FP8 ? D : 2 * D;          // bytes of one pool row (slot, head)
+    static constexpr int kKS = 2 * D + 32;                // compute-tile row strides
+    static constexpr int kVS = 2 * D + 16;
+    static constexpr int kKTile = kBK * kKS;
+    static constexpr int kVTile = kBK * kVS;
+    static constexpr int kKRow = FP8 ? D : kKS;           // stage row strides
+    static constexpr int kVRow = FP8 ? D : kVS;
+    static constexpr int kStageK = kBK * kKRow;           // V rows start here
+    static constexpr int kStageBytes = kStageK + kBK * kVRow;
+    static constexpr int kConvOff = kStages * kStageBytes;
+    static constexpr int kConvBytes = FP8 ? kKTile + kVTile : 0;
+    static constexpr int kBarOff = kConvOff + kConvBytes;
+    static constexpr int kBytes = kBarOff + 8 * kStages;
 };
 
+// Gather of one 64-key tile: thread t < 64 copies key t's K row, thread 64 + t its V row,
+// each with one cp.async.bulk (a whole 128- or 256-byte row) completing on the stage's
+// mbarrier.  Every thread arrives once per phase (expecting its own bytes, or none when
+// the key is past the item or its slot is invalid, in which case it zeroes the row).
 template <int D, bool FP8>
-struct DecodeSmem {
-    static constexpr int kRawRow = FP8 ? D : 2 * D;           // bytes per pool row
-    static constexpr int kRawTile = kBK * kRawRow;
-    static constexpr int kStageBytes = 2 * kRawTile;            // K + V
-    static constexpr int kConvBytes = FP8 ? 2 * TileGeom<D>::kTileBytes : 0;
-    static constexpr int kBytes = kStages * kStageBytes + kConvBytes;
-};
+struct BulkLoader {
+    using L = DLayout<D, FP8>;
 
-// Gather one key tile (K and V) into `stage` with cp.async.  Thread t moves chunk c = t % CPR
-// of keys t / CPR + KPI * i.
-template <int D, bool FP8>
-struct TileLoader {
-    static constexpr int kRawRow = DecodeSmem<D, FP8>::kRawRow;
-    static constexpr int kCPR = kRawRow / 16;  // 16-byte chunks per row
-    static constexpr int kKPI = 128 / kCPR;    // keys per pass of the CTA
-    static constexpr int kNI = kBK / kKPI;     // passes per tile
-
-    static PKV_DEV void slots(const DecodeParams &p, const int32_t *rt, int kpos0, int k1, int32_t (&s)[kNI]) {
-        const int t = threadIdx.x;
-#pragma unroll
-        for (int i = 0; i < kNI; ++i) {
-            const int kp = kpos0 + t / kCPR + kKPI * i;
-            s[i] = kp < k1 ? __ldg(rt + kp) : -1;
-        }
+    static PKV_DEV int32_t slot(const int32_t *rt, int kpos0, int k1) {
+        const int kp = kpos0 + (threadIdx.x & 63);
+        return kp < k1 ? __ldg(rt + kp) : -1;
     }
 
-    static PKV_DEV void issue(const DecodeParams &p, uint8_t *stage, int g, const int32_t (&s)[kNI]) {
+    static PKV_DEV void issue(const DecodeParams &p, uint8_t *stage, uint64_t *bar, int g, int32_t slot) {
         const int t = threadIdx.x;
-        const int c = t % kCPR;
+        const bool is_v = t >= 64;
+        const int key = t & 63;
+        uint8_t *dst = stage + (is_v ? L::kStageK + key * L::kVRow : key * L::kKRow);
+        if (slot >= 0 && (int64_t)slot < p.num_slots) {
+            const uint8_t *src = (is_v ? p.v_pool : p.k_pool) + ((int64_t)slot * p.hkv + g) * L::kRow;
+            mbar_arrive_expect_tx(bar, L::kRow);
+            bulk_copy_g2s(smem_u32(dst), src, L::kRow, bar);
+        } else {
+            if (slot >= 0) set_error(p.err, DERR_SLOT_RANGE);
 #pragma unroll
-        for (int i = 0; i < kNI; ++i) {
-            const int key = t / kCPR + kKPI * i;
-            int32_t slot = s[i];
-            uint32_t bytes = 16;
-            if (slot < 0 || (int64_t)slot >= p.num_slots) {
-                if (slot >= 0) set_error(p.err, DERR_SLOT_RANGE);
-                slot = 0;
-                bytes = 0;  // zero-fill
-            }
-            const int64_t row = ((int64_t)slot * p.hkv + g) * kRawRow + c * 16;
-            uint32_t dk, dv;
-            if constexpr (FP8) {
-                dk = smem_u32(stage) + key * kRawRow + c * 16;
-                dv = dk + DecodeSmem<D, FP8>::kRawTile;
-            } else {
-                dk = smem_u32(stage) + TileGeom<D>::chunk_off(key, c);
-                dv = dk + DecodeSmem<D, FP8>::kRawTile;
-            }
-            cp_async_16(dk, p.k_pool + row, bytes);
-            cp_async_16(dv, p.v_pool + row, bytes);
+            for (int i = 0; i < L::kRow / 16; ++i) reinterpret_cast<uint4 *>(dst)[i] = make_uint4(0u, 0u, 0u, 0u);
+            fence_proxy_async_smem();  // a later bulk copy rewrites this row
+            mbar_arrive(bar);
         }
     }
 };
 
-// fp8: convert a raw stage (rows of D codes) into swizzled bf16 tiles.
+// fp8: convert a raw stage (rows of D codes) into the padded bf16 compute tiles.
 template <int D>
 PKV_DEV void convert_fp8_stage(const uint8_t *raw, uint8_t *conv) {
-    constexpr int kRawTile = kBK * D;
+    using L = DLayout<D, true>;
     constexpr int kChunks = kBK * D / 16;  // 16 codes per chunk, per tensor
     for (int i = threadIdx.x; i < 2 * kChunks; i += blockDim.x) {
         const int tensor = i / kChunks, ci = i % kChunks;
         const int key = ci / (D / 16), c = ci % (D / 16);
-        const uint4 x = *reinterpret_cast<const uint4 *>(raw + tensor * kRawTile + key * D + c * 16);
+        const uint4 x = *reinterpret_cast<const uint4 *>(raw + tensor * L::kStageK + key * D + c * 16);
         const uint32_t w[4] = {x.x, x.y, x.z, x.w};
         uint32_t y[8];
 #pragma unroll
@@ -146,9 +130,9 @@ PKV_DEV void convert_fp8_stage(const uint8_t *raw, uint8_t *conv) {
             y[2 * k] = e4m3x2_to_bf16x2((uint16_t)(w[k] & 0xFFFFu));
             y[2 * k + 1] = e4m3x2_to_bf16x2((uint16_t)(w[k] >> 16));
         }
-        uint8_t *dst = conv + tensor * TileGeom<D>::kTileBytes;
-        *reinterpret_cast<uint4 *>(dst + TileGeom<D>::chunk_off(key, 2 * c)) = make_uint4(y[0], y[1], y[2], y[3]);
-        *reinterpret_cast<uint4 *>(dst + TileGeom<D>::chunk_off(key, 2 * c + 1)) = make_uint4(y[4], y[5], y[6], y[7]);
+        uint8_t *dst = conv + (tensor ? L::kKTile + key * L::kVS : key * L::kKS) + c * 32;
+        reinterpret_cast<uint4 *>(dst)[0] = make_uint4(y[0], y[1], y[2], y[3]);
+        reinterpret_cast<uint4 *>(dst)[1] = make_uint4(y[4], y[5], y[6], y[7]);
     }
 }
 
@@ -174,7 +158,7 @@ PKV_DEV void warp_tile(WarpState<D> &st, const uint8_t *kt, const uint8_t *vt, i
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int key = (nt0 + nt) * 8 + r;
-            const uint2 b2 = *reinterpret_cast<const uint2 *>(kt + TileGeom<D>::off(key, ks * 16 + 4 * c));
+            const uint2 b2 = *reinterpret_cast<const uint2 *>(kt + key * (2 * D + 32) + (ks * 16 + 4 * c) * 2);
             const uint32_t b[2] = {b2.x, b2.y};
             mma_bf16_16816(s[nt], st.qf[ks], b);
         }
@@ -234,7 +218,7 @@ PKV_DEV void warp_tile(WarpState<D> &st, const uint8_t *kt, const uint8_t *vt, i
         for (int nd = 0; nd < D / 8; nd += 2) {
             const int dchunk = nd + (mat >> 1);
             uint32_t bv[4];
-            ldmatrix_x4_trans(bv, smem_u32(vt) + TileGeom<D>::chunk_off(key, dchunk));
+            ldmatrix_x4_trans(bv, smem_u32(vt) + key * (2 * D + 16) + dchunk * 16);
             mma_bf16_16816(st.acc[nd], a, bv);
             mma_bf16_16816(st.acc[nd + 1], a, bv + 2);
         }
@@ -244,9 +228,10 @@ PKV_DEV void warp_tile(WarpState<D> &st, const uint8_t *kt, const uint8_t *vt, i
 template <int D, int G, bool FP8>
 __global__ void __launch_bounds__(128, 2) decode_kernel(const DecodeParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    using SM = DecodeSmem<D, FP8>;
-    using LD = TileLoader<D, FP8>;
+    using L = DLayout<D, FP8>;
+    using LD = BulkLoader<D, FP8>;
     constexpr int RPW = 16 / G;  // requests per warp in a span item
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
 
     const DecodeItem it = p.items[blockIdx.x];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -295,44 +280,51 @@ __global__ void __launch_bounds__(128, 2) decode_kernel(const DecodeParams p) {
 #pragma unroll
     for (int nd = 0; nd < D / 8; ++nd) st.acc[nd][0] = st.acc[nd][1] = st.acc[nd][2] = st.acc[nd][3] = 0.f;
 
-    // ---- pipeline: prologue
-    uint8_t *conv = smem + kStages * SM::kStageBytes;
-    int32_t slots_next[LD::kNI];
-#pragma unroll
-    for (int s = 0; s < kStages - 1; ++s) {
-        if (s < ntiles) {
-            int32_t sl[LD::kNI];
-            LD::slots(p, rt, k0 + s * kBK, k1, sl);
-            LD::issue(p, smem + s * SM::kStageBytes, g, sl);
-        }
-        cp_async_commit();
+    // ---- pipeline: one mbarrier per stage, every thread arrives once per phase
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], blockDim.x);
+        fence_mbar_init();
     }
-    if (kStages - 1 < ntiles) LD::slots(p, rt, k0 + (kStages - 1) * kBK, k1, slots_next);
+    __syncthreads();
+    uint8_t *conv = smem + L::kConvOff;
+#pragma unroll
+    for (int s = 0; s < kStages - 1; ++s)
+        if (s < ntiles) LD::issue(p, smem + s * L::kStageBytes, &bars[s], g, LD::slot(rt, k0 + s * kBK, k1));
+    int32_t slot_next = (kStages - 1 < ntiles) ? LD::slot(rt, k0 + (kStages - 1) * kBK, k1) : -1;
 
-    for (int j = 0; j < ntiles; ++j) {
-        cp_async_wait<kStages - 2>();
-        __syncthreads();
-        const int jn = j + kStages - 1;
-        if (jn < ntiles) LD::issue(p, smem + (jn % kStages) * SM::kStageBytes, g, slots_next);
-        cp_async_commit();
-        if (jn + 1 < ntiles) LD::slots(p, rt, k0 + (jn + 1) * kBK, k1, slots_next);
+    int j = 0;
+    bool aborted = false;
+    for (; j < ntiles; ++j) {
+        const bool ok = mbar_wait(&bars[j % kStages], (j / kStages) & 1);
+        if (__syncthreads_or(!ok)) {  // every thread leaves together
+            if (threadIdx.x == 0) set_error(p.err, DERR_TIMEOUT | 0x20);
+            aborted = true;
+            break;
+        }
+        const int jn = j + kStages - 1;  // refill the stage consumed at j - 1
+        if (jn < ntiles) LD::issue(p, smem + (jn % kStages) * L::kStageBytes, &bars[jn % kStages], g, slot_next);
+        if (jn + 1 < ntiles) slot_next = LD::slot(rt, k0 + (jn + 1) * kBK, k1);
 
-        const uint8_t *stage = smem + (j % kStages) * SM::kStageBytes;
-        const uint8_t *kt = stage, *vt = stage + SM::kRawTile;
+        const uint8_t *stage = smem + (j % kStages) * L::kStageBytes;
+        const uint8_t *kt = stage, *vt = stage + L::kStageK;
         if constexpr (FP8) {
             convert_fp8_stage<D>(stage, conv);
             __syncthreads();
             kt = conv;
-            vt = conv + TileGeom<D>::kTileBytes;
+            vt = conv + L::kKTile;
         }
         const int kpos_tile = k0 + j * kBK;
         if (it.mode == 0)
             warp_tile<D, 8>(st, kt, vt, 0, kpos_tile, k1, p.scale_log2);
         else
             warp_tile<D, 2>(st, kt, vt, 2 * warp, kpos_tile, k1, p.scale_log2);
-        if constexpr (FP8) __syncthreads();  // conv buffer is rewritten next tile
+        if constexpr (FP8) __syncthreads();  // conv tiles are rewritten next tile
     }
-    cp_async_wait<0>();
+    if (aborted) {
+        // let the copies still in flight land (bounded) before the CTA exits
+        for (int jj = j; jj < ntiles && jj < j + kStages - 1; ++jj) mbar_wait(&bars[jj % kStages], (jj / kStages) & 1);
+        return;
+    }
 
     // ---- epilogue
 #pragma unroll
@@ -436,7 +428,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeItem *__restrict_
 
 template <int D, int G, bool FP8>
 static int launch_decode(const DecodeParams &p, int nitems, cudaStream_t s) {
-    constexpr int smem = DecodeSmem<D, FP8>::kBytes;
+    constexpr int smem = DLayout<D, FP8>::kBytes;
     static_assert(smem >= (64 + 4 * 8 * D) * 4, "tail reduction must fit in the ring");
     auto kern = decode_kernel<D, G, FP8>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)

@@ -80,9 +80,18 @@ PKV_DEV bool mbar_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // ---------------------------------------------------------------------------------------
-// cp.async (Ampere-style, 16 bytes, L2 only).  src_bytes < 16 zero-fills the rest.
+// cp.async (Ampere-style, 16 bytes, L2 only).  src_bytes < 16 zero-fills the rest.  No
+// memory clobber: completion is ordered by cp.async.wait_group (which has one), and without
+// it the compiler may hoist the shared-memory slot loads that feed the next copies.
 PKV_DEV void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes));
+}
+// One contiguous global -> shared copy (16-byte aligned addresses, size a multiple of 16),
+// completing as transaction bytes on `bar` (async proxy, no thread waits for it).
+PKV_DEV void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
 }
 PKV_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>

@@ -190,7 +190,8 @@ PKV_DEV void warp_tile(WarpState<D> &st, const uint8_t *kt, const uint8_t *vt, i
     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float pv = ex2(s[nt][e] - mu[e >> 1]);
+            // round to the bf16 weight the P.V product uses, and sum exactly that
+            const float pv = __bfloat162float(__float2bfloat16_rn(ex2(s[nt][e] - mu[e >> 1])));
             s[nt][e] = pv;
             ls[e >> 1] += pv;
         }

@@ -259,14 +259,25 @@ struct DecodeItem {      // 32 bytes
     int32_t pad;
 };
 
-struct ExtendItem {      // 32 bytes
+constexpr int kMaxSegs = 4;
+struct ExtendItem {      // 64 bytes
     int32_t g;           // KV head
-    int32_t src;         // batch index whose req_to_token row holds the keys
     int32_t tok0;        // first query token (row of q / o)
-    int32_t ntok;        // query tokens in the tile
-    int32_t qpos0;       // position of tok0; token t sees keys <= qpos0 + t
-    int32_t k0, k1;      // key positions [k0, k1)
+    int32_t ntok;        // query tokens (<= 2 * 128 / G)
+    int32_t qpos0;       // position of tok0; token t sees positions <= qpos0 + t
+    int32_t pos0;        // context position of the first key of segment 0
+    int32_t nseg;        // key segments, consecutive in context positions
     int32_t rec;         // -1: write o directly; else first partial record (one per token)
+    int32_t pad;
+    int32_t key0[kMaxSegs];   // first gathered key of each segment (row of the workspace)
+    int32_t nkeys[kMaxSegs];  // keys of each segment
+};
+
+struct GatherUnit {      // 16 bytes: copy `len` slot rows of one request row into the workspace
+    int32_t src;         // batch index whose req_to_token row holds the slots
+    int32_t pos0;        // first position
+    int32_t len;         // positions (<= 32)
+    int32_t key0;        // destination key index
 };
 
 struct MergeItem {       // 16 bytes

@@ -28,9 +28,11 @@
 namespace {
 
 struct DecodeItem { int32_t g, mode, nreq, row_off, src, k0, k1, pad; };
-struct ExtendItem { int32_t g, src, tok0, ntok, qpos0, k0, k1, rec; };
+constexpr int kMaxSegs = 4;
+struct ExtendItem { int32_t g, tok0, ntok, qpos0, pos0, nseg, rec, pad, key0[kMaxSegs], nkeys[kMaxSegs]; };
+struct GatherUnit { int32_t src, pos0, len, key0; };
 struct MergeItem { int32_t out_row, rec0, nrec, rec_stride; };
-static_assert(sizeof(DecodeItem) == 32 && sizeof(ExtendItem) == 32 && sizeof(MergeItem) == 16, "layout");
+static_assert(sizeof(DecodeItem) == 32 && sizeof(ExtendItem) == 64 && sizeof(MergeItem) == 16, "layout");
 
 constexpr size_t kHeader = 256;
 size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
@@ -230,7 +232,7 @@ extern "C" int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int
         if (qo_indptr[r + 1] - qo_indptr[r] != extend_lens[r]) return PKV_E_INVALID;
     }
     const int32_t G = num_q_heads / num_kv_heads;
-    const int32_t TQ = 128 / G;
+    const int32_t TQ2 = 2 * (128 / G);  // query tokens per item (two 128-row tiles)
     const int32_t total_q = qo_indptr[batch];
 
     std::vector<std::vector<int32_t>> spans_of;
@@ -241,59 +243,74 @@ extern "C" int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int
     for (int32_t r = 0; r < batch; ++r)
         if (tail_start[r] > seq_lens[r] - extend_lens[r]) return PKV_E_INVALID;
 
-    // parts per token of request r: one per span plus the causal remainder
-    int32_t kmax = 1;
-    for (int32_t r = 0; r < batch; ++r) kmax = std::max<int32_t>(kmax, (int32_t)spans_of[r].size() + 1);
-    const bool cascaded = kmax > 1;
+    // key runs, gathered once each into the workspace: every span, then every request's
+    // remaining positions [tail_start, seq_len).  A request whose path has more shared
+    // spans than an item holds segments gathers its whole context as one run instead.
+    struct Run { int32_t src, pos0, len, key0; };
+    std::vector<Run> runs;
+    int64_t nkeys = 0;
+    auto add_run = [&](int32_t src, int32_t pos0, int32_t len) {
+        runs.push_back({src, pos0, len, (int32_t)nkeys});
+        nkeys += len;
+        return (int32_t)runs.size() - 1;
+    };
+    std::vector<int32_t> span_run;
+    if (cascade)
+        for (int32_t s = 0; s < cascade->num_spans; ++s)
+            span_run.push_back(add_run(cascade->span_req[s], cascade->span_start[s], cascade->span_len[s]));
+    std::vector<std::vector<int32_t>> segs_of(batch);  // run indices, in context order
+    for (int32_t r = 0; r < batch; ++r) {
+        if ((int32_t)spans_of[r].size() + 1 <= kMaxSegs) {
+            for (int32_t sp : spans_of[r]) segs_of[r].push_back(span_run[sp]);
+            segs_of[r].push_back(add_run(r, tail_start[r], seq_lens[r] - tail_start[r]));
+        } else {
+            segs_of[r].push_back(add_run(r, 0, seq_lens[r]));
+        }
+    }
+    if (nkeys >= ((int64_t)1 << 31)) return PKV_E_UNSUPPORTED;
+    std::vector<GatherUnit> units;
+    for (const Run &R : runs)
+        for (int32_t c = 0; c < R.len; c += 32) units.push_back({R.src, R.pos0 + c, std::min(32, R.len - c), R.key0 + c});
 
+    // items: up to 2 x 128/G query tokens of one request x one KV head, over its segments;
+    // the last segment is cut at the last query token's position (causal)
     std::vector<ExtendItem> items;
     std::vector<MergeItem> merges;
     int32_t num_span_items = 0;
-    if (cascaded) {
-        // part index of span s for its members = position of s in their span list
-        for (int32_t s = 0; s < cascade->num_spans; ++s) {
-            const int32_t m0 = cascade->grp_indptr[s], m1 = cascade->grp_indptr[s + 1];
-            // contiguous runs of consecutive batch indices among the members
-            std::vector<int32_t> mem(cascade->grp_req + m0, cascade->grp_req + m1);
-            std::sort(mem.begin(), mem.end());
-            for (size_t i = 0; i < mem.size();) {
-                size_t j = i + 1;
-                int32_t part = (int32_t)(std::find(spans_of[mem[i]].begin(), spans_of[mem[i]].end(), s) -
-                                         spans_of[mem[i]].begin());
-                while (j < mem.size() && mem[j] == mem[j - 1] + 1 &&
-                       (int32_t)(std::find(spans_of[mem[j]].begin(), spans_of[mem[j]].end(), s) -
-                                 spans_of[mem[j]].begin()) == part)
-                    ++j;
-                const int32_t t0 = qo_indptr[mem[i]], t1 = qo_indptr[mem[j - 1] + 1];
-                for (int32_t a = t0; a < t1; a += TQ) {
-                    const int32_t n = std::min(TQ, t1 - a);
-                    for (int32_t g = 0; g < num_kv_heads; ++g) {
-                        items.push_back({g, cascade->span_req[s], a, n, 1 << 30, cascade->span_start[s],
-                                         cascade->span_start[s] + cascade->span_len[s], part * total_q + a});
-                        ++num_span_items;
-                    }
-                }
-                i = j;
+    for (int32_t r = 0; r < batch; ++r) {
+        const int32_t e = extend_lens[r], p = seq_lens[r] - e;
+        const auto &sg = segs_of[r];
+        for (int32_t i0 = 0; i0 < e; i0 += TQ2) {
+            const int32_t n = std::min(TQ2, e - i0);
+            ExtendItem it{};
+            it.tok0 = qo_indptr[r] + i0;
+            it.ntok = n;
+            it.qpos0 = p + i0;
+            it.pos0 = runs[sg[0]].pos0;
+            it.nseg = (int32_t)sg.size();
+            it.rec = -1;
+            int32_t end = p + i0 + n;  // one past the last visible position
+            for (size_t k = 0; k < sg.size(); ++k) {
+                const Run &R = runs[sg[k]];
+                it.key0[k] = R.key0;
+                it.nkeys[k] = k + 1 == sg.size() ? end - R.pos0 : R.len;
+            }
+            if (it.nseg > 1) ++num_span_items;
+            for (int32_t g = 0; g < num_kv_heads; ++g) {
+                it.g = g;
+                items.push_back(it);
             }
         }
     }
-    for (int32_t r = 0; r < batch; ++r) {
-        const int32_t e = extend_lens[r], p = seq_lens[r] - e;
-        const int32_t part = (int32_t)spans_of[r].size();
-        for (int32_t i0 = 0; i0 < e; i0 += TQ) {
-            const int32_t n = std::min(TQ, e - i0);
-            const int32_t tok0 = qo_indptr[r] + i0;
-            for (int32_t g = 0; g < num_kv_heads; ++g)
-                items.push_back({g, r, tok0, n, p + i0, tail_start[r], p + i0 + n,
-                                 cascaded ? part * total_q + tok0 : -1});
-        }
-        if (cascaded)
-            for (int32_t t = qo_indptr[r]; t < qo_indptr[r + 1]; ++t)
-                merges.push_back({t, t, part + 1, total_q});
-    }
-    std::stable_sort(items.begin(), items.end(), [](const ExtendItem &x, const ExtendItem &y) {
-        return (int64_t)(x.k1 - x.k0) * x.ntok > (int64_t)(y.k1 - y.k0) * y.ntok;
-    });
+    auto cost = [](const ExtendItem &x) {
+        int64_t k = 0;
+        for (int32_t i = 0; i < x.nseg; ++i) k += x.nkeys[i];
+        return k * x.ntok;
+    };
+    std::stable_sort(items.begin(), items.end(),
+                     [&](const ExtendItem &x, const ExtendItem &y) { return cost(x) > cost(y); });
+    const bool cascaded = false;
+    const int32_t kmax = 1;
 
     std::memset(info, 0, sizeof(*info));
     info->op = 2;
@@ -309,10 +326,15 @@ extern "C" int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int
     size_t off = 0;
     info->offsets[0] = (int64_t)off; off = align16(off + items.size() * sizeof(ExtendItem));
     info->offsets[3] = (int64_t)off; off = align16(off + merges.size() * sizeof(MergeItem));
+    info->offsets[4] = (int64_t)off; off = align16(off + units.size() * sizeof(GatherUnit));
+    info->offsets[5] = (int64_t)units.size();
+    info->offsets[6] = nkeys;
     std::vector<uint8_t> blob(std::max<size_t>(off, 16), 0);
     put(blob, (size_t)info->offsets[0], items);
     put(blob, (size_t)info->offsets[3], merges);
-    info->workspace_bytes = kHeader + (size_t)info->num_records * num_q_heads * head_dim * 4 +
-                            (size_t)info->num_records * num_q_heads * 2 * 4;
+    put(blob, (size_t)info->offsets[4], units);
+    const size_t rec_bytes = (size_t)info->num_records * num_q_heads * (head_dim + 2) * 4;
+    info->workspace_bytes = kHeader + ((rec_bytes + 255) & ~size_t(255)) +
+                            2 * (size_t)nkeys * num_kv_heads * head_dim * 2;
     return emit(blob, plan, plan_cap, info);
 }

@@ -15,8 +15,9 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 DEC = np.dtype([("g", "<i4"), ("mode", "<i4"), ("nreq", "<i4"), ("row_off", "<i4"), ("src", "<i4"),
                 ("k0", "<i4"), ("k1", "<i4"), ("pad", "<i4")])
-EXT = np.dtype([("g", "<i4"), ("src", "<i4"), ("tok0", "<i4"), ("ntok", "<i4"), ("qpos0", "<i4"),
-                ("k0", "<i4"), ("k1", "<i4"), ("rec", "<i4")])
+EXT = np.dtype([("g", "<i4"), ("tok0", "<i4"), ("ntok", "<i4"), ("qpos0", "<i4"), ("pos0", "<i4"),
+                ("nseg", "<i4"), ("rec", "<i4"), ("pad", "<i4"), ("key0", "<i4", (4,)), ("nkeys", "<i4", (4,))])
+GU = np.dtype([("src", "<i4"), ("pos0", "<i4"), ("len", "<i4"), ("key0", "<i4")])
 MRG = np.dtype([("out_row", "<i4"), ("rec0", "<i4"), ("nrec", "<i4"), ("stride", "<i4")])
 
 
@@ -112,21 +113,37 @@ def test_extend_plan_covers_causal_triangle(cascade):
     plan = pkv.plan_extend(seq, ext, qo, 32, 8, 128, casc)
     info = plan.info
     items = _sections(plan, EXT, info.num_items, info.offsets[0])
+    units = _sections(plan, GU, info.offsets[5], info.offsets[4])
+    # gathered key -> (source request, position); every gathered key is written once
+    nk = int(info.offsets[6])
+    g_src, g_pos = np.full(nk, -1), np.full(nk, -1)
+    for u in units:
+        for i in range(u["len"]):
+            assert g_src[u["key0"] + i] == -1
+            g_src[u["key0"] + i], g_pos[u["key0"] + i] = u["src"], u["pos0"] + i
+    assert np.all(g_src >= 0)
     T = int(qo[-1])
     req_of_tok = np.repeat(np.arange(4), ext)
     pos_of_tok = np.concatenate([np.arange(pre[r], seq[r]) for r in range(4)])
+    members = {0: {0, 1, 2}, 1: {0, 1, 2}, 2: {0, 1, 2}, 3: {3}}
     cover = np.zeros((T, 8, int(seq.max())), np.int32)
     for it in items:
+        assert it["rec"] == -1 and 1 <= it["nseg"] <= 4
         for t in range(it["ntok"]):
             tok = it["tok0"] + t
-            lim = min(it["k1"] - 1, it["qpos0"] + t)
-            cover[tok, it["g"], it["k0"]:lim + 1] += 1
-            if casc is None:
-                assert it["rec"] == -1
+            pos = it["pos0"]
+            for sgi in range(it["nseg"]):
+                for k in range(it["nkeys"][sgi]):
+                    if pos + k <= it["qpos0"] + t:
+                        gk = it["key0"][sgi] + k
+                        assert g_pos[gk] == pos + k
+                        assert g_src[gk] == req_of_tok[tok] or (casc is not None and g_src[gk] in members[req_of_tok[tok]])
+                        cover[tok, it["g"], pos + k] += 1
+                pos += it["nkeys"][sgi]
     for tok in range(T):
         want = np.zeros(cover.shape[2], np.int32)
         want[:pos_of_tok[tok] + 1] = 1
         assert np.array_equal(cover[tok, 0], want), tok
         assert np.all(cover[tok] == cover[tok, 0])
     if cascade:
-        assert info.num_merge == T and info.num_span_items > 0
+        assert info.num_span_items > 0 and int(info.offsets[6]) < int(seq.sum())  # the span is gathered once

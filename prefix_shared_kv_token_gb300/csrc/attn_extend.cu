@@ -28,8 +28,10 @@
 //                 memory only when the running max grows by more than 2^8 (p <= 256 stays
 //                 exact), and then without waiting: S_q of tile j completing implies PV_q of
 //                 tile j-1 completed (tcgen05 ops complete in issue order).
-//      setmaxnreg moves registers from the producer/MMA warpgroup (56) to the softmax
-//      warpgroups (224).  Every wait is bounded (2 s); on expiry the CTA records
+//      The softmax holds a row's 128 scores in registers (one tcgen05.ld pass), takes the
+//      row max as a tree, folds scale and max into one FFMA per score and skips the mask on
+//      full tiles; the kernel fits the 168-register budget of 384 threads without spilling.
+//      Every wait is bounded (2 s); on expiry the CTA records
 //      PKV_DERR_TIMEOUT, its roles stop, in-flight work drains and tensor memory is freed.
 
 #include <algorithm>
@@ -154,6 +156,29 @@ __global__ void __launch_bounds__(256) gather_kernel(const GatherParams p) {
     }
 }
 
+// p = 2^(s * scale - m) for the 128 scores of one row (masked scores are -inf and give 0),
+// packed to bf16 pairs and stored over the row's first 64 S columns in tensor memory.  ls
+// accumulates the bf16 weights, so the normalised weights the P.V product uses add up to one
+// exactly.  (Moving part of the exponentials to an FMA-pipe polynomial was measured slower:
+// the softmax is bound by instruction issue, not by the MUFU.)
+PKV_DEV void exp_pack_regs(const uint32_t *sv, uint32_t col, float sc, float neg_mu, float *ls) {
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+            const float x0 = fmaf(__uint_as_float(sv[hb * 64 + 2 * c]), sc, neg_mu);
+            const float x1 = fmaf(__uint_as_float(sv[hb * 64 + 2 * c + 1]), sc, neg_mu);
+            const float p0 = ex2(x0);
+            const float p1 = ex2(x1);
+            pk[c] = pack_bf16x2(p0, p1);
+            ls[(c & 1) * 2] += bf16_lo(pk[c]);
+            ls[(c & 1) * 2 + 1] += bf16_hi(pk[c]);
+        }
+        tmem_st32(col + hb * 32, pk);
+    }
+}
+
 // ------------------------------------------------------------------------------------------
 // dense extend over gathered runs
 
@@ -177,11 +202,14 @@ __global__ void __launch_bounds__(384, 1)
     __syncthreads();
     if (s_skip) return;
 
-    const ExtendItem it = p.items[blockIdx.x];
+    const ExtendItem *itp = p.items + blockIdx.x;  // segment arrays are read through this
+    struct {
+        int32_t g, tok0, ntok, qpos0, pos0, nseg, rec;
+    } const it = {itp->g, itp->tok0, itp->ntok, itp->qpos0, itp->pos0, itp->nseg, itp->rec};
     const int g = it.g;
     const int nseg = min(max(it.nseg, 0), kMaxSegs);
     int ntiles = 0;  // key tiles over all segments (each segment starts a new tile)
-    for (int sg = 0; sg < nseg; ++sg) ntiles += (it.nkeys[sg] + kBN - 1) / kBN;
+    for (int sg = 0; sg < nseg; ++sg) ntiles += (itp->nkeys[sg] + kBN - 1) / kBN;
     const int nq = it.ntok > TQ ? 2 : 1;  // query tiles in use
 
     if (threadIdx.x == 0) {
@@ -210,7 +238,6 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tmem = bars->tmem_base;
 
     if (warp < 4) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
         if (warp == 0 && lane == 0) {
             // ================= TMA producer =================
             prefetch_tmap(&qmap);
@@ -228,8 +255,8 @@ __global__ void __launch_bounds__(384, 1)
                 const int s = j % ST;
                 if (j >= ST && !xwait(&bars->kvempty[s], ((j / ST) - 1) & 1, bars, p.err, 5)) break;
                 const uint32_t k_s = sbase + C::kStageOff + (s * 2) * C::kKTile;
-                const int key = it.key0[sg] + lt * kBN;
-                if (++lt * kBN >= it.nkeys[sg]) {
+                const int key = itp->key0[sg] + lt * kBN;
+                if (++lt * kBN >= itp->nkeys[sg]) {
                     ++sg;
                     lt = 0;
                 }
@@ -301,7 +328,6 @@ __global__ void __launch_bounds__(384, 1)
             mbar_wait(&bars->drain, 0);
         }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
         // ================= softmax + epilogue, query tile q =================
         const int q = (warp - 4) >> 2;
         const int r = threadIdx.x - 128 - q * 128;              // row = TMEM lane
@@ -315,29 +341,41 @@ __global__ void __launch_bounds__(384, 1)
             bool ok = true;
             int sg = 0, lt = 0, segpos = it.pos0;  // segment, tile within it, its first position
             for (int j = 0; j < ntiles; ++j) {
-                if (!xwait(&bars->sfull[q], j & 1, bars, p.err, 8)) { ok = false; break; }
+                // lanes leave together: a split warp must not reach the .sync.aligned tcgen05 ops
+                if (!__all_sync(0xffffffffu, xwait(&bars->sfull[q], j & 1, bars, p.err, 8))) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
-                uint32_t sv[kBN];
-#pragma unroll
-                for (int c4 = 0; c4 < kBN / 32; ++c4) tmem_ld32(colS + c4 * 32, sv + c4 * 32);
-                tmem_ld_wait();
                 const int kl0 = lt * kBN;                       // key index of column 0 in the segment
                 const int kp0 = segpos + kl0;                   // its context position
-                const int nvalid = min(kBN, it.nkeys[sg] - kl0);
-                if (++lt * kBN >= it.nkeys[sg]) {
-                    segpos += it.nkeys[sg];
+                const int nvalid = min(kBN, itp->nkeys[sg] - kl0);
+                if (++lt * kBN >= itp->nkeys[sg]) {
+                    segpos += itp->nkeys[sg];
                     ++sg;
                     lt = 0;
                 }
                 const int ncaus = lim - kp0 + 1;                // columns <= lim
                 const int lastc = min(nvalid, ncaus);           // columns [0, lastc) visible
-                float mt = -INFINITY;
+                // warp-uniform: the tcgen05.ld/st below are .sync.aligned, so every lane of
+                // the warp must take the same path (lastc differs between rows of a causal tile)
+                const bool full = __all_sync(0xffffffffu, lastc >= kBN);
+                uint32_t sv[kBN];
 #pragma unroll
-                for (int c = 0; c < kBN; ++c) {
-                    const float x = c < lastc ? __uint_as_float(sv[c]) * p.scale_log2 : -INFINITY;
-                    sv[c] = __float_as_uint(x);
-                    mt = fmaxf(mt, x);
+                for (int c4 = 0; c4 < kBN / 32; ++c4) tmem_ld32(colS + c4 * 32, sv + c4 * 32);
+                tmem_ld_wait();
+                if (!full) {
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c) if (c >= lastc) sv[c] = __float_as_uint(-INFINITY);
                 }
+                float mx[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(sv[k]);
+#pragma unroll
+                for (int c = 8; c < kBN; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(sv[c]));
+#pragma unroll
+                for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], mx[k + 4]);
+                const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.scale_log2;
                 float alpha = 1.f;
                 bool rescale = false;
                 if (mt > m + kRescaleThreshold || m == -INFINITY) {
@@ -345,32 +383,22 @@ __global__ void __launch_bounds__(384, 1)
                     rescale = (j > 0) && (m != -INFINITY);
                     m = mt;
                 }
-                const float mu = (m == -INFINITY) ? 0.f : m;
-                float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-                for (int hb = 0; hb < 2; ++hb) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const float p0 = ex2(__uint_as_float(sv[hb * 64 + 2 * c]) - mu);
-                        const float p1 = ex2(__uint_as_float(sv[hb * 64 + 2 * c + 1]) - mu);
-                        pk[c] = pack_bf16x2(p0, p1);
-                        // the denominator sums the bf16 weights the P.V product uses, so the
-                        // normalised weights add up to one exactly
-                        ls0 += bf16_lo(pk[c]);
-                        ls1 += bf16_hi(pk[c]);
-                    }
-                    tmem_st32(colS + hb * 32, pk);
-                }
+                const float neg_mu = (m == -INFINITY) ? 0.f : -m;
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                exp_pack_regs(sv, colS, p.scale_log2, neg_mu, ls);
+                const float ls0 = ls[0] + ls[2], ls1 = ls[1] + ls[3];
                 l = l * alpha + (ls0 + ls1);
-                if (rescale) {  // PV of tile j-1 is complete: S of tile j was issued after it
+                // PV of tile j-1 is complete: S of tile j was issued after it.  The whole warp
+                // rescales when any of its rows must (.sync.aligned), the others by 1.
+                if (__any_sync(0xffffffffu, rescale)) {
+                    const float f = rescale ? alpha : 1.f;
 #pragma unroll 1
                     for (int c4 = 0; c4 < D / 32; ++c4) {
                         uint32_t ov[32];
                         tmem_ld32(colO + c4 * 32, ov);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+                        for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * f);
                         tmem_st32(colO + c4 * 32, ov);
                     }
                 }
@@ -378,7 +406,7 @@ __global__ void __launch_bounds__(384, 1)
                 tc_fence_before();
                 mbar_arrive(&bars->pfull[q]);
             }
-            if (ok && xwait(&bars->ofinal[q], 0, bars, p.err, 10)) {
+            if (__all_sync(0xffffffffu, ok && xwait(&bars->ofinal[q], 0, bars, p.err, 10))) {
                 tc_fence_after();
                 const bool valid = t < it.ntok;
                 const int tok = it.tok0 + t;

@@ -180,6 +180,15 @@ PKV_DEV void tmem_st32(uint32_t taddr, const uint32_t *r) {
         : "memory");
 }
 
+PKV_DEV void tmem_st16(uint32_t taddr, const uint32_t *r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
 // Shared-memory matrix descriptor for tcgen05.mma (128-byte swizzle, version 1).
 //   start: byte address in shared memory; lbo / sbo: leading / stride byte offsets.
 PKV_DEV uint64_t sdesc_sw128(uint32_t start, uint32_t lbo, uint32_t sbo) {

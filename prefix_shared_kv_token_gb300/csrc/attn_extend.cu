@@ -169,9 +169,7 @@ PKV_DEV void exp_pack_regs(const uint32_t *sv, uint32_t col, float sc, float neg
         for (int c = 0; c < 32; ++c) {
             const float x0 = fmaf(__uint_as_float(sv[hb * 64 + 2 * c]), sc, neg_mu);
             const float x1 = fmaf(__uint_as_float(sv[hb * 64 + 2 * c + 1]), sc, neg_mu);
-            const float p0 = ex2(x0);
-            const float p1 = ex2(x1);
-            pk[c] = pack_bf16x2(p0, p1);
+            pk[c] = ex2_bf16x2(pack_bf16x2(x0, x1));  // two weights per MUFU op, already packed
             ls[(c & 1) * 2] += bf16_lo(pk[c]);
             ls[(c & 1) * 2 + 1] += bf16_hi(pk[c]);
         }

@@ -232,6 +232,14 @@ PKV_DEV float ex2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// 2^x for two bf16 values at once (ex2.approx.ftz.bf16x2): the exponent is rounded to bf16
+// first, a relative weight error of about |x| * 2^-9 * ln 2 -- the same order as rounding the
+// weight itself to bf16, which the P.V product does anyway.  -inf gives +0.
+PKV_DEV uint32_t ex2_bf16x2(uint32_t x) {
+    uint32_t y;
+    asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
 PKV_DEV uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(lo), "f"(hi));

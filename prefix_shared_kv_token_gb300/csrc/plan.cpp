@@ -258,13 +258,28 @@ extern "C" int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int
     if (cascade)
         for (int32_t s = 0; s < cascade->num_spans; ++s)
             span_run.push_back(add_run(cascade->span_req[s], cascade->span_start[s], cascade->span_len[s]));
-    std::vector<std::vector<int32_t>> segs_of(batch);  // run indices, in context order
+    // segments per request: (run, keys used), in context order.  The last shared span is cut
+    // to a multiple of the 128-key tile and its remainder joins the request's own gathered
+    // tail, so no key tile is spent on a few leftover span keys.
+    struct Seg { int32_t run, len; };
+    std::vector<std::vector<Seg>> segs_of(batch);
     for (int32_t r = 0; r < batch; ++r) {
-        if ((int32_t)spans_of[r].size() + 1 <= kMaxSegs) {
-            for (int32_t sp : spans_of[r]) segs_of[r].push_back(span_run[sp]);
-            segs_of[r].push_back(add_run(r, tail_start[r], seq_lens[r] - tail_start[r]));
+        const int32_t ns = (int32_t)spans_of[r].size();
+        if (ns + 1 <= kMaxSegs) {
+            int32_t rem = 0;
+            for (int32_t k = 0; k < ns; ++k) {
+                const int32_t sp = spans_of[r][k];
+                int32_t len = cascade->span_len[sp];
+                if (k == ns - 1) {
+                    rem = len % 128;
+                    len -= rem;
+                }
+                if (len > 0) segs_of[r].push_back({span_run[sp], len});
+            }
+            const int32_t t0 = tail_start[r] - rem;
+            segs_of[r].push_back({add_run(r, t0, seq_lens[r] - t0), seq_lens[r] - t0});
         } else {
-            segs_of[r].push_back(add_run(r, 0, seq_lens[r]));
+            segs_of[r].push_back({add_run(r, 0, seq_lens[r]), seq_lens[r]});
         }
     }
     if (nkeys >= ((int64_t)1 << 31)) return PKV_E_UNSUPPORTED;
@@ -286,14 +301,14 @@ extern "C" int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int
             it.tok0 = qo_indptr[r] + i0;
             it.ntok = n;
             it.qpos0 = p + i0;
-            it.pos0 = runs[sg[0]].pos0;
+            it.pos0 = runs[sg[0].run].pos0;
             it.nseg = (int32_t)sg.size();
             it.rec = -1;
             int32_t end = p + i0 + n;  // one past the last visible position
             for (size_t k = 0; k < sg.size(); ++k) {
-                const Run &R = runs[sg[k]];
+                const Run &R = runs[sg[k].run];
                 it.key0[k] = R.key0;
-                it.nkeys[k] = k + 1 == sg.size() ? end - R.pos0 : R.len;
+                it.nkeys[k] = k + 1 == sg.size() ? end - R.pos0 : sg[k].len;
             }
             if (it.nseg > 1) ++num_span_items;
             for (int32_t g = 0; g < num_kv_heads; ++g) {

@@ -54,6 +54,7 @@ struct ExtendParams {
     float scale_log2;
     float v_scale;
     const ExtendItem *items;
+    int32_t num_items;
     float *rec_acc;
     float *rec_ml;
     int32_t *err;
@@ -75,7 +76,7 @@ struct XCfg {
 };
 
 struct XBars {
-    uint64_t q;
+    uint64_t q, qempty;
     uint64_t kfull[kXStages], vfull[kXStages], kvempty[kXStages];
     uint64_t sfull[2], pfull[2], ofinal[2];
     uint64_t drain;
@@ -180,6 +181,32 @@ PKV_DEV void exp_pack_regs(const uint32_t *sv, uint32_t col, float sc, float neg
 // ------------------------------------------------------------------------------------------
 // dense extend over gathered runs
 
+// Per-item fields every role reads.
+struct XItem {
+    int32_t g, tok0, ntok, qpos0, pos0, nseg, rec, ntiles, nq;
+};
+PKV_DEV XItem load_item(const ExtendItem *itp, int tq) {
+    XItem x;
+    x.g = itp->g;
+    x.tok0 = itp->tok0;
+    x.ntok = itp->ntok;
+    x.qpos0 = itp->qpos0;
+    x.pos0 = itp->pos0;
+    x.nseg = min(max(itp->nseg, 0), kMaxSegs);
+    x.rec = itp->rec;
+    x.ntiles = 0;  // key tiles over all segments (each segment starts a new tile)
+    for (int sg = 0; sg < x.nseg; ++sg) x.ntiles += (itp->nkeys[sg] + kBN - 1) / kBN;
+    x.nq = x.ntok > tq ? 2 : 1;  // query tiles in use
+    return x;
+}
+
+// Persistent: one CTA per SM walks items blockIdx.x, blockIdx.x + gridDim.x, ... (the plan
+// sorts them longest first).  Tensor memory and barriers live for the whole launch; every
+// role keeps its own running phase counters across items.  The next item's Q load waits only
+// for the last S MMAs of the current item (qempty), and its first S MMAs may run while the
+// softmax warpgroups are still in the current item's epilogue (they read O, not S); the next
+// item's first P.V, which overwrites O, needs that warpgroup's next P and so comes after its
+// epilogue.
 template <int D, int G>
 __global__ void __launch_bounds__(384, 1)
     extend_kernel(const ExtendParams p, const __grid_constant__ CUtensorMap qmap,
@@ -193,6 +220,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t sbase = smem_u32(smem);
     XBars *bars = reinterpret_cast<XBars *>(smem + C::kBarOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nitems = p.num_items;
 
     // once any CTA of this launch gave up on a wait, the rest exit instead of waiting too
     __shared__ int32_t s_skip;
@@ -200,18 +228,9 @@ __global__ void __launch_bounds__(384, 1)
     __syncthreads();
     if (s_skip) return;
 
-    const ExtendItem *itp = p.items + blockIdx.x;  // segment arrays are read through this
-    struct {
-        int32_t g, tok0, ntok, qpos0, pos0, nseg, rec;
-    } const it = {itp->g, itp->tok0, itp->ntok, itp->qpos0, itp->pos0, itp->nseg, itp->rec};
-    const int g = it.g;
-    const int nseg = min(max(it.nseg, 0), kMaxSegs);
-    int ntiles = 0;  // key tiles over all segments (each segment starts a new tile)
-    for (int sg = 0; sg < nseg; ++sg) ntiles += (itp->nkeys[sg] + kBN - 1) / kBN;
-    const int nq = it.ntok > TQ ? 2 : 1;  // query tiles in use
-
     if (threadIdx.x == 0) {
         mbar_init(&bars->q, 1);
+        mbar_init(&bars->qempty, 1);
         for (int s = 0; s < ST; ++s) {
             mbar_init(&bars->kfull[s], 1);
             mbar_init(&bars->vfull[s], 1);
@@ -235,115 +254,141 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp < 4) {
-        if (warp == 0 && lane == 0) {
+    if (warp == 0) {
+        if (lane == 0) {
             // ================= TMA producer =================
             prefetch_tmap(&qmap);
             prefetch_tmap(&kmap);
             prefetch_tmap(&vmap);
-            mbar_arrive_expect_tx(&bars->q, nq * C::kQTile);
-            for (int q = 0; q < nq; ++q)
+            int tp = 0, nql = 0;  // tiles and Q loads issued by this CTA
+            bool ok = true;
+            for (int i = blockIdx.x; ok && i < nitems; i += gridDim.x) {
+                const ExtendItem *itp = p.items + i;
+                const XItem it = load_item(itp, TQ);
+                if (nql > 0 && !xwait(&bars->qempty, (nql - 1) & 1, bars, p.err, 6)) break;
+                mbar_arrive_expect_tx(&bars->q, it.nq * C::kQTile);
+                for (int q = 0; q < it.nq; ++q)
 #pragma unroll
-                for (int b = 0; b < NBLK; ++b)
-                    tma_load_3d(sbase + C::kQOff + q * C::kQTile + b * C::kBlkQ, &qmap, b * 64, g * G,
-                                it.tok0 + q * TQ, &bars->q);
-            int issued = 0;
-            int sg = 0, lt = 0;  // segment and tile within it
-            for (int j = 0; j < ntiles; ++j) {
-                const int s = j % ST;
-                if (j >= ST && !xwait(&bars->kvempty[s], ((j / ST) - 1) & 1, bars, p.err, 5)) break;
-                const uint32_t k_s = sbase + C::kStageOff + (s * 2) * C::kKTile;
-                const int key = itp->key0[sg] + lt * kBN;
-                if (++lt * kBN >= itp->nkeys[sg]) {
-                    ++sg;
-                    lt = 0;
+                    for (int b = 0; b < NBLK; ++b)
+                        tma_load_3d(sbase + C::kQOff + q * C::kQTile + b * C::kBlkQ, &qmap, b * 64, it.g * G,
+                                    it.tok0 + q * TQ, &bars->q);
+                ++nql;
+                int sg = 0, lt = 0;  // segment and tile within it
+                for (int j = 0; j < it.ntiles; ++j, ++tp) {
+                    const int s = tp % ST;
+                    if (tp >= ST && !xwait(&bars->kvempty[s], ((tp / ST) - 1) & 1, bars, p.err, 5)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t k_s = sbase + C::kStageOff + (s * 2) * C::kKTile;
+                    const int key = itp->key0[sg] + lt * kBN;
+                    if (++lt * kBN >= itp->nkeys[sg]) {
+                        ++sg;
+                        lt = 0;
+                    }
+                    mbar_arrive_expect_tx(&bars->kfull[s], C::kKTile);
+#pragma unroll
+                    for (int b = 0; b < NBLK; ++b)
+                        tma_load_3d(k_s + b * C::kBlkK, &kmap, b * 64, it.g, key, &bars->kfull[s]);
+                    mbar_arrive_expect_tx(&bars->vfull[s], C::kKTile);
+#pragma unroll
+                    for (int b = 0; b < NBLK; ++b)
+                        tma_load_3d(k_s + C::kKTile + b * C::kBlkK, &vmap, b * 64, it.g, key, &bars->vfull[s]);
                 }
-                mbar_arrive_expect_tx(&bars->kfull[s], C::kKTile);
-#pragma unroll
-                for (int b = 0; b < NBLK; ++b) tma_load_3d(k_s + b * C::kBlkK, &kmap, b * 64, g, key, &bars->kfull[s]);
-                mbar_arrive_expect_tx(&bars->vfull[s], C::kKTile);
-#pragma unroll
-                for (int b = 0; b < NBLK; ++b)
-                    tma_load_3d(k_s + C::kKTile + b * C::kBlkK, &vmap, b * 64, g, key, &bars->vfull[s]);
-                issued = j + 1;
             }
             if (*reinterpret_cast<volatile int32_t *>(&bars->abort_flag)) {
                 // aborted: let this thread's copies still in flight land (bounded) before exit
-                mbar_wait(&bars->q, 0);
-                for (int j = issued > ST ? issued - ST : 0; j < issued; ++j) {
-                    mbar_wait(&bars->kfull[j % ST], (j / ST) & 1);
-                    mbar_wait(&bars->vfull[j % ST], (j / ST) & 1);
+                if (nql > 0) mbar_wait(&bars->q, (nql - 1) & 1);
+                for (int t = tp > ST ? tp - ST : 0; t < tp; ++t) {
+                    mbar_wait(&bars->kfull[t % ST], (t / ST) & 1);
+                    mbar_wait(&bars->vfull[t % ST], (t / ST) & 1);
                 }
             }
-        } else if (warp == 1 && lane == 0) {
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
             // ================= MMA issuer =================
             constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, 0, 0);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, 0, 1);
-            bool ok = xwait(&bars->q, 0, bars, p.err, 1);
-            auto issue_s = [&](int q, int j) -> bool {
-                const int s = j % ST;
-                if (q == 0 && !xwait(&bars->kfull[s], (j / ST) & 1, bars, p.err, 4)) return false;
-                tc_fence_after();
-                const uint32_t q_s = sbase + C::kQOff + q * C::kQTile;
-                const uint32_t k_s = sbase + C::kStageOff + (s * 2) * C::kKTile;
+            int tm = 0, ip = 0;       // tiles and items before the current one
+            int cp[2] = {0, 0};       // phases consumed on pfull[q]
+            bool ok = true;
+            for (int i = blockIdx.x; ok && i < nitems; i += gridDim.x, ++ip) {
+                const XItem it = load_item(p.items + i, TQ);
+                if (!xwait(&bars->q, ip & 1, bars, p.err, 1)) break;
+                auto issue_s = [&](int q, int j) -> bool {
+                    const int tg = tm + j, s = tg % ST;
+                    if (q == 0 && !xwait(&bars->kfull[s], (tg / ST) & 1, bars, p.err, 4)) return false;
+                    tc_fence_after();
+                    const uint32_t q_s = sbase + C::kQOff + q * C::kQTile;
+                    const uint32_t k_s = sbase + C::kStageOff + (s * 2) * C::kKTile;
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint64_t qd = sdesc_sw128(q_s + (ks >> 2) * C::kBlkQ + (ks & 3) * 32, 16, 1024);
-                    const uint64_t kd = sdesc_sw128(k_s + (ks >> 2) * C::kBlkK + (ks & 3) * 32, 16, 1024);
-                    mma_ss(tmem + C::kColS + q * kBN, qd, kd, idesc_qk, ks > 0 ? 1u : 0u);
-                }
-                tc_commit(&bars->sfull[q]);
-                return true;
-            };
-            auto issue_pv = [&](int q, int j) -> bool {
-                const int s = j % ST;
-                if (!xwait(&bars->pfull[q], j & 1, bars, p.err, 2)) return false;
-                if (q == 0 && !xwait(&bars->vfull[s], (j / ST) & 1, bars, p.err, 3)) return false;
-                tc_fence_after();
-                const uint32_t v_s = sbase + C::kStageOff + (s * 2 + 1) * C::kKTile;
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint64_t qd = sdesc_sw128(q_s + (ks >> 2) * C::kBlkQ + (ks & 3) * 32, 16, 1024);
+                        const uint64_t kd = sdesc_sw128(k_s + (ks >> 2) * C::kBlkK + (ks & 3) * 32, 16, 1024);
+                        mma_ss(tmem + C::kColS + q * kBN, qd, kd, idesc_qk, ks > 0 ? 1u : 0u);
+                    }
+                    tc_commit(&bars->sfull[q]);
+                    if (j == it.ntiles - 1 && q == it.nq - 1) tc_commit(&bars->qempty);  // Q no longer read
+                    return true;
+                };
+                auto issue_pv = [&](int q, int j) -> bool {
+                    const int tg = tm + j, s = tg % ST;
+                    if (!xwait(&bars->pfull[q], cp[q] & 1, bars, p.err, 2)) return false;
+                    ++cp[q];
+                    if (q == 0 && !xwait(&bars->vfull[s], (tg / ST) & 1, bars, p.err, 3)) return false;
+                    tc_fence_after();
+                    const uint32_t v_s = sbase + C::kStageOff + (s * 2 + 1) * C::kKTile;
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint64_t vd = sdesc_sw128(v_s + kk * 16 * 128, C::kBlkK, 1024);
-                    mma_ts(tmem + C::kColO + q * D, tmem + C::kColS + q * kBN + kk * 8, vd, idesc_pv,
-                           (j > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kBN / 16; ++kk) {
+                        const uint64_t vd = sdesc_sw128(v_s + kk * 16 * 128, C::kBlkK, 1024);
+                        mma_ts(tmem + C::kColO + q * D, tmem + C::kColS + q * kBN + kk * 8, vd, idesc_pv,
+                               (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    if (q == it.nq - 1) tc_commit(&bars->kvempty[s]);
+                    if (j == it.ntiles - 1) tc_commit(&bars->ofinal[q]);
+                    return true;
+                };
+                ok = issue_s(0, 0) && (it.nq < 2 || issue_s(1, 0));
+                for (int j = 0; ok && j < it.ntiles; ++j) {
+                    if (!issue_pv(0, j)) { ok = false; break; }
+                    if (j + 1 < it.ntiles && !issue_s(0, j + 1)) { ok = false; break; }
+                    if (it.nq > 1) {
+                        if (!issue_pv(1, j)) { ok = false; break; }
+                        if (j + 1 < it.ntiles && !issue_s(1, j + 1)) { ok = false; break; }
+                    }
                 }
-                if (q == nq - 1) tc_commit(&bars->kvempty[s]);
-                if (j == ntiles - 1) tc_commit(&bars->ofinal[q]);
-                return true;
-            };
-            if (ok) ok = issue_s(0, 0);
-            if (ok && nq > 1) ok = issue_s(1, 0);
-            for (int j = 0; ok && j < ntiles; ++j) {
-                if (!issue_pv(0, j)) { ok = false; break; }
-                if (j + 1 < ntiles && !issue_s(0, j + 1)) { ok = false; break; }
-                if (nq > 1) {
-                    if (!issue_pv(1, j)) { ok = false; break; }
-                    if (j + 1 < ntiles && !issue_s(1, j + 1)) { ok = false; break; }
-                }
+                tm += it.ntiles;
             }
             // every MMA issued so far completes before tensor memory is freed
             tc_commit(&bars->drain);
             mbar_wait(&bars->drain, 0);
         }
-    } else {
+        __syncwarp();
+    } else if (warp >= 4) {
         // ================= softmax + epilogue, query tile q =================
         const int q = (warp - 4) >> 2;
         const int r = threadIdx.x - 128 - q * 128;              // row = TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t colS = tmem + lane_base + C::kColS + q * kBN;
         const uint32_t colO = tmem + lane_base + C::kColO + q * D;
-        const int t = q * TQ + r / G;                           // token within the item
-        const int lim = it.qpos0 + t;                           // last visible position
-        if (q < nq) {
+        int cw = 0, co = 0;  // phases consumed on sfull[q] and ofinal[q]
+        for (int i = blockIdx.x; i < nitems; i += gridDim.x) {
+            const ExtendItem *itp = p.items + i;
+            const XItem it = load_item(itp, TQ);
+            if (q >= it.nq) continue;
+            const int t = q * TQ + r / G;                       // token within the item
+            const int lim = it.qpos0 + t;                       // last visible position
             float m = -INFINITY, l = 0.f;
             bool ok = true;
             int sg = 0, lt = 0, segpos = it.pos0;  // segment, tile within it, its first position
-            for (int j = 0; j < ntiles; ++j) {
+            for (int j = 0; j < it.ntiles; ++j) {
                 // lanes leave together: a split warp must not reach the .sync.aligned tcgen05 ops
-                if (!__all_sync(0xffffffffu, xwait(&bars->sfull[q], j & 1, bars, p.err, 8))) {
+                if (!__all_sync(0xffffffffu, xwait(&bars->sfull[q], cw & 1, bars, p.err, 8))) {
                     ok = false;
                     break;
                 }
+                ++cw;
                 tc_fence_after();
                 const int kl0 = lt * kBN;                       // key index of column 0 in the segment
                 const int kp0 = segpos + kl0;                   // its context position
@@ -404,42 +449,43 @@ __global__ void __launch_bounds__(384, 1)
                 tc_fence_before();
                 mbar_arrive(&bars->pfull[q]);
             }
-            if (__all_sync(0xffffffffu, ok && xwait(&bars->ofinal[q], 0, bars, p.err, 10))) {
-                tc_fence_after();
-                const bool valid = t < it.ntok;
-                const int tok = it.tok0 + t;
-                const int head = g * G + (r % G);
+            if (!__all_sync(0xffffffffu, ok && xwait(&bars->ofinal[q], co & 1, bars, p.err, 10))) break;
+            ++co;
+            tc_fence_after();
+            const bool valid = t < it.ntok;
+            const int tok = it.tok0 + t;
+            const int head = it.g * G + (r % G);
 #pragma unroll 1
-                for (int c4 = 0; c4 < D / 32; ++c4) {
-                    uint32_t ov[32];
-                    tmem_ld32(colO + c4 * 32, ov);
-                    tmem_ld_wait();
-                    if (!valid) continue;
-                    if (it.rec < 0) {
-                        const float inv = l > 0.f ? p.v_scale / l : 0.f;
-                        uint4 *dst = reinterpret_cast<uint4 *>(p.o + ((int64_t)tok * p.hq + head) * D + c4 * 32);
+            for (int c4 = 0; c4 < D / 32; ++c4) {
+                uint32_t ov[32];
+                tmem_ld32(colO + c4 * 32, ov);
+                tmem_ld_wait();
+                if (!valid) continue;
+                if (it.rec < 0) {
+                    const float inv = l > 0.f ? p.v_scale / l : 0.f;
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + ((int64_t)tok * p.hq + head) * D + c4 * 32);
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint32_t w[4];
+                    for (int v = 0; v < 4; ++v) {
+                        uint32_t w[4];
 #pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                w[k] = pack_bf16x2(__uint_as_float(ov[v * 8 + 2 * k]) * inv,
-                                                   __uint_as_float(ov[v * 8 + 2 * k + 1]) * inv);
-                            dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
-                        }
-                    } else {
-                        const int64_t rb = (int64_t)(it.rec + t) * p.hq + head;
-                        float4 *dst = reinterpret_cast<float4 *>(p.rec_acc + rb * D + c4 * 32);
-#pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            dst[v] = make_float4(__uint_as_float(ov[4 * v]) * p.v_scale,
-                                                 __uint_as_float(ov[4 * v + 1]) * p.v_scale,
-                                                 __uint_as_float(ov[4 * v + 2]) * p.v_scale,
-                                                 __uint_as_float(ov[4 * v + 3]) * p.v_scale);
-                        if (c4 == 0) *reinterpret_cast<float2 *>(p.rec_ml + rb * 2) = make_float2(m, l);
+                        for (int k = 0; k < 4; ++k)
+                            w[k] = pack_bf16x2(__uint_as_float(ov[v * 8 + 2 * k]) * inv,
+                                               __uint_as_float(ov[v * 8 + 2 * k + 1]) * inv);
+                        dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
                     }
+                } else {
+                    const int64_t rb = (int64_t)(it.rec + t) * p.hq + head;
+                    float4 *dst = reinterpret_cast<float4 *>(p.rec_acc + rb * D + c4 * 32);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        dst[v] = make_float4(__uint_as_float(ov[4 * v]) * p.v_scale,
+                                             __uint_as_float(ov[4 * v + 1]) * p.v_scale,
+                                             __uint_as_float(ov[4 * v + 2]) * p.v_scale,
+                                             __uint_as_float(ov[4 * v + 3]) * p.v_scale);
+                    if (c4 == 0) *reinterpret_cast<float2 *>(p.rec_ml + rb * 2) = make_float2(m, l);
                 }
             }
+            tc_fence_before();  // the next item's first P.V overwrites O after our next arrive
         }
     }
 
@@ -461,7 +507,7 @@ static int launch_extend(const ExtendParams &p, const CUtensorMap &qm, const CUt
     auto kern = extend_kernel<D, G>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return PKV_E_CUDA;
-    kern<<<nitems, 384, smem, s>>>(p, qm, km, vm);
+    kern<<<std::min(nitems, num_sms()), 384, smem, s>>>(p, qm, km, vm);  // persistent
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_E_CUDA;
 }
 
@@ -560,6 +606,7 @@ extern "C" int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, con
     p.scale_log2 = sm_scale * (fp8 ? pool->k_scale : 1.f) * kLog2eX;
     p.v_scale = fp8 ? pool->v_scale : 1.f;
     p.items = reinterpret_cast<const ExtendItem *>(plan + info->offsets[0]);
+    p.num_items = info->num_items;
     p.err = reinterpret_cast<int32_t *>(ws);
     p.rec_acc = rec_acc;
     p.rec_ml = rec_ml;

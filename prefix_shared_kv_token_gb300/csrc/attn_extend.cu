@@ -163,19 +163,28 @@ __global__ void __launch_bounds__(256) gather_kernel(const GatherParams p) {
 // exactly.  (Moving part of the exponentials to an FMA-pipe polynomial was measured slower:
 // the softmax is bound by instruction issue, not by the MUFU.)
 PKV_DEV void exp_pack_regs(const uint32_t *sv, uint32_t col, float sc, float neg_mu, float *ls) {
+    // packed fp32 pairs: one fma.f32x2 / add.f32x2 per two scores (issue slots are the limit)
+    const uint64_t sc2 = f2_pack(sc, sc), mu2 = f2_pack(neg_mu, neg_mu);
+    uint64_t acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
     for (int hb = 0; hb < 2; ++hb) {
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-            const float x0 = fmaf(__uint_as_float(sv[hb * 64 + 2 * c]), sc, neg_mu);
-            const float x1 = fmaf(__uint_as_float(sv[hb * 64 + 2 * c + 1]), sc, neg_mu);
+            const uint64_t x = f2_fma(f2_pack(__uint_as_float(sv[hb * 64 + 2 * c]),
+                                              __uint_as_float(sv[hb * 64 + 2 * c + 1])), sc2, mu2);
+            float x0, x1;
+            f2_unpack(x, x0, x1);
             pk[c] = ex2_bf16x2(pack_bf16x2(x0, x1));  // two weights per MUFU op, already packed
-            ls[(c & 1) * 2] += bf16_lo(pk[c]);
-            ls[(c & 1) * 2 + 1] += bf16_hi(pk[c]);
+            acc[c & 1] = f2_add(acc[c & 1], f2_pack(bf16_lo(pk[c]), bf16_hi(pk[c])));
         }
         tmem_st32(col + hb * 32, pk);
     }
+    float a0, a1, b0, b1;
+    f2_unpack(acc[0], a0, a1);
+    f2_unpack(acc[1], b0, b1);
+    ls[0] += a0 + b0;
+    ls[1] += a1 + b1;
 }
 
 // ------------------------------------------------------------------------------------------
@@ -411,14 +420,13 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                     for (int c = 0; c < kBN; ++c) if (c >= lastc) sv[c] = __float_as_uint(-INFINITY);
                 }
-                float mx[8];
+                float mx[4];  // 3-input max: two new scores per instruction, 4 chains
 #pragma unroll
-                for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(sv[k]);
+                for (int k = 0; k < 4; ++k) mx[k] = __uint_as_float(sv[k]);
 #pragma unroll
-                for (int c = 8; c < kBN; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(sv[c]));
-#pragma unroll
-                for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], mx[k + 4]);
-                const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.scale_log2;
+                for (int c = 4; c < kBN; c += 2)
+                    mx[(c >> 1) & 3] = fmax3(mx[(c >> 1) & 3], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
+                const float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]) * p.scale_log2;
                 float alpha = 1.f;
                 bool rescale = false;
                 if (mt > m + kRescaleThreshold || m == -INFINITY) {

@@ -128,32 +128,56 @@ __global__ void __launch_bounds__(256) gather_kernel(const GatherParams p) {
         if (threadIdx.x == 0) set_error(p.err, DERR_POSITION);
         return;
     }
-    const int32_t *rt = p.req_to_token + (int64_t)row * p.rt_stride + u.pos0;
+    // the unit's slots, checked once
+    __shared__ int32_t s_slot[32];
+    if (threadIdx.x < u.len) {
+        int32_t slot = __ldg(p.req_to_token + (int64_t)row * p.rt_stride + u.pos0 + threadIdx.x);
+        if (slot < 0 || (int64_t)slot >= p.num_slots) {
+            set_error(p.err, DERR_SLOT_RANGE);
+            slot = -1;  // zero row
+        }
+        s_slot[threadIdx.x] = slot;
+    }
+    __syncthreads();
     const int elems = p.hkv * D;                 // per slot row
     const int vec_out = elems / 8;               // 16-byte bf16 vectors per output row
-    const int total = 2 * u.len * vec_out;
-    for (int i = threadIdx.x; i < total; i += blockDim.x) {
-        const int tensor = i / (u.len * vec_out);
-        const int rem = i - tensor * u.len * vec_out;
-        const int key = rem / vec_out, v = rem - key * vec_out;
-        const int32_t slot = __ldg(rt + key);
-        uint4 y = make_uint4(0u, 0u, 0u, 0u);
-        if (slot >= 0 && (int64_t)slot < p.num_slots) {
+    const bool pow2 = (vec_out & (vec_out - 1)) == 0;
+    const int vshift = 31 - __clz(vec_out);
+    const int per_tensor = u.len * vec_out;
+    constexpr int kInFlight = 4;                 // independent loads per thread before stores
+    for (int base = threadIdx.x; base < 2 * per_tensor; base += kInFlight * blockDim.x) {
+        uint4 y[kInFlight];
+#pragma unroll
+        for (int k = 0; k < kInFlight; ++k) {
+            const int i = base + k * blockDim.x;
+            y[k] = make_uint4(0u, 0u, 0u, 0u);
+            if (i >= 2 * per_tensor) continue;
+            const int tensor = i >= per_tensor;
+            const int rem = i - tensor * per_tensor;
+            const int key = pow2 ? rem >> vshift : rem / vec_out, v = rem - key * vec_out;
+            const int32_t slot = s_slot[key];
+            if (slot < 0) continue;
             const uint8_t *pool = tensor ? p.v_pool : p.k_pool;
             if constexpr (!FP8) {
-                y = __ldg(reinterpret_cast<const uint4 *>(pool + (int64_t)slot * elems * 2) + v);
+                y[k] = __ldg(reinterpret_cast<const uint4 *>(pool + (int64_t)slot * elems * 2) + v);
             } else {
                 const uint2 x = __ldg(reinterpret_cast<const uint2 *>(pool + (int64_t)slot * elems) + v);
-                y.x = e4m3x2_to_bf16x2((uint16_t)(x.x & 0xFFFFu));
-                y.y = e4m3x2_to_bf16x2((uint16_t)(x.x >> 16));
-                y.z = e4m3x2_to_bf16x2((uint16_t)(x.y & 0xFFFFu));
-                y.w = e4m3x2_to_bf16x2((uint16_t)(x.y >> 16));
+                y[k].x = e4m3x2_to_bf16x2((uint16_t)(x.x & 0xFFFFu));
+                y[k].y = e4m3x2_to_bf16x2((uint16_t)(x.x >> 16));
+                y[k].z = e4m3x2_to_bf16x2((uint16_t)(x.y & 0xFFFFu));
+                y[k].w = e4m3x2_to_bf16x2((uint16_t)(x.y >> 16));
             }
-        } else {
-            set_error(p.err, DERR_SLOT_RANGE);
         }
-        uint16_t *out = tensor ? p.v_out : p.k_out;
-        reinterpret_cast<uint4 *>(out + (int64_t)(u.key0 + key) * elems)[v] = y;
+#pragma unroll
+        for (int k = 0; k < kInFlight; ++k) {
+            const int i = base + k * blockDim.x;
+            if (i >= 2 * per_tensor) continue;
+            const int tensor = i >= per_tensor;
+            const int rem = i - tensor * per_tensor;
+            const int key = pow2 ? rem >> vshift : rem / vec_out, v = rem - key * vec_out;
+            uint16_t *out = tensor ? p.v_out : p.k_out;
+            reinterpret_cast<uint4 *>(out + (int64_t)(u.key0 + key) * elems)[v] = y[k];
+        }
     }
 }
 
@@ -165,7 +189,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const GatherParams p) {
 PKV_DEV void exp_pack_regs(const uint32_t *sv, uint32_t col, float sc, float neg_mu, float *ls) {
     // packed fp32 pairs: one fma.f32x2 / add.f32x2 per two scores (issue slots are the limit)
     const uint64_t sc2 = f2_pack(sc, sc), mu2 = f2_pack(neg_mu, neg_mu);
-    uint64_t acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int hb = 0; hb < 2; ++hb) {
         uint32_t pk[32];
@@ -176,15 +200,12 @@ PKV_DEV void exp_pack_regs(const uint32_t *sv, uint32_t col, float sc, float neg
             float x0, x1;
             f2_unpack(x, x0, x1);
             pk[c] = ex2_bf16x2(pack_bf16x2(x0, x1));  // two weights per MUFU op, already packed
-            acc[c & 1] = f2_add(acc[c & 1], f2_pack(bf16_lo(pk[c]), bf16_hi(pk[c])));
+            add_bf16x2_f32(pk[c], acc[(c & 1) * 2], acc[(c & 1) * 2 + 1]);
         }
         tmem_st32(col + hb * 32, pk);
     }
-    float a0, a1, b0, b1;
-    f2_unpack(acc[0], a0, a1);
-    f2_unpack(acc[1], b0, b1);
-    ls[0] += a0 + b0;
-    ls[1] += a1 + b1;
+    ls[0] += acc[0] + acc[2];
+    ls[1] += acc[1] + acc[3];
 }
 
 // ------------------------------------------------------------------------------------------

@@ -249,6 +249,12 @@ PKV_DEV uint64_t f2_add(uint64_t a, uint64_t b) {
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
+// acc + the two bf16 halves of v, accumulated in fp32 (mixed-precision add.f32.bf16)
+PKV_DEV void add_bf16x2_f32(uint32_t v, float &acc_lo, float &acc_hi) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tadd.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;\n\t}"
+        : "+f"(acc_lo), "+f"(acc_hi)
+        : "r"(v));
+}
 PKV_DEV float fmax3(float a, float b, float c) {
     float r;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));

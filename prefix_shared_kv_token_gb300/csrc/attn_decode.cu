@@ -10,22 +10,28 @@
 // Language Models using SGLang" summary, §RadixAttention) and requests whose paths share a
 // radix-tree node share its slots ("[SGLang] RadixAttention ...", "Radix Tree 구조도").
 //
-// GB300 design
-//   * One CTA (4 warps) per work item from the host plan.  A *span* item reads a shared
-//     node's keys once for up to 64/G member requests (each warp owns 16 query rows =
-//     16/G requests x G heads, so the tensor-core M dimension is full); a *tail* item reads
-//     one request's unshared keys, and the 4 warps split every key tile.
-//   * K/V rows (256 B per head for d = 128) are gathered with 16-byte cp.async into a
-//     3-stage shared-memory ring laid out in 128-byte swizzled half-rows (chunk ^ key % 8),
-//     so fragment loads and ldmatrix.trans are bank-conflict free.  Slot indices for the
-//     tile after next are prefetched into registers while the current tile computes.
-//   * QK^T and PV use mma.sync m16n8k16 (bf16 in, fp32 accumulate); the d-order inside each
-//     k-step is permuted identically for Q and K so every lane loads 8 contiguous bytes.
-//   * Online softmax in the log2 domain; partial states (m, l, acc) of items that cover
-//     part of a request go to workspace records and a merge kernel combines them with the
-//     log-sum-exp identity.  Tail items combine their 4 warps through shared memory first.
-//   * fp8 pools: raw e4m3 tiles land in the ring and are converted exactly to bf16 tiles in
-//     shared memory; k_scale folds into the logit scale, v_scale into the output.
+// GB300 design: decode is a stream of K/V bytes, so the kernel is built to keep HBM busy.
+//   * Persistent CTAs (the plan sizes the grid to the SMs) each walk a fixed, load-balanced
+//     list of work items.  An item is (shared span chunk x up to 16/G member requests) or
+//     (one request's unshared key chunk), over a *head group* of hg <= 8 KV heads.
+//   * One producer warp streams 16-key tiles through a shared-memory ring without pausing
+//     between items: for each key it issues one cp.async.bulk of the slot's whole head-group
+//     row (hg * d elements, contiguous in the pool: 2 KB for 8 bf16 heads of 128) for K and
+//     one for V, completing as transaction bytes on the stage's mbarrier.  Rows land at a
+//     padded stride so the fragment loads below are bank-conflict free.
+//   * Consumer warp w owns KV head g0 + w: its 16 MMA rows are the item's requests x G query
+//     heads.  QK^T and PV use mma.sync m16n8k16 (bf16 in, fp32 accumulate; the d-order in
+//     each k-step is permuted identically for Q and K so every lane loads 8 contiguous
+//     bytes), with an online softmax in the log2 domain.  The next item's query fragments
+//     are fetched while the current item runs.
+//   * An item that covers part of a request writes a partial record (m, l, acc); a merge
+//     kernel combines a request's records with the log-sum-exp identity.  An item that
+//     covers a whole request writes its output directly.
+//   * fp8 pools: raw e4m3 rows land in the ring and each warp converts its own head's rows
+//     exactly to bf16 in a private tile (releasing the stage at once); k_scale folds into
+//     the logit scale, v_scale into the output.
+//   * Every wait is bounded (2 s); on expiry the CTA records PKV_DERR_TIMEOUT, its warps
+//     stop, and the producer lets its copies in flight land before it exits.
 
 #include "../../include/pkv.h"
 #include "common.cuh"
@@ -38,6 +44,7 @@ struct DecodeParams {
     const uint8_t *v_pool;
     int64_t num_slots;
     int32_t hkv, hq;
+    int32_t hg;         // KV heads per item = consumer warps
     const int32_t *req_to_token;
     int64_t rt_stride;
     int32_t rt_rows;
@@ -49,6 +56,7 @@ struct DecodeParams {
     float scale_log2;   // sm_scale * k_scale * log2(e)
     float v_scale;
     const DecodeItem *items;
+    const int32_t *cta_off;  // items of CTA b: [cta_off[b], cta_off[b + 1])
     const int32_t *row_req;
     const int32_t *row_rec;
     float *rec_acc;     // [rec][hq][D]
@@ -56,121 +64,152 @@ struct DecodeParams {
     int32_t *err;
 };
 
-constexpr int kBK = 64;       // keys per tile
-constexpr int kStages = 3;
+constexpr int kBK = 16;       // keys per tile
+constexpr int kHdr = 256;     // barriers, abort flag, per-stage tile info
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Shared-memory geometry.  Compute tiles hold bf16 rows of 64 keys at a padded stride so that
-// the mma.sync fragment loads (8 bytes per lane, K) and ldmatrix.trans (16-byte rows, V) are
-// bank-conflict free: K rows at 2D + 32 bytes, V rows at 2D + 16 bytes.  A bf16 pool is
-// gathered straight into these tiles; an fp8 pool lands as raw rows of D codes and is
-// converted into a separate pair of compute tiles.
+// Per-stage description written by the producer before it arms the stage.
+struct TileInfo {
+    int32_t kpos;   // position of the tile's first key
+    int32_t k1;     // one past the item's last key
+    int32_t item;   // plan item
+    int32_t flags;  // kFirst | kLast, or kEnd (no keys: the CTA's list is done)
+};
+constexpr int32_t kFirst = 1, kLast = 2, kEnd = 4;
+
+// Shared-memory geometry for a head group of hg KV heads.  bf16: K rows at a stride of
+// 32 (mod 128) bytes, V rows at 16 (mod 128), so the 8-byte K fragment loads and the
+// 16-byte ldmatrix.trans rows of a warp hit distinct banks.  fp8: raw rows of hg * D codes;
+// each consumer warp converts its head into a private bf16 tile with those strides.
 template <int D, bool FP8>
-struct DLayout {
-    static constexpr int kRow = FP8 ? D : 2 * D;          // bytes of one pool row (slot, head)
-    static constexpr int kKS = 2 * D + 32;                // compute-tile row strides
-    static constexpr int kVS = 2 * D + 16;
-    static constexpr int kKTile = kBK * kKS;
-    static constexpr int kVTile = kBK * kVS;
-    static constexpr int kKRow = FP8 ? D : kKS;           // stage row strides
-    static constexpr int kVRow = FP8 ? D : kVS;
-    static constexpr int kStageK = kBK * kKRow;           // V rows start here
-    static constexpr int kStageBytes = kStageK + kBK * kVRow;
-    static constexpr int kConvOff = kStages * kStageBytes;
-    static constexpr int kConvBytes = FP8 ? kKTile + kVTile : 0;
-    static constexpr int kBarOff = kConvOff + kConvBytes;
-    static constexpr int kBytes = kBarOff + 8 * kStages;
+struct DGeo {
+    static constexpr int kStages = FP8 ? 4 : 3;
+    static constexpr int kConvK = 2 * D + 32, kConvV = 2 * D + 16;
+    static constexpr int kConvBytes = kBK * (kConvK + kConvV);  // per consumer warp
+    int rowb;   // pool bytes of one key's head-group row, per tensor
+    int sk, sv; // stage row strides
+    int stage;  // bytes per stage
+    int conv;   // offset of the conversion tiles (fp8)
+    int bytes;  // dynamic shared memory
+    __host__ __device__ explicit DGeo(int hg) {
+        rowb = hg * D * (FP8 ? 1 : 2);
+        sk = FP8 ? rowb : rowb + 32;
+        sv = FP8 ? rowb : rowb + 16;
+        stage = kBK * (sk + sv);
+        conv = kHdr + kStages * stage;
+        bytes = conv + (FP8 ? hg * kConvBytes : 0);
+    }
 };
 
-// Gather of one 64-key tile: thread t < 64 copies key t's K row, thread 64 + t its V row,
-// each with one cp.async.bulk (a whole 128- or 256-byte row) completing on the stage's
-// mbarrier.  Every thread arrives once per phase (expecting its own bytes, or none when
-// the key is past the item or its slot is invalid, in which case it zeroes the row).
-template <int D, bool FP8>
-struct BulkLoader {
-    using L = DLayout<D, FP8>;
-
-    static PKV_DEV int32_t slot(const int32_t *rt, int kpos0, int k1) {
-        const int kp = kpos0 + (threadIdx.x & 63);
-        return kp < k1 ? __ldg(rt + kp) : -1;
-    }
-
-    static PKV_DEV void issue(const DecodeParams &p, uint8_t *stage, uint64_t *bar, int g, int32_t slot) {
-        const int t = threadIdx.x;
-        const bool is_v = t >= 64;
-        const int key = t & 63;
-        uint8_t *dst = stage + (is_v ? L::kStageK + key * L::kVRow : key * L::kKRow);
-        if (slot >= 0 && (int64_t)slot < p.num_slots) {
-            const uint8_t *src = (is_v ? p.v_pool : p.k_pool) + ((int64_t)slot * p.hkv + g) * L::kRow;
-            mbar_arrive_expect_tx(bar, L::kRow);
-            bulk_copy_g2s(smem_u32(dst), src, L::kRow, bar);
-        } else {
-            if (slot >= 0) set_error(p.err, DERR_SLOT_RANGE);
-#pragma unroll
-            for (int i = 0; i < L::kRow / 16; ++i) reinterpret_cast<uint4 *>(dst)[i] = make_uint4(0u, 0u, 0u, 0u);
-            fence_proxy_async_smem();  // a later bulk copy rewrites this row
-            mbar_arrive(bar);
+PKV_DEV bool dwait(uint64_t *bar, uint32_t parity, int32_t *abort_flag, int32_t *err, int where) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0) {
+            if (*reinterpret_cast<volatile int32_t *>(abort_flag)) return false;
+            if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+                set_error(err, DERR_TIMEOUT | where);
+                *reinterpret_cast<volatile int32_t *>(abort_flag) = 1;
+                return false;
+            }
         }
     }
+}
+
+// Query fragments of one item for consumer warp w: rows i = r and r + 8 of the 16-row tile
+// (request i / G of the item, query head (g0 + w) * G + i % G); rows past nreq * G are zero.
+template <int D, int G>
+struct ItemRows {
+    uint32_t qf[D / 16][4];
+    int32_t req[2];
+    int32_t g0, row_off;
 };
 
-// fp8: convert a raw stage (rows of D codes) into the padded bf16 compute tiles.
+template <int D, int G>
+PKV_DEV void load_rows(const DecodeParams &p, int item, int w, ItemRows<D, G> &x) {
+    const int lane = threadIdx.x & 31, r = lane >> 2, c = lane & 3;
+    const DecodeItem it = p.items[item];
+    x.g0 = it.g0;
+    x.row_off = it.row_off;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int i = r + 8 * h;
+        x.req[h] = i < it.nreq * G ? __ldg(p.row_req + it.row_off + i / G) : -1;
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int head = (it.g0 + w) * G + (r + 8 * h) % G;
+        const uint16_t *qrow = p.q + ((int64_t)(x.req[h] < 0 ? 0 : x.req[h]) * p.hq + head) * D + 4 * c;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            uint2 v = make_uint2(0u, 0u);
+            if (x.req[h] >= 0) v = __ldg(reinterpret_cast<const uint2 *>(qrow + ks * 16));
+            x.qf[ks][h] = v.x;       // k-slots 2c, 2c+1
+            x.qf[ks][2 + h] = v.y;   // k-slots 2c+8, 2c+9
+        }
+    }
+}
+
+// fp8: convert this warp's head (codes at column `col` of each raw row) into its bf16 tiles.
 template <int D>
-PKV_DEV void convert_fp8_stage(const uint8_t *raw, uint8_t *conv) {
-    using L = DLayout<D, true>;
+PKV_DEV void convert_head(const uint8_t *raw, int rowb, int col, uint8_t *conv) {
+    using Gm = DGeo<D, true>;
+    const int lane = threadIdx.x & 31;
     constexpr int kChunks = kBK * D / 16;  // 16 codes per chunk, per tensor
-    for (int i = threadIdx.x; i < 2 * kChunks; i += blockDim.x) {
-        const int tensor = i / kChunks, ci = i % kChunks;
-        const int key = ci / (D / 16), c = ci % (D / 16);
-        const uint4 x = *reinterpret_cast<const uint4 *>(raw + tensor * L::kStageK + key * D + c * 16);
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll 2
+    for (int i = lane; i < 2 * kChunks; i += 32) {
+        const int tensor = i >= kChunks, ci = i - tensor * kChunks;
+        const int key = ci / (D / 16), cc = ci % (D / 16);
+        const uint4 x = *reinterpret_cast<const uint4 *>(raw + (tensor * kBK + key) * rowb + col + cc * 16);
+        const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
         uint32_t y[8];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            y[2 * k] = e4m3x2_to_bf16x2((uint16_t)(w[k] & 0xFFFFu));
-            y[2 * k + 1] = e4m3x2_to_bf16x2((uint16_t)(w[k] >> 16));
+            y[2 * k] = e4m3x2_to_bf16x2((uint16_t)(wd[k] & 0xFFFFu));
+            y[2 * k + 1] = e4m3x2_to_bf16x2((uint16_t)(wd[k] >> 16));
         }
-        uint8_t *dst = conv + (tensor ? L::kKTile + key * L::kVS : key * L::kKS) + c * 32;
+        uint8_t *dst = conv + (tensor ? kBK * Gm::kConvK + key * Gm::kConvV : key * Gm::kConvK) + cc * 32;
         reinterpret_cast<uint4 *>(dst)[0] = make_uint4(y[0], y[1], y[2], y[3]);
         reinterpret_cast<uint4 *>(dst)[1] = make_uint4(y[4], y[5], y[6], y[7]);
     }
 }
 
-// Per-warp online-softmax state over 16 query rows (this lane: rows r and r + 8).
+// Online-softmax state of one warp over its 16 rows (this lane: rows r and r + 8).
 template <int D>
 struct WarpState {
     float acc[D / 8][4];
     float m[2], l[2];
-    uint32_t qf[D / 16][4];
 };
 
-// One tile's contribution for this warp: n-tiles [nt0, nt0 + NT) of the key tile.
-template <int D, int NT>
-PKV_DEV void warp_tile(WarpState<D> &st, const uint8_t *kt, const uint8_t *vt, int nt0, int kpos_tile, int k1,
-                       float scale_log2) {
+// One 16-key tile for this warp.  kt / vt point at key 0 of the warp's head; sk / sv are
+// the row strides.  Keys at positions >= k1 are masked.
+template <int D>
+PKV_DEV void tile16(WarpState<D> &st, const uint32_t (&qf)[D / 16][4], const uint8_t *kt, int sk, const uint8_t *vt,
+                    int sv, int kpos, int k1, float scale_log2) {
     const int lane = threadIdx.x & 31;
     const int r = lane >> 2, c = lane & 3;
-    float s[NT][4];
+    float s[2][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+    for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int key = (nt0 + nt) * 8 + r;
-            const uint2 b2 = *reinterpret_cast<const uint2 *>(kt + key * (2 * D + 32) + (ks * 16 + 4 * c) * 2);
+        for (int nt = 0; nt < 2; ++nt) {
+            const uint2 b2 = *reinterpret_cast<const uint2 *>(kt + (nt * 8 + r) * sk + (ks * 16 + 4 * c) * 2);
             const uint32_t b[2] = {b2.x, b2.y};
-            mma_bf16_16816(s[nt], st.qf[ks], b);
+            mma_bf16_16816(s[nt], qf[ks], b);
         }
     }
-    // mask, scale, running max
+    // scale, mask (only an item's last tile can hold keys past k1), running max
+    const bool ragged = kpos + kBK > k1;
     float mt[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
+    for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const int kp = kpos_tile + (nt0 + nt) * 8 + 2 * c + (e & 1);
-            const float x = kp < k1 ? s[nt][e] * scale_log2 : -INFINITY;
+            float x = s[nt][e] * scale_log2;
+            if (ragged && kpos + nt * 8 + 2 * c + (e & 1) >= k1) x = -INFINITY;
             s[nt][e] = x;
             mt[e >> 1] = fmaxf(mt[e >> 1], x);
         }
@@ -185,19 +224,20 @@ PKV_DEV void warp_tile(WarpState<D> &st, const uint8_t *kt, const uint8_t *vt, i
         alpha[h] = ex2(st.m[h] - mu[h]);
         st.m[h] = mn;
     }
-    float ls[2] = {0.f, 0.f};
+    // weights rounded to the bf16 the P.V product uses; the row sums add exactly those
+    uint32_t a[4];  // A fragment: row r keys 0-7, row r+8 keys 0-7, row r keys 8-15, row r+8 keys 8-15
+    float ls[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
+    for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            // round to the bf16 weight the P.V product uses, and sum exactly that
-            const float pv = __bfloat162float(__float2bfloat16_rn(ex2(s[nt][e] - mu[e >> 1])));
-            s[nt][e] = pv;
-            ls[e >> 1] += pv;
+        for (int hh = 0; hh < 2; ++hh) {
+            const uint32_t pk = pack_bf16x2(ex2(s[nt][2 * hh] - mu[hh]), ex2(s[nt][2 * hh + 1] - mu[hh]));
+            add_bf16x2_f32(pk, ls[hh][0], ls[hh][1]);
+            a[2 * nt + hh] = pk;
         }
     }
 #pragma unroll
-    for (int h = 0; h < 2; ++h) st.l[h] = st.l[h] * alpha[h] + ls[h];
+    for (int h = 0; h < 2; ++h) st.l[h] = st.l[h] * alpha[h] + (ls[h][0] + ls[h][1]);
 #pragma unroll
     for (int nd = 0; nd < D / 8; ++nd) {
         st.acc[nd][0] *= alpha[0];
@@ -205,236 +245,242 @@ PKV_DEV void warp_tile(WarpState<D> &st, const uint8_t *kt, const uint8_t *vt, i
         st.acc[nd][2] *= alpha[1];
         st.acc[nd][3] *= alpha[1];
     }
-    // O += P V
+    // O += P V: V rows are keys; ldmatrix.trans yields the k-major B fragments
     const int mat = lane >> 3, mi = lane & 7;
+    const uint32_t vrow = smem_u32(vt) + ((mat & 1) * 8 + mi) * sv;
 #pragma unroll
-    for (int kk = 0; kk < NT / 2; ++kk) {
-        uint32_t a[4];
-        a[0] = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
-        a[1] = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
-        a[2] = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-        a[3] = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-        const int key = (nt0 + 2 * kk) * 8 + (mat & 1) * 8 + mi;
-#pragma unroll
-        for (int nd = 0; nd < D / 8; nd += 2) {
-            const int dchunk = nd + (mat >> 1);
-            uint32_t bv[4];
-            ldmatrix_x4_trans(bv, smem_u32(vt) + key * (2 * D + 16) + dchunk * 16);
-            mma_bf16_16816(st.acc[nd], a, bv);
-            mma_bf16_16816(st.acc[nd + 1], a, bv + 2);
-        }
+    for (int nd = 0; nd < D / 8; nd += 2) {
+        uint32_t bv[4];
+        ldmatrix_x4_trans(bv, vrow + (nd + (mat >> 1)) * 16);
+        mma_bf16_16816(st.acc[nd], a, bv);
+        mma_bf16_16816(st.acc[nd + 1], a, bv + 2);
     }
 }
 
 template <int D, int G, bool FP8>
-__global__ void __launch_bounds__(128, 2) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(288, (D == 64 ? 2 : 1)) decode_kernel(const DecodeParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    using L = DLayout<D, FP8>;
-    using LD = BulkLoader<D, FP8>;
-    constexpr int RPW = 16 / G;  // requests per warp in a span item
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
-
-    const DecodeItem it = p.items[blockIdx.x];
+    using Gm = DGeo<D, FP8>;
+    constexpr int S = Gm::kStages;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *empty = full + 4;
+    int32_t *abort_flag = reinterpret_cast<int32_t *>(smem + 64);
+    TileInfo *tinfo = reinterpret_cast<TileInfo *>(smem + 128);
+    uint8_t *ring = smem + kHdr;
+    const Gm geo(p.hg);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = lane >> 2, c = lane & 3;
-    const int g = it.g;
+    const int c0 = __ldg(p.cta_off + blockIdx.x), c1 = __ldg(p.cta_off + blockIdx.x + 1);
 
-    // ---- key source row and range
-    const int row = __ldg(p.req_pool_indices + it.src);
-    const int k0 = it.k0;
-    const int k1 = it.k1 < 0 ? __ldg(p.seq_lens + it.src) : it.k1;
-    if (row < 0 || row >= p.rt_rows || k0 < 0 || k1 > p.rt_stride || k1 <= k0) {
-        if (threadIdx.x == 0) set_error(p.err, DERR_POSITION);
-        return;
-    }
-    const int32_t *rt = p.req_to_token + (int64_t)row * p.rt_stride;
-    const int ntiles = (k1 - k0 + kBK - 1) / kBK;
-
-    // ---- query fragments (rows r and r + 8 of this warp)
-    WarpState<D> st;
-    int req_of[2] = {-1, -1}, head_of[2] = {0, 0};
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int i = r + 8 * h;
-        if (it.mode == 0) {
-            const int ri = warp * RPW + i / G;
-            if (ri < it.nreq) req_of[h] = __ldg(p.row_req + it.row_off + ri);
-        } else if (i < G) {
-            req_of[h] = __ldg(p.row_req + it.row_off);
-        }
-        head_of[h] = g * G + (i % G);
-        st.m[h] = -INFINITY;
-        st.l[h] = 0.f;
-    }
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint2 v = make_uint2(0u, 0u);
-            if (req_of[h] >= 0)
-                v = __ldg(reinterpret_cast<const uint2 *>(p.q + ((int64_t)req_of[h] * p.hq + head_of[h]) * D + ks * 16 +
-                                                          4 * c));
-            st.qf[ks][h] = v.x;       // k-slots 2c, 2c+1
-            st.qf[ks][2 + h] = v.y;   // k-slots 2c+8, 2c+9
-        }
-    }
-#pragma unroll
-    for (int nd = 0; nd < D / 8; ++nd) st.acc[nd][0] = st.acc[nd][1] = st.acc[nd][2] = st.acc[nd][3] = 0.f;
-
-    // ---- pipeline: one mbarrier per stage, every thread arrives once per phase
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], blockDim.x);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], p.hg);
+        }
+        *abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
-    uint8_t *conv = smem + L::kConvOff;
-#pragma unroll
-    for (int s = 0; s < kStages - 1; ++s)
-        if (s < ntiles) LD::issue(p, smem + s * L::kStageBytes, &bars[s], g, LD::slot(rt, k0 + s * kBK, k1));
-    int32_t slot_next = (kStages - 1 < ntiles) ? LD::slot(rt, k0 + (kStages - 1) * kBK, k1) : -1;
 
-    int j = 0;
-    bool aborted = false;
-    for (; j < ntiles; ++j) {
-        const bool ok = mbar_wait(&bars[j % kStages], (j / kStages) & 1);
-        if (__syncthreads_or(!ok)) {  // every thread leaves together
-            if (threadIdx.x == 0) set_error(p.err, DERR_TIMEOUT | 0x20);
-            aborted = true;
-            break;
-        }
-        const int jn = j + kStages - 1;  // refill the stage consumed at j - 1
-        if (jn < ntiles) LD::issue(p, smem + (jn % kStages) * L::kStageBytes, &bars[jn % kStages], g, slot_next);
-        if (jn + 1 < ntiles) slot_next = LD::slot(rt, k0 + (jn + 1) * kBK, k1);
-
-        const uint8_t *stage = smem + (j % kStages) * L::kStageBytes;
-        const uint8_t *kt = stage, *vt = stage + L::kStageK;
-        if constexpr (FP8) {
-            convert_fp8_stage<D>(stage, conv);
-            __syncthreads();
-            kt = conv;
-            vt = conv + L::kKTile;
-        }
-        const int kpos_tile = k0 + j * kBK;
-        if (it.mode == 0)
-            warp_tile<D, 8>(st, kt, vt, 0, kpos_tile, k1, p.scale_log2);
-        else
-            warp_tile<D, 2>(st, kt, vt, 2 * warp, kpos_tile, k1, p.scale_log2);
-        if constexpr (FP8) __syncthreads();  // conv tiles are rewritten next tile
-    }
-    if (aborted) {
-        // let the copies still in flight land (bounded) before the CTA exits
-        for (int jj = j; jj < ntiles && jj < j + kStages - 1; ++jj) mbar_wait(&bars[jj % kStages], (jj / kStages) & 1);
-        return;
-    }
-
-    // ---- epilogue
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        st.l[h] += __shfl_xor_sync(0xffffffffu, st.l[h], 1);
-        st.l[h] += __shfl_xor_sync(0xffffffffu, st.l[h], 2);
-    }
-    if (it.mode == 0) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            if (req_of[h] < 0) continue;
-            const int ri = warp * RPW + (r + 8 * h) / G;
-            const int rec = __ldg(p.row_rec + it.row_off + ri);
-            const int64_t base = (int64_t)req_of[h] * p.hq + head_of[h];
-            if (rec < 0) {
-                const float inv = p.v_scale / st.l[h];
-                uint32_t *dst = reinterpret_cast<uint32_t *>(p.o + base * D);
-#pragma unroll
-                for (int nd = 0; nd < D / 8; ++nd)
-                    dst[(nd * 8 + 2 * c) / 2] = pack_bf16x2(st.acc[nd][2 * h] * inv, st.acc[nd][2 * h + 1] * inv);
-            } else {
-                const int64_t rb = (int64_t)rec * p.hq + head_of[h];
-                float2 *dst = reinterpret_cast<float2 *>(p.rec_acc + rb * D);
-#pragma unroll
-                for (int nd = 0; nd < D / 8; ++nd)
-                    dst[(nd * 8 + 2 * c) / 2] =
-                        make_float2(st.acc[nd][2 * h] * p.v_scale, st.acc[nd][2 * h + 1] * p.v_scale);
-                if (c == 0) *reinterpret_cast<float2 *>(p.rec_ml + rb * 2) = make_float2(st.m[h], st.l[h]);
+    if (warp == p.hg) {
+        // ------------------------------------------------------------------ producer warp
+        // lanes 0-15: K row of key `lane` of the tile; lanes 16-31: V row of key `lane - 16`
+        const int key = lane & 15;
+        const bool is_v = lane >= 16;
+        const uint8_t *pool = is_v ? p.v_pool : p.k_pool;
+        const int64_t head_bytes = (int64_t)D * (FP8 ? 1 : 2);
+        int t = 0;
+        bool aborted = false;
+        for (int i = c0; i < c1 && !aborted; ++i) {
+            const DecodeItem it = p.items[i];
+            const int row = __ldg(p.req_pool_indices + it.src);
+            const int k0 = it.k0;
+            const int k1 = it.k1 < 0 ? __ldg(p.seq_lens + it.src) : it.k1;
+            if (row < 0 || row >= p.rt_rows || k0 < 0 || k1 > p.rt_stride || k1 <= k0) {
+                if (lane == 0) set_error(p.err, DERR_POSITION);
+                continue;
+            }
+            const int32_t *rt = p.req_to_token + (int64_t)row * p.rt_stride;
+            const int nt = (k1 - k0 + kBK - 1) / kBK;
+            int32_t slot = k0 + key < k1 ? __ldg(rt + k0 + key) : -1;
+            for (int j = 0; j < nt; ++j, ++t) {
+                const int s = t % S;
+                if (t >= S && !__all_sync(0xffffffffu, dwait(&empty[s], ((t / S) - 1) & 1, abort_flag, p.err, 0x31))) {
+                    aborted = true;  // warp-uniform: every lane leaves together
+                    break;
+                }
+                const int kp = k0 + j * kBK + key;
+                const bool in = kp < k1;
+                const bool valid = in && slot >= 0 && (int64_t)slot < p.num_slots;
+                if (in && !valid) set_error(p.err, DERR_SLOT_RANGE);
+                uint8_t *dst = ring + s * geo.stage + (is_v ? kBK * geo.sk + key * geo.sv : key * geo.sk);
+                // no copy: a V row past the item's end, or either row of a bad slot, reads as
+                // zeros (keys past the end are masked, so their K rows are left as they are)
+                if (!valid && (in || is_v)) {
+                    for (int b = 0; b < geo.rowb; b += 16) *reinterpret_cast<uint4 *>(dst + b) = make_uint4(0u, 0u, 0u, 0u);
+                    fence_proxy_async_smem();  // a later bulk copy rewrites this row
+                }
+                const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
+                __syncwarp();
+                if (lane == 0) {
+                    TileInfo ti;
+                    ti.kpos = k0 + j * kBK;
+                    ti.k1 = k1;
+                    ti.item = i;
+                    ti.flags = (j == 0 ? kFirst : 0) | (j == nt - 1 ? kLast : 0);
+                    tinfo[s] = ti;
+                    mbar_arrive_expect_tx(&full[s], nvalid * (uint32_t)geo.rowb);
+                }
+                __syncwarp();
+                if (valid)
+                    bulk_copy_g2s(smem_u32(dst), pool + ((int64_t)slot * p.hkv + it.g0) * head_bytes, (uint32_t)geo.rowb,
+                                  &full[s]);
+                slot = (j + 1 < nt && kp + kBK < k1) ? __ldg(rt + kp + kBK) : -1;
             }
         }
+        if (!aborted) {
+            const int s = t % S;
+            if (t >= S && !__all_sync(0xffffffffu, dwait(&empty[s], ((t / S) - 1) & 1, abort_flag, p.err, 0x32))) {
+                aborted = true;
+            } else if (lane == 0) {
+                tinfo[s].flags = kEnd;
+                mbar_arrive(&full[s]);
+            }
+        }
+        if (aborted) {
+            // let the copies still in flight land (bounded) before the CTA exits
+            for (int u = t - S < 0 ? 0 : t - S; u < t; ++u) mbar_wait(&full[u % S], (u / S) & 1);
+        }
         return;
     }
-    // tail item: combine the 4 warps (rows 0..G-1 live in lanes with r < G, h = 0)
-    __syncthreads();
-    float *red_m = reinterpret_cast<float *>(smem);         // [4][8]
-    float *red_l = red_m + 32;                              // [4][8]
-    float *red_acc = red_l + 32;                            // [4][8][D]
-    if (r < G) {
-        if (c == 0) {
-            red_m[warp * 8 + r] = st.m[0];
-            red_l[warp * 8 + r] = st.l[0];
-        }
-#pragma unroll
-        for (int nd = 0; nd < D / 8; ++nd) {
-            red_acc[(warp * 8 + r) * D + nd * 8 + 2 * c] = st.acc[nd][0];
-            red_acc[(warp * 8 + r) * D + nd * 8 + 2 * c + 1] = st.acc[nd][1];
-        }
+
+    // ---------------------------------------------------------------------- consumer warps
+    const int w = warp;
+    const int r = lane >> 2, c = lane & 3;
+    WarpState<D> st;
+    ItemRows<D, G> cur, nxt;
+    int nxt_item = -1;
+    if (c0 < c1) {
+        load_rows<D, G>(p, c0, w, nxt);
+        nxt_item = c0;
     }
-    __syncthreads();
-    const int req = __ldg(p.row_req + it.row_off);
-    const int rec = __ldg(p.row_rec + it.row_off);
-    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-        const int i = idx / D, d = idx % D;
-        float M = -INFINITY;
+    int32_t rec[2] = {-1, -1};
+    uint8_t *conv = smem + geo.conv + w * Gm::kConvBytes;
+    for (int t = 0;; ++t) {
+        const int s = t % S;
+        if (!__all_sync(0xffffffffu, dwait(&full[s], (t / S) & 1, abort_flag, p.err, 0x33))) return;
+        const TileInfo ti = tinfo[s];
+        if (ti.flags & kEnd) return;
+        if (ti.flags & kFirst) {
+            if (nxt_item == ti.item)
+                cur = nxt;
+            else
+                load_rows<D, G>(p, ti.item, w, cur);
 #pragma unroll
-        for (int w = 0; w < 4; ++w) M = fmaxf(M, red_m[w * 8 + i]);
-        const float Mu = M == -INFINITY ? 0.f : M;
-        float L = 0.f, O = 0.f;
+            for (int h = 0; h < 2; ++h) {
+                rec[h] = cur.req[h] >= 0 ? __ldg(p.row_rec + cur.row_off + (r + 8 * h) / G) : -1;
+                st.m[h] = -INFINITY;
+                st.l[h] = 0.f;
+            }
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const float wt = ex2(red_m[w * 8 + i] - Mu);
-            L += red_l[w * 8 + i] * wt;
-            O += red_acc[(w * 8 + i) * D + d] * wt;
+            for (int nd = 0; nd < D / 8; ++nd) st.acc[nd][0] = st.acc[nd][1] = st.acc[nd][2] = st.acc[nd][3] = 0.f;
+            // fetch the next item's rows while this one runs
+            nxt_item = ti.item + 1 < c1 ? ti.item + 1 : -1;
+            if (nxt_item >= 0) load_rows<D, G>(p, nxt_item, w, nxt);
         }
-        const int head = g * G + i;
-        if (rec < 0) {
-            const float v = L > 0.f ? O * p.v_scale / L : 0.f;
-            p.o[((int64_t)req * p.hq + head) * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+        const uint8_t *stage = ring + s * geo.stage;
+        if constexpr (FP8) {
+            convert_head<D>(stage, geo.rowb, w * D, conv);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            tile16<D>(st, cur.qf, conv, Gm::kConvK, conv + kBK * Gm::kConvK, Gm::kConvV, ti.kpos, ti.k1, p.scale_log2);
+            __syncwarp();  // the conversion tiles are rewritten for the next tile
         } else {
-            const int64_t rb = (int64_t)rec * p.hq + head;
-            p.rec_acc[rb * D + d] = O * p.v_scale;
-            if (d == 0) *reinterpret_cast<float2 *>(p.rec_ml + rb * 2) = make_float2(M, L);
+            const int col = w * D * 2;
+            tile16<D>(st, cur.qf, stage + col, geo.sk, stage + kBK * geo.sk + col, geo.sv, ti.kpos, ti.k1,
+                      p.scale_log2);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+        if (ti.flags & kLast) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                st.l[h] += __shfl_xor_sync(0xffffffffu, st.l[h], 1);
+                st.l[h] += __shfl_xor_sync(0xffffffffu, st.l[h], 2);
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (cur.req[h] < 0) continue;
+                const int head = (cur.g0 + w) * G + (r + 8 * h) % G;
+                if (rec[h] < 0) {
+                    const float inv = p.v_scale / st.l[h];
+                    uint32_t *dst = reinterpret_cast<uint32_t *>(p.o + ((int64_t)cur.req[h] * p.hq + head) * D);
+#pragma unroll
+                    for (int nd = 0; nd < D / 8; ++nd)
+                        dst[(nd * 8 + 2 * c) / 2] = pack_bf16x2(st.acc[nd][2 * h] * inv, st.acc[nd][2 * h + 1] * inv);
+                } else {
+                    const int64_t rb = (int64_t)rec[h] * p.hq + head;
+                    float2 *dst = reinterpret_cast<float2 *>(p.rec_acc + rb * D);
+#pragma unroll
+                    for (int nd = 0; nd < D / 8; ++nd)
+                        dst[(nd * 8 + 2 * c) / 2] =
+                            make_float2(st.acc[nd][2 * h] * p.v_scale, st.acc[nd][2 * h + 1] * p.v_scale);
+                    if (c == 0) *reinterpret_cast<float2 *>(p.rec_ml + rb * 2) = make_float2(st.m[h], st.l[h]);
+                }
+            }
         }
     }
 }
 
-// Combine partial states: o = sum_k 2^(m_k - M) acc_k / sum_k 2^(m_k - M) l_k.
+// Combine partial states: o = sum_k 2^(m_k - M) acc_k / sum_k 2^(m_k - M) l_k.  One warp per
+// (row, query head); each lane owns D / 32 consecutive elements.
 template <int D>
 __global__ void __launch_bounds__(256) merge_kernel(const MergeItem *__restrict__ merges, const float *__restrict__ rec_acc,
                                                     const float *__restrict__ rec_ml, uint16_t *__restrict__ o, int hq) {
     const MergeItem mi = merges[blockIdx.x];
-    for (int idx = threadIdx.x; idx < hq * D; idx += blockDim.x) {
-        const int h = idx / D, d = idx % D;
-        float M = -INFINITY;
-        for (int k = 0; k < mi.nrec; ++k) {
-            const int64_t rb = (int64_t)(mi.rec0 + k * mi.rec_stride) * hq + h;
-            M = fmaxf(M, rec_ml[rb * 2]);
+    const int h = blockIdx.y * 8 + (threadIdx.x >> 5);
+    if (h >= hq) return;
+    const int lane = threadIdx.x & 31;
+    constexpr int V = D / 32;
+    float M = -INFINITY;
+    for (int k = 0; k < mi.nrec; ++k) M = fmaxf(M, rec_ml[((int64_t)(mi.rec0 + k * mi.rec_stride) * hq + h) * 2]);
+    const float Mu = M == -INFINITY ? 0.f : M;
+    float L = 0.f, O[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) O[v] = 0.f;
+#pragma unroll 4
+    for (int k = 0; k < mi.nrec; ++k) {
+        const int64_t rb = (int64_t)(mi.rec0 + k * mi.rec_stride) * hq + h;
+        const float2 ml = *reinterpret_cast<const float2 *>(rec_ml + rb * 2);
+        const float wt = ex2(ml.x - Mu);
+        L += ml.y * wt;
+        float a[V];
+        if constexpr (V == 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(rec_acc + rb * D + lane * 4);
+            a[0] = x.x;
+            a[1] = x.y;
+            a[2] = x.z;
+            a[3] = x.w;
+        } else {
+            const float2 x = *reinterpret_cast<const float2 *>(rec_acc + rb * D + lane * 2);
+            a[0] = x.x;
+            a[1] = x.y;
         }
-        const float Mu = M == -INFINITY ? 0.f : M;
-        float L = 0.f, O = 0.f;
-        for (int k = 0; k < mi.nrec; ++k) {
-            const int64_t rb = (int64_t)(mi.rec0 + k * mi.rec_stride) * hq + h;
-            const float2 ml = *reinterpret_cast<const float2 *>(rec_ml + rb * 2);
-            const float wt = ex2(ml.x - Mu);
-            L += ml.y * wt;
-            O += rec_acc[rb * D + d] * wt;
-        }
-        o[((int64_t)mi.out_row * hq + h) * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(L > 0.f ? O / L : 0.f));
+#pragma unroll
+        for (int v = 0; v < V; ++v) O[v] += a[v] * wt;
     }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    uint32_t *dst = reinterpret_cast<uint32_t *>(o + ((int64_t)mi.out_row * hq + h) * D + lane * V);
+#pragma unroll
+    for (int v = 0; v < V; v += 2) dst[v / 2] = pack_bf16x2(O[v] * inv, O[v + 1] * inv);
 }
 
 template <int D, int G, bool FP8>
-static int launch_decode(const DecodeParams &p, int nitems, cudaStream_t s) {
-    constexpr int smem = DLayout<D, FP8>::kBytes;
-    static_assert(smem >= (64 + 4 * 8 * D) * 4, "tail reduction must fit in the ring");
+static int launch_decode(const DecodeParams &p, int nctas, cudaStream_t s) {
+    const DGeo<D, FP8> geo(p.hg);
     auto kern = decode_kernel<D, G, FP8>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, geo.bytes) != cudaSuccess)
         return PKV_E_CUDA;
-    kern<<<nitems, 128, smem, s>>>(p);
+    kern<<<nctas, 32 * (p.hg + 1), geo.bytes, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_E_CUDA;
 }
 
@@ -457,10 +503,11 @@ int launch_merge(const pkv_plan_info *info, const void *plan_dev, const float *r
                  uint16_t *o, cudaStream_t s) {
     if (info->num_merge == 0) return PKV_OK;
     const MergeItem *m = reinterpret_cast<const MergeItem *>(static_cast<const uint8_t *>(plan_dev) + info->offsets[3]);
+    const dim3 grid((unsigned)info->num_merge, (unsigned)((info->num_q_heads + 7) / 8));
     if (info->head_dim == 128)
-        merge_kernel<128><<<info->num_merge, 256, 0, s>>>(m, rec_acc, rec_ml, o, info->num_q_heads);
+        merge_kernel<128><<<grid, 256, 0, s>>>(m, rec_acc, rec_ml, o, info->num_q_heads);
     else
-        merge_kernel<64><<<info->num_merge, 256, 0, s>>>(m, rec_acc, rec_ml, o, info->num_q_heads);
+        merge_kernel<64><<<grid, 256, 0, s>>>(m, rec_acc, rec_ml, o, info->num_q_heads);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_E_CUDA;
 }
 
@@ -488,6 +535,10 @@ extern "C" int pkv_attn_decode(const pkv_pool *pool, const pkv_batch *batch, con
     int rc = check_call(pool, batch, q, o, info, plan_dev, workspace, ws_bytes, 1);
     if (rc) return rc;
     if (info->num_items == 0) return PKV_OK;
+    const int64_t nctas = info->offsets[SEC_NUM_CTAS], hg = info->offsets[SEC_HEAD_GROUP];
+    if (nctas < 1 || nctas > info->num_items || (hg != 1 && hg != 2 && hg != 4 && hg != 8) ||
+        pool->num_kv_heads % hg)
+        return PKV_E_PLAN;
     const uint8_t *plan = static_cast<const uint8_t *>(plan_dev);
     DecodeParams p;
     p.k_pool = static_cast<const uint8_t *>(pool->k);
@@ -495,6 +546,7 @@ extern "C" int pkv_attn_decode(const pkv_pool *pool, const pkv_batch *batch, con
     p.num_slots = pool->num_slots;
     p.hkv = pool->num_kv_heads;
     p.hq = info->num_q_heads;
+    p.hg = (int32_t)hg;
     p.req_to_token = batch->req_to_token;
     p.rt_stride = batch->stride;
     p.rt_rows = batch->num_rows;
@@ -506,17 +558,18 @@ extern "C" int pkv_attn_decode(const pkv_pool *pool, const pkv_batch *batch, con
     const bool fp8 = pool->dtype == PKV_FP8_E4M3;
     p.scale_log2 = sm_scale * (fp8 ? pool->k_scale : 1.f) * kLog2e;
     p.v_scale = fp8 ? pool->v_scale : 1.f;
-    p.items = reinterpret_cast<const DecodeItem *>(plan + info->offsets[0]);
-    p.row_req = reinterpret_cast<const int32_t *>(plan + info->offsets[1]);
-    p.row_rec = reinterpret_cast<const int32_t *>(plan + info->offsets[2]);
+    p.items = reinterpret_cast<const DecodeItem *>(plan + info->offsets[SEC_ITEMS]);
+    p.cta_off = reinterpret_cast<const int32_t *>(plan + info->offsets[SEC_CTA_OFF]);
+    p.row_req = reinterpret_cast<const int32_t *>(plan + info->offsets[SEC_ROW_REQ]);
+    p.row_rec = reinterpret_cast<const int32_t *>(plan + info->offsets[SEC_ROW_REC]);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     p.err = reinterpret_cast<int32_t *>(ws);
     p.rec_acc = reinterpret_cast<float *>(ws + kWorkspaceHeader);
     p.rec_ml = p.rec_acc + (size_t)info->num_records * info->num_q_heads * info->head_dim;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int G = info->num_q_heads / info->num_kv_heads;
-    rc = info->head_dim == 128 ? dispatch_g<128>(G, fp8, p, info->num_items, s)
-                               : dispatch_g<64>(G, fp8, p, info->num_items, s);
+    rc = info->head_dim == 128 ? dispatch_g<128>(G, fp8, p, (int)nctas, s)
+                               : dispatch_g<64>(G, fp8, p, (int)nctas, s);
     if (rc) return rc;
     return launch_merge(info, plan_dev, p.rec_acc, p.rec_ml, p.o, s);
 }

@@ -295,9 +295,9 @@ PKV_DEV uint16_t f32x2_to_e4m3x2(float lo, float hi) {
 // ---------------------------------------------------------------------------------------
 // plan blob layouts (host planner <-> kernels)
 struct DecodeItem {      // 32 bytes
-    int32_t g;           // KV head
-    int32_t mode;        // 0: shared span, rows = several requests; 1: one request, warps split keys
-    int32_t nreq;        // requests (rows / G) in this item
+    int32_t g0;          // first KV head of the item's head group (heads g0 .. g0 + hg - 1)
+    int32_t mode;        // 0: shared span (several member requests), 1: one request's tail
+    int32_t nreq;        // requests in this item (<= 16 / G: one 16-row MMA tile per head)
     int32_t row_off;     // into item_req[] / item_rec[]
     int32_t src;         // batch index whose req_to_token row holds the keys
     int32_t k0;          // first key position
@@ -335,6 +335,9 @@ struct MergeItem {       // 16 bytes
 
 // plan_info.offsets[] slots
 enum PlanSection { SEC_ITEMS = 0, SEC_ROW_REQ = 1, SEC_ROW_REC = 2, SEC_MERGE = 3 };
+// decode: offsets[4] = per-CTA item ranges (int32 [n + 1]), offsets[5] = n CTAs,
+// offsets[6] = KV heads per item (hg)
+enum DecodePlanSlot { SEC_CTA_OFF = 4, SEC_NUM_CTAS = 5, SEC_HEAD_GROUP = 6 };
 
 constexpr size_t kWorkspaceHeader = 256;  // error word + padding
 

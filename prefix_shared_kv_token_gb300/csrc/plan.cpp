@@ -3,13 +3,14 @@
 // the merges that combine those records.
 //
 // Decode ([SG] summary §RadixAttention: each running request decodes over its whole cached
-// context): work = (shared span or unshared tail) x KV head x key chunk.  A span item reads
-// the span's slots once for all member requests of the span (a radix-tree node on several
-// paths: "Radix Tree 구조도" -- the two branches under [1,2,3] share its KV); a tail item reads
-// one request's remaining positions.  Every (request, span chunk) and (request, tail chunk)
-// owns one partial record (m, l, acc) unless the request has a single item, which then
-// writes its output directly.  Items are ordered longest first so the hardware block
-// scheduler packs them like LPT.
+// context): work = (shared span chunk x up to 16/G member requests, or one request's
+// unshared key chunk) x head group of <= 8 KV heads.  A span item reads the span's slots
+// once for a group of its member requests (a radix-tree node on several paths: "Radix Tree
+// 구조도" -- the two branches under [1,2,3] share its KV); a tail item reads one request's
+// remaining positions.  Every (request, span chunk) and (request, tail chunk) owns one
+// partial record (m, l, acc) unless the request has a single item, which then writes its
+// output directly.  The kernel's CTAs are persistent: the planner deals the items to them
+// longest first onto the least loaded CTA (LPT), and each CTA walks its own list.
 //
 // Extend (only the uncached remainder is prefilled, [SG] §RadixAttention): work = tile of
 // up to 128/G query tokens x KV head over keys [k0, k1), causal within the request.  With a
@@ -21,13 +22,15 @@
 #include <cstdint>
 #include <cstring>
 #include <numeric>
+#include <queue>
+#include <utility>
 #include <vector>
 
 #include "../../include/pkv.h"
 
 namespace {
 
-struct DecodeItem { int32_t g, mode, nreq, row_off, src, k0, k1, pad; };
+struct DecodeItem { int32_t g0, mode, nreq, row_off, src, k0, k1, pad; };
 constexpr int kMaxSegs = 4;
 struct ExtendItem { int32_t g, tok0, ntok, qpos0, pos0, nseg, rec, pad, key0[kMaxSegs], nkeys[kMaxSegs]; };
 struct GatherUnit { int32_t src, pos0, len, key0; };
@@ -97,6 +100,18 @@ int emit(const std::vector<uint8_t> &blob, void *plan, size_t plan_cap, pkv_plan
 
 }  // namespace
 
+// Persistent decode CTAs per SM for a head group of hg KV heads: the kernel runs hg + 1
+// warps with a 3-stage ring of 16-key tiles (bf16 layout, the larger one).  Registers are
+// allocated per warp from each of the 4 sub-partitions' 16,384; the kernel is compiled for
+// 168 registers a thread at d = 128 and 96 at d = 64.
+int decode_ctas_per_sm(int32_t hg, int32_t d) {
+    const int64_t warps = hg + 1;
+    const int64_t smem = 256 + 3 * 16 * (4 * (int64_t)hg * d + 48) + 1024;
+    const int64_t warps_per_sm = 4 * (16384 / (32 * (d == 128 ? 168 : 96)));
+    int64_t n = std::min<int64_t>({232448 / smem, warps_per_sm / warps, 64 / warps, 8});
+    return (int)std::max<int64_t>(n, 1);
+}
+
 extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t num_q_heads,
                                int32_t num_kv_heads, int32_t head_dim, const pkv_cascade *cascade,
                                const pkv_plan_opts *opts, void *plan, size_t plan_cap,
@@ -108,9 +123,13 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
         if (seq_lens[r] < 1) return PKV_E_INVALID;
     const int32_t G = num_q_heads / num_kv_heads;
     const int32_t chunk = (opts && opts->chunk_keys > 0) ? opts->chunk_keys : 256;
-    const int32_t span_chunk = (opts && opts->span_chunk > 0) ? opts->span_chunk : 4096;
+    const int32_t span_chunk = (opts && opts->span_chunk > 0) ? opts->span_chunk : 1024;
+    const int32_t num_sms = (opts && opts->num_sms > 0) ? opts->num_sms : 152;
     const bool dyn_tail = opts && opts->dynamic_tail;
-    const int32_t rows_per_cta = 4 * (16 / G);  // requests per span item: 4 warps x 16 rows
+    const int32_t R = 16 / G;  // requests per span item: one 16-row MMA tile per KV head
+    // head group: KV heads read together per key (one contiguous pool row), <= 8
+    int32_t hg = 8;
+    while (num_kv_heads % hg) hg /= 2;
 
     std::vector<std::vector<int32_t>> spans_of;
     std::vector<int32_t> tail_start;
@@ -139,9 +158,11 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
     std::vector<int32_t> next_rec(batch, 0);
 
     std::vector<DecodeItem> items;
+    std::vector<int64_t> cost;  // load-balancing weight: keys, span re-reads (L2 hits) at 3/5
     std::vector<int32_t> row_req, row_rec;
     std::vector<MergeItem> merges;
     int32_t num_span_items = 0;
+    constexpr int64_t kItemOverhead = 40;  // in fifths of a key
 
     if (cascade) {
         for (int32_t s = 0; s < cascade->num_spans; ++s) {
@@ -149,8 +170,8 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
             const int32_t m0 = cascade->grp_indptr[s], m1 = cascade->grp_indptr[s + 1];
             for (int32_t c0 = 0; c0 < len; c0 += span_chunk) {
                 const int32_t c1 = std::min(len, c0 + span_chunk);
-                for (int32_t a = m0; a < m1; a += rows_per_cta) {
-                    const int32_t b = std::min(m1, a + rows_per_cta);
+                for (int32_t a = m0; a < m1; a += R) {
+                    const int32_t b = std::min(m1, a + R);
                     const int32_t off = (int32_t)row_req.size();
                     for (int32_t i = a; i < b; ++i) {
                         const int32_t r = cascade->grp_req[i];
@@ -158,8 +179,9 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
                         row_rec.push_back(rec_base[r] < 0 ? -1 : rec_base[r] + next_rec[r]);
                         next_rec[r] += 1;
                     }
-                    for (int32_t g = 0; g < num_kv_heads; ++g) {
-                        items.push_back({g, 0, b - a, off, cascade->span_req[s], st + c0, st + c1, 0});
+                    for (int32_t g0 = 0; g0 < num_kv_heads; g0 += hg) {
+                        items.push_back({g0, 0, b - a, off, cascade->span_req[s], st + c0, st + c1, 0});
+                        cost.push_back((int64_t)(c1 - c0) * (a == m0 ? 5 : 3) + kItemOverhead);
                         ++num_span_items;
                     }
                 }
@@ -175,22 +197,44 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
             row_rec.push_back(rec_base[r] < 0 ? -1 : rec_base[r] + next_rec[r]);
             next_rec[r] += 1;
             const bool last = k1 == L;
-            for (int32_t g = 0; g < num_kv_heads; ++g)
-                items.push_back({g, 1, 1, off, r, k0, (last && dyn_tail) ? -1 : k1, 0});
+            for (int32_t g0 = 0; g0 < num_kv_heads; g0 += hg) {
+                items.push_back({g0, 1, 1, off, r, k0, (last && dyn_tail) ? -1 : k1, 0});
+                cost.push_back((int64_t)(k1 - k0) * 5 + kItemOverhead);
+            }
         }
     }
     for (int32_t r = 0; r < batch; ++r)
         if (rec_base[r] >= 0) merges.push_back({r, rec_base[r], nrec[r], 1});
 
-    // longest first; span items weigh more (several requests' rows per key)
-    std::stable_sort(items.begin(), items.end(), [&](const DecodeItem &x, const DecodeItem &y) {
-        auto cost = [&](const DecodeItem &it) {
-            int64_t k1 = it.k1 < 0 ? seq_lens[it.src] : it.k1;
-            int64_t keys = k1 - it.k0;
-            return it.mode == 0 ? keys * 4 + keys * it.nreq / 4 : keys * 4;
-        };
-        return cost(x) > cost(y);
-    });
+    // persistent CTAs: longest-processing-time-first onto the least loaded CTA; each CTA
+    // then runs its items in that (descending) order
+    const int32_t n_items = (int32_t)items.size();
+    const int32_t nctas = std::max<int32_t>(
+        1, std::min<int64_t>(n_items, (int64_t)num_sms * decode_ctas_per_sm(hg, head_dim)));
+    std::vector<int32_t> order(n_items);
+    std::iota(order.begin(), order.end(), 0);
+    std::stable_sort(order.begin(), order.end(), [&](int32_t x, int32_t y) { return cost[x] > cost[y]; });
+    std::vector<std::vector<int32_t>> per_cta(nctas);
+    {
+        using Slot = std::pair<int64_t, int32_t>;  // (load, cta): lowest load, then lowest index
+        std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+        for (int32_t b = 0; b < nctas; ++b) heap.push({0, b});
+        for (int32_t x : order) {
+            Slot sl = heap.top();
+            heap.pop();
+            per_cta[sl.second].push_back(x);
+            sl.first += cost[x];
+            heap.push(sl);
+        }
+    }
+    std::vector<DecodeItem> placed;
+    std::vector<int32_t> cta_off(1, 0);
+    placed.reserve(items.size());
+    for (int32_t b = 0; b < nctas; ++b) {
+        for (int32_t x : per_cta[b]) placed.push_back(items[x]);
+        cta_off.push_back((int32_t)placed.size());
+    }
+    if (n_items == 0) cta_off.push_back(0);
 
     std::memset(info, 0, sizeof(*info));
     info->op = 1;
@@ -198,21 +242,25 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
     info->num_q_heads = num_q_heads;
     info->num_kv_heads = num_kv_heads;
     info->head_dim = head_dim;
-    info->num_items = (int32_t)items.size();
+    info->num_items = n_items;
     info->num_span_items = num_span_items;
     info->num_records = num_records;
     info->num_merge = (int32_t)merges.size();
     info->total_q = batch;
     size_t off = 0;
-    info->offsets[0] = (int64_t)off; off = align16(off + items.size() * sizeof(DecodeItem));
+    info->offsets[0] = (int64_t)off; off = align16(off + placed.size() * sizeof(DecodeItem));
     info->offsets[1] = (int64_t)off; off = align16(off + row_req.size() * sizeof(int32_t));
     info->offsets[2] = (int64_t)off; off = align16(off + row_rec.size() * sizeof(int32_t));
     info->offsets[3] = (int64_t)off; off = align16(off + merges.size() * sizeof(MergeItem));
+    info->offsets[4] = (int64_t)off; off = align16(off + cta_off.size() * sizeof(int32_t));
+    info->offsets[5] = nctas;
+    info->offsets[6] = hg;
     std::vector<uint8_t> blob(std::max<size_t>(off, 16), 0);
-    put(blob, (size_t)info->offsets[0], items);
+    put(blob, (size_t)info->offsets[0], placed);
     put(blob, (size_t)info->offsets[1], row_req);
     put(blob, (size_t)info->offsets[2], row_rec);
     put(blob, (size_t)info->offsets[3], merges);
+    put(blob, (size_t)info->offsets[4], cta_off);
     info->workspace_bytes = kHeader + (size_t)num_records * num_q_heads * head_dim * 4 +
                             (size_t)num_records * num_q_heads * 2 * 4;
     return emit(blob, plan, plan_cap, info);

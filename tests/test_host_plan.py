@@ -13,7 +13,7 @@ from prefix_shared_kv_token_gb300 import _lib
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
-DEC = np.dtype([("g", "<i4"), ("mode", "<i4"), ("nreq", "<i4"), ("row_off", "<i4"), ("src", "<i4"),
+DEC = np.dtype([("g0", "<i4"), ("mode", "<i4"), ("nreq", "<i4"), ("row_off", "<i4"), ("src", "<i4"),
                 ("k0", "<i4"), ("k1", "<i4"), ("pad", "<i4")])
 EXT = np.dtype([("g", "<i4"), ("tok0", "<i4"), ("ntok", "<i4"), ("qpos0", "<i4"), ("pos0", "<i4"),
                 ("nseg", "<i4"), ("rec", "<i4"), ("pad", "<i4"), ("key0", "<i4", (4,)), ("nkeys", "<i4", (4,))])
@@ -43,13 +43,20 @@ def _decode_cover(plan, seq, hkv, cascade_spans=None):
     row_rec = np.frombuffer(plan.blob[info.offsets[2]:info.offsets[2] + 4 * nrows].tobytes(), np.int32)
     merges = _sections(plan, MRG, info.num_merge, info.offsets[3])
     B = len(seq)
+    # persistent CTAs: contiguous per-CTA item ranges that partition the item list
+    nctas, hg = int(info.offsets[5]), int(info.offsets[6])
+    assert hg in (1, 2, 4, 8) and hkv % hg == 0 and 1 <= nctas <= max(1, info.num_items)
+    cta_off = np.frombuffer(plan.blob[info.offsets[4]:info.offsets[4] + 4 * (nctas + 1)].tobytes(), np.int32)
+    assert cta_off[0] == 0 and cta_off[-1] == info.num_items and np.all(np.diff(cta_off) >= 1)
+    G = info.num_q_heads // hkv
     cover = [np.zeros((hkv, seq[r]), np.int32) for r in range(B)]
     recs_seen = {}
     for it in items:
+        assert it["g0"] % hg == 0 and 1 <= it["nreq"] <= 16 // G
         for i in range(it["nreq"]):
             r = row_req[it["row_off"] + i]
             k1 = it["k1"] if it["k1"] >= 0 else seq[r]
-            cover[r][it["g"], it["k0"]:k1] += 1
+            cover[r][it["g0"]:it["g0"] + hg, it["k0"]:k1] += 1
             recs_seen.setdefault(r, set()).add(row_rec[it["row_off"] + i])
     for r in range(B):
         assert np.all(cover[r] == 1), r
@@ -80,8 +87,34 @@ def test_decode_plan_with_cascade():
                        grp_req=np.array([0, 1, 2, 3, 4, 5, 0, 1, 2], np.int32))
     plan = pkv.plan_decode(seq, 8, 2, 64, casc)
     items = _decode_cover(plan, seq, 2)
-    assert plan.info.num_span_items == 4
-    assert sum(1 for it in items if it["mode"] == 0) == 4
+    # G = 4: 4 member requests per span item, both KV heads in one item -> 2 + 1 span items
+    assert plan.info.num_span_items == 3
+    assert sum(1 for it in items if it["mode"] == 0) == 3
+
+
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (48, 12), (16, 16), (8, 1), (64, 8)])
+def test_decode_plan_head_groups(hq, hkv):
+    rng = np.random.default_rng(1)
+    seq = rng.integers(1, 700, size=23).astype(np.int32)
+    plan = pkv.plan_decode(seq, hq, hkv, 128, None)
+    _decode_cover(plan, seq, hkv)
+    hg = int(plan.info.offsets[6])
+    assert hg == max(h for h in (1, 2, 4, 8) if hkv % h == 0)
+
+
+def test_decode_plan_balances_ctas():
+    # LPT: no CTA carries more than the mean load plus one item
+    rng = np.random.default_rng(2)
+    seq = rng.integers(100, 3000, size=300).astype(np.int32)
+    plan = pkv.plan_decode(seq, 32, 8, 128, None, {"chunk_keys": 256, "num_sms": 20})
+    items = _decode_cover(plan, seq, 8)
+    info = plan.info
+    nctas = int(info.offsets[5])
+    assert nctas == 20
+    cta_off = np.frombuffer(plan.blob[info.offsets[4]:info.offsets[4] + 4 * (nctas + 1)].tobytes(), np.int32)
+    keys = (items["k1"] - items["k0"]).astype(np.int64)
+    load = np.array([keys[cta_off[b]:cta_off[b + 1]].sum() for b in range(nctas)])
+    assert load.max() <= keys.sum() / nctas + keys.max()
 
 
 def test_decode_plan_rejects_bad_cascade():

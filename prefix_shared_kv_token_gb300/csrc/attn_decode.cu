@@ -257,6 +257,60 @@ PKV_DEV void tile16(WarpState<D> &st, const uint32_t (&qf)[D / 16][4], const uin
     }
 }
 
+// The producer's walk over its CTA's tiles: items [c0, c1) in order (an item whose
+// positions are out of range is reported and skipped), each item's tiles cyclically from
+// its start tile.  next_tile() returns the next tile with this lane's slot load issued, or a
+// tile flagged kEnd after the last one.
+struct TileCursor {
+    int i, j, nt, jj, k0, k1, g0;
+    const int32_t *rt;
+};
+struct TileSlot {
+    TileInfo info;
+    int32_t slot;  // this lane's key (lane & 15) of the tile; -1 past the item's end
+    int32_t g0;
+};
+
+PKV_DEV TileSlot next_tile(const DecodeParams &p, TileCursor &cur, int c1, int key) {
+    TileSlot e;
+    while (cur.j >= cur.nt) {
+        if (cur.i + 1 >= c1) {
+            cur.i = c1;
+            e.info.kpos = e.info.k1 = 0;
+            e.info.item = -1;
+            e.info.flags = kEnd;
+            e.slot = -1;
+            e.g0 = 0;
+            return e;
+        }
+        ++cur.i;
+        const DecodeItem it = p.items[cur.i];
+        const int row = __ldg(p.req_pool_indices + it.src);
+        const int k1 = it.k1 < 0 ? __ldg(p.seq_lens + it.src) : it.k1;
+        if (row < 0 || row >= p.rt_rows || it.k0 < 0 || k1 > p.rt_stride || k1 <= it.k0) {
+            if ((threadIdx.x & 31) == 0) set_error(p.err, DERR_POSITION);
+            continue;
+        }
+        cur.k0 = it.k0;
+        cur.k1 = k1;
+        cur.g0 = it.g0;
+        cur.nt = (k1 - it.k0 + kBK - 1) / kBK;
+        cur.j = 0;
+        cur.jj = it.rot > 0 ? it.rot % cur.nt : 0;  // the softmax does not depend on key order
+        cur.rt = p.req_to_token + (int64_t)row * p.rt_stride;
+    }
+    e.info.kpos = cur.k0 + cur.jj * kBK;
+    e.info.k1 = cur.k1;
+    e.info.item = cur.i;
+    e.info.flags = (cur.j == 0 ? kFirst : 0) | (cur.j == cur.nt - 1 ? kLast : 0);
+    e.g0 = cur.g0;
+    const int kp = e.info.kpos + key;
+    e.slot = kp < cur.k1 ? __ldg(cur.rt + kp) : -1;
+    ++cur.j;
+    cur.jj = cur.jj + 1 == cur.nt ? 0 : cur.jj + 1;
+    return e;
+}
+
 template <int D, int G, bool FP8>
 __global__ void __launch_bounds__(288, (D == 64 ? 2 : 1)) decode_kernel(const DecodeParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -288,63 +342,52 @@ __global__ void __launch_bounds__(288, (D == 64 ? 2 : 1)) decode_kernel(const De
         const bool is_v = lane >= 16;
         const uint8_t *pool = is_v ? p.v_pool : p.k_pool;
         const int64_t head_bytes = (int64_t)D * (FP8 ? 1 : 2);
+        // the slots of the next 4 tiles are in flight while the current tile is issued
+        TileCursor cur;
+        cur.i = c0 - 1;
+        cur.j = cur.nt = 0;
+        TileSlot e0 = next_tile(p, cur, c1, key), e1 = next_tile(p, cur, c1, key);
+        TileSlot e2 = next_tile(p, cur, c1, key), e3 = next_tile(p, cur, c1, key);
         int t = 0;
         bool aborted = false;
-        for (int i = c0; i < c1 && !aborted; ++i) {
-            const DecodeItem it = p.items[i];
-            const int row = __ldg(p.req_pool_indices + it.src);
-            const int k0 = it.k0;
-            const int k1 = it.k1 < 0 ? __ldg(p.seq_lens + it.src) : it.k1;
-            if (row < 0 || row >= p.rt_rows || k0 < 0 || k1 > p.rt_stride || k1 <= k0) {
-                if (lane == 0) set_error(p.err, DERR_POSITION);
-                continue;
-            }
-            const int32_t *rt = p.req_to_token + (int64_t)row * p.rt_stride;
-            const int nt = (k1 - k0 + kBK - 1) / kBK;
-            int32_t slot = k0 + key < k1 ? __ldg(rt + k0 + key) : -1;
-            for (int j = 0; j < nt; ++j, ++t) {
-                const int s = t % S;
-                if (t >= S && !__all_sync(0xffffffffu, dwait(&empty[s], ((t / S) - 1) & 1, abort_flag, p.err, 0x31))) {
-                    aborted = true;  // warp-uniform: every lane leaves together
-                    break;
-                }
-                const int kp = k0 + j * kBK + key;
-                const bool in = kp < k1;
-                const bool valid = in && slot >= 0 && (int64_t)slot < p.num_slots;
-                if (in && !valid) set_error(p.err, DERR_SLOT_RANGE);
-                uint8_t *dst = ring + s * geo.stage + (is_v ? kBK * geo.sk + key * geo.sv : key * geo.sk);
-                // no copy: a V row past the item's end, or either row of a bad slot, reads as
-                // zeros (keys past the end are masked, so their K rows are left as they are)
-                if (!valid && (in || is_v)) {
-                    for (int b = 0; b < geo.rowb; b += 16) *reinterpret_cast<uint4 *>(dst + b) = make_uint4(0u, 0u, 0u, 0u);
-                    fence_proxy_async_smem();  // a later bulk copy rewrites this row
-                }
-                const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
-                __syncwarp();
-                if (lane == 0) {
-                    TileInfo ti;
-                    ti.kpos = k0 + j * kBK;
-                    ti.k1 = k1;
-                    ti.item = i;
-                    ti.flags = (j == 0 ? kFirst : 0) | (j == nt - 1 ? kLast : 0);
-                    tinfo[s] = ti;
-                    mbar_arrive_expect_tx(&full[s], nvalid * (uint32_t)geo.rowb);
-                }
-                __syncwarp();
-                if (valid)
-                    bulk_copy_g2s(smem_u32(dst), pool + ((int64_t)slot * p.hkv + it.g0) * head_bytes, (uint32_t)geo.rowb,
-                                  &full[s]);
-                slot = (j + 1 < nt && kp + kBK < k1) ? __ldg(rt + kp + kBK) : -1;
-            }
-        }
-        if (!aborted) {
+        for (;; ++t) {
             const int s = t % S;
-            if (t >= S && !__all_sync(0xffffffffu, dwait(&empty[s], ((t / S) - 1) & 1, abort_flag, p.err, 0x32))) {
-                aborted = true;
-            } else if (lane == 0) {
-                tinfo[s].flags = kEnd;
-                mbar_arrive(&full[s]);
+            if (t >= S && !__all_sync(0xffffffffu, dwait(&empty[s], ((t / S) - 1) & 1, abort_flag, p.err, 0x31))) {
+                aborted = true;  // warp-uniform: every lane leaves together
+                break;
             }
+            if (e0.info.flags & kEnd) {
+                if (lane == 0) {
+                    tinfo[s].flags = kEnd;
+                    mbar_arrive(&full[s]);
+                }
+                break;
+            }
+            const int kp = e0.info.kpos + key;
+            const bool in = kp < e0.info.k1;
+            const bool valid = in && e0.slot >= 0 && (int64_t)e0.slot < p.num_slots;
+            if (in && !valid) set_error(p.err, DERR_SLOT_RANGE);
+            uint8_t *dst = ring + s * geo.stage + (is_v ? kBK * geo.sk + key * geo.sv : key * geo.sk);
+            // no copy: a V row past the item's end, or either row of a bad slot, reads as zeros
+            // (keys past the end are masked, so their K rows are left as they are)
+            if (!valid && (in || is_v)) {
+                for (int b = 0; b < geo.rowb; b += 16) *reinterpret_cast<uint4 *>(dst + b) = make_uint4(0u, 0u, 0u, 0u);
+                fence_proxy_async_smem();  // a later bulk copy rewrites this row
+            }
+            const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
+            __syncwarp();
+            if (lane == 0) {
+                tinfo[s] = e0.info;
+                mbar_arrive_expect_tx(&full[s], nvalid * (uint32_t)geo.rowb);
+            }
+            __syncwarp();
+            if (valid)
+                bulk_copy_g2s(smem_u32(dst), pool + ((int64_t)e0.slot * p.hkv + e0.g0) * head_bytes, (uint32_t)geo.rowb,
+                              &full[s]);
+            e0 = e1;
+            e1 = e2;
+            e2 = e3;
+            e3 = next_tile(p, cur, c1, key);
         }
         if (aborted) {
             // let the copies still in flight land (bounded) before the CTA exits
@@ -534,9 +577,9 @@ extern "C" int pkv_attn_decode(const pkv_pool *pool, const pkv_batch *batch, con
     using namespace pkv;
     int rc = check_call(pool, batch, q, o, info, plan_dev, workspace, ws_bytes, 1);
     if (rc) return rc;
-    if (info->num_items == 0) return PKV_OK;
+    if (info->num_items == 0 && info->offsets[8] == 0) return PKV_OK;
     const int64_t nctas = info->offsets[SEC_NUM_CTAS], hg = info->offsets[SEC_HEAD_GROUP];
-    if (nctas < 1 || nctas > info->num_items || (hg != 1 && hg != 2 && hg != 4 && hg != 8) ||
+    if (nctas < 1 || (info->num_items > 0 && nctas > info->num_items) || (hg != 1 && hg != 2 && hg != 4 && hg != 8) ||
         pool->num_kv_heads % hg)
         return PKV_E_PLAN;
     const uint8_t *plan = static_cast<const uint8_t *>(plan_dev);
@@ -567,9 +610,14 @@ extern "C" int pkv_attn_decode(const pkv_pool *pool, const pkv_batch *batch, con
     p.rec_acc = reinterpret_cast<float *>(ws + kWorkspaceHeader);
     p.rec_ml = p.rec_acc + (size_t)info->num_records * info->num_q_heads * info->head_dim;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int G = info->num_q_heads / info->num_kv_heads;
-    rc = info->head_dim == 128 ? dispatch_g<128>(G, fp8, p, (int)nctas, s)
-                               : dispatch_g<64>(G, fp8, p, (int)nctas, s);
+    // widely shared spans on the tensor cores first, then everything else, then the merge
+    rc = decode_span_tensor(pool, batch, q, sm_scale, info, plan, ws, p.rec_acc, p.rec_ml, s);
     if (rc) return rc;
+    if (info->num_items > 0) {
+        const int G = info->num_q_heads / info->num_kv_heads;
+        rc = info->head_dim == 128 ? dispatch_g<128>(G, fp8, p, (int)nctas, s)
+                                   : dispatch_g<64>(G, fp8, p, (int)nctas, s);
+        if (rc) return rc;
+    }
     return launch_merge(info, plan_dev, p.rec_acc, p.rec_ml, p.o, s);
 }

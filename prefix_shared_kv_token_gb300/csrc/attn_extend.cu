@@ -57,6 +57,7 @@ struct ExtendParams {
     int32_t num_items;
     float *rec_acc;
     float *rec_ml;
+    const int32_t *rec_list;  // NULL: token t of an item writes record rec + t; else rec_list[rec + t]
     int32_t *err;
 };
 
@@ -503,7 +504,7 @@ __global__ void __launch_bounds__(384, 1)
                         dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 } else {
-                    const int64_t rb = (int64_t)(it.rec + t) * p.hq + head;
+                    const int64_t rb = (int64_t)(p.rec_list ? __ldg(p.rec_list + it.rec + t) : it.rec + t) * p.hq + head;
                     float4 *dst = reinterpret_cast<float4 *>(p.rec_acc + rb * D + c4 * 32);
 #pragma unroll
                     for (int v = 0; v < 8; ++v)
@@ -566,6 +567,98 @@ int check_call(const pkv_pool *pool, const pkv_batch *batch, const void *q, void
 int launch_merge(const pkv_plan_info *info, const void *plan_dev, const float *rec_acc, const float *rec_ml,
                  uint16_t *o, cudaStream_t s);
 
+// Tensor maps: Q as [rows][Hq][D] (box 64 x G x 128/G); gathered K/V as [keys][Hkv][D] (box
+// 64 x 1 x 128): every box lands as 128 rows of 128 bytes, 128-byte swizzled.
+static int make_maps(const void *q, int64_t qrows, const uint16_t *kg, const uint16_t *vg, int64_t nkeys, int D,
+                     int hq, int hkv, CUtensorMap *qm, CUtensorMap *km, CUtensorMap *vm) {
+    const int G = hq / hkv;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)hq, (cuuint64_t)std::max<int64_t>(qrows, 1)};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)hq * D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(128 / G)};
+    if (encode_tiled(qm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return PKV_E_CUDA;
+    cuuint64_t kdims[3] = {(cuuint64_t)D, (cuuint64_t)hkv, (cuuint64_t)std::max<int64_t>(nkeys, 1)};
+    cuuint64_t kstrides[2] = {(cuuint64_t)D * 2, (cuuint64_t)hkv * D * 2};
+    cuuint32_t kbox[3] = {64, 1, 128};
+    if (encode_tiled(km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(kg), kdims, kstrides, kbox,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
+        encode_tiled(vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(vg), kdims, kstrides, kbox,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return PKV_E_CUDA;
+    return PKV_OK;
+}
+
+// Copy query rows q[src[i]] (Hq * D bf16 each) to row i of a contiguous buffer.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4 *__restrict__ q, uint4 *__restrict__ out,
+                                                         const int32_t *__restrict__ src, int batch, int row_vecs,
+                                                         int32_t *err) {
+    const int r = __ldg(src + blockIdx.x);
+    if (r < 0 || r >= batch) {
+        if (threadIdx.x == 0) set_error(err, DERR_POSITION);
+        return;
+    }
+    for (int i = threadIdx.x; i < row_vecs; i += blockDim.x)
+        out[(int64_t)blockIdx.x * row_vecs + i] = __ldg(q + (int64_t)r * row_vecs + i);
+}
+
+// Decode over shared spans with many members, on the tensor cores: the plan's spans are
+// gathered once into the workspace (bf16 [key][Hkv][D]), the member requests' query rows
+// are gathered next to them, and extend-kernel items (two 128-row query tiles of 128/G
+// members x G heads, one KV head, a chunk of the span; no mask: every query comes after
+// the span) write each member's partial record for the chunk.
+int decode_span_tensor(const pkv_pool *pool, const pkv_batch *batch, const void *q, float sm_scale,
+                       const pkv_plan_info *info, const uint8_t *plan, uint8_t *ws, float *rec_acc, float *rec_ml,
+                       cudaStream_t s) {
+    const int64_t nx = info->offsets[8], nunits = info->offsets[10], nkeys = info->offsets[11];
+    const int64_t nq = info->offsets[13];
+    if (nx == 0) return PKV_OK;
+    const int D = info->head_dim, hq = info->num_q_heads, hkv = info->num_kv_heads, G = hq / hkv;
+    const bool fp8 = pool->dtype == PKV_FP8_E4M3;
+    int32_t *err = reinterpret_cast<int32_t *>(ws);
+    uint16_t *kg = reinterpret_cast<uint16_t *>(ws + info->offsets[15]);
+    uint16_t *vg = kg + (size_t)nkeys * hkv * D;
+    const size_t qoff = ((size_t)info->offsets[15] + 2 * (size_t)nkeys * hkv * D * 2 + 255) & ~size_t(255);
+    uint16_t *qg = reinterpret_cast<uint16_t *>(ws + qoff);
+
+    GatherParams gp;
+    gp.k_pool = static_cast<const uint8_t *>(pool->k);
+    gp.v_pool = static_cast<const uint8_t *>(pool->v);
+    gp.num_slots = pool->num_slots;
+    gp.hkv = hkv;
+    gp.req_to_token = batch->req_to_token;
+    gp.rt_stride = batch->stride;
+    gp.rt_rows = batch->num_rows;
+    gp.req_pool_indices = batch->req_pool_indices;
+    gp.units = reinterpret_cast<const GatherUnit *>(plan + info->offsets[9]);
+    gp.k_out = kg;
+    gp.v_out = vg;
+    gp.err = err;
+    int rc = D == 128 ? launch_gather<128>(gp, fp8, (int)nunits, s) : launch_gather<64>(gp, fp8, (int)nunits, s);
+    if (rc) return rc;
+    gather_rows_kernel<<<(unsigned)nq, 256, 0, s>>>(static_cast<const uint4 *>(q), reinterpret_cast<uint4 *>(qg),
+                                                    reinterpret_cast<const int32_t *>(plan + info->offsets[12]),
+                                                    batch->batch, hq * D / 8, err);
+    if (cudaGetLastError() != cudaSuccess) return PKV_E_CUDA;
+
+    CUtensorMap qm, km, vm;
+    rc = make_maps(qg, nq, kg, vg, nkeys, D, hq, hkv, &qm, &km, &vm);
+    if (rc) return rc;
+    ExtendParams p;
+    p.o = nullptr;  // every item writes records
+    p.hkv = hkv;
+    p.hq = hq;
+    p.scale_log2 = sm_scale * (fp8 ? pool->k_scale : 1.f) * kLog2eX;
+    p.v_scale = fp8 ? pool->v_scale : 1.f;
+    p.items = reinterpret_cast<const ExtendItem *>(plan + info->offsets[7]);
+    p.num_items = (int32_t)nx;
+    p.err = err;
+    p.rec_acc = rec_acc;
+    p.rec_ml = rec_ml;
+    p.rec_list = reinterpret_cast<const int32_t *>(plan + info->offsets[14]);
+    return D == 128 ? dispatch_extend<128>(G, p, qm, km, vm, (int)nx, s) : dispatch_extend<64>(G, p, qm, km, vm, (int)nx, s);
+}
+
 }  // namespace pkv
 
 extern "C" int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, const void *q, void *o, float sm_scale,
@@ -608,25 +701,9 @@ extern "C" int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, con
         if (rc) return rc;
     }
 
-    // tensor maps: Q as [T][Hq][D] (box 64 x G x 128/G); gathered K/V as [keys][Hkv][D]
-    // (box 64 x 1 x 128): every box lands as 128 rows of 128 bytes, 128-byte swizzled
     CUtensorMap qm, km, vm;
-    {
-        cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)hq, (cuuint64_t)std::max(info->total_q, 1)};
-        cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)hq * D * 2};
-        cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(128 / G)};
-        if (encode_tiled(&qm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box,
-                         CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
-            return PKV_E_CUDA;
-        cuuint64_t kdims[3] = {(cuuint64_t)D, (cuuint64_t)hkv, (cuuint64_t)std::max<int64_t>(nkeys, 1)};
-        cuuint64_t kstrides[2] = {(cuuint64_t)D * 2, (cuuint64_t)hkv * D * 2};
-        cuuint32_t kbox[3] = {64, 1, 128};
-        if (encode_tiled(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kg, kdims, kstrides, kbox,
-                         CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
-            encode_tiled(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, vg, kdims, kstrides, kbox,
-                         CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
-            return PKV_E_CUDA;
-    }
+    rc = make_maps(q, info->total_q, kg, vg, nkeys, D, hq, hkv, &qm, &km, &vm);
+    if (rc) return rc;
 
     ExtendParams p;
     p.o = static_cast<uint16_t *>(o);
@@ -639,6 +716,7 @@ extern "C" int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, con
     p.err = reinterpret_cast<int32_t *>(ws);
     p.rec_acc = rec_acc;
     p.rec_ml = rec_ml;
+    p.rec_list = nullptr;
     rc = D == 128 ? dispatch_extend<128>(G, p, qm, km, vm, info->num_items, s)
                   : dispatch_extend<64>(G, p, qm, km, vm, info->num_items, s);
     if (rc) return rc;

@@ -28,4 +28,10 @@ CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType dtype, cuuint32_t ra
                       const cuuint64_t *dims, const cuuint64_t *strides_bytes, const cuuint32_t *box,
                       CUtensorMapSwizzle swizzle);
 
+// Tensor-core pass of a decode plan over its widely shared spans (gather, query-row gather,
+// extend kernel writing partial records); no-op when the plan has none.
+int decode_span_tensor(const pkv_pool *pool, const pkv_batch *batch, const void *q, float sm_scale,
+                       const pkv_plan_info *info, const uint8_t *plan, uint8_t *ws, float *rec_acc, float *rec_ml,
+                       cudaStream_t s);
+
 }  // namespace pkv

@@ -30,7 +30,7 @@
 
 namespace {
 
-struct DecodeItem { int32_t g0, mode, nreq, row_off, src, k0, k1, pad; };
+struct DecodeItem { int32_t g0, mode, nreq, row_off, src, k0, k1, rot; };
 constexpr int kMaxSegs = 4;
 struct ExtendItem { int32_t g, tok0, ntok, qpos0, pos0, nseg, rec, pad, key0[kMaxSegs], nkeys[kMaxSegs]; };
 struct GatherUnit { int32_t src, pos0, len, key0; };
@@ -38,6 +38,9 @@ struct MergeItem { int32_t out_row, rec0, nrec, rec_stride; };
 static_assert(sizeof(DecodeItem) == 32 && sizeof(ExtendItem) == 64 && sizeof(MergeItem) == 16, "layout");
 
 constexpr size_t kHeader = 256;
+// decode: a shared span goes to the tensor-core path from this many member requests and keys
+constexpr int32_t kTensorMinMembers = 12;
+constexpr int32_t kTensorMinKeys = 256;
 size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
 int check_heads(int32_t hq, int32_t hkv, int32_t d) {
@@ -127,6 +130,7 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
     const int32_t num_sms = (opts && opts->num_sms > 0) ? opts->num_sms : 152;
     const bool dyn_tail = opts && opts->dynamic_tail;
     const int32_t R = 16 / G;  // requests per span item: one 16-row MMA tile per KV head
+    const int32_t TQ2 = 2 * (128 / G);  // requests per tensor-core span item (two 128-row tiles)
     // head group: KV heads read together per key (one contiguous pool row), <= 8
     int32_t hg = 8;
     while (num_kv_heads % hg) hg /= 2;
@@ -136,18 +140,37 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
     rc = spans_per_request(cascade, batch, seq_lens, &spans_of, &tail_start);
     if (rc) return rc;
 
+    // Shared spans with many member requests go to the tensor-core path: the span's keys
+    // are gathered once into the workspace and attended as a dense block by 2 x 128/G of its
+    // member requests per item (extend kernel), instead of re-reading the span per group of
+    // 16/G requests.  Key chunks are sized for about one item per SM, at least 512 keys.
+    const int32_t nspans = cascade ? cascade->num_spans : 0;
+    std::vector<int32_t> sp_chunk(nspans, span_chunk);
+    std::vector<char> sp_tensor(nspans, 0);
+    std::vector<char> in_tensor(batch, 0);
+    for (int32_t s = 0; s < nspans; ++s) {
+        const int32_t m = cascade->grp_indptr[s + 1] - cascade->grp_indptr[s], len = cascade->span_len[s];
+        if (m < kTensorMinMembers || len < kTensorMinKeys) continue;
+        sp_tensor[s] = 1;
+        const int64_t per_chunk = (int64_t)((m + TQ2 - 1) / TQ2) * num_kv_heads;
+        const int32_t nch = (int32_t)std::max<int64_t>(
+            1, std::min<int64_t>((num_sms + per_chunk - 1) / per_chunk, (len + 511) / 512));
+        sp_chunk[s] = ((len + nch - 1) / nch + 127) / 128 * 128;
+        for (int32_t i = cascade->grp_indptr[s]; i < cascade->grp_indptr[s + 1]; ++i) in_tensor[cascade->grp_req[i]] = 1;
+    }
+
     // records per request: its span chunks (in path order), then its tail chunks
     auto nchunks = [](int32_t len, int32_t c) { return len <= 0 ? 0 : (len + c - 1) / c; };
     std::vector<int32_t> nrec(batch, 0), rec_base(batch, 0);
     for (int32_t r = 0; r < batch; ++r) {
         int32_t n = 0;
-        for (int32_t s : spans_of[r]) n += nchunks(cascade->span_len[s], span_chunk);
+        for (int32_t s : spans_of[r]) n += nchunks(cascade->span_len[s], sp_chunk[s]);
         n += nchunks(seq_lens[r] - tail_start[r], chunk);
         nrec[r] = n;
     }
     int32_t num_records = 0;
     for (int32_t r = 0; r < batch; ++r) {
-        if (nrec[r] >= 2) {
+        if (nrec[r] >= 2 || in_tensor[r]) {  // tensor-core items always write records
             rec_base[r] = num_records;
             num_records += nrec[r];
         } else {
@@ -164,10 +187,50 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
     int32_t num_span_items = 0;
     constexpr int64_t kItemOverhead = 40;  // in fifths of a key
 
+    // tensor-core span items (extend-kernel layout), their gathered keys and query rows
+    std::vector<ExtendItem> xitems;
+    std::vector<GatherUnit> units;
+    std::vector<int32_t> qsrc, rec_list;
+    int64_t nkeys = 0;
+
     if (cascade) {
         for (int32_t s = 0; s < cascade->num_spans; ++s) {
             const int32_t st = cascade->span_start[s], len = cascade->span_len[s];
             const int32_t m0 = cascade->grp_indptr[s], m1 = cascade->grp_indptr[s + 1];
+            if (sp_tensor[s]) {
+                const int32_t key0 = (int32_t)nkeys, q0 = (int32_t)qsrc.size();
+                for (int32_t c = 0; c < len; c += 32)
+                    units.push_back({cascade->span_req[s], st + c, std::min(32, len - c), key0 + c});
+                nkeys += len;
+                for (int32_t i = m0; i < m1; ++i) qsrc.push_back(cascade->grp_req[i]);
+                for (int32_t c0 = 0; c0 < len; c0 += sp_chunk[s]) {
+                    const int32_t c1 = std::min(len, c0 + sp_chunk[s]);
+                    for (int32_t a = m0; a < m1; a += TQ2) {
+                        const int32_t b = std::min(m1, a + TQ2);
+                        const int32_t roff = (int32_t)rec_list.size();
+                        for (int32_t i = a; i < b; ++i) {
+                            const int32_t r = cascade->grp_req[i];
+                            rec_list.push_back(rec_base[r] + next_rec[r]);
+                            next_rec[r] += 1;
+                        }
+                        for (int32_t g = 0; g < num_kv_heads; ++g) {
+                            ExtendItem it{};
+                            it.g = g;
+                            it.tok0 = q0 + (a - m0);
+                            it.ntok = b - a;
+                            it.qpos0 = 1 << 30;  // every query comes after the span: no mask
+                            it.pos0 = st + c0;
+                            it.nseg = 1;
+                            it.rec = roff;
+                            it.key0[0] = key0 + c0;
+                            it.nkeys[0] = c1 - c0;
+                            xitems.push_back(it);
+                            ++num_span_items;
+                        }
+                    }
+                }
+                continue;
+            }
             for (int32_t c0 = 0; c0 < len; c0 += span_chunk) {
                 const int32_t c1 = std::min(len, c0 + span_chunk);
                 for (int32_t a = m0; a < m1; a += R) {
@@ -179,8 +242,13 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
                         row_rec.push_back(rec_base[r] < 0 ? -1 : rec_base[r] + next_rec[r]);
                         next_rec[r] += 1;
                     }
+                    // member groups of one chunk start at staggered tiles, so the CTAs that
+                    // read the chunk at the same time spread over it instead of queueing on
+                    // the same L2 lines
+                    const int32_t ntile = (c1 - c0 + 15) / 16, ngrp = (m1 - m0 + R - 1) / R;
+                    const int32_t rot = (int32_t)((int64_t)((a - m0) / R) * ntile / ngrp);
                     for (int32_t g0 = 0; g0 < num_kv_heads; g0 += hg) {
-                        items.push_back({g0, 0, b - a, off, cascade->span_req[s], st + c0, st + c1, 0});
+                        items.push_back({g0, 0, b - a, off, cascade->span_req[s], st + c0, st + c1, rot});
                         cost.push_back((int64_t)(c1 - c0) * (a == m0 ? 5 : 3) + kItemOverhead);
                         ++num_span_items;
                     }
@@ -236,6 +304,11 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
     }
     if (n_items == 0) cta_off.push_back(0);
 
+    if (nkeys >= ((int64_t)1 << 31)) return PKV_E_UNSUPPORTED;
+    std::stable_sort(xitems.begin(), xitems.end(), [](const ExtendItem &x, const ExtendItem &y) {
+        return (int64_t)x.nkeys[0] * x.ntok > (int64_t)y.nkeys[0] * y.ntok;
+    });
+
     std::memset(info, 0, sizeof(*info));
     info->op = 1;
     info->batch = batch;
@@ -255,14 +328,31 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
     info->offsets[4] = (int64_t)off; off = align16(off + cta_off.size() * sizeof(int32_t));
     info->offsets[5] = nctas;
     info->offsets[6] = hg;
+    info->offsets[7] = (int64_t)off; off = align16(off + xitems.size() * sizeof(ExtendItem));
+    info->offsets[8] = (int64_t)xitems.size();
+    info->offsets[9] = (int64_t)off; off = align16(off + units.size() * sizeof(GatherUnit));
+    info->offsets[10] = (int64_t)units.size();
+    info->offsets[11] = nkeys;
+    info->offsets[12] = (int64_t)off; off = align16(off + qsrc.size() * sizeof(int32_t));
+    info->offsets[13] = (int64_t)qsrc.size();
+    info->offsets[14] = (int64_t)off; off = align16(off + rec_list.size() * sizeof(int32_t));
     std::vector<uint8_t> blob(std::max<size_t>(off, 16), 0);
     put(blob, (size_t)info->offsets[0], placed);
     put(blob, (size_t)info->offsets[1], row_req);
     put(blob, (size_t)info->offsets[2], row_rec);
     put(blob, (size_t)info->offsets[3], merges);
     put(blob, (size_t)info->offsets[4], cta_off);
-    info->workspace_bytes = kHeader + (size_t)num_records * num_q_heads * head_dim * 4 +
-                            (size_t)num_records * num_q_heads * 2 * 4;
+    put(blob, (size_t)info->offsets[7], xitems);
+    put(blob, (size_t)info->offsets[9], units);
+    put(blob, (size_t)info->offsets[12], qsrc);
+    put(blob, (size_t)info->offsets[14], rec_list);
+    // workspace: header | records (acc, ml) | gathered K | gathered V | gathered query rows
+    auto align256 = [](size_t x) { return (x + 255) & ~size_t(255); };
+    size_t ws = align256(kHeader + (size_t)num_records * num_q_heads * (head_dim + 2) * 4);
+    info->offsets[15] = (int64_t)ws;
+    ws += 2 * (size_t)nkeys * num_kv_heads * head_dim * 2;
+    ws = align256(ws) + qsrc.size() * (size_t)num_q_heads * head_dim * 2;
+    info->workspace_bytes = ws;
     return emit(blob, plan, plan_cap, info);
 }
 

@@ -157,6 +157,26 @@ def test_decode_small(cascade, hq, hkv, d):
         assert calls["decode"].plan.info.num_span_items > 0
 
 
+@pytest.mark.parametrize("hq,hkv,d", [(32, 8, 128), (8, 8, 128), (16, 8, 64), (64, 8, 128), (8, 2, 64)])
+def test_decode_tensor_core_spans(hq, hkv, d):
+    # a 700-key prefix shared by 40 requests: attended on the tensor cores as a dense block
+    w = W.batched_decode(seed=36, n_req=40, prefix=700, lo=1, hi=300, hq=hq, hkv=hkv, d=d, num_slots=40000)
+    pc, calls = run_step(w)
+    assert int(calls["decode"].plan.info.offsets[8]) > 0
+    check_outputs(w, calls)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8_e4m3"])
+def test_decode_tensor_core_nested_spans(dtype):
+    # root shared by 256 leaves, 16 depth-1 nodes shared by 16 leaves each (both tensor-core
+    # spans), unique 256-key leaves; plus 4 extending branches in the same batch
+    w = W.tot_mixed(seed=37, root_len=512, depth=2, branch=16, seg=256, n_new_branches=4, num_slots=90000,
+                    dtype=dtype)
+    pc, calls = run_step(w)
+    assert int(calls["decode"].plan.info.offsets[8]) > 0
+    check_outputs(w, calls)
+
+
 @pytest.mark.parametrize("cascade", [True, False])
 def test_decode_fp8_small(cascade):
     w = W.batched_decode(seed=32, n_req=9, prefix=150, lo=20, hi=200, num_slots=8000, dtype="fp8_e4m3")

@@ -14,7 +14,7 @@ from prefix_shared_kv_token_gb300 import _lib
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 DEC = np.dtype([("g0", "<i4"), ("mode", "<i4"), ("nreq", "<i4"), ("row_off", "<i4"), ("src", "<i4"),
-                ("k0", "<i4"), ("k1", "<i4"), ("pad", "<i4")])
+                ("k0", "<i4"), ("k1", "<i4"), ("rot", "<i4")])
 EXT = np.dtype([("g", "<i4"), ("tok0", "<i4"), ("ntok", "<i4"), ("qpos0", "<i4"), ("pos0", "<i4"),
                 ("nseg", "<i4"), ("rec", "<i4"), ("pad", "<i4"), ("key0", "<i4", (4,)), ("nkeys", "<i4", (4,))])
 GU = np.dtype([("src", "<i4"), ("pos0", "<i4"), ("len", "<i4"), ("key0", "<i4")])
@@ -53,11 +53,36 @@ def _decode_cover(plan, seq, hkv, cascade_spans=None):
     recs_seen = {}
     for it in items:
         assert it["g0"] % hg == 0 and 1 <= it["nreq"] <= 16 // G
+        if it["k1"] >= 0:
+            assert 0 <= it["rot"] < (it["k1"] - it["k0"] + 15) // 16
         for i in range(it["nreq"]):
             r = row_req[it["row_off"] + i]
             k1 = it["k1"] if it["k1"] >= 0 else seq[r]
             cover[r][it["g0"]:it["g0"] + hg, it["k0"]:k1] += 1
             recs_seen.setdefault(r, set()).add(row_rec[it["row_off"] + i])
+    # tensor-core span items: query rows gathered from members, keys gathered from the span
+    nx, nu, nk, nq = (int(info.offsets[i]) for i in (8, 10, 11, 13))
+    if nx:
+        xitems = _sections(plan, EXT, nx, info.offsets[7])
+        units = _sections(plan, GU, nu, info.offsets[9])
+        qsrc = np.frombuffer(plan.blob[info.offsets[12]:info.offsets[12] + 4 * nq].tobytes(), np.int32)
+        nrl = max(int(it["rec"]) + int(it["ntok"]) for it in xitems)
+        rec_list = np.frombuffer(plan.blob[info.offsets[14]:info.offsets[14] + 4 * nrl].tobytes(), np.int32)
+        g_src, g_pos = np.full(nk, -1), np.full(nk, -1)
+        for u in units:
+            for i in range(u["len"]):
+                assert g_src[u["key0"] + i] == -1
+                g_src[u["key0"] + i], g_pos[u["key0"] + i] = u["src"], u["pos0"] + i
+        assert np.all(g_src >= 0)
+        assert 0 < int(info.workspace_bytes) and int(info.offsets[15]) % 256 == 0
+        for it in xitems:
+            assert it["nseg"] == 1 and 1 <= it["ntok"] <= 2 * (128 // G) and it["rec"] >= 0
+            keys = np.arange(it["key0"][0], it["key0"][0] + it["nkeys"][0])
+            for t in range(it["ntok"]):
+                r = int(qsrc[it["tok0"] + t])
+                assert np.all(g_pos[keys] <= it["qpos0"] + t)  # unmasked: the span precedes the query
+                cover[r][it["g"], g_pos[keys]] += 1
+                recs_seen.setdefault(r, set()).add(int(rec_list[it["rec"] + t]))
     for r in range(B):
         assert np.all(cover[r] == 1), r
     merged = {int(m["out_row"]): m for m in merges}
@@ -90,6 +115,27 @@ def test_decode_plan_with_cascade():
     # G = 4: 4 member requests per span item, both KV heads in one item -> 2 + 1 span items
     assert plan.info.num_span_items == 3
     assert sum(1 for it in items if it["mode"] == 0) == 3
+
+
+@pytest.mark.parametrize("G", [1, 4, 8])
+def test_decode_plan_tensor_spans(G):
+    # a 700-key span shared by 40 requests (tensor-core path), a nested 300-key span shared by
+    # 14 of them (tensor-core path) and a 100-key span shared by 3 (decode kernel)
+    rng = np.random.default_rng(3)
+    B = 45
+    seq = (1000 + rng.integers(1, 400, size=B)).astype(np.int32)
+    span_req = np.array([0, 0, 40], np.int32)
+    span_start = np.array([0, 700, 0], np.int32)
+    span_len = np.array([700, 300, 100], np.int32)
+    grp = [list(range(40)), list(range(14)), [40, 41, 42]]
+    casc = pkv.Cascade(span_req=span_req, span_start=span_start, span_len=span_len,
+                       grp_indptr=np.cumsum([0] + [len(g) for g in grp]).astype(np.int32),
+                       grp_req=np.concatenate(grp).astype(np.int32))
+    plan = pkv.plan_decode(seq, 8 * G, 8, 128, casc)
+    _decode_cover(plan, seq, 8)
+    info = plan.info
+    assert int(info.offsets[8]) > 0 and int(info.offsets[11]) == 1000  # both big spans gathered once
+    assert int(info.offsets[13]) == 40 + 14
 
 
 @pytest.mark.parametrize("hq,hkv", [(32, 8), (48, 12), (16, 16), (8, 1), (64, 8)])

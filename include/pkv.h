@@ -194,6 +194,13 @@ int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, const void *q,
  * PKV_E_DEVICE with the raw word in *raw when raw != NULL). */
 int pkv_get_device_error(void *workspace, void *stream, int32_t *raw);
 
+/* Measurement hook (no counterpart in the pages: it exists so a benchmark can time the
+ * tensor-core kernel alone).  The next pkv_attn_extend call records the CUDA event `start`
+ * on its stream right before its attention kernel and `stop` right after it -- after the
+ * key gather, before the merge -- and then clears the hook.  start, stop: cudaEvent_t
+ * handles owned by the caller; NULL, NULL clears it.  Process-wide, not thread-safe. */
+int pkv_set_kernel_events(void *start, void *stop);
+
 /* pkv_attn_decode for callers that cannot allocate device memory (no counterpart in the
  * pages: it exists for embedding).  Some callers have no workspace to pass at call time --
  * a serving loop that froze its device-memory budget after start-up, or a host program

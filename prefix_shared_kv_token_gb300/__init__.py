@@ -28,7 +28,7 @@ from ._lib import (PKV_BF16, PKV_FP8_E4M3, PkvBatch, PkvCascade, PkvError, PkvPl
                    check, lib)
 
 __all__ = ["Pool", "Batch", "Plan", "Cascade", "kv_store", "plan_decode", "plan_extend", "attn_decode",
-           "attn_extend", "get_device_error", "RadixTree", "Allocator", "PkvError", "version"]
+           "attn_extend", "get_device_error", "set_kernel_events", "RadixTree", "Allocator", "PkvError", "version"]
 
 
 def version() -> int:
@@ -196,6 +196,18 @@ def get_device_error(workspace, stream=None) -> int:
     if rc not in (0, -7):
         check("pkv_get_device_error", rc)
     return raw.value
+
+
+def set_kernel_events(start=None, stop=None) -> None:
+    """Times the attention kernel of the next attn_extend call alone: ``start`` / ``stop``
+    (torch.cuda.Event with timing enabled) are recorded right before and after it."""
+    def handle(ev):
+        if ev is None:
+            return None
+        if not ev.cuda_event:       # torch creates the CUDA event on its first record
+            ev.record()
+        return C.c_void_p(ev.cuda_event)
+    check("pkv_set_kernel_events", lib.pkv_set_kernel_events(handle(start), handle(stop)))
 
 
 # ----------------------------------------------------------------------------------------

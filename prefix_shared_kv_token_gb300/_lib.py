@@ -71,6 +71,7 @@ SIGNATURES = {
     "pkv_attn_extend": (C.c_int, [C.POINTER(PkvPool), C.POINTER(PkvBatch), _P, _P, _F, C.POINTER(PkvPlanInfo), _P,
                                   _P, _SZ, _P]),
     "pkv_get_device_error": (C.c_int, [_P, _P, _PI32]),
+    "pkv_set_kernel_events": (C.c_int, [_P, _P]),
     "pkv_attn_decode_noalloc": (C.c_int, [C.POINTER(PkvPool), C.POINTER(PkvBatch), _P, _P, _F,
                                           C.POINTER(PkvPlanInfo), _P, _P]),
     "pkv_tree_new": (_P, []),

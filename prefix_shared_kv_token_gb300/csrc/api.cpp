@@ -49,6 +49,8 @@ CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType dtype, cuuint32_t ra
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+void *g_kernel_events[2] = {nullptr, nullptr};
+
 }  // namespace pkv
 
 extern "C" {
@@ -69,6 +71,13 @@ const char *pkv_strerror(int code) {
 }
 
 int pkv_version(void) { return 100; }
+
+int pkv_set_kernel_events(void *start, void *stop) {
+    if ((start == nullptr) != (stop == nullptr)) return PKV_E_INVALID;
+    pkv::g_kernel_events[0] = start;
+    pkv::g_kernel_events[1] = stop;
+    return PKV_OK;
+}
 
 int pkv_get_device_error(void *workspace, void *stream, int32_t *raw) {
     if (!workspace) return PKV_E_INVALID;

@@ -475,7 +475,9 @@ __global__ void __launch_bounds__(288, (D == 64 ? 2 : 1)) decode_kernel(const De
 }
 
 // Combine partial states: o = sum_k 2^(m_k - M) acc_k / sum_k 2^(m_k - M) l_k.  One warp per
-// (row, query head); each lane owns D / 32 consecutive elements.
+// (row, query head); each lane owns D / 32 consecutive elements.  One pass over the records,
+// four at a time with all their loads in flight, rescaling the running sums when the
+// maximum grows.
 template <int D>
 __global__ void __launch_bounds__(256) merge_kernel(const MergeItem *__restrict__ merges, const float *__restrict__ rec_acc,
                                                     const float *__restrict__ rec_ml, uint16_t *__restrict__ o, int hq) {
@@ -483,33 +485,50 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeItem *__restrict_
     const int h = blockIdx.y * 8 + (threadIdx.x >> 5);
     if (h >= hq) return;
     const int lane = threadIdx.x & 31;
-    constexpr int V = D / 32;
-    float M = -INFINITY;
-    for (int k = 0; k < mi.nrec; ++k) M = fmaxf(M, rec_ml[((int64_t)(mi.rec0 + k * mi.rec_stride) * hq + h) * 2]);
-    const float Mu = M == -INFINITY ? 0.f : M;
-    float L = 0.f, O[V];
+    constexpr int V = D / 32, B = 4;
+    float M = -INFINITY, L = 0.f, O[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) O[v] = 0.f;
-#pragma unroll 4
-    for (int k = 0; k < mi.nrec; ++k) {
-        const int64_t rb = (int64_t)(mi.rec0 + k * mi.rec_stride) * hq + h;
-        const float2 ml = *reinterpret_cast<const float2 *>(rec_ml + rb * 2);
-        const float wt = ex2(ml.x - Mu);
-        L += ml.y * wt;
-        float a[V];
-        if constexpr (V == 4) {
-            const float4 x = *reinterpret_cast<const float4 *>(rec_acc + rb * D + lane * 4);
-            a[0] = x.x;
-            a[1] = x.y;
-            a[2] = x.z;
-            a[3] = x.w;
-        } else {
-            const float2 x = *reinterpret_cast<const float2 *>(rec_acc + rb * D + lane * 2);
-            a[0] = x.x;
-            a[1] = x.y;
-        }
+    for (int k0 = 0; k0 < mi.nrec; k0 += B) {
+        float2 ml[B];
+        float a[B][V];
 #pragma unroll
-        for (int v = 0; v < V; ++v) O[v] += a[v] * wt;
+        for (int j = 0; j < B; ++j) {
+            ml[j] = make_float2(-INFINITY, 0.f);
+#pragma unroll
+            for (int v = 0; v < V; ++v) a[j][v] = 0.f;
+            if (k0 + j < mi.nrec) {
+                const int64_t rb = (int64_t)(mi.rec0 + (k0 + j) * mi.rec_stride) * hq + h;
+                ml[j] = __ldg(reinterpret_cast<const float2 *>(rec_ml + rb * 2));
+                if constexpr (V == 4) {
+                    const float4 x = __ldg(reinterpret_cast<const float4 *>(rec_acc + rb * D + lane * 4));
+                    a[j][0] = x.x;
+                    a[j][1] = x.y;
+                    a[j][2] = x.z;
+                    a[j][3] = x.w;
+                } else {
+                    const float2 x = __ldg(reinterpret_cast<const float2 *>(rec_acc + rb * D + lane * 2));
+                    a[j][0] = x.x;
+                    a[j][1] = x.y;
+                }
+            }
+        }
+        float mb = M;
+#pragma unroll
+        for (int j = 0; j < B; ++j) mb = fmaxf(mb, ml[j].x);
+        if (mb == -INFINITY) continue;  // nothing seen yet (records of empty ranges)
+        const float alpha = ex2(M - mb);  // 0 when M is -inf
+        L *= alpha;
+#pragma unroll
+        for (int v = 0; v < V; ++v) O[v] *= alpha;
+#pragma unroll
+        for (int j = 0; j < B; ++j) {
+            const float wt = ex2(ml[j].x - mb);  // 0 for padding entries
+            L += ml[j].y * wt;
+#pragma unroll
+            for (int v = 0; v < V; ++v) O[v] += a[j][v] * wt;
+        }
+        M = mb;
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     uint32_t *dst = reinterpret_cast<uint32_t *>(o + ((int64_t)mi.out_row * hq + h) * D + lane * V);

@@ -717,8 +717,12 @@ extern "C" int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, con
     p.rec_acc = rec_acc;
     p.rec_ml = rec_ml;
     p.rec_list = nullptr;
+    void *ev0 = g_kernel_events[0], *ev1 = g_kernel_events[1];
+    g_kernel_events[0] = g_kernel_events[1] = nullptr;
+    if (ev0 && cudaEventRecord(static_cast<cudaEvent_t>(ev0), s) != cudaSuccess) return PKV_E_CUDA;
     rc = D == 128 ? dispatch_extend<128>(G, p, qm, km, vm, info->num_items, s)
                   : dispatch_extend<64>(G, p, qm, km, vm, info->num_items, s);
     if (rc) return rc;
+    if (ev1 && cudaEventRecord(static_cast<cudaEvent_t>(ev1), s) != cudaSuccess) return PKV_E_CUDA;
     return launch_merge(info, plan_dev, rec_acc, rec_ml, p.o, s);
 }

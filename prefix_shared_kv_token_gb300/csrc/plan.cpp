@@ -43,6 +43,13 @@ constexpr int32_t kTensorMinMembers = 12;
 constexpr int32_t kTensorMinKeys = 256;
 size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
+// Keys per gather unit (one CTA each): up to 32, fewer when the gather is small, so that it
+// still spreads over about 4 CTAs per SM.
+int32_t gather_unit_keys(int64_t total_keys, int32_t num_sms) {
+    const int64_t per = (total_keys + 4 * (int64_t)num_sms - 1) / (4 * (int64_t)num_sms);
+    return (int32_t)std::min<int64_t>(32, std::max<int64_t>(4, per));
+}
+
 int check_heads(int32_t hq, int32_t hkv, int32_t d) {
     if (hq <= 0 || hkv <= 0 || hq % hkv) return PKV_E_INVALID;
     int32_t G = hq / hkv;
@@ -199,8 +206,7 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
             const int32_t m0 = cascade->grp_indptr[s], m1 = cascade->grp_indptr[s + 1];
             if (sp_tensor[s]) {
                 const int32_t key0 = (int32_t)nkeys, q0 = (int32_t)qsrc.size();
-                for (int32_t c = 0; c < len; c += 32)
-                    units.push_back({cascade->span_req[s], st + c, std::min(32, len - c), key0 + c});
+                units.push_back({cascade->span_req[s], st, len, key0});  // split into units below
                 nkeys += len;
                 for (int32_t i = m0; i < m1; ++i) qsrc.push_back(cascade->grp_req[i]);
                 for (int32_t c0 = 0; c0 < len; c0 += sp_chunk[s]) {
@@ -305,6 +311,13 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
     if (n_items == 0) cta_off.push_back(0);
 
     if (nkeys >= ((int64_t)1 << 31)) return PKV_E_UNSUPPORTED;
+    {
+        const int32_t uk = gather_unit_keys(nkeys, num_sms);
+        std::vector<GatherUnit> runs;
+        runs.swap(units);
+        for (const GatherUnit &R : runs)
+            for (int32_t c = 0; c < R.len; c += uk) units.push_back({R.src, R.pos0 + c, std::min(uk, R.len - c), R.key0 + c});
+    }
     std::stable_sort(xitems.begin(), xitems.end(), [](const ExtendItem &x, const ExtendItem &y) {
         return (int64_t)x.nkeys[0] * x.ntok > (int64_t)y.nkeys[0] * y.ntok;
     });
@@ -360,7 +373,7 @@ extern "C" int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int
                                const int32_t *qo_indptr, int32_t num_q_heads, int32_t num_kv_heads,
                                int32_t head_dim, const pkv_cascade *cascade, const pkv_plan_opts *opts,
                                void *plan, size_t plan_cap, pkv_plan_info *info) {
-    (void)opts;
+    const int32_t num_sms = (opts && opts->num_sms > 0) ? opts->num_sms : 152;
     if (!info || batch < 0 || (batch > 0 && (!seq_lens || !extend_lens || !qo_indptr))) return PKV_E_INVALID;
     int rc = check_heads(num_q_heads, num_kv_heads, head_dim);
     if (rc) return rc;
@@ -422,8 +435,9 @@ extern "C" int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int
     }
     if (nkeys >= ((int64_t)1 << 31)) return PKV_E_UNSUPPORTED;
     std::vector<GatherUnit> units;
+    const int32_t uk = gather_unit_keys(nkeys, num_sms);
     for (const Run &R : runs)
-        for (int32_t c = 0; c < R.len; c += 32) units.push_back({R.src, R.pos0 + c, std::min(32, R.len - c), R.key0 + c});
+        for (int32_t c = 0; c < R.len; c += uk) units.push_back({R.src, R.pos0 + c, std::min(uk, R.len - c), R.key0 + c});
 
     // items: up to 2 x 128/G query tokens of one request x one KV head, over its segments;
     // the last segment is cut at the last query token's position (causal)

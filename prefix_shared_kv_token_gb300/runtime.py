@@ -82,6 +82,17 @@ class Call:
         self.store(stream)
         self.attend(stream)
 
+    def launches(self) -> int:
+        """Kernels one run() launches: the store, then the attention call's kernels."""
+        info = self.plan.info
+        n = 1 if self.out_cache_loc.numel() > 0 else 0
+        if self.kind == "extend":
+            n += (1 if info.offsets[5] > 0 else 0) + 1           # key gather, extend kernel
+        else:
+            n += 3 if info.offsets[8] > 0 else 0                  # tensor-core spans: gathers + kernel
+            n += 1 if info.num_items > 0 else 0                   # decode kernel
+        return n + (1 if info.num_merge > 0 else 0)
+
     # ---- end-to-end variant: inputs from pinned host buffers, output back to the host
     def pin_host(self):
         h = self.host

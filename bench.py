@@ -107,9 +107,10 @@ class ClockSampler:
 
 
 def kernel_hash(kind):
-    src = {"extend": "attn_extend.cu", "decode": "attn_decode.cu", "store": "kv_store.cu"}[kind]
+    # the sources of every kernel the measured region runs (decode also runs the extend kernel)
+    srcs = {"extend": ("attn_extend.cu",), "decode": ("attn_decode.cu", "attn_extend.cu"), "store": ("kv_store.cu",)}
     h = hashlib.sha256()
-    for f in (src, "common.cuh"):
+    for f in srcs[kind] + ("common.cuh",):
         with open(os.path.join(ROOT, "prefix_shared_kv_token_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

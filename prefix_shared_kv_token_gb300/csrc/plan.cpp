@@ -132,8 +132,8 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
     for (int32_t r = 0; r < batch; ++r)
         if (seq_lens[r] < 1) return PKV_E_INVALID;
     const int32_t G = num_q_heads / num_kv_heads;
-    const int32_t chunk = (opts && opts->chunk_keys > 0) ? opts->chunk_keys : 256;
-    const int32_t span_chunk = (opts && opts->span_chunk > 0) ? opts->span_chunk : 1024;
+    int32_t chunk = (opts && opts->chunk_keys > 0) ? opts->chunk_keys : 256;
+    int32_t span_chunk = (opts && opts->span_chunk > 0) ? opts->span_chunk : 1024;
     const int32_t num_sms = (opts && opts->num_sms > 0) ? opts->num_sms : 152;
     const bool dyn_tail = opts && opts->dynamic_tail;
     const int32_t R = 16 / G;  // requests per span item: one 16-row MMA tile per KV head
@@ -164,6 +164,24 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
             1, std::min<int64_t>((num_sms + per_chunk - 1) / per_chunk, (len + 511) / 512));
         sp_chunk[s] = ((len + nch - 1) / nch + 127) / 128 * 128;
         for (int32_t i = cascade->grp_indptr[s]; i < cascade->grp_indptr[s + 1]; ++i) in_tensor[cascade->grp_req[i]] = 1;
+    }
+
+    // A small batch is cut finer (default chunk sizes only): the decode kernel's keys, span
+    // re-reads included, are split into about two items per persistent CTA, at least 64
+    // keys each.
+    {
+        int64_t work = 0;
+        for (int32_t r = 0; r < batch; ++r) work += seq_lens[r] - tail_start[r];
+        for (int32_t s = 0; s < nspans; ++s)
+            if (!sp_tensor[s])
+                work += (int64_t)cascade->span_len[s] *
+                        ((cascade->grp_indptr[s + 1] - cascade->grp_indptr[s] + R - 1) / R);
+        const int64_t target = 2 * (int64_t)num_sms * decode_ctas_per_sm(hg, head_dim) / (num_kv_heads / hg);
+        const int32_t fine = (int32_t)std::max<int64_t>(64, ((work + target - 1) / std::max<int64_t>(target, 1) + 15) / 16 * 16);
+        if (!(opts && opts->chunk_keys > 0)) chunk = std::min(chunk, fine);
+        if (!(opts && opts->span_chunk > 0))
+            for (int32_t s = 0; s < nspans; ++s)
+                if (!sp_tensor[s]) sp_chunk[s] = std::min(span_chunk, fine);
     }
 
     // records per request: its span chunks (in path order), then its tail chunks
@@ -237,8 +255,8 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
                 }
                 continue;
             }
-            for (int32_t c0 = 0; c0 < len; c0 += span_chunk) {
-                const int32_t c1 = std::min(len, c0 + span_chunk);
+            for (int32_t c0 = 0; c0 < len; c0 += sp_chunk[s]) {
+                const int32_t c1 = std::min(len, c0 + sp_chunk[s]);
                 for (int32_t a = m0; a < m1; a += R) {
                     const int32_t b = std::min(m1, a + R);
                     const int32_t off = (int32_t)row_req.size();

@@ -110,7 +110,7 @@ def test_decode_plan_with_cascade():
     casc = pkv.Cascade(span_req=np.array([0, 1], np.int32), span_start=np.array([0, 100], np.int32),
                        span_len=np.array([100, 30], np.int32), grp_indptr=np.array([0, 6, 9], np.int32),
                        grp_req=np.array([0, 1, 2, 3, 4, 5, 0, 1, 2], np.int32))
-    plan = pkv.plan_decode(seq, 8, 2, 64, casc)
+    plan = pkv.plan_decode(seq, 8, 2, 64, casc, {"span_chunk": 4096, "chunk_keys": 256})
     items = _decode_cover(plan, seq, 2)
     # G = 4: 4 member requests per span item, both KV heads in one item -> 2 + 1 span items
     assert plan.info.num_span_items == 3
@@ -146,6 +146,16 @@ def test_decode_plan_head_groups(hq, hkv):
     _decode_cover(plan, seq, hkv)
     hg = int(plan.info.offsets[6])
     assert hg == max(h for h in (1, 2, 4, 8) if hkv % h == 0)
+
+
+def test_decode_plan_cuts_small_batches_finer():
+    # 64 requests x 300 unshared keys: 256-key chunks would leave most CTAs idle
+    seq = np.full(64, 300, np.int32)
+    plan = pkv.plan_decode(seq, 32, 8, 128, None)
+    items = _decode_cover(plan, seq, 8)
+    assert len(items) >= 2 * 152 * 0.9 and (items["k1"] - items["k0"]).max() < 256
+    big = pkv.plan_decode(seq, 32, 8, 128, None, {"chunk_keys": 256})   # explicit size is kept
+    assert (_decode_cover(big, seq, 8)["k1"] - _decode_cover(big, seq, 8)["k0"]).max() == 256
 
 
 def test_decode_plan_balances_ctas():

@@ -144,7 +144,7 @@ typedef struct pkv_plan_info {
     int32_t total_q;           /* query tokens in the call                                  */
     size_t  plan_bytes;        /* size of the plan blob                                     */
     size_t  workspace_bytes;   /* device workspace the call needs (>= 256)                  */
-    int64_t offsets[16];       /* byte offsets and counts of the blob's sections (internal) */
+    int64_t offsets[24];       /* byte offsets and counts of the blob's sections (internal) */
 } pkv_plan_info;
 
 /* Decode plan: one query token per request, at position seq_lens[r] - 1, attending to the

@@ -47,7 +47,7 @@ class PkvPlanInfo(C.Structure):
     _fields_ = [("op", C.c_int32), ("batch", C.c_int32), ("num_q_heads", C.c_int32), ("num_kv_heads", C.c_int32),
                 ("head_dim", C.c_int32), ("num_items", C.c_int32), ("num_span_items", C.c_int32),
                 ("num_records", C.c_int32), ("num_merge", C.c_int32), ("total_q", C.c_int32),
-                ("plan_bytes", C.c_size_t), ("workspace_bytes", C.c_size_t), ("offsets", C.c_int64 * 16)]
+                ("plan_bytes", C.c_size_t), ("workspace_bytes", C.c_size_t), ("offsets", C.c_int64 * 24)]
 
 
 _P = C.c_void_p

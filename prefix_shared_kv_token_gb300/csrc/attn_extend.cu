@@ -55,6 +55,7 @@ struct ExtendParams {
     float v_scale;
     const ExtendItem *items;
     int32_t num_items;
+    const int32_t *cta_off;   // items of CTA b: [cta_off[b], cta_off[b + 1])
     float *rec_acc;
     float *rec_ml;
     const int32_t *rec_list;  // NULL: token t of an item writes record rec + t; else rec_list[rec + t]
@@ -231,8 +232,8 @@ PKV_DEV XItem load_item(const ExtendItem *itp, int tq) {
     return x;
 }
 
-// Persistent: one CTA per SM walks items blockIdx.x, blockIdx.x + gridDim.x, ... (the plan
-// sorts them longest first).  Tensor memory and barriers live for the whole launch; every
+// Persistent: one CTA per SM walks its own list of items (the plan deals them longest
+// first onto the least loaded CTA).  Tensor memory and barriers live for the whole launch; every
 // role keeps its own running phase counters across items.  The next item's Q load waits only
 // for the last S MMAs of the current item (qempty), and its first S MMAs may run while the
 // softmax warpgroups are still in the current item's epilogue (they read O, not S); the next
@@ -251,7 +252,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t sbase = smem_u32(smem);
     XBars *bars = reinterpret_cast<XBars *>(smem + C::kBarOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nitems = p.num_items;
+    const int i0 = __ldg(p.cta_off + blockIdx.x), i1 = __ldg(p.cta_off + blockIdx.x + 1);
 
     // once any CTA of this launch gave up on a wait, the rest exit instead of waiting too
     __shared__ int32_t s_skip;
@@ -293,7 +294,7 @@ __global__ void __launch_bounds__(384, 1)
             prefetch_tmap(&vmap);
             int tp = 0, nql = 0;  // tiles and Q loads issued by this CTA
             bool ok = true;
-            for (int i = blockIdx.x; ok && i < nitems; i += gridDim.x) {
+            for (int i = i0; ok && i < i1; ++i) {
                 const ExtendItem *itp = p.items + i;
                 const XItem it = load_item(itp, TQ);
                 if (nql > 0 && !xwait(&bars->qempty, (nql - 1) & 1, bars, p.err, 6)) break;
@@ -344,7 +345,7 @@ __global__ void __launch_bounds__(384, 1)
             int tm = 0, ip = 0;       // tiles and items before the current one
             int cp[2] = {0, 0};       // phases consumed on pfull[q]
             bool ok = true;
-            for (int i = blockIdx.x; ok && i < nitems; i += gridDim.x, ++ip) {
+            for (int i = i0; ok && i < i1; ++i, ++ip) {
                 const XItem it = load_item(p.items + i, TQ);
                 if (!xwait(&bars->q, ip & 1, bars, p.err, 1)) break;
                 auto issue_s = [&](int q, int j) -> bool {
@@ -404,7 +405,7 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t colS = tmem + lane_base + C::kColS + q * kBN;
         const uint32_t colO = tmem + lane_base + C::kColO + q * D;
         int cw = 0, co = 0;  // phases consumed on sfull[q] and ofinal[q]
-        for (int i = blockIdx.x; i < nitems; i += gridDim.x) {
+        for (int i = i0; i < i1; ++i) {
             const ExtendItem *itp = p.items + i;
             const XItem it = load_item(itp, TQ);
             if (q >= it.nq) continue;
@@ -531,13 +532,13 @@ __global__ void __launch_bounds__(384, 1)
 
 template <int D, int G>
 static int launch_extend(const ExtendParams &p, const CUtensorMap &qm, const CUtensorMap &km, const CUtensorMap &vm,
-                         int nitems, cudaStream_t s) {
+                         int nctas, cudaStream_t s) {
     constexpr int smem = XCfg<D>::kSmem;
     static_assert(smem <= 232448, "shared memory budget");
     auto kern = extend_kernel<D, G>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return PKV_E_CUDA;
-    kern<<<std::min(nitems, num_sms()), 384, smem, s>>>(p, qm, km, vm);  // persistent
+    kern<<<nctas, 384, smem, s>>>(p, qm, km, vm);  // persistent: the plan's CTA lists
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_E_CUDA;
 }
 
@@ -656,7 +657,11 @@ int decode_span_tensor(const pkv_pool *pool, const pkv_batch *batch, const void 
     p.rec_acc = rec_acc;
     p.rec_ml = rec_ml;
     p.rec_list = reinterpret_cast<const int32_t *>(plan + info->offsets[14]);
-    return D == 128 ? dispatch_extend<128>(G, p, qm, km, vm, (int)nx, s) : dispatch_extend<64>(G, p, qm, km, vm, (int)nx, s);
+    p.cta_off = reinterpret_cast<const int32_t *>(plan + info->offsets[16]);
+    const int64_t nctas = info->offsets[17];
+    if (nctas < 1 || nctas > nx) return PKV_E_PLAN;
+    return D == 128 ? dispatch_extend<128>(G, p, qm, km, vm, (int)nctas, s)
+                    : dispatch_extend<64>(G, p, qm, km, vm, (int)nctas, s);
 }
 
 }  // namespace pkv
@@ -720,8 +725,11 @@ extern "C" int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, con
     void *ev0 = g_kernel_events[0], *ev1 = g_kernel_events[1];
     g_kernel_events[0] = g_kernel_events[1] = nullptr;
     if (ev0 && cudaEventRecord(static_cast<cudaEvent_t>(ev0), s) != cudaSuccess) return PKV_E_CUDA;
-    rc = D == 128 ? dispatch_extend<128>(G, p, qm, km, vm, info->num_items, s)
-                  : dispatch_extend<64>(G, p, qm, km, vm, info->num_items, s);
+    p.cta_off = reinterpret_cast<const int32_t *>(plan + info->offsets[7]);
+    const int64_t nctas = info->offsets[8];
+    if (nctas < 1 || nctas > info->num_items) return PKV_E_PLAN;
+    rc = D == 128 ? dispatch_extend<128>(G, p, qm, km, vm, (int)nctas, s)
+                  : dispatch_extend<64>(G, p, qm, km, vm, (int)nctas, s);
     if (rc) return rc;
     if (ev1 && cudaEventRecord(static_cast<cudaEvent_t>(ev1), s) != cudaSuccess) return PKV_E_CUDA;
     return launch_merge(info, plan_dev, rec_acc, rec_ml, p.o, s);

@@ -43,6 +43,44 @@ constexpr int32_t kTensorMinMembers = 12;
 constexpr int32_t kTensorMinKeys = 256;
 size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
+// Persistent CTAs: deal items longest-processing-time-first onto the least loaded of nctas
+// CTAs (ties: lowest index); each CTA then runs its items in that (descending) order.
+// Returns the items CTA-major and the CTA ranges cta_off[nctas + 1].
+template <class T>
+void lpt_deal(const std::vector<T> &items, const std::vector<int64_t> &cost, int32_t nctas, std::vector<T> *placed,
+              std::vector<int32_t> *cta_off) {
+    const int32_t n = (int32_t)items.size();
+    std::vector<int32_t> order(n);
+    std::iota(order.begin(), order.end(), 0);
+    std::stable_sort(order.begin(), order.end(), [&](int32_t x, int32_t y) { return cost[x] > cost[y]; });
+    std::vector<std::vector<int32_t>> per_cta(nctas);
+    using Slot = std::pair<int64_t, int32_t>;  // (load, cta)
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+    for (int32_t b = 0; b < nctas; ++b) heap.push({0, b});
+    for (int32_t x : order) {
+        Slot sl = heap.top();
+        heap.pop();
+        per_cta[sl.second].push_back(x);
+        sl.first += cost[x];
+        heap.push(sl);
+    }
+    placed->clear();
+    placed->reserve(items.size());
+    cta_off->assign(1, 0);
+    for (int32_t b = 0; b < nctas; ++b) {
+        for (int32_t x : per_cta[b]) placed->push_back(items[x]);
+        cta_off->push_back((int32_t)placed->size());
+    }
+}
+
+// Extend-kernel item weight: key tiles x (1 + query tiles) -- a two-tile item overlaps one
+// tile's softmax with the other's MMAs, so it costs less than twice a one-tile item.
+int64_t extend_item_cost(const ExtendItem &x, int32_t tq) {
+    int64_t tiles = 0;
+    for (int32_t i = 0; i < x.nseg; ++i) tiles += (x.nkeys[i] + 127) / 128;
+    return tiles * (1 + (x.ntok > tq ? 2 : 1)) + 2;
+}
+
 // Keys per gather unit (one CTA each): up to 32, fewer when the gather is small, so that it
 // still spreads over about 4 CTAs per SM.
 int32_t gather_unit_keys(int64_t total_keys, int32_t num_sms) {
@@ -298,34 +336,13 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
     for (int32_t r = 0; r < batch; ++r)
         if (rec_base[r] >= 0) merges.push_back({r, rec_base[r], nrec[r], 1});
 
-    // persistent CTAs: longest-processing-time-first onto the least loaded CTA; each CTA
-    // then runs its items in that (descending) order
+    // persistent CTAs: longest-processing-time-first onto the least loaded CTA
     const int32_t n_items = (int32_t)items.size();
     const int32_t nctas = std::max<int32_t>(
         1, std::min<int64_t>(n_items, (int64_t)num_sms * decode_ctas_per_sm(hg, head_dim)));
-    std::vector<int32_t> order(n_items);
-    std::iota(order.begin(), order.end(), 0);
-    std::stable_sort(order.begin(), order.end(), [&](int32_t x, int32_t y) { return cost[x] > cost[y]; });
-    std::vector<std::vector<int32_t>> per_cta(nctas);
-    {
-        using Slot = std::pair<int64_t, int32_t>;  // (load, cta): lowest load, then lowest index
-        std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
-        for (int32_t b = 0; b < nctas; ++b) heap.push({0, b});
-        for (int32_t x : order) {
-            Slot sl = heap.top();
-            heap.pop();
-            per_cta[sl.second].push_back(x);
-            sl.first += cost[x];
-            heap.push(sl);
-        }
-    }
     std::vector<DecodeItem> placed;
-    std::vector<int32_t> cta_off(1, 0);
-    placed.reserve(items.size());
-    for (int32_t b = 0; b < nctas; ++b) {
-        for (int32_t x : per_cta[b]) placed.push_back(items[x]);
-        cta_off.push_back((int32_t)placed.size());
-    }
+    std::vector<int32_t> cta_off;
+    lpt_deal(items, cost, nctas, &placed, &cta_off);
     if (n_items == 0) cta_off.push_back(0);
 
     if (nkeys >= ((int64_t)1 << 31)) return PKV_E_UNSUPPORTED;
@@ -336,9 +353,14 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
         for (const GatherUnit &R : runs)
             for (int32_t c = 0; c < R.len; c += uk) units.push_back({R.src, R.pos0 + c, std::min(uk, R.len - c), R.key0 + c});
     }
-    std::stable_sort(xitems.begin(), xitems.end(), [](const ExtendItem &x, const ExtendItem &y) {
-        return (int64_t)x.nkeys[0] * x.ntok > (int64_t)y.nkeys[0] * y.ntok;
-    });
+    std::vector<ExtendItem> xplaced;
+    std::vector<int32_t> xcta_off;
+    const int32_t xctas = std::max<int32_t>(1, std::min<int32_t>((int32_t)xitems.size(), num_sms));
+    {
+        std::vector<int64_t> xcost;
+        for (const ExtendItem &x : xitems) xcost.push_back(extend_item_cost(x, TQ2 / 2));
+        lpt_deal(xitems, xcost, xctas, &xplaced, &xcta_off);
+    }
 
     std::memset(info, 0, sizeof(*info));
     info->op = 1;
@@ -359,21 +381,24 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
     info->offsets[4] = (int64_t)off; off = align16(off + cta_off.size() * sizeof(int32_t));
     info->offsets[5] = nctas;
     info->offsets[6] = hg;
-    info->offsets[7] = (int64_t)off; off = align16(off + xitems.size() * sizeof(ExtendItem));
-    info->offsets[8] = (int64_t)xitems.size();
+    info->offsets[7] = (int64_t)off; off = align16(off + xplaced.size() * sizeof(ExtendItem));
+    info->offsets[8] = (int64_t)xplaced.size();
     info->offsets[9] = (int64_t)off; off = align16(off + units.size() * sizeof(GatherUnit));
     info->offsets[10] = (int64_t)units.size();
     info->offsets[11] = nkeys;
     info->offsets[12] = (int64_t)off; off = align16(off + qsrc.size() * sizeof(int32_t));
     info->offsets[13] = (int64_t)qsrc.size();
     info->offsets[14] = (int64_t)off; off = align16(off + rec_list.size() * sizeof(int32_t));
+    info->offsets[16] = (int64_t)off; off = align16(off + xcta_off.size() * sizeof(int32_t));
+    info->offsets[17] = xctas;
     std::vector<uint8_t> blob(std::max<size_t>(off, 16), 0);
     put(blob, (size_t)info->offsets[0], placed);
     put(blob, (size_t)info->offsets[1], row_req);
     put(blob, (size_t)info->offsets[2], row_rec);
     put(blob, (size_t)info->offsets[3], merges);
     put(blob, (size_t)info->offsets[4], cta_off);
-    put(blob, (size_t)info->offsets[7], xitems);
+    put(blob, (size_t)info->offsets[7], xplaced);
+    put(blob, (size_t)info->offsets[16], xcta_off);
     put(blob, (size_t)info->offsets[9], units);
     put(blob, (size_t)info->offsets[12], qsrc);
     put(blob, (size_t)info->offsets[14], rec_list);
@@ -487,13 +512,14 @@ extern "C" int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int
             }
         }
     }
-    auto cost = [](const ExtendItem &x) {
-        int64_t k = 0;
-        for (int32_t i = 0; i < x.nseg; ++i) k += x.nkeys[i];
-        return k * x.ntok;
-    };
-    std::stable_sort(items.begin(), items.end(),
-                     [&](const ExtendItem &x, const ExtendItem &y) { return cost(x) > cost(y); });
+    std::vector<ExtendItem> placed;
+    std::vector<int32_t> cta_off;
+    const int32_t nctas = std::max<int32_t>(1, std::min<int32_t>((int32_t)items.size(), num_sms));
+    {
+        std::vector<int64_t> cost;
+        for (const ExtendItem &x : items) cost.push_back(extend_item_cost(x, TQ2 / 2));
+        lpt_deal(items, cost, nctas, &placed, &cta_off);
+    }
     const bool cascaded = false;
     const int32_t kmax = 1;
 
@@ -509,13 +535,16 @@ extern "C" int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int
     info->num_merge = (int32_t)merges.size();
     info->total_q = total_q;
     size_t off = 0;
-    info->offsets[0] = (int64_t)off; off = align16(off + items.size() * sizeof(ExtendItem));
+    info->offsets[0] = (int64_t)off; off = align16(off + placed.size() * sizeof(ExtendItem));
     info->offsets[3] = (int64_t)off; off = align16(off + merges.size() * sizeof(MergeItem));
     info->offsets[4] = (int64_t)off; off = align16(off + units.size() * sizeof(GatherUnit));
     info->offsets[5] = (int64_t)units.size();
     info->offsets[6] = nkeys;
+    info->offsets[7] = (int64_t)off; off = align16(off + cta_off.size() * sizeof(int32_t));
+    info->offsets[8] = nctas;
     std::vector<uint8_t> blob(std::max<size_t>(off, 16), 0);
-    put(blob, (size_t)info->offsets[0], items);
+    put(blob, (size_t)info->offsets[0], placed);
+    put(blob, (size_t)info->offsets[7], cta_off);
     put(blob, (size_t)info->offsets[3], merges);
     put(blob, (size_t)info->offsets[4], units);
     const size_t rec_bytes = (size_t)info->num_records * num_q_heads * (head_dim + 2) * 4;

@@ -35,6 +35,14 @@ def _sections(plan, dtype, n, off):
     return np.frombuffer(b[off:off + n * dtype.itemsize].tobytes(), dtype=dtype)
 
 
+def _check_cta_ranges(plan, off, nctas, nitems):
+    # persistent CTAs: contiguous per-CTA item ranges that partition the item list
+    nctas = int(nctas)
+    assert 1 <= nctas <= max(1, nitems)
+    cta = np.frombuffer(plan.blob[off:off + 4 * (nctas + 1)].tobytes(), np.int32)
+    assert cta[0] == 0 and cta[-1] == nitems and np.all(np.diff(cta) >= (1 if nitems else 0))
+
+
 def _decode_cover(plan, seq, hkv, cascade_spans=None):
     info = plan.info
     items = _sections(plan, DEC, info.num_items, info.offsets[0])
@@ -64,6 +72,7 @@ def _decode_cover(plan, seq, hkv, cascade_spans=None):
     nx, nu, nk, nq = (int(info.offsets[i]) for i in (8, 10, 11, 13))
     if nx:
         xitems = _sections(plan, EXT, nx, info.offsets[7])
+        _check_cta_ranges(plan, info.offsets[16], info.offsets[17], nx)
         units = _sections(plan, GU, nu, info.offsets[9])
         qsrc = np.frombuffer(plan.blob[info.offsets[12]:info.offsets[12] + 4 * nq].tobytes(), np.int32)
         nrl = max(int(it["rec"]) + int(it["ntok"]) for it in xitems)
@@ -202,6 +211,7 @@ def test_extend_plan_covers_causal_triangle(cascade):
     plan = pkv.plan_extend(seq, ext, qo, 32, 8, 128, casc)
     info = plan.info
     items = _sections(plan, EXT, info.num_items, info.offsets[0])
+    _check_cta_ranges(plan, info.offsets[7], info.offsets[8], info.num_items)
     units = _sections(plan, GU, info.offsets[5], info.offsets[4])
     # gathered key -> (source request, position); every gathered key is written once
     nk = int(info.offsets[6])

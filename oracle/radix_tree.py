@@ -24,6 +24,23 @@ Readings where the page leaves a step open (each is also listed in the design no
   * LRU priority is last_access_time, ties broken by node id (creation order);
   * the root is created with lock_ref = 1 (as in the page's diagram) and is never
     evicted or counted in the evictable / protected sizes.
+
+Eviction policies ("Eviction 전략": lru, lfu, slru, fifo, mru, filo, priority, with the
+node fields hit_count and priority of "핵심 자료구조: TreeNode").  The page prints only the
+LRU ordering and how priority moves on insert and split; the other orderings are the
+plainest reading of their names, smallest key evicted first, ties by node id:
+  * lru       (last_access_time)
+  * lfu       (hit_count, last_access_time)
+  * slru      (hit_count >= SLRU_PROTECT, last_access_time): the probationary segment (fewer
+              than SLRU_PROTECT hits) goes first, each segment in LRU order
+  * fifo      (node id): the node created first
+  * mru       (-last_access_time)
+  * filo      (-node id): the node created last
+  * priority  (priority, last_access_time): lowest priority first
+hit_count: every node on the path a match_prefix returns (root excluded) gains one hit,
+counted after any split.  priority: an insert raises its start node's priority to at least
+its own and gives it to the leaf it creates; a split's upper part takes the child's
+priority (as printed in "노드 분할"); new nodes otherwise start at 0 hits.
 """
 
 from __future__ import annotations
@@ -31,8 +48,12 @@ from __future__ import annotations
 import heapq
 
 
+POLICIES = ("lru", "lfu", "slru", "fifo", "mru", "filo", "priority")
+SLRU_PROTECT = 2  # hits that move a node into SLRU's protected segment
+
+
 class TreeNode:
-    def __init__(self, node_id: int, now: int):
+    def __init__(self, node_id: int, now: int, priority: int = 0):
         self.id = node_id
         self.children: dict[int, "TreeNode"] = {}
         self.parent: TreeNode | None = None
@@ -40,6 +61,27 @@ class TreeNode:
         self.value: list[int] = []
         self.lock_ref = 0
         self.last_access_time = now
+        self.hit_count = 0
+        self.priority = priority
+
+
+def eviction_key(policy: str, n: TreeNode):
+    """Heap key of an evictable leaf under ``policy`` (smallest evicted first)."""
+    if policy == "lru":
+        return (n.last_access_time, n.id)
+    if policy == "lfu":
+        return (n.hit_count, n.last_access_time, n.id)
+    if policy == "slru":
+        return (1 if n.hit_count >= SLRU_PROTECT else 0, n.last_access_time, n.id)
+    if policy == "fifo":
+        return (n.id,)
+    if policy == "mru":
+        return (-n.last_access_time, n.id)
+    if policy == "filo":
+        return (-n.id,)
+    if policy == "priority":
+        return (n.priority, n.last_access_time, n.id)
+    raise ValueError(policy)
 
 
 def _key_match(a, b) -> int:
@@ -53,7 +95,10 @@ def _key_match(a, b) -> int:
 
 
 class RadixCache:
-    def __init__(self):
+    def __init__(self, policy: str = "lru"):
+        if policy not in POLICIES:
+            raise ValueError(policy)
+        self.policy = policy
         self._next_id = 0
         self.clock = 0
         self.root = self._new_node()
@@ -61,8 +106,8 @@ class RadixCache:
         self.evictable_size_ = 0
         self.protected_size_ = 0
 
-    def _new_node(self) -> TreeNode:
-        n = TreeNode(self._next_id, self.clock)
+    def _new_node(self, priority: int = 0) -> TreeNode:
+        n = TreeNode(self._next_id, self.clock, priority)
         self._next_id += 1
         return n
 
@@ -86,10 +131,14 @@ class RadixCache:
             values.extend(child.value)
             node = child
             key = key[n:]
+        hit = node
+        while hit is not self.root:
+            hit.hit_count += 1
+            hit = hit.parent
         return values, node
 
     def _split_node(self, key, child: TreeNode, split_len: int) -> TreeNode:
-        upper = self._new_node()
+        upper = self._new_node(child.priority)
         upper.children = {key[split_len]: child}
         upper.parent = child.parent
         upper.lock_ref = child.lock_ref
@@ -102,7 +151,7 @@ class RadixCache:
         return upper
 
     # ---- insert ------------------------------------------------------------------
-    def insert(self, key, value) -> int:
+    def insert(self, key, value, priority: int = 0) -> int:
         """Insert ``key`` -> ``value``; returns how many leading tokens were already cached
         (the caller frees those entries of ``value``, they duplicate cached slots)."""
         assert len(key) == len(value)
@@ -110,6 +159,7 @@ class RadixCache:
         key, value = list(key), list(value)
         node = self.root
         node.last_access_time = self.clock
+        node.priority = max(node.priority, priority)
         total = 0
         while key and key[0] in node.children:
             node = node.children[key[0]]
@@ -119,7 +169,7 @@ class RadixCache:
             if n < len(node.key):
                 node = self._split_node(node.key, node, n)
         if key:
-            leaf = self._new_node()
+            leaf = self._new_node(priority)
             leaf.parent = node
             leaf.key = key
             leaf.value = value
@@ -137,21 +187,22 @@ class RadixCache:
         return out
 
     def evict(self, num_tokens: int):
-        """Free at least ``num_tokens`` slots from unlocked leaves, least recently used
-        first; returns the freed slot values in the order they were freed."""
-        heap = [(n.last_access_time, n.id, n) for n in self._all_nodes()
+        """Free at least ``num_tokens`` slots from unlocked leaves in the policy's order
+        (LRU: least recently used first); returns the freed slot values in the order they
+        were freed."""
+        heap = [(eviction_key(self.policy, n), n) for n in self._all_nodes()
                 if n is not self.root and not n.children and n.lock_ref == 0]
         heapq.heapify(heap)
         freed, evicted = [], 0
         while evicted < num_tokens and heap:
-            _, _, x = heapq.heappop(heap)
+            _, x = heapq.heappop(heap)
             freed.extend(x.value)
             evicted += len(x.value)
             parent = x.parent
             del parent.children[x.key[0]]
             self.evictable_size_ -= len(x.key)
             if not parent.children and parent.lock_ref == 0:
-                heapq.heappush(heap, (parent.last_access_time, parent.id, parent))
+                heapq.heappush(heap, (eviction_key(self.policy, parent), parent))
         return freed
 
     # ---- locking -----------------------------------------------------------------

@@ -230,8 +230,31 @@ int pkv_attn_decode_noalloc(const pkv_pool *pool, const pkv_batch *batch, const 
 
 typedef struct pkv_tree pkv_tree;
 
+/* A new tree evicts least recently used first (PKV_EVICT_LRU). */
 pkv_tree *pkv_tree_new(void);
 void pkv_tree_free(pkv_tree *t);
+
+/* Eviction policies ([RC] "Eviction 전략" names lru, lfu, slru, fifo, mru, filo and
+ * priority, and gives nodes a hit_count and a priority; [RC] "핵심 자료구조: TreeNode").
+ * The page prints only the LRU order; each other order is the plainest reading of its
+ * name.  Smallest key first, ties by node id:
+ *   LRU (last access) | LFU (hits, last access) | SLRU (hits >= 2, last access: nodes with
+ *   fewer than 2 hits go first) | FIFO (node id: created first) | MRU (-last access) |
+ *   FILO (-node id) | PRIORITY (priority, last access: lowest priority first).
+ * Hits: every node of the path a match_prefix returns gains one (after any split). */
+enum {
+    PKV_EVICT_LRU = 0,
+    PKV_EVICT_LFU = 1,
+    PKV_EVICT_SLRU = 2,
+    PKV_EVICT_FIFO = 3,
+    PKV_EVICT_MRU = 4,
+    PKV_EVICT_FILO = 5,
+    PKV_EVICT_PRIORITY = 6
+};
+
+/* Select the order later pkv_tree_evict calls use (any time; PKV_E_UNSUPPORTED for an
+ * unknown policy). */
+int pkv_tree_set_policy(pkv_tree *t, int policy);
 
 /* Longest cached prefix of key[0..n) ([RC] "프리픽스 매칭"): writes its slots to values
  * (up to values_cap of them), the matched length to *matched and the last node on the
@@ -246,7 +269,13 @@ int pkv_tree_match_prefix(pkv_tree *t, const int32_t *key, int64_t n, int32_t *v
 int pkv_tree_insert(pkv_tree *t, const int32_t *key, const int32_t *value, int64_t n,
                     int64_t *prefix_len);
 
-/* Evict unlocked leaves, least recently used first, until at least num_tokens slots are
+/* pkv_tree_insert with a priority ([RC] "삽입": the start node's priority is raised to at
+ * least `priority` and a created leaf gets it; "노드 분할": a split's upper part keeps the
+ * child's priority).  pkv_tree_insert is this call with priority 0. */
+int pkv_tree_insert_priority(pkv_tree *t, const int32_t *key, const int32_t *value, int64_t n,
+                             int64_t priority, int64_t *prefix_len);
+
+/* Evict unlocked leaves in the tree's policy order (least recently used first by default) until at least num_tokens slots are
  * freed or nothing is evictable ([RC] "Eviction 전략").  A parent that becomes an unlocked
  * leaf joins the candidates.  Freed slots go to freed[0 .. *num_freed) in eviction order
  * (PKV_E_WORKSPACE if freed_cap is too small; nothing is evicted then). */
@@ -261,8 +290,9 @@ int pkv_tree_dec_lock_ref(pkv_tree *t, int64_t node, int64_t *delta);
 int pkv_tree_sizes(pkv_tree *t, int64_t *evictable, int64_t *protected_size,
                    int64_t *total, int64_t *num_nodes);
 
-/* Canonical dump for tests: per live node in id order, 6 + 2*len int64 entries
- * (id, parent id, lock_ref, last_access_time, len, num_children, key[len], value[len]).
+/* Canonical dump for tests: per live node in id order, 8 + 2*len int64 entries
+ * (id, parent id, lock_ref, last_access_time, len, num_children, hit_count, priority,
+ * key[len], value[len]).
  * *used gets the entries needed; PKV_E_WORKSPACE when cap is smaller (nothing written). */
 int pkv_tree_dump(pkv_tree *t, int64_t *out, int64_t cap, int64_t *used);
 

@@ -215,10 +215,17 @@ def set_kernel_events(start=None, stop=None) -> None:
 
 
 class RadixTree:
-    def __init__(self):
+    POLICIES = ("lru", "lfu", "slru", "fifo", "mru", "filo", "priority")   # = PKV_EVICT_* order
+
+    def __init__(self, policy: str = "lru"):
         self._h = lib.pkv_tree_new()
         if not self._h:
             raise MemoryError("pkv_tree_new")
+        if policy != "lru":
+            self.set_policy(policy)
+
+    def set_policy(self, policy: str) -> None:
+        check("pkv_tree_set_policy", lib.pkv_tree_set_policy(self._h, self.POLICIES.index(policy)))
 
     def __del__(self):
         if getattr(self, "_h", None):
@@ -233,11 +240,12 @@ class RadixTree:
                                                                  C.byref(matched), C.byref(last)))
         return out[:matched.value], last.value
 
-    def insert(self, key, value) -> int:
+    def insert(self, key, value, priority: int = 0) -> int:
         key, value = _i32(key), _i32(value)
         assert len(key) == len(value)
         n = C.c_int64(0)
-        check("pkv_tree_insert", lib.pkv_tree_insert(self._h, _ptr(key), _ptr(value), len(key), C.byref(n)))
+        check("pkv_tree_insert_priority", lib.pkv_tree_insert_priority(self._h, _ptr(key), _ptr(value), len(key),
+                                                                       int(priority), C.byref(n)))
         return n.value
 
     def sizes(self):
@@ -263,18 +271,19 @@ class RadixTree:
         return d.value
 
     def dump(self):
-        """[(id, parent, lock_ref, time, key tuple, value tuple, num_children)] in id order."""
+        """[(id, parent, lock_ref, time, key tuple, value tuple, num_children, hit_count, priority)]
+        in id order."""
         used = C.c_int64(0)
         check("pkv_tree_dump", lib.pkv_tree_dump(self._h, None, 0, C.byref(used)))
         buf = np.zeros(max(used.value, 1), dtype=np.int64)
         check("pkv_tree_dump", lib.pkv_tree_dump(self._h, _ptr(buf), len(buf), C.byref(used)))
         rows, i = [], 0
         while i < used.value:
-            nid, par, lock, t, n, nch = (int(x) for x in buf[i:i + 6])
-            key = tuple(int(x) for x in buf[i + 6:i + 6 + n])
-            val = tuple(int(x) for x in buf[i + 6 + n:i + 6 + 2 * n])
-            rows.append((nid, par, lock, t, key, val, nch))
-            i += 6 + 2 * n
+            nid, par, lock, t, n, nch, hits, prio = (int(x) for x in buf[i:i + 8])
+            key = tuple(int(x) for x in buf[i + 8:i + 8 + n])
+            val = tuple(int(x) for x in buf[i + 8 + n:i + 8 + 2 * n])
+            rows.append((nid, par, lock, t, key, val, nch, hits, prio))
+            i += 8 + 2 * n
         return rows
 
     def cascade(self, last_nodes, min_group: int = 2) -> Cascade:

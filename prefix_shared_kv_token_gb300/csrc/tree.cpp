@@ -15,11 +15,21 @@
 // per match_prefix / insert; the insert walk only stamps the node it starts from and the
 // nodes it creates; LRU ties break by node id; the root starts with lock_ref 1.
 //
+// Eviction policies ("Eviction 전략": lru, lfu, slru, fifo, mru, filo, priority, using the
+// node fields hit_count and priority).  Only the LRU order and how priority moves on insert
+// and split are printed; the rest is the plainest reading of each name, smallest key first,
+// ties by node id: lru (last access), lfu (hits, last access), slru (hits >= 2, last access:
+// the probationary segment first), fifo (id), mru (-last access), filo (-id), priority
+// (priority, last access).  A match_prefix adds one hit to every node of the path it
+// returns (after any split); an insert raises its start node's priority to its own and gives
+// it to the leaf it creates; a split's upper part takes the child's priority.
+//
 // The cascade extraction (pkv_tree_cascade) turns the nodes shared by several requests of a
 // batch into spans for the attention kernels: the tree already knows which prefix KV is
 // shared ("Radix Tree 구조도": both branches under [1,2,3] share its KV).
 
 #include <algorithm>
+#include <array>
 #include <cstdint>
 #include <cstring>
 #include <deque>
@@ -40,8 +50,12 @@ struct Node {
     std::vector<int32_t> value;
     int64_t lock_ref = 0;
     int64_t last_access_time = 0;
+    int64_t hit_count = 0;
+    int64_t priority = 0;
     bool alive = true;
 };
+
+constexpr int64_t kSlruProtect = 2;  // hits that move a node into SLRU's protected segment
 
 }  // namespace
 
@@ -51,6 +65,7 @@ struct pkv_tree {
     int64_t evictable = 0;
     int64_t protected_ = 0;
     int64_t live = 0;
+    int policy = PKV_EVICT_LRU;
 
     pkv_tree() {
         Node root;
@@ -60,10 +75,11 @@ struct pkv_tree {
         live = 1;
     }
 
-    int64_t new_node() {
+    int64_t new_node(int64_t priority = 0) {
         Node n;
         n.id = (int64_t)nodes.size();
         n.last_access_time = clock;
+        n.priority = priority;
         nodes.push_back(std::move(n));
         ++live;
         return nodes.back().id;
@@ -77,7 +93,7 @@ struct pkv_tree {
 
     // Split `child` after split_len tokens; returns the new upper node.
     int64_t split(int64_t child, int64_t split_len) {
-        int64_t up = new_node();  // may reallocate `nodes`: index by id only
+        int64_t up = new_node(nodes[child].priority);  // may reallocate `nodes`: index by id only
         Node &c = nodes[child];
         Node &u = nodes[up];
         u.parent = c.parent;
@@ -114,13 +130,15 @@ struct pkv_tree {
             node = child;
             pos += m;
         }
+        for (int64_t x = node; x != 0; x = nodes[x].parent) nodes[x].hit_count += 1;
         return node;
     }
 
-    int64_t insert(const int32_t *key, const int32_t *value, int64_t n) {
+    int64_t insert(const int32_t *key, const int32_t *value, int64_t n, int64_t priority) {
         ++clock;
         int64_t node = 0;
         nodes[0].last_access_time = clock;
+        nodes[0].priority = std::max(nodes[0].priority, priority);
         int64_t pos = 0, total = 0;
         while (pos < n) {
             auto it = nodes[node].children.find(key[pos]);
@@ -133,7 +151,7 @@ struct pkv_tree {
             if (m < (int64_t)nodes[node].key.size()) node = split(node, m);
         }
         if (pos < n) {
-            int64_t leaf = new_node();
+            int64_t leaf = new_node(priority);
             Node &l = nodes[leaf];
             l.parent = node;
             l.key.assign(key + pos, key + n);
@@ -148,11 +166,26 @@ struct pkv_tree {
         return x.alive && x.id != 0 && x.children.empty() && x.lock_ref == 0;
     }
 
+    // Heap key of an evictable leaf under the tree's policy (smallest evicted first; the id
+    // breaks every tie and is the last component).
+    using Key = std::array<int64_t, 3>;
+    Key eviction_key(const Node &x) const {
+        switch (policy) {
+            case PKV_EVICT_LFU: return {x.hit_count, x.last_access_time, x.id};
+            case PKV_EVICT_SLRU: return {x.hit_count >= kSlruProtect ? 1 : 0, x.last_access_time, x.id};
+            case PKV_EVICT_FIFO: return {x.id, 0, 0};
+            case PKV_EVICT_MRU: return {-x.last_access_time, x.id, 0};
+            case PKV_EVICT_FILO: return {-x.id, 0, 0};
+            case PKV_EVICT_PRIORITY: return {x.priority, x.last_access_time, x.id};
+            default: return {x.last_access_time, x.id, 0};
+        }
+    }
+
     void evict(int64_t num_tokens, std::vector<int32_t> *freed) {
-        using Item = std::pair<std::pair<int64_t, int64_t>, int64_t>;  // ((time, id), id)
+        using Item = std::pair<Key, int64_t>;  // (key, id)
         std::priority_queue<Item, std::vector<Item>, std::greater<Item>> heap;
         for (const Node &x : nodes)
-            if (evictable_leaf(x)) heap.push({{x.last_access_time, x.id}, x.id});
+            if (evictable_leaf(x)) heap.push({eviction_key(x), x.id});
         int64_t evicted = 0;
         while (evicted < num_tokens && !heap.empty()) {
             int64_t id = heap.top().second;
@@ -168,8 +201,7 @@ struct pkv_tree {
             std::vector<int32_t>().swap(x.key);
             std::vector<int32_t>().swap(x.value);
             --live;
-            if (p.children.empty() && p.lock_ref == 0)
-                heap.push({{p.last_access_time, p.id}, p.id});
+            if (p.children.empty() && p.lock_ref == 0 && p.id != 0) heap.push({eviction_key(p), p.id});
         }
     }
 
@@ -240,9 +272,21 @@ int pkv_tree_match_prefix(pkv_tree *t, const int32_t *key, int64_t n, int32_t *v
 
 int pkv_tree_insert(pkv_tree *t, const int32_t *key, const int32_t *value, int64_t n,
                     int64_t *prefix_len) {
+    return pkv_tree_insert_priority(t, key, value, n, 0, prefix_len);
+}
+
+int pkv_tree_insert_priority(pkv_tree *t, const int32_t *key, const int32_t *value, int64_t n,
+                             int64_t priority, int64_t *prefix_len) {
     if (!t || n < 0 || (n > 0 && (!key || !value))) return PKV_E_INVALID;
-    int64_t total = t->insert(key, value, n);
+    int64_t total = t->insert(key, value, n, priority);
     if (prefix_len) *prefix_len = total;
+    return PKV_OK;
+}
+
+int pkv_tree_set_policy(pkv_tree *t, int policy) {
+    if (!t) return PKV_E_INVALID;
+    if (policy < PKV_EVICT_LRU || policy > PKV_EVICT_PRIORITY) return PKV_E_UNSUPPORTED;
+    t->policy = policy;
     return PKV_OK;
 }
 
@@ -302,7 +346,7 @@ int pkv_tree_dump(pkv_tree *t, int64_t *out, int64_t cap, int64_t *used) {
     if (!t || !used) return PKV_E_INVALID;
     int64_t need = 0;
     for (const Node &x : t->nodes)
-        if (x.alive) need += 6 + 2 * (int64_t)x.key.size();
+        if (x.alive) need += 8 + 2 * (int64_t)x.key.size();
     *used = need;
     if (!out || cap < need) return out ? PKV_E_WORKSPACE : PKV_OK;
     int64_t k = 0;
@@ -314,6 +358,8 @@ int pkv_tree_dump(pkv_tree *t, int64_t *out, int64_t cap, int64_t *used) {
         out[k++] = x.last_access_time;
         out[k++] = (int64_t)x.key.size();
         out[k++] = (int64_t)x.children.size();
+        out[k++] = x.hit_count;
+        out[k++] = x.priority;
         for (int32_t v : x.key) out[k++] = v;
         for (int32_t v : x.value) out[k++] = v;
     }

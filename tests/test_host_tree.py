@@ -15,7 +15,7 @@ def _oracle_dump(t: RadixCache):
     rows = []
     for n in t._all_nodes():
         rows.append((n.id, -1 if n.parent is None else n.parent.id, n.lock_ref, n.last_access_time,
-                     tuple(n.key), tuple(n.value), len(n.children)))
+                     tuple(n.key), tuple(n.value), len(n.children), n.hit_count, n.priority))
     return sorted(rows)
 
 
@@ -32,10 +32,11 @@ def test_worked_example_cpp():
     assert len(shared) == 1 and shared[0][6] == 2
 
 
-@pytest.mark.parametrize("seed", range(8))
-def test_random_ops_bit_exact(seed):
+@pytest.mark.parametrize("policy", RadixTree.POLICIES)
+@pytest.mark.parametrize("seed", range(4))
+def test_random_ops_bit_exact(seed, policy):
     rng = random.Random(seed)
-    a, b = RadixCache(), RadixTree()
+    a, b = RadixCache(policy), RadixTree(policy)
     locked = []
     nxt = 0
     for _ in range(400):
@@ -44,7 +45,8 @@ def test_random_ops_bit_exact(seed):
         if op < 0.35:
             v = list(range(nxt, nxt + len(key)))
             nxt += len(key)
-            assert a.insert(key, v) == b.insert(key, v)
+            prio = rng.randint(0, 3)
+            assert a.insert(key, v, prio) == b.insert(key, v, prio)
         elif op < 0.6:
             va, na = a.match_prefix(key)
             vb, nb = b.match_prefix(key)
@@ -126,3 +128,26 @@ def test_cascade_spans_tile_shared_prefixes():
     assert (10, 5, [0, 1, 3]) in spans
     assert (15, 1, [0, 3]) in spans
     assert len(spans) == 3
+
+
+@pytest.mark.parametrize("policy,order", [("lru", "BAC"), ("mru", "CAB"), ("lfu", "BCA"), ("slru", "BCA"),
+                                          ("fifo", "ABC"), ("filo", "CBA"), ("priority", "BCA")])
+def test_policy_orders_cpp(policy, order):
+    # the hand-worked history of the oracle's policy pins, on the C++ tree
+    t = RadixTree(policy)
+    t.insert([1, 2, 3], [10, 11, 12], priority=5)
+    t.insert([4, 5], [20, 21], priority=1)
+    t.insert([6], [30], priority=3)
+    t.match_prefix([1, 2, 3])
+    t.match_prefix([1, 2, 3, 9])
+    t.match_prefix([6, 7])
+    values = {"A": [10, 11, 12], "B": [20, 21], "C": [30]}
+    assert [t.evict(1).tolist() for _ in range(3)] == [values[x] for x in order]
+
+
+def test_unknown_policy_rejected():
+    from prefix_shared_kv_token_gb300 import _lib
+    t = RadixTree()
+    assert _lib.lib.pkv_tree_set_policy(t._h, 7) == -2      # PKV_E_UNSUPPORTED
+    with pytest.raises(ValueError):
+        RadixTree("random")

@@ -186,11 +186,44 @@ __global__ void __launch_bounds__(256) gather_kernel(const GatherParams p) {
 // p = 2^(s * scale - m) for the 128 scores of one row (masked scores are -inf and give 0),
 // packed to bf16 pairs and stored over the row's first 64 S columns in tensor memory.  ls
 // accumulates the bf16 weights, so the normalised weights the P.V product uses add up to one
-// exactly.  (Moving part of the exponentials to an FMA-pipe polynomial was measured slower:
+// exactly.  The exponentials run relative to mref = max(m, tile max), so their arguments are
+// <= 0 (the bf16x2 exponential's error stays at the bf16 rounding of the weight); when the
+// tile max is above the row's lazily kept m, SCALE multiplies by f2 = 2^(mref - m) (<= 2^8,
+// bf16).  (Moving part of the exponentials to an FMA-pipe polynomial was measured slower:
 // the softmax is bound by instruction issue, not by the MUFU.)
-PKV_DEV void exp_pack_regs(const uint32_t *sv, uint32_t col, float sc, float neg_mu, float *ls) {
+// The precise variant (rows that see few keys, at the very start of a prompt; their items
+// run in a separate instantiation of the kernel so the common path keeps its registers):
+// fp32 weights p (times f) written as bf16 high parts over S columns [0, 64) and bf16 low
+// parts p - high over columns [64, 128); the MMA issuer feeds both to P.V.  ls sums the fp32
+// weights.
+PKV_DEV void exp_pack_precise(const uint32_t *sv, uint32_t col, float sc, float neg_mref, float f, float *ls) {
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float p0 = ex2(fmaf(__uint_as_float(sv[hb * 64 + 2 * c]), sc, neg_mref)) * f;
+                const float p1 = ex2(fmaf(__uint_as_float(sv[hb * 64 + 2 * c + 1]), sc, neg_mref)) * f;
+                const uint32_t h = pack_bf16x2(p0, p1);
+                if (part == 0) {
+                    pk[c] = h;
+                    ls[0] += p0;
+                    ls[1] += p1;
+                } else {
+                    pk[c] = pack_bf16x2(p0 - bf16_lo(h), p1 - bf16_hi(h));
+                }
+            }
+            tmem_st32(col + part * 64 + hb * 32, pk);
+        }
+    }
+}
+
+template <bool SCALE>
+PKV_DEV void exp_pack_regs(const uint32_t *sv, uint32_t col, float sc, float neg_mref, uint32_t f2, float *ls) {
     // packed fp32 pairs: one fma.f32x2 / add.f32x2 per two scores (issue slots are the limit)
-    const uint64_t sc2 = f2_pack(sc, sc), mu2 = f2_pack(neg_mu, neg_mu);
+    const uint64_t sc2 = f2_pack(sc, sc), mu2 = f2_pack(neg_mref, neg_mref);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int hb = 0; hb < 2; ++hb) {
@@ -202,6 +235,7 @@ PKV_DEV void exp_pack_regs(const uint32_t *sv, uint32_t col, float sc, float neg
             float x0, x1;
             f2_unpack(x, x0, x1);
             pk[c] = ex2_bf16x2(pack_bf16x2(x0, x1));  // two weights per MUFU op, already packed
+            if constexpr (SCALE) pk[c] = mul_bf16x2(pk[c], f2);
             add_bf16x2_f32(pk[c], acc[(c & 1) * 2], acc[(c & 1) * 2 + 1]);
         }
         tmem_st32(col + hb * 32, pk);
@@ -239,7 +273,7 @@ PKV_DEV XItem load_item(const ExtendItem *itp, int tq) {
 // softmax warpgroups are still in the current item's epilogue (they read O, not S); the next
 // item's first P.V, which overwrites O, needs that warpgroup's next P and so comes after its
 // epilogue.
-template <int D, int G>
+template <int D, int G, bool PRECISE>
 __global__ void __launch_bounds__(384, 1)
     extend_kernel(const ExtendParams p, const __grid_constant__ CUtensorMap qmap,
                   const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
@@ -377,6 +411,13 @@ __global__ void __launch_bounds__(384, 1)
                         mma_ts(tmem + C::kColO + q * D, tmem + C::kColS + q * kBN + kk * 8, vd, idesc_pv,
                                (j > 0 || kk > 0) ? 1u : 0u);
                     }
+                    if constexpr (PRECISE) {  // + the weights' bf16 low parts, columns [64, 128) of S
+#pragma unroll
+                        for (int kk = 0; kk < kBN / 16; ++kk) {
+                            const uint64_t vd = sdesc_sw128(v_s + kk * 16 * 128, C::kBlkK, 1024);
+                            mma_ts(tmem + C::kColO + q * D, tmem + C::kColS + q * kBN + 64 + kk * 8, vd, idesc_pv, 1u);
+                        }
+                    }
                     if (q == it.nq - 1) tc_commit(&bars->kvempty[s]);
                     if (j == it.ntiles - 1) tc_commit(&bars->ofinal[q]);
                     return true;
@@ -457,9 +498,18 @@ __global__ void __launch_bounds__(384, 1)
                     rescale = (j > 0) && (m != -INFINITY);
                     m = mt;
                 }
-                const float neg_mu = (m == -INFINITY) ? 0.f : -m;
+                // exponent reference: the larger of m and the tile max (arguments <= 0)
+                const float mref = fmaxf(m, mt);
+                const float neg_mref = (mref == -INFINITY) ? 0.f : -mref;
                 float ls[4] = {0.f, 0.f, 0.f, 0.f};
-                exp_pack_regs(sv, colS, p.scale_log2, neg_mu, ls);
+                if constexpr (PRECISE) {
+                    exp_pack_precise(sv, colS, p.scale_log2, neg_mref, mt > m ? ex2(mt - m) : 1.f, ls);
+                } else if (__any_sync(0xffffffffu, mt > m)) {
+                    const float f = mt > m ? ex2(mt - m) : 1.f;  // <= 2^8 (m is then finite)
+                    exp_pack_regs<true>(sv, colS, p.scale_log2, neg_mref, pack_bf16x2(f, f), ls);
+                } else {
+                    exp_pack_regs<false>(sv, colS, p.scale_log2, neg_mref, 0u, ls);
+                }
                 const float ls0 = ls[0] + ls[2], ls1 = ls[1] + ls[3];
                 l = l * alpha + (ls0 + ls1);
                 // PV of tile j-1 is complete: S of tile j was issued after it.  The whole warp
@@ -530,28 +580,34 @@ __global__ void __launch_bounds__(384, 1)
     }
 }
 
-template <int D, int G>
+template <int D, int G, bool PRECISE>
 static int launch_extend(const ExtendParams &p, const CUtensorMap &qm, const CUtensorMap &km, const CUtensorMap &vm,
                          int nctas, cudaStream_t s) {
     constexpr int smem = XCfg<D>::kSmem;
     static_assert(smem <= 232448, "shared memory budget");
-    auto kern = extend_kernel<D, G>;
+    auto kern = extend_kernel<D, G, PRECISE>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return PKV_E_CUDA;
     kern<<<nctas, 384, smem, s>>>(p, qm, km, vm);  // persistent: the plan's CTA lists
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_E_CUDA;
 }
 
-template <int D>
-static int dispatch_extend(int G, const ExtendParams &p, const CUtensorMap &qm, const CUtensorMap &km,
-                           const CUtensorMap &vm, int n, cudaStream_t s) {
+template <int D, bool PRECISE>
+static int dispatch_g(int G, const ExtendParams &p, const CUtensorMap &qm, const CUtensorMap &km, const CUtensorMap &vm,
+                      int n, cudaStream_t s) {
     switch (G) {
-        case 1: return launch_extend<D, 1>(p, qm, km, vm, n, s);
-        case 2: return launch_extend<D, 2>(p, qm, km, vm, n, s);
-        case 4: return launch_extend<D, 4>(p, qm, km, vm, n, s);
-        case 8: return launch_extend<D, 8>(p, qm, km, vm, n, s);
+        case 1: return launch_extend<D, 1, PRECISE>(p, qm, km, vm, n, s);
+        case 2: return launch_extend<D, 2, PRECISE>(p, qm, km, vm, n, s);
+        case 4: return launch_extend<D, 4, PRECISE>(p, qm, km, vm, n, s);
+        case 8: return launch_extend<D, 8, PRECISE>(p, qm, km, vm, n, s);
         default: return PKV_E_UNSUPPORTED;
     }
+}
+
+template <int D>
+static int dispatch_extend(int G, const ExtendParams &p, const CUtensorMap &qm, const CUtensorMap &km,
+                           const CUtensorMap &vm, int n, cudaStream_t s, bool precise = false) {
+    return precise ? dispatch_g<D, true>(G, p, qm, km, vm, n, s) : dispatch_g<D, false>(G, p, qm, km, vm, n, s);
 }
 
 template <int D>
@@ -725,12 +781,19 @@ extern "C" int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, con
     void *ev0 = g_kernel_events[0], *ev1 = g_kernel_events[1];
     g_kernel_events[0] = g_kernel_events[1] = nullptr;
     if (ev0 && cudaEventRecord(static_cast<cudaEvent_t>(ev0), s) != cudaSuccess) return PKV_E_CUDA;
-    p.cta_off = reinterpret_cast<const int32_t *>(plan + info->offsets[7]);
-    const int64_t nctas = info->offsets[8];
-    if (nctas < 1 || nctas > info->num_items) return PKV_E_PLAN;
-    rc = D == 128 ? dispatch_extend<128>(G, p, qm, km, vm, (int)nctas, s)
-                  : dispatch_extend<64>(G, p, qm, km, vm, (int)nctas, s);
-    if (rc) return rc;
+    // the main item list, then (if any) the items whose rows see few keys (precise weights)
+    for (int part = 0; part < 2; ++part) {
+        const int64_t nitems = part == 0 ? info->num_items - info->offsets[10] : info->offsets[10];
+        if (nitems == 0) continue;
+        p.items = reinterpret_cast<const ExtendItem *>(plan + info->offsets[part == 0 ? 0 : 9]);
+        p.num_items = (int32_t)nitems;
+        p.cta_off = reinterpret_cast<const int32_t *>(plan + info->offsets[part == 0 ? 7 : 11]);
+        const int64_t nctas = info->offsets[part == 0 ? 8 : 12];
+        if (nctas < 1 || nctas > nitems) return PKV_E_PLAN;
+        rc = D == 128 ? dispatch_extend<128>(G, p, qm, km, vm, (int)nctas, s, part == 1)
+                      : dispatch_extend<64>(G, p, qm, km, vm, (int)nctas, s, part == 1);
+        if (rc) return rc;
+    }
     if (ev1 && cudaEventRecord(static_cast<cudaEvent_t>(ev1), s) != cudaSuccess) return PKV_E_CUDA;
     return launch_merge(info, plan_dev, rec_acc, rec_ml, p.o, s);
 }

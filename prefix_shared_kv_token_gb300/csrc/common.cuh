@@ -262,11 +262,17 @@ PKV_DEV float fmax3(float a, float b, float c) {
 }
 
 // 2^x for two bf16 values at once (ex2.approx.ftz.bf16x2): the exponent is rounded to bf16
-// first, a relative weight error of about |x| * 2^-9 * ln 2 -- the same order as rounding the
-// weight itself to bf16, which the P.V product does anyway.  -inf gives +0.
+// first, a relative weight error of about |x| * 2^-9 * ln 2.  Callers keep x <= 0, where the
+// absolute error 2^x * |x| * 2^-9 * ln 2 stays below 2^-9 of the largest weight -- the order
+// of rounding the weight itself to bf16, which the P.V product does anyway.  -inf gives +0.
 PKV_DEV uint32_t ex2_bf16x2(uint32_t x) {
     uint32_t y;
     asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+PKV_DEV uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t y;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(y) : "r"(a), "r"(b));
     return y;
 }
 PKV_DEV uint32_t pack_bf16x2(float lo, float hi) {
@@ -306,6 +312,13 @@ struct DecodeItem {      // 32 bytes
 };
 
 constexpr int kMaxSegs = 4;
+// Rows that see fewer than kPreciseKeys keys give each weight a large share of the output,
+// where rounding the weights to bf16 for the P.V product costs more than the output's own
+// bf16 rounding leaves room for.  Items holding such rows (flagged by the planner) feed P.V
+// with the weights split into bf16 high and low parts (two products into one accumulator)
+// and sum the fp32 weights.
+constexpr int kPreciseKeys = 32;
+constexpr int32_t kItemPrecise = 1;
 struct ExtendItem {      // 64 bytes
     int32_t g;           // KV head
     int32_t tok0;        // first query token (row of q / o)
@@ -314,7 +327,7 @@ struct ExtendItem {      // 64 bytes
     int32_t pos0;        // context position of the first key of segment 0
     int32_t nseg;        // key segments, consecutive in context positions
     int32_t rec;         // -1: write o directly; else first partial record (one per token)
-    int32_t pad;
+    int32_t flags;       // kItemPrecise: some row sees fewer than kPreciseKeys keys
     int32_t key0[kMaxSegs];   // first gathered key of each segment (row of the workspace)
     int32_t nkeys[kMaxSegs];  // keys of each segment
 };

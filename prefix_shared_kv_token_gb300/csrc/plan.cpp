@@ -32,7 +32,9 @@ namespace {
 
 struct DecodeItem { int32_t g0, mode, nreq, row_off, src, k0, k1, rot; };
 constexpr int kMaxSegs = 4;
-struct ExtendItem { int32_t g, tok0, ntok, qpos0, pos0, nseg, rec, pad, key0[kMaxSegs], nkeys[kMaxSegs]; };
+struct ExtendItem { int32_t g, tok0, ntok, qpos0, pos0, nseg, rec, flags, key0[kMaxSegs], nkeys[kMaxSegs]; };
+// rows seeing fewer keys than this get bf16 high + low weights in the kernels (see common.cuh)
+constexpr int32_t kPreciseKeys = 32;
 struct GatherUnit { int32_t src, pos0, len, key0; };
 struct MergeItem { int32_t out_row, rec0, nrec, rec_stride; };
 static_assert(sizeof(DecodeItem) == 32 && sizeof(ExtendItem) == 64 && sizeof(MergeItem) == 16, "layout");
@@ -496,6 +498,7 @@ extern "C" int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int
             it.tok0 = qo_indptr[r] + i0;
             it.ntok = n;
             it.qpos0 = p + i0;
+            it.flags = p + i0 + 1 < kPreciseKeys ? 1 : 0;  // its first row sees p + i0 + 1 keys
             it.pos0 = runs[sg[0].run].pos0;
             it.nseg = (int32_t)sg.size();
             it.rec = -1;
@@ -512,14 +515,27 @@ extern "C" int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int
             }
         }
     }
-    std::vector<ExtendItem> placed;
-    std::vector<int32_t> cta_off;
-    const int32_t nctas = std::max<int32_t>(1, std::min<int32_t>((int32_t)items.size(), num_sms));
+    // two lists, each dealt onto its own persistent CTAs: the common items, then the items
+    // holding rows that see few keys (a separate launch with precise weights); stored back to
+    // back, so items [0, num_items) cover both
+    std::vector<ExtendItem> placed, placed_x;
+    std::vector<int32_t> cta_off, cta_off_x;
+    int32_t nctas = 1, nctas_x = 0;
     {
-        std::vector<int64_t> cost;
-        for (const ExtendItem &x : items) cost.push_back(extend_item_cost(x, TQ2 / 2));
-        lpt_deal(items, cost, nctas, &placed, &cta_off);
+        std::vector<ExtendItem> common, precise;
+        for (const ExtendItem &x : items) (x.flags & 1 ? precise : common).push_back(x);
+        auto deal = [&](const std::vector<ExtendItem> &v, std::vector<ExtendItem> *out, std::vector<int32_t> *off) {
+            const int32_t n = std::max<int32_t>(1, std::min<int32_t>((int32_t)v.size(), num_sms));
+            std::vector<int64_t> cost;
+            for (const ExtendItem &x : v) cost.push_back(extend_item_cost(x, TQ2 / 2));
+            lpt_deal(v, cost, n, out, off);
+            return n;
+        };
+        nctas = deal(common, &placed, &cta_off);
+        if (!precise.empty()) nctas_x = deal(precise, &placed_x, &cta_off_x);
     }
+    const int32_t n_main = (int32_t)placed.size();
+    placed.insert(placed.end(), placed_x.begin(), placed_x.end());
     const bool cascaded = false;
     const int32_t kmax = 1;
 
@@ -542,9 +558,14 @@ extern "C" int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int
     info->offsets[6] = nkeys;
     info->offsets[7] = (int64_t)off; off = align16(off + cta_off.size() * sizeof(int32_t));
     info->offsets[8] = nctas;
+    info->offsets[9] = info->offsets[0] + (int64_t)n_main * (int64_t)sizeof(ExtendItem);
+    info->offsets[10] = (int64_t)placed_x.size();
+    info->offsets[11] = (int64_t)off; off = align16(off + cta_off_x.size() * sizeof(int32_t));
+    info->offsets[12] = nctas_x;
     std::vector<uint8_t> blob(std::max<size_t>(off, 16), 0);
     put(blob, (size_t)info->offsets[0], placed);
     put(blob, (size_t)info->offsets[7], cta_off);
+    put(blob, (size_t)info->offsets[11], cta_off_x);
     put(blob, (size_t)info->offsets[3], merges);
     put(blob, (size_t)info->offsets[4], units);
     const size_t rec_bytes = (size_t)info->num_records * num_q_heads * (head_dim + 2) * 4;

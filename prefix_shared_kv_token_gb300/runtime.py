@@ -66,10 +66,29 @@ class Call:
     last_nodes: list
     host: dict = field(default_factory=dict)
     cascade: object = None
+    contexts: list = field(default_factory=list)   # per request: (tokens, req_to_token row, cached length)
+    requests: list = field(default_factory=list)
 
     @property
     def num_queries(self) -> int:
         return int(self.q.shape[0])
+
+    def layer(self, pool: Pool, w) -> "Call":
+        """The same call for another layer of the model: that layer's pool, and its queries and
+        new K/V rows from ``w`` (a workload of the same structure whose requests match this
+        call's one for one).  Tables, plan and slots are shared by all layers."""
+        reqs = [w.requests[r.rid] for r in self.requests]
+        kn, vn = [], []
+        for r, (_, row, cached) in zip(reqs, self.contexts):
+            kb, vb = _ctx_kv(w, r, cached, len(row))
+            kn.append(kb)
+            vn.append(vb)
+        dev = self.q.device
+        q = _bf16_dev(np.concatenate([r.q for r in reqs]), dev)
+        return Call(self.kind, pool, self.batch, self.plan, self.plan_dev, torch.zeros_like(self.workspace), q,
+                    torch.empty_like(q), self.out_cache_loc, _bf16_dev(np.concatenate(kn), dev),
+                    _bf16_dev(np.concatenate(vn), dev), w.sm_scale, self.last_nodes, cascade=self.cascade,
+                    contexts=self.contexts, requests=reqs)
 
     def store(self, stream=None):
         kv_store(self.pool, self.k_new, self.v_new, self.out_cache_loc, self.workspace, stream)
@@ -166,9 +185,10 @@ class PrefixCache:
         kv_store(self.pool, k, v, loc, self.err)
 
     # ---- one attention call of a step
-    def prepare(self, kind, cascade=True, opts=None, min_group=2) -> Call:
+    def prepare(self, kind, cascade=True, opts=None, min_group=2, requests=None) -> Call:
+        """One attention call over the workload's requests of ``kind`` (or the given subset)."""
         w = self.w
-        reqs = [r for r in w.requests if r.kind == kind]
+        reqs = [r for r in (w.requests if requests is None else requests) if r.kind == kind]
         rows, last_nodes, seq, ext, new_all, kn, vn, qs = [], [], [], [], [], [], [], []
         for r in reqs:
             toks = _ctx_tokens(w, r)
@@ -213,9 +233,36 @@ class PrefixCache:
         loc = torch.from_numpy(np.concatenate(new_all).astype(np.int32)).to(dev)
         k_new = _bf16_dev(np.concatenate(kn), dev)
         v_new = _bf16_dev(np.concatenate(vn), dev)
-        return Call(kind, self.pool, batch, plan, plan_dev, ws, q, o, loc, k_new, v_new, w.sm_scale, last_nodes,
+        call = Call(kind, self.pool, batch, plan, plan_dev, ws, q, o, loc, k_new, v_new, w.sm_scale, last_nodes,
                     cascade=casc)
+        call.contexts = [(_ctx_tokens(w, r), row, len(row) - r.n_new) for r, row in zip(reqs, rows)]
+        call.requests = reqs
+        return call
 
     def release(self, call: Call):
         for n in call.last_nodes:
+            self.tree.dec_lock_ref(n)
+
+    def prepare_chunked(self, opts=None) -> list:
+        """Chunked prefill of a workload whose ``meta["chunk"]`` numbers each extend request's
+        step: one call per step, planned over the chunks the earlier steps cached.  The tree
+        learns each step's tokens when the step is planned (host only), so all the calls can be
+        planned ahead; run them in order."""
+        steps = self.w.meta["chunk"]
+        calls = []
+        for c in sorted(set(steps)):
+            reqs = [r for r, k in zip(self.w.requests, steps) if k == c]
+            call = self.prepare("extend", opts=opts, requests=reqs)
+            self.commit(call)
+            calls.append(call)
+        return calls
+
+    def commit(self, call: Call):
+        """After the call ran: cache every request's whole context (its new tokens join the
+        tree with the slots they were stored in) and unlock its path, as a server does when a
+        prefill chunk or a request finishes."""
+        for (toks, row, cached), n in zip(call.contexts, call.last_nodes):
+            pre = self.tree.insert(toks, row)
+            if pre > cached:   # another request of the call inserted the same new tokens first
+                self.alloc.release(row[cached:pre])
             self.tree.dec_lock_ref(n)

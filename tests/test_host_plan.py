@@ -16,7 +16,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 DEC = np.dtype([("g0", "<i4"), ("mode", "<i4"), ("nreq", "<i4"), ("row_off", "<i4"), ("src", "<i4"),
                 ("k0", "<i4"), ("k1", "<i4"), ("rot", "<i4")])
 EXT = np.dtype([("g", "<i4"), ("tok0", "<i4"), ("ntok", "<i4"), ("qpos0", "<i4"), ("pos0", "<i4"),
-                ("nseg", "<i4"), ("rec", "<i4"), ("pad", "<i4"), ("key0", "<i4", (4,)), ("nkeys", "<i4", (4,))])
+                ("nseg", "<i4"), ("rec", "<i4"), ("flags", "<i4"), ("key0", "<i4", (4,)), ("nkeys", "<i4", (4,))])
 GU = np.dtype([("src", "<i4"), ("pos0", "<i4"), ("len", "<i4"), ("key0", "<i4")])
 MRG = np.dtype([("out_row", "<i4"), ("rec0", "<i4"), ("nrec", "<i4"), ("stride", "<i4")])
 
@@ -211,7 +211,13 @@ def test_extend_plan_covers_causal_triangle(cascade):
     plan = pkv.plan_extend(seq, ext, qo, 32, 8, 128, casc)
     info = plan.info
     items = _sections(plan, EXT, info.num_items, info.offsets[0])
-    _check_cta_ranges(plan, info.offsets[7], info.offsets[8], info.num_items)
+    nx = int(info.offsets[10])   # rows that see few keys: their own list, after the common one
+    _check_cta_ranges(plan, info.offsets[7], info.offsets[8], info.num_items - nx)
+    if nx:
+        _check_cta_ranges(plan, info.offsets[11], info.offsets[12], nx)
+        assert int(info.offsets[9]) == int(info.offsets[0]) + 64 * (info.num_items - nx)
+    for k, it in enumerate(items):   # flagged exactly when its first row sees fewer than 32 keys
+        assert bool(it["flags"] & 1) == (it["qpos0"] + 1 < 32) and (k >= info.num_items - nx) == bool(it["flags"] & 1)
     units = _sections(plan, GU, info.offsets[5], info.offsets[4])
     # gathered key -> (source request, position); every gathered key is written once
     nk = int(info.offsets[6])

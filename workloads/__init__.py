@@ -17,6 +17,7 @@ from .generate import (  # noqa: F401
     batched_decode,
     multiturn_decode,
     tot_mixed,
+    chunked_prefill,
     config,
     CONFIG_NAMES,
 )

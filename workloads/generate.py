@@ -249,6 +249,25 @@ def tot_mixed(seed=5, root_len=4096, depth=3, branch=4, seg=256, n_new_branches=
     return b.finish("tot_mixed_fp8", seed, num_slots, dtype)
 
 
+def chunked_prefill(seed=6, n_req=16, prompt=8192, chunk=1024, hq=32, hkv=8, d=128, num_slots=1 << 21,
+                    dtype="bf16"):
+    """Long prompts prefilled chunk by chunk: prompt i is a chain of ``chunk``-token segments
+    (the last one shorter when ``chunk`` does not divide ``prompt``), with one extend request
+    per segment.  Step c runs the c-th request of every prompt, over that prompt's earlier
+    chunks, which steps 0 .. c-1 cached.  ``meta["chunk"]`` gives each request's step."""
+    b = _Builder(seed, hq, hkv, d, num_slots)
+    steps = []
+    for _ in range(n_req):
+        parent, pos, c = -1, 0, 0
+        while pos < prompt:
+            n = min(chunk, prompt - pos)
+            parent = b.segment(parent, n)
+            b.request(parent, "extend", n)
+            steps.append(c)
+            pos, c = pos + n, c + 1
+    return b.finish("chunked_prefill", seed, num_slots, dtype, meta={"chunk": steps})
+
+
 def config(k: int) -> Workload:
     """The five full-size workloads, seed = configuration number."""
     return {1: tiny_decode, 2: fewshot_extend, 3: batched_decode, 4: multiturn_decode,

@@ -713,11 +713,22 @@ int decode_span_tensor(const pkv_pool *pool, const pkv_batch *batch, const void 
     p.rec_acc = rec_acc;
     p.rec_ml = rec_ml;
     p.rec_list = reinterpret_cast<const int32_t *>(plan + info->offsets[14]);
-    p.cta_off = reinterpret_cast<const int32_t *>(plan + info->offsets[16]);
-    const int64_t nctas = info->offsets[17];
-    if (nctas < 1 || nctas > nx) return PKV_E_PLAN;
-    return D == 128 ? dispatch_extend<128>(G, p, qm, km, vm, (int)nctas, s)
-                    : dispatch_extend<64>(G, p, qm, km, vm, (int)nctas, s);
+    // the spans' items, then the short requests' items (precise weights)
+    const ExtendItem *items = reinterpret_cast<const ExtendItem *>(plan + info->offsets[7]);
+    const int64_t nprec = info->offsets[18];
+    for (int part = 0; part < 2; ++part) {
+        const int64_t n = part == 0 ? nx - nprec : nprec;
+        if (n == 0) continue;
+        p.items = items + (part == 0 ? 0 : nx - nprec);
+        p.num_items = (int32_t)n;
+        p.cta_off = reinterpret_cast<const int32_t *>(plan + info->offsets[part == 0 ? 16 : 19]);
+        const int64_t nctas = info->offsets[part == 0 ? 17 : 20];
+        if (nctas < 1 || nctas > n || nprec > nx) return PKV_E_PLAN;
+        int rc = D == 128 ? dispatch_extend<128>(G, p, qm, km, vm, (int)nctas, s, part == 1)
+                          : dispatch_extend<64>(G, p, qm, km, vm, (int)nctas, s, part == 1);
+        if (rc) return rc;
+    }
+    return PKV_OK;
 }
 
 }  // namespace pkv

@@ -206,12 +206,20 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
         for (int32_t i = cascade->grp_indptr[s]; i < cascade->grp_indptr[s + 1]; ++i) in_tensor[cascade->grp_req[i]] = 1;
     }
 
+    // Requests whose whole context is shorter than kPreciseKeys keys leave the decode kernel:
+    // each becomes one tensor-core item over its own gathered context with precise (bf16
+    // high + low) weights, and takes no part in span items.
+    std::vector<char> short_req(batch, 0);
+    for (int32_t r = 0; r < batch; ++r)
+        if (seq_lens[r] < kPreciseKeys) short_req[r] = in_tensor[r] = 1;
+
     // A small batch is cut finer (default chunk sizes only): the decode kernel's keys, span
     // re-reads included, are split into about two items per persistent CTA, at least 64
     // keys each.
     {
         int64_t work = 0;
-        for (int32_t r = 0; r < batch; ++r) work += seq_lens[r] - tail_start[r];
+        for (int32_t r = 0; r < batch; ++r)
+            if (!short_req[r]) work += seq_lens[r] - tail_start[r];
         for (int32_t s = 0; s < nspans; ++s)
             if (!sp_tensor[s])
                 work += (int64_t)cascade->span_len[s] *
@@ -231,7 +239,7 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
         int32_t n = 0;
         for (int32_t s : spans_of[r]) n += nchunks(cascade->span_len[s], sp_chunk[s]);
         n += nchunks(seq_lens[r] - tail_start[r], chunk);
-        nrec[r] = n;
+        nrec[r] = short_req[r] ? 1 : n;
     }
     int32_t num_records = 0;
     for (int32_t r = 0; r < batch; ++r) {
@@ -295,13 +303,17 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
                 }
                 continue;
             }
-            for (int32_t c0 = 0; c0 < len; c0 += sp_chunk[s]) {
+            std::vector<int32_t> mem;  // members read through the decode kernel
+            for (int32_t i = m0; i < m1; ++i)
+                if (!short_req[cascade->grp_req[i]]) mem.push_back(cascade->grp_req[i]);
+            const int32_t nm = (int32_t)mem.size();
+            for (int32_t c0 = 0; c0 < len && nm > 0; c0 += sp_chunk[s]) {
                 const int32_t c1 = std::min(len, c0 + sp_chunk[s]);
-                for (int32_t a = m0; a < m1; a += R) {
-                    const int32_t b = std::min(m1, a + R);
+                for (int32_t a = 0; a < nm; a += R) {
+                    const int32_t b = std::min(nm, a + R);
                     const int32_t off = (int32_t)row_req.size();
                     for (int32_t i = a; i < b; ++i) {
-                        const int32_t r = cascade->grp_req[i];
+                        const int32_t r = mem[i];
                         row_req.push_back(r);
                         row_rec.push_back(rec_base[r] < 0 ? -1 : rec_base[r] + next_rec[r]);
                         next_rec[r] += 1;
@@ -309,11 +321,11 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
                     // member groups of one chunk start at staggered tiles, so the CTAs that
                     // read the chunk at the same time spread over it instead of queueing on
                     // the same L2 lines
-                    const int32_t ntile = (c1 - c0 + 15) / 16, ngrp = (m1 - m0 + R - 1) / R;
-                    const int32_t rot = (int32_t)((int64_t)((a - m0) / R) * ntile / ngrp);
+                    const int32_t ntile = (c1 - c0 + 15) / 16, ngrp = (nm + R - 1) / R;
+                    const int32_t rot = (int32_t)((int64_t)(a / R) * ntile / ngrp);
                     for (int32_t g0 = 0; g0 < num_kv_heads; g0 += hg) {
                         items.push_back({g0, 0, b - a, off, cascade->span_req[s], st + c0, st + c1, rot});
-                        cost.push_back((int64_t)(c1 - c0) * (a == m0 ? 5 : 3) + kItemOverhead);
+                        cost.push_back((int64_t)(c1 - c0) * (a == 0 ? 5 : 3) + kItemOverhead);
                         ++num_span_items;
                     }
                 }
@@ -322,7 +334,7 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
     }
     for (int32_t r = 0; r < batch; ++r) {
         const int32_t t0 = tail_start[r], L = seq_lens[r];
-        for (int32_t k0 = t0; k0 < L; k0 += chunk) {
+        for (int32_t k0 = t0; k0 < L && !short_req[r]; k0 += chunk) {
             const int32_t k1 = std::min(L, k0 + chunk);
             const int32_t off = (int32_t)row_req.size();
             row_req.push_back(r);
@@ -333,6 +345,31 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
                 items.push_back({g0, 1, 1, off, r, k0, (last && dyn_tail) ? -1 : k1, 0});
                 cost.push_back((int64_t)(k1 - k0) * 5 + kItemOverhead);
             }
+        }
+    }
+    // short requests: one precise tensor-core item per KV head over the whole context
+    std::vector<ExtendItem> xprecise;
+    for (int32_t r = 0; r < batch; ++r) {
+        if (!short_req[r]) continue;
+        const int32_t L = seq_lens[r], key0 = (int32_t)nkeys, q0 = (int32_t)qsrc.size(), roff = (int32_t)rec_list.size();
+        units.push_back({r, 0, L, key0});  // split into units below
+        nkeys += L;
+        qsrc.push_back(r);
+        rec_list.push_back(rec_base[r]);
+        next_rec[r] += 1;
+        for (int32_t g = 0; g < num_kv_heads; ++g) {
+            ExtendItem it{};
+            it.g = g;
+            it.tok0 = q0;
+            it.ntok = 1;
+            it.qpos0 = L - 1;
+            it.pos0 = 0;
+            it.nseg = 1;
+            it.rec = roff;
+            it.flags = 1;  // precise weights
+            it.key0[0] = key0;
+            it.nkeys[0] = L;
+            xprecise.push_back(it);
         }
     }
     for (int32_t r = 0; r < batch; ++r)
@@ -355,14 +392,21 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
         for (const GatherUnit &R : runs)
             for (int32_t c = 0; c < R.len; c += uk) units.push_back({R.src, R.pos0 + c, std::min(uk, R.len - c), R.key0 + c});
     }
-    std::vector<ExtendItem> xplaced;
-    std::vector<int32_t> xcta_off;
-    const int32_t xctas = std::max<int32_t>(1, std::min<int32_t>((int32_t)xitems.size(), num_sms));
-    {
+    // tensor-core items: the spans' list, then the short requests' (precise) list, back to
+    // back, each dealt onto its own persistent CTAs
+    std::vector<ExtendItem> xplaced, xplaced_p;
+    std::vector<int32_t> xcta_off, xcta_off_p;
+    auto xdeal = [&](const std::vector<ExtendItem> &v, std::vector<ExtendItem> *out, std::vector<int32_t> *off) {
+        if (v.empty()) return 0;
+        const int32_t n = std::max<int32_t>(1, std::min<int32_t>((int32_t)v.size(), num_sms));
         std::vector<int64_t> xcost;
-        for (const ExtendItem &x : xitems) xcost.push_back(extend_item_cost(x, TQ2 / 2));
-        lpt_deal(xitems, xcost, xctas, &xplaced, &xcta_off);
-    }
+        for (const ExtendItem &x : v) xcost.push_back(extend_item_cost(x, TQ2 / 2));
+        lpt_deal(v, xcost, n, out, off);
+        return n;
+    };
+    const int32_t xctas = xdeal(xitems, &xplaced, &xcta_off);
+    const int32_t xctas_p = xdeal(xprecise, &xplaced_p, &xcta_off_p);
+    xplaced.insert(xplaced.end(), xplaced_p.begin(), xplaced_p.end());
 
     std::memset(info, 0, sizeof(*info));
     info->op = 1;
@@ -393,6 +437,9 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
     info->offsets[14] = (int64_t)off; off = align16(off + rec_list.size() * sizeof(int32_t));
     info->offsets[16] = (int64_t)off; off = align16(off + xcta_off.size() * sizeof(int32_t));
     info->offsets[17] = xctas;
+    info->offsets[18] = (int64_t)xplaced_p.size();
+    info->offsets[19] = (int64_t)off; off = align16(off + xcta_off_p.size() * sizeof(int32_t));
+    info->offsets[20] = xctas_p;
     std::vector<uint8_t> blob(std::max<size_t>(off, 16), 0);
     put(blob, (size_t)info->offsets[0], placed);
     put(blob, (size_t)info->offsets[1], row_req);
@@ -401,6 +448,7 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
     put(blob, (size_t)info->offsets[4], cta_off);
     put(blob, (size_t)info->offsets[7], xplaced);
     put(blob, (size_t)info->offsets[16], xcta_off);
+    put(blob, (size_t)info->offsets[19], xcta_off_p);
     put(blob, (size_t)info->offsets[9], units);
     put(blob, (size_t)info->offsets[12], qsrc);
     put(blob, (size_t)info->offsets[14], rec_list);

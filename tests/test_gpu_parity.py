@@ -199,6 +199,18 @@ def test_multiturn_small():
     check_pool(w, pc)
 
 
+@pytest.mark.parametrize("hq,hkv,d", [(32, 8, 128), (8, 2, 64)])
+def test_decode_short_contexts(hq, hkv, d):
+    # contexts of 2 .. 31 keys: each weight carries a large share of the output, the case the
+    # kernels feed with bf16 high + low weights
+    b = W.generate._Builder(38, hq, hkv, d, 4096)
+    for n in range(2, 32):
+        b.request(b.segment(-1, n), "decode", 1)
+    w = b.finish("short", 38, 4096)
+    _, calls = run_step(w)
+    check_outputs(w, calls)
+
+
 def test_decode_context_of_one_token():
     b = W.generate._Builder(35, 8, 2, 64, 64)
     leaves = [b.segment(-1, 1) for _ in range(3)]      # contexts of a single (query) token

@@ -55,7 +55,7 @@ def _decode_cover(plan, seq, hkv, cascade_spans=None):
     nctas, hg = int(info.offsets[5]), int(info.offsets[6])
     assert hg in (1, 2, 4, 8) and hkv % hg == 0 and 1 <= nctas <= max(1, info.num_items)
     cta_off = np.frombuffer(plan.blob[info.offsets[4]:info.offsets[4] + 4 * (nctas + 1)].tobytes(), np.int32)
-    assert cta_off[0] == 0 and cta_off[-1] == info.num_items and np.all(np.diff(cta_off) >= 1)
+    assert cta_off[0] == 0 and cta_off[-1] == info.num_items and np.all(np.diff(cta_off) >= (1 if info.num_items else 0))
     G = info.num_q_heads // hkv
     cover = [np.zeros((hkv, seq[r]), np.int32) for r in range(B)]
     recs_seen = {}
@@ -72,7 +72,12 @@ def _decode_cover(plan, seq, hkv, cascade_spans=None):
     nx, nu, nk, nq = (int(info.offsets[i]) for i in (8, 10, 11, 13))
     if nx:
         xitems = _sections(plan, EXT, nx, info.offsets[7])
-        _check_cta_ranges(plan, info.offsets[16], info.offsets[17], nx)
+        nprec = int(info.offsets[18])   # short requests' items (precise weights), after the spans'
+        if nx > nprec:
+            _check_cta_ranges(plan, info.offsets[16], info.offsets[17], nx - nprec)
+        if nprec:
+            _check_cta_ranges(plan, info.offsets[19], info.offsets[20], nprec)
+        assert all(bool(it["flags"] & 1) == (k >= nx - nprec) for k, it in enumerate(xitems))
         units = _sections(plan, GU, nu, info.offsets[9])
         qsrc = np.frombuffer(plan.blob[info.offsets[12]:info.offsets[12] + 4 * nq].tobytes(), np.int32)
         nrl = max(int(it["rec"]) + int(it["ntok"]) for it in xitems)
@@ -155,6 +160,25 @@ def test_decode_plan_head_groups(hq, hkv):
     _decode_cover(plan, seq, hkv)
     hg = int(plan.info.offsets[6])
     assert hg == max(h for h in (1, 2, 4, 8) if hkv % h == 0)
+
+
+def test_decode_plan_short_contexts_go_precise():
+    # contexts shorter than 32 keys: one precise tensor-core item per KV head, whole context,
+    # no decode-kernel items; a longer request in the same batch stays in the decode kernel
+    seq = np.array([2, 31, 17, 32, 500], np.int32)
+    casc = pkv.Cascade(span_req=np.array([3], np.int32), span_start=np.array([0], np.int32),
+                       span_len=np.array([2], np.int32), grp_indptr=np.array([0, 5], np.int32),
+                       grp_req=np.array([0, 1, 2, 3, 4], np.int32))
+    plan = pkv.plan_decode(seq, 32, 8, 128, casc)
+    items = _decode_cover(plan, seq, 8)
+    info = plan.info
+    assert int(info.offsets[18]) == 3 * 8
+    row_req = np.frombuffer(plan.blob[info.offsets[1]:info.offsets[2]].tobytes(), np.int32)
+    reqs = {int(row_req[it["row_off"] + i]) for it in items for i in range(it["nreq"])}
+    assert reqs == {3, 4}
+    only_short = pkv.plan_decode(np.array([5, 9], np.int32), 32, 8, 128, None)
+    assert only_short.info.num_items == 0
+    _decode_cover(only_short, np.array([5, 9], np.int32), 8)
 
 
 def test_decode_plan_cuts_small_batches_finer():

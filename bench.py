@@ -164,6 +164,9 @@ def load_workload(args):
     """The configuration's workload; --pool-slots only shrinks the pool (same tokens/values
     up to the slot permutation), for profiler captures that must stay a few GB."""
     import workloads as W
+    if args.workload == "chunked_prefill":
+        # 16 prompts of 8,192 tokens prefilled in 1,024-token chunks (one call per chunk)
+        return W.chunked_prefill(seed=6, **({"num_slots": args.pool_slots} if args.pool_slots else {}))
     if not args.pool_slots:
         return W.config(args.config)
     gen = {1: W.tiny_decode, 2: W.fewshot_extend, 3: W.batched_decode, 4: W.multiturn_decode, 5: W.tot_mixed}
@@ -184,9 +187,12 @@ def run_ours(args, rank, world):
     w = load_workload(args)
     facts = workload_facts(w)
     pc = PrefixCache(w, device=str(dev))
-    pc.populate()
-    calls = [pc.prepare(kind, cascade=not args.no_cascade) for kind in ("extend", "decode")
-             if any(r.kind == kind for r in w.requests)]
+    if w.name == "chunked_prefill":
+        calls = pc.prepare_chunked()       # one extend call per chunk, over the chunks before it
+    else:
+        pc.populate()
+        calls = [pc.prepare(kind, cascade=not args.no_cascade) for kind in ("extend", "decode")
+                 if any(r.kind == kind for r in w.requests)]
     stream = torch.cuda.current_stream()
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
 
@@ -208,8 +214,9 @@ def run_ours(args, rank, world):
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 + 2 * len(calls))] for _ in range(K)]
     # the extend call's tensor-core kernel alone (after its key gather, before its merge)
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    for a, b in kev:
+    kev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in calls]
+           for _ in range(K)]
+    for a, b in (pair for step in kev for pair in step):
         a.record(stream)
         b.record(stream)
     if world > 1:
@@ -226,7 +233,7 @@ def run_ours(args, rank, world):
             e[1].record(stream)
             for i, c in enumerate(calls):
                 if c.kind == "extend":
-                    pkv.set_kernel_events(kev[k][0], kev[k][1])
+                    pkv.set_kernel_events(*kev[k][i])
                 e[2 + 2 * i].record(stream)
                 c.attend()
                 e[3 + 2 * i].record(stream)
@@ -250,10 +257,14 @@ def run_ours(args, rank, world):
         torch.cuda.synchronize()
     step_ms = [ev[k][0].elapsed_time(ev[k][-1]) for k in range(K)]
     store_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
-    attn_ms = {c.kind: [ev[k][2 + 2 * i].elapsed_time(ev[k][3 + 2 * i]) for k in range(K)]
-               for i, c in enumerate(calls)}
+    attn_ms = {}
+    for i, c in enumerate(calls):   # per kind: all of the step's calls of that kind
+        t = [ev[k][2 + 2 * i].elapsed_time(ev[k][3 + 2 * i]) for k in range(K)]
+        attn_ms[c.kind] = [x + y for x, y in zip(attn_ms[c.kind], t)] if c.kind in attn_ms else t
     e2e_ms = [a.elapsed_time(b) for a, b in e2e_ev]
-    ext_kernel_ms = [a.elapsed_time(b) for a, b in kev] if any(c.kind == "extend" for c in calls) else None
+    # per step: the extend kernels of all the step's extend calls
+    ext_kernel_ms = [sum(a.elapsed_time(b) for (a, b), c in zip(kev[k], calls) if c.kind == "extend")
+                     for k in range(K)] if any(c.kind == "extend" for c in calls) else None
     for c in calls:
         if pkv.get_device_error(c.workspace) != 0:
             raise RuntimeError("device error word set during the timed steps")
@@ -293,7 +304,7 @@ def run_ours(args, rank, world):
     launches_per_step = sum(c.launches() for c in calls)
     h2d = sum(c.h2d_bytes() for c in calls)
     d2h = sum(c.d2h_bytes() for c in calls)
-    cfg = {"workload": w.name, "config_id": args.config, "requests": len(w.requests),
+    cfg = {"workload": w.name, "config_id": None if args.workload else args.config, "requests": len(w.requests),
            "heads_q_kv": f"{w.num_q_heads}/{w.num_kv_heads}", "head_dim": w.head_dim, "pool_dtype": w.dtype,
            "pool_slots": w.num_slots, "cascade": not args.no_cascade,
            "l2": "flushed between timed steps (512 MiB write outside the step events)",
@@ -373,7 +384,8 @@ def run_reference(args, rank, world):
     return {"metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(secs_total * 1e3 / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "config_id": args.config, "requests": len(w.requests)},
+            "config": {"workload": w.name, "config_id": None if args.workload else args.config,
+                       "requests": len(w.requests)},
             "impl": "reference", "cpu_baseline": cb,
             "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -391,6 +403,8 @@ def main():
     ap.add_argument("--no-cascade", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pool-slots", type=int, default=0)
+    ap.add_argument("--workload", default="", choices=["", "chunked_prefill"],
+                    help="chunked_prefill: long prompts prefilled chunk by chunk (instead of --config)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

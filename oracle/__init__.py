@@ -17,6 +17,9 @@ kv_store     scatter of new K/V rows into pool slots; bf16 copy or fp8 quantisat
 attention    scaled-dot-product attention per request in float64 (contiguous form and
              the pool-gather form), and the log-sum-exp merge of partial states.
 step         the expected outputs of one workload step (every request, or a sample).
+schedule     cache-aware ordering of a waiting queue: longest cached prefix first
+             ("Efficiently Programming Large Language Models using SGLang" summary,
+             §Cache-Aware Scheduling), and first-come-first-served.
 
 Parity pins (tests/test_oracle_*.py) tie each function to something other than itself:
 the pages' worked radix example and split example, brute-force tries, torch's independent

@@ -282,6 +282,21 @@ int pkv_tree_insert_priority(pkv_tree *t, const int32_t *key, const int32_t *val
 int pkv_tree_evict(pkv_tree *t, int64_t num_tokens, int32_t *freed, int64_t freed_cap,
                    int64_t *num_freed);
 
+/* Cached prefix length of key[0..n) (*len), without changing the tree: no split, no access
+ * time, no hit.  For a scheduler that compares waiting requests before admitting any. */
+int pkv_tree_match_len(pkv_tree *t, const int32_t *key, int64_t n, int64_t *len);
+
+/* Cache-aware scheduling ([SG] summary §Cache-Aware Scheduling: requests whose prefix is
+ * longest in the radix tree go first, so cached prefixes are used before they are evicted;
+ * reported ~30 % above first-come-first-served on few-shot workloads).  The n waiting
+ * requests are token lists tokens[offsets[i] .. offsets[i+1]) (host, CSR).  order[0..n)
+ * receives the admission order: PKV_SCHED_LPM = longest cached prefix first, ties in queue
+ * order; PKV_SCHED_FCFS = queue order.  match_len[0..n) (may be NULL) receives each
+ * request's cached prefix length.  The tree is not changed. */
+enum { PKV_SCHED_LPM = 0, PKV_SCHED_FCFS = 1 };
+int pkv_schedule(pkv_tree *t, const int32_t *tokens, const int64_t *offsets, int32_t n, int policy,
+                 int32_t *order, int64_t *match_len);
+
 /* lock_ref on the path node..root ([RC] "참조 카운트: lock_ref"); locked nodes are never
  * evicted.  *delta (may be NULL) gets the change of the evictable size. */
 int pkv_tree_inc_lock_ref(pkv_tree *t, int64_t node, int64_t *delta);

@@ -248,6 +248,26 @@ class RadixTree:
                                                                        int(priority), C.byref(n)))
         return n.value
 
+    def match_len(self, key) -> int:
+        """Cached prefix length of ``key``; the tree is not changed."""
+        key = _i32(key)
+        n = C.c_int64(0)
+        check("pkv_tree_match_len", lib.pkv_tree_match_len(self._h, _ptr(key), len(key), C.byref(n)))
+        return n.value
+
+    def schedule(self, queue, policy: str = "lpm"):
+        """Admission order of ``queue`` (token lists): "lpm" longest cached prefix first (ties
+        in queue order) or "fcfs"; returns (order, cached prefix lengths)."""
+        offs = np.zeros(len(queue) + 1, dtype=np.int64)
+        for i, q in enumerate(queue):
+            offs[i + 1] = offs[i] + len(q)
+        toks = _i32(np.concatenate([np.asarray(q, dtype=np.int32) for q in queue]) if queue else [])
+        order = np.zeros(max(len(queue), 1), dtype=np.int32)
+        lens = np.zeros(max(len(queue), 1), dtype=np.int64)
+        check("pkv_schedule", lib.pkv_schedule(self._h, _ptr(toks), _ptr(offs), len(queue),
+                                               {"lpm": 0, "fcfs": 1}[policy], _ptr(order), _ptr(lens)))
+        return order[:len(queue)].tolist(), lens[:len(queue)].tolist()
+
     def sizes(self):
         e, p, t, n = C.c_int64(0), C.c_int64(0), C.c_int64(0), C.c_int64(0)
         check("pkv_tree_sizes", lib.pkv_tree_sizes(self._h, C.byref(e), C.byref(p), C.byref(t), C.byref(n)))

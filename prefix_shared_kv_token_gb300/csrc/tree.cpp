@@ -134,6 +134,21 @@ struct pkv_tree {
         return node;
     }
 
+    // Cached prefix length of key without touching the tree (no split, no time, no hit).
+    int64_t peek(const int32_t *key, int64_t n) const {
+        int64_t node = 0, pos = 0;
+        while (pos < n) {
+            auto it = nodes[node].children.find(key[pos]);
+            if (it == nodes[node].children.end()) break;
+            const Node &c = nodes[it->second];
+            int64_t m = key_match(c.key.data(), (int64_t)c.key.size(), key + pos, n - pos);
+            pos += m;
+            if (m < (int64_t)c.key.size()) break;
+            node = c.id;
+        }
+        return pos;
+    }
+
     int64_t insert(const int32_t *key, const int32_t *value, int64_t n, int64_t priority) {
         ++clock;
         int64_t node = 0;
@@ -305,6 +320,30 @@ int pkv_tree_evict(pkv_tree *t, int64_t num_tokens, int32_t *freed, int64_t free
         std::memcpy(freed, f.data(), sizeof(int32_t) * f.size());
     }
     *num_freed = (int64_t)f.size();
+    return PKV_OK;
+}
+
+int pkv_tree_match_len(pkv_tree *t, const int32_t *key, int64_t n, int64_t *len) {
+    if (!t || n < 0 || (n > 0 && !key) || !len) return PKV_E_INVALID;
+    *len = t->peek(key, n);
+    return PKV_OK;
+}
+
+int pkv_schedule(pkv_tree *t, const int32_t *tokens, const int64_t *offsets, int32_t n, int policy,
+                 int32_t *order, int64_t *match_len) {
+    if (!t || n < 0 || (n > 0 && (!offsets || !order))) return PKV_E_INVALID;
+    if (policy != PKV_SCHED_LPM && policy != PKV_SCHED_FCFS) return PKV_E_UNSUPPORTED;
+    std::vector<int64_t> len((size_t)n);
+    for (int32_t i = 0; i < n; ++i) {
+        const int64_t a = offsets[i], b = offsets[i + 1];
+        if (a < 0 || b < a || (b > a && !tokens)) return PKV_E_INVALID;
+        len[(size_t)i] = t->peek(tokens + a, b - a);
+    }
+    for (int32_t i = 0; i < n; ++i) order[i] = i;
+    if (policy == PKV_SCHED_LPM)
+        std::stable_sort(order, order + n, [&](int32_t x, int32_t y) { return len[(size_t)x] > len[(size_t)y]; });
+    if (match_len)
+        for (int32_t i = 0; i < n; ++i) match_len[i] = len[(size_t)i];
     return PKV_OK;
 }
 

@@ -151,3 +151,20 @@ def test_unknown_policy_rejected():
     assert _lib.lib.pkv_tree_set_policy(t._h, 7) == -2      # PKV_E_UNSUPPORTED
     with pytest.raises(ValueError):
         RadixTree("random")
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_schedule_matches_oracle(seed):
+    from oracle.schedule import schedule
+    rng = random.Random(100 + seed)
+    a, b = RadixCache(), RadixTree()
+    for i in range(80):
+        k = [rng.randint(0, 4) for _ in range(rng.randint(1, 14))]
+        v = list(range(100 * i, 100 * i + len(k)))
+        assert a.insert(k, v) == b.insert(k, v)
+    queue = [[rng.randint(0, 4) for _ in range(rng.randint(0, 16))] for _ in range(50)]
+    before = sorted(b.dump())
+    for policy in ("lpm", "fcfs"):
+        assert b.schedule(queue, policy) == schedule(a, queue, policy)
+    assert sorted(b.dump()) == before            # scheduling leaves the tree as it was
+    assert [b.match_len(q) for q in queue] == schedule(a, queue)[1]

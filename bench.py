@@ -177,6 +177,52 @@ def load_workload(args):
 # our arm
 
 
+def run_serving(args):
+    """Multi-step serving of a 256-request few-shot stream (8 groups x 32 requests sharing a
+    1,800-token prefix, unique 50-150-token questions, 32-64 generated tokens, all waiting from
+    step 0 in an interleaved group order) with at most 64 running on a 16,384-slot pool (the
+    stream needs ~52k slots even with sharing), once admitting longest-cached-prefix first and
+    once first-come-first-served.  A step is one
+    serving step (admissions + prefill + one decode token per running request); the timed
+    region is the whole run.  value = prompt + generated tokens served per second of device
+    time (CUDA events around every kv_store + attention call)."""
+    import torch
+    import workloads as W
+    from prefix_shared_kv_token_gb300.serving import ServingSim
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    warm = W.serving_stream(seed=70, n_groups=2, per_group=4, shared=300, unique=(10, 20), out=(2, 3))
+    ServingSim(warm, capacity=4096).run()
+    stream = W.serving_stream(seed=7, per_step=256)
+    served = sum(len(r.prompt) + r.out_len for r in stream.requests)
+    cap = args.pool_slots or 16384
+    res = {}
+    with ClockSampler(0) as clocks:
+        for policy in ("lpm", "fcfs"):
+            sim = ServingSim(stream, capacity=cap, policy=policy, max_running=64, prefill_budget=16384)
+            t0 = time.perf_counter()
+            sim.run()
+            st = sim.summary()
+            st["wall_s"] = round(time.perf_counter() - t0, 3)
+            st["served_tokens_per_s_device"] = round(served / (st["device_ms"] / 1e3), 1)
+            st["served_tokens_per_s_wall"] = round(served / st["wall_s"], 1)
+            res[policy] = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in st.items()}
+    lpm = res["lpm"]
+    return {
+        "metric": METRIC, "value": lpm["served_tokens_per_s_device"], "unit": "tokens/s", "n_gpus": 1,
+        "steps": lpm["steps"], "warmup": 1, "ms_per_step": round(lpm["device_ms"] / lpm["steps"], 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "serving_stream", "requests": len(stream.requests), "pool_slots": cap,
+                   "max_running": 64, "prefill_budget": 16384, "heads_q_kv": "32/8", "head_dim": 128,
+                   "l2": "not flushed (a serving run; steps follow each other)"},
+        "e2e": {"value": lpm["served_tokens_per_s_wall"], "unit": "tokens/s (host + device wall clock)"},
+        "serving": res,
+        "lpm_over_fcfs": {"device_time": round(res["fcfs"]["device_ms"] / lpm["device_ms"], 3),
+                          "hit_rate": [lpm["hit_rate"], res["fcfs"]["hit_rate"]]},
+        "clocks": clocks.summary(),
+    }
+
+
 def run_ours(args, rank, world):
     import torch
     import workloads as W
@@ -403,8 +449,9 @@ def main():
     ap.add_argument("--no-cascade", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pool-slots", type=int, default=0)
-    ap.add_argument("--workload", default="", choices=["", "chunked_prefill"],
-                    help="chunked_prefill: long prompts prefilled chunk by chunk (instead of --config)")
+    ap.add_argument("--workload", default="", choices=["", "chunked_prefill", "serving"],
+                    help="chunked_prefill: long prompts prefilled chunk by chunk; serving: a multi-step "
+                         "serving run, longest-prefix-first against first-come-first-served (instead of --config)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -416,6 +463,11 @@ def main():
         if rank != 0:
             return
         print(json.dumps(run_reference(args, rank, world)))
+        return
+
+    if args.workload == "serving":
+        if rank == 0:
+            print(json.dumps(run_serving(args)))
         return
 
     if world > 1:

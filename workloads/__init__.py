@@ -18,6 +18,12 @@ from .generate import (  # noqa: F401
     multiturn_decode,
     tot_mixed,
     chunked_prefill,
+    StreamRequest,
+    ServingStream,
+    serving_stream,
+    token_kv,
+    stream_query,
+    generated_token,
     config,
     CONFIG_NAMES,
 )

@@ -268,6 +268,78 @@ def chunked_prefill(seed=6, n_req=16, prompt=8192, chunk=1024, hq=32, hkv=8, d=1
     return b.finish("chunked_prefill", seed, num_slots, dtype, meta={"chunk": steps})
 
 
+# --------------------------------------------------------------------------------------
+# a serving stream: requests arriving over steps, each generating tokens one step at a time
+
+
+@dataclass
+class StreamRequest:
+    rid: int
+    prompt: np.ndarray      # int32 token ids
+    out_len: int            # tokens to generate (one decode step each)
+    arrival: int            # step at which the request joins the waiting queue
+    group: int              # few-shot prompt group (shared prefix)
+
+
+@dataclass
+class ServingStream:
+    name: str
+    seed: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    sm_scale: float
+    requests: list
+
+
+def serving_stream(seed=7, n_groups=8, per_group=32, shared=1800, unique=(50, 150), out=(32, 64),
+                   per_step=16, hq=32, hkv=8, d=128) -> ServingStream:
+    """Few-shot serving: ``n_groups`` prompt groups, each a ``shared``-token prefix (the
+    examples) followed by a unique U[unique] question per request; every request then
+    generates U[out] tokens.  Requests arrive ``per_step`` at a time, the groups interleaved
+    in a seeded random order, so arrival order mixes the groups."""
+    rng = np.random.default_rng(seed)
+    prefixes = []
+    for _ in range(n_groups):
+        t = rng.integers(0, VOCAB, size=shared).astype(np.int32)
+        while any(len(p) and p[0] == t[0] for p in prefixes):
+            t[0] = np.int32(rng.integers(0, VOCAB))
+        prefixes.append(t)
+    groups = rng.permutation(np.repeat(np.arange(n_groups), per_group))
+    reqs = []
+    for i, g in enumerate(groups):
+        q = rng.integers(0, VOCAB, size=int(rng.integers(unique[0], unique[1] + 1))).astype(np.int32)
+        reqs.append(StreamRequest(i, np.concatenate([prefixes[g], q]), int(rng.integers(out[0], out[1] + 1)),
+                                  i // per_step, int(g)))
+    sm_scale = float(np.float32(1.0) / np.sqrt(np.float32(d)))
+    return ServingStream("serving_stream", seed, hq, hkv, d, sm_scale, reqs)
+
+
+def token_kv(seed: int, tokens, positions, hkv: int, d: int):
+    """bf16 bits of K and V ([n, hkv, d] uint16) for context entries (token id, position):
+    N(0, 1) values drawn from a generator keyed by (seed, token, position) alone, so equal
+    prefixes have equal K/V wherever they occur."""
+    n = len(tokens)
+    k = np.empty((n, hkv, d), np.uint16)
+    v = np.empty((n, hkv, d), np.uint16)
+    for i, (t, p) in enumerate(zip(tokens, positions)):
+        x = np.random.default_rng([seed, 1, int(t), int(p)]).standard_normal(2 * hkv * d, dtype=np.float32)
+        k[i] = to_bf16_bits(x[:hkv * d]).reshape(hkv, d)
+        v[i] = to_bf16_bits(x[hkv * d:]).reshape(hkv, d)
+    return k, v
+
+
+def stream_query(seed: int, rid: int, pos: int, hq: int, d: int):
+    """bf16 bits [hq, d] of request rid's query at context position pos."""
+    x = np.random.default_rng([seed, 3, int(rid), int(pos)]).standard_normal(hq * d, dtype=np.float32)
+    return to_bf16_bits(x).reshape(hq, d)
+
+
+def generated_token(seed: int, rid: int, j: int) -> int:
+    """Token id of request rid's j-th generated token."""
+    return int(np.random.default_rng([seed, 2, int(rid), int(j)]).integers(0, VOCAB))
+
+
 def config(k: int) -> Workload:
     """The five full-size workloads, seed = configuration number."""
     return {1: tiny_decode, 2: fewshot_extend, 3: batched_decode, 4: multiturn_decode,

@@ -105,7 +105,7 @@ class PkvError(RuntimeError):
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
-            f"{LIB_PATH} is missing: build it first (python -m prefix_shared_kv_token_gb300.build, or "
+            f"{LIB_PATH} is missing: build it first (python prefix_shared_kv_token_gb300/build.py, or "
             "__graft_entry__.build()); there is no fallback implementation")
     lib = C.CDLL(LIB_PATH)
     for name, (res, args) in SIGNATURES.items():

@@ -1,8 +1,9 @@
 """Compile the CUDA / C++ sources into the in-tree shared library ``libpkv.so``.
 
 nvcc only (no cmake): every translation unit is compiled in parallel for sm_103a, then
-linked into one shared object next to this file.  Run ``python -m
-prefix_shared_kv_token_gb300.build`` or call :func:`build`.
+linked into one shared object next to this file.  Run ``python
+prefix_shared_kv_token_gb300/build.py`` (importing the package needs the library already
+built) or call :func:`build`.
 """
 
 from __future__ import annotations

@@ -16,8 +16,8 @@
 //      per key).  Whole 2 KB slot rows move as 16-byte vectors; a bandwidth-bound kernel.
 //   2. extend_kernel: one CTA = two 128-row query tiles (each 128/G tokens x the G heads of
 //      KV head g) against one run's keys [0, nkeys), 128 keys per K/V tile.
-//        warp 0   TMA producer: Q tiles (3-D tile loads of q) and K/V tiles (3-D tile loads
-//                 of the gathered run, 128-byte swizzle) into a 2-stage ring;
+//        warps 0/2 TMA producers: Q tiles (3-D tile loads of q) and K tiles (warp 0), V
+//                 tiles (warp 2) of the gathered run, 128-byte swizzle, into a 2-stage ring;
 //        warp 1   tcgen05.mma issuer (one thread): S_q = Q_q K^T into tensor memory, then
 //                 O_q += P_q V with P_q read from tensor memory (the A operand) and V as an
 //                 MN-major shared-memory operand.  Issue order S0_j S1_j | PV0_j S0_j+1
@@ -28,6 +28,10 @@
 //                 memory only when the running max grows by more than 2^8 (p <= 256 stays
 //                 exact), and then without waiting: S_q of tile j completing implies PV_q of
 //                 tile j-1 completed (tcgen05 ops complete in issue order).
+//      An item with one query tile over several key tiles is split: warpgroup 0 takes the
+//      even key tiles into S0/O0, warpgroup 1 the odd ones into S1/O1 (both against Q tile
+//      0), each with its own running max and sum; the epilogue combines the two states, each
+//      warpgroup writing half of the head dimension.
 //      The softmax holds a row's 128 scores in registers (one tcgen05.ld pass), takes the
 //      row max as a tree, folds scale and max into one FFMA per score and skips the mask on
 //      full tiles; the kernel fits the 168-register budget of 384 threads without spilling.
@@ -47,6 +51,7 @@ constexpr int kBN = 128;  // keys per K/V tile
 constexpr int kXStages = 2;
 constexpr float kLog2eX = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kBarSplit = 1;               // named barrier of the two softmax warpgroups
 
 struct ExtendParams {
     uint16_t *o;
@@ -79,7 +84,7 @@ struct XCfg {
 
 struct XBars {
     uint64_t q, qempty;
-    uint64_t kfull[kXStages], vfull[kXStages], kvempty[kXStages];
+    uint64_t kfull[kXStages], vfull[kXStages], kvempty[kXStages], kempty[kXStages];
     uint64_t sfull[2], pfull[2], ofinal[2];
     uint64_t drain;
     uint32_t tmem_base;
@@ -250,6 +255,7 @@ PKV_DEV void exp_pack_regs(const uint32_t *sv, uint32_t col, float sc, float neg
 // Per-item fields every role reads.
 struct XItem {
     int32_t g, tok0, ntok, qpos0, pos0, nseg, rec, ntiles, nq;
+    bool split;  // one query tile over >= 2 key tiles: both softmax warpgroups take it
 };
 PKV_DEV XItem load_item(const ExtendItem *itp, int tq) {
     XItem x;
@@ -263,7 +269,38 @@ PKV_DEV XItem load_item(const ExtendItem *itp, int tq) {
     x.ntiles = 0;  // key tiles over all segments (each segment starts a new tile)
     for (int sg = 0; sg < x.nseg; ++sg) x.ntiles += (itp->nkeys[sg] + kBN - 1) / kBN;
     x.nq = x.ntok > tq ? 2 : 1;  // query tiles in use
+    // split: warpgroup 0 takes the even key tiles and warpgroup 1 the odd ones, each with its
+    // own running max, sum and accumulator (S_q, O_q), combined in the epilogue
+    x.split = x.nq == 1 && x.ntiles >= 2;
     return x;
+}
+
+// Epilogue of one row: 32 accumulator columns [32 c4, 32 c4 + 32) of query token t (global
+// token tok, head `head`) -- normalised to bf16 in o, or kept as an fp32 partial record
+// (acc, and (m, l) with the first columns).
+template <int D>
+PKV_DEV void write_out(const ExtendParams &p, const XItem &it, int t, int tok, int head, int c4, const uint32_t *ov,
+                       float m, float l) {
+    if (it.rec < 0) {
+        const float inv = l > 0.f ? p.v_scale / l : 0.f;
+        uint4 *dst = reinterpret_cast<uint4 *>(p.o + ((int64_t)tok * p.hq + head) * D + c4 * 32);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                w[e] = pack_bf16x2(__uint_as_float(ov[v * 8 + 2 * e]) * inv, __uint_as_float(ov[v * 8 + 2 * e + 1]) * inv);
+            dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    } else {
+        const int64_t rb = (int64_t)(p.rec_list ? __ldg(p.rec_list + it.rec + t) : it.rec + t) * p.hq + head;
+        float4 *dst = reinterpret_cast<float4 *>(p.rec_acc + rb * D + c4 * 32);
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+            dst[v] = make_float4(__uint_as_float(ov[4 * v]) * p.v_scale, __uint_as_float(ov[4 * v + 1]) * p.v_scale,
+                                 __uint_as_float(ov[4 * v + 2]) * p.v_scale, __uint_as_float(ov[4 * v + 3]) * p.v_scale);
+        if (c4 == 0) *reinterpret_cast<float2 *>(p.rec_ml + rb * 2) = make_float2(m, l);
+    }
 }
 
 // Persistent: one CTA per SM walks its own list of items (the plan deals them longest
@@ -290,6 +327,7 @@ __global__ void __launch_bounds__(384, 1)
 
     // once any CTA of this launch gave up on a wait, the rest exit instead of waiting too
     __shared__ int32_t s_skip;
+    __shared__ float2 s_ml[2][kBM];  // split items: each warpgroup's running (max, sum) per row
     if (threadIdx.x == 0) s_skip = (*reinterpret_cast<volatile int32_t *>(p.err) & DERR_TIMEOUT) != 0;
     __syncthreads();
     if (s_skip) return;
@@ -301,6 +339,7 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(&bars->kfull[s], 1);
             mbar_init(&bars->vfull[s], 1);
             mbar_init(&bars->kvempty[s], 1);
+            mbar_init(&bars->kempty[s], 1);
         }
         for (int q = 0; q < 2; ++q) {
             mbar_init(&bars->sfull[q], 1);
@@ -320,55 +359,64 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp == 0) {
+    if (warp == 0 || warp == 2) {
         if (lane == 0) {
-            // ================= TMA producer =================
-            prefetch_tmap(&qmap);
-            prefetch_tmap(&kmap);
-            prefetch_tmap(&vmap);
-            int tp = 0, nql = 0;  // tiles and Q loads issued by this CTA
+            // ================= TMA producers =================
+            // warp 0 loads Q and the K tiles, warp 2 the V tiles.  A stage is released by
+            // kvempty after its last P.V; a split item's tile also releases its K half early
+            // (kempty, after its S), so the next K tile loads while the P.V still holds V.
+            const bool kside = warp == 0;
+            const CUtensorMap *map = kside ? &kmap : &vmap;
+            uint64_t *full = kside ? bars->kfull : bars->vfull;
+            const uint32_t half = kside ? 0u : (uint32_t)C::kKTile;
+            prefetch_tmap(map);
+            if (kside) prefetch_tmap(&qmap);
+            int tp = 0, nql = 0;             // tiles and Q loads issued by this thread
+            uint32_t split_mask = 0;         // bit s: stage s's previous tile came from a split item
+            uint32_t kpar = 0;               // bit s: parity of the kempty commits due on stage s
             bool ok = true;
             for (int i = i0; ok && i < i1; ++i) {
                 const ExtendItem *itp = p.items + i;
                 const XItem it = load_item(itp, TQ);
-                if (nql > 0 && !xwait(&bars->qempty, (nql - 1) & 1, bars, p.err, 6)) break;
-                mbar_arrive_expect_tx(&bars->q, it.nq * C::kQTile);
-                for (int q = 0; q < it.nq; ++q)
+                if (kside) {
+                    if (nql > 0 && !xwait(&bars->qempty, (nql - 1) & 1, bars, p.err, 6)) break;
+                    mbar_arrive_expect_tx(&bars->q, it.nq * C::kQTile);
+                    for (int q = 0; q < it.nq; ++q)
 #pragma unroll
-                    for (int b = 0; b < NBLK; ++b)
-                        tma_load_3d(sbase + C::kQOff + q * C::kQTile + b * C::kBlkQ, &qmap, b * 64, it.g * G,
-                                    it.tok0 + q * TQ, &bars->q);
-                ++nql;
+                        for (int b = 0; b < NBLK; ++b)
+                            tma_load_3d(sbase + C::kQOff + q * C::kQTile + b * C::kBlkQ, &qmap, b * 64, it.g * G,
+                                        it.tok0 + q * TQ, &bars->q);
+                    ++nql;
+                }
                 int sg = 0, lt = 0;  // segment and tile within it
                 for (int j = 0; j < it.ntiles; ++j, ++tp) {
                     const int s = tp % ST;
-                    if (tp >= ST && !xwait(&bars->kvempty[s], ((tp / ST) - 1) & 1, bars, p.err, 5)) {
-                        ok = false;
-                        break;
+                    if (tp >= ST) {
+                        const bool early = kside && ((split_mask >> s) & 1u);
+                        uint64_t *bar = early ? &bars->kempty[s] : &bars->kvempty[s];
+                        const uint32_t par = early ? ((kpar >> s) & 1u) ^ 1u : (uint32_t)((tp / ST) - 1) & 1u;
+                        if (!xwait(bar, par, bars, p.err, kside ? 5 : 7)) {
+                            ok = false;
+                            break;
+                        }
                     }
-                    const uint32_t k_s = sbase + C::kStageOff + (s * 2) * C::kKTile;
+                    split_mask = (split_mask & ~(1u << s)) | ((uint32_t)it.split << s);
+                    kpar ^= (uint32_t)it.split << s;
+                    const uint32_t dst = sbase + C::kStageOff + (s * 2) * C::kKTile + half;
                     const int key = itp->key0[sg] + lt * kBN;
                     if (++lt * kBN >= itp->nkeys[sg]) {
                         ++sg;
                         lt = 0;
                     }
-                    mbar_arrive_expect_tx(&bars->kfull[s], C::kKTile);
+                    mbar_arrive_expect_tx(&full[s], C::kKTile);
 #pragma unroll
-                    for (int b = 0; b < NBLK; ++b)
-                        tma_load_3d(k_s + b * C::kBlkK, &kmap, b * 64, it.g, key, &bars->kfull[s]);
-                    mbar_arrive_expect_tx(&bars->vfull[s], C::kKTile);
-#pragma unroll
-                    for (int b = 0; b < NBLK; ++b)
-                        tma_load_3d(k_s + C::kKTile + b * C::kBlkK, &vmap, b * 64, it.g, key, &bars->vfull[s]);
+                    for (int b = 0; b < NBLK; ++b) tma_load_3d(dst + b * C::kBlkK, map, b * 64, it.g, key, &full[s]);
                 }
             }
             if (*reinterpret_cast<volatile int32_t *>(&bars->abort_flag)) {
                 // aborted: let this thread's copies still in flight land (bounded) before exit
-                if (nql > 0) mbar_wait(&bars->q, (nql - 1) & 1);
-                for (int t = tp > ST ? tp - ST : 0; t < tp; ++t) {
-                    mbar_wait(&bars->kfull[t % ST], (t / ST) & 1);
-                    mbar_wait(&bars->vfull[t % ST], (t / ST) & 1);
-                }
+                if (kside && nql > 0) mbar_wait(&bars->q, (nql - 1) & 1);
+                for (int t = tp > ST ? tp - ST : 0; t < tp; ++t) mbar_wait(&full[t % ST], (t / ST) & 1);
             }
         }
     } else if (warp == 1) {
@@ -377,59 +425,112 @@ __global__ void __launch_bounds__(384, 1)
             constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, 0, 0);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, 0, 1);
             int tm = 0, ip = 0;       // tiles and items before the current one
-            int cp[2] = {0, 0};       // phases consumed on pfull[q]
+            uint32_t cpar = 0;        // bit q: parity of the next phase to consume on pfull[q]
             bool ok = true;
             for (int i = i0; ok && i < i1; ++i, ++ip) {
                 const XItem it = load_item(p.items + i, TQ);
                 if (!xwait(&bars->q, ip & 1, bars, p.err, 1)) break;
-                auto issue_s = [&](int q, int j) -> bool {
-                    const int tg = tm + j, s = tg % ST;
-                    if (q == 0 && !xwait(&bars->kfull[s], (tg / ST) & 1, bars, p.err, 4)) return false;
-                    tc_fence_after();
-                    const uint32_t q_s = sbase + C::kQOff + q * C::kQTile;
-                    const uint32_t k_s = sbase + C::kStageOff + (s * 2) * C::kKTile;
+                if (!it.split) {
+                    auto issue_s = [&](int q, int j) -> bool {
+                        const int tg = tm + j, s = tg % ST;
+                        if (q == 0 && !xwait(&bars->kfull[s], (tg / ST) & 1, bars, p.err, 4)) return false;
+                        tc_fence_after();
+                        const uint32_t q_s = sbase + C::kQOff + q * C::kQTile;
+                        const uint32_t k_s = sbase + C::kStageOff + (s * 2) * C::kKTile;
 #pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint64_t qd = sdesc_sw128(q_s + (ks >> 2) * C::kBlkQ + (ks & 3) * 32, 16, 1024);
-                        const uint64_t kd = sdesc_sw128(k_s + (ks >> 2) * C::kBlkK + (ks & 3) * 32, 16, 1024);
-                        mma_ss(tmem + C::kColS + q * kBN, qd, kd, idesc_qk, ks > 0 ? 1u : 0u);
-                    }
-                    tc_commit(&bars->sfull[q]);
-                    if (j == it.ntiles - 1 && q == it.nq - 1) tc_commit(&bars->qempty);  // Q no longer read
-                    return true;
-                };
-                auto issue_pv = [&](int q, int j) -> bool {
-                    const int tg = tm + j, s = tg % ST;
-                    if (!xwait(&bars->pfull[q], cp[q] & 1, bars, p.err, 2)) return false;
-                    ++cp[q];
-                    if (q == 0 && !xwait(&bars->vfull[s], (tg / ST) & 1, bars, p.err, 3)) return false;
-                    tc_fence_after();
-                    const uint32_t v_s = sbase + C::kStageOff + (s * 2 + 1) * C::kKTile;
-#pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk) {
-                        const uint64_t vd = sdesc_sw128(v_s + kk * 16 * 128, C::kBlkK, 1024);
-                        mma_ts(tmem + C::kColO + q * D, tmem + C::kColS + q * kBN + kk * 8, vd, idesc_pv,
-                               (j > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    if constexpr (PRECISE) {  // + the weights' bf16 low parts, columns [64, 128) of S
+                        for (int ks = 0; ks < D / 16; ++ks) {
+                            const uint64_t qd = sdesc_sw128(q_s + (ks >> 2) * C::kBlkQ + (ks & 3) * 32, 16, 1024);
+                            const uint64_t kd = sdesc_sw128(k_s + (ks >> 2) * C::kBlkK + (ks & 3) * 32, 16, 1024);
+                            mma_ss(tmem + C::kColS + q * kBN, qd, kd, idesc_qk, ks > 0 ? 1u : 0u);
+                        }
+                        tc_commit(&bars->sfull[q]);
+                        if (j == it.ntiles - 1 && q == it.nq - 1) tc_commit(&bars->qempty);  // Q no longer read
+                        return true;
+                    };
+                    auto issue_pv = [&](int q, int j) -> bool {
+                        const int tg = tm + j, s = tg % ST;
+                        if (!xwait(&bars->pfull[q], (cpar >> q) & 1u, bars, p.err, 2)) return false;
+                        cpar ^= 1u << q;
+                        if (q == 0 && !xwait(&bars->vfull[s], (tg / ST) & 1, bars, p.err, 3)) return false;
+                        tc_fence_after();
+                        const uint32_t v_s = sbase + C::kStageOff + (s * 2 + 1) * C::kKTile;
 #pragma unroll
                         for (int kk = 0; kk < kBN / 16; ++kk) {
                             const uint64_t vd = sdesc_sw128(v_s + kk * 16 * 128, C::kBlkK, 1024);
-                            mma_ts(tmem + C::kColO + q * D, tmem + C::kColS + q * kBN + 64 + kk * 8, vd, idesc_pv, 1u);
+                            mma_ts(tmem + C::kColO + q * D, tmem + C::kColS + q * kBN + kk * 8, vd, idesc_pv,
+                                   (j > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        if constexpr (PRECISE) {  // + the weights' bf16 low parts, columns [64, 128) of S
+#pragma unroll
+                            for (int kk = 0; kk < kBN / 16; ++kk) {
+                                const uint64_t vd = sdesc_sw128(v_s + kk * 16 * 128, C::kBlkK, 1024);
+                                mma_ts(tmem + C::kColO + q * D, tmem + C::kColS + q * kBN + 64 + kk * 8, vd, idesc_pv,
+                                       1u);
+                            }
+                        }
+                        if (q == it.nq - 1) tc_commit(&bars->kvempty[s]);
+                        if (j == it.ntiles - 1) tc_commit(&bars->ofinal[q]);
+                        return true;
+                    };
+                    ok = issue_s(0, 0) && (it.nq < 2 || issue_s(1, 0));
+                    for (int j = 0; ok && j < it.ntiles; ++j) {
+                        if (!issue_pv(0, j)) { ok = false; break; }
+                        if (j + 1 < it.ntiles && !issue_s(0, j + 1)) { ok = false; break; }
+                        if (it.nq > 1) {
+                            if (!issue_pv(1, j)) { ok = false; break; }
+                            if (j + 1 < it.ntiles && !issue_s(1, j + 1)) { ok = false; break; }
                         }
                     }
-                    if (q == it.nq - 1) tc_commit(&bars->kvempty[s]);
-                    if (j == it.ntiles - 1) tc_commit(&bars->ofinal[q]);
-                    return true;
-                };
-                ok = issue_s(0, 0) && (it.nq < 2 || issue_s(1, 0));
-                for (int j = 0; ok && j < it.ntiles; ++j) {
-                    if (!issue_pv(0, j)) { ok = false; break; }
-                    if (j + 1 < it.ntiles && !issue_s(0, j + 1)) { ok = false; break; }
-                    if (it.nq > 1) {
-                        if (!issue_pv(1, j)) { ok = false; break; }
-                        if (j + 1 < it.ntiles && !issue_s(1, j + 1)) { ok = false; break; }
-                    }
+                } else {
+                    // split item: key tile j goes to S_{j&1} / O_{j&1}, all with Q tile 0.  Order
+                    // S(0) S(1) | PV(0) S(2) | PV(1) S(3) | ... -- the same ping-pong as above.
+                    // Each tile has a stage of its own, so its K half is released (kempty) once
+                    // its S is done and the next K tile loads while this one's P.V still waits.
+                    auto split_s = [&](int j) -> bool {
+                        const int q = j & 1, tg = tm + j, s = tg % ST;
+                        if (!xwait(&bars->kfull[s], (tg / ST) & 1, bars, p.err, 4)) return false;
+                        tc_fence_after();
+                        const uint32_t q_s = sbase + C::kQOff;
+                        const uint32_t k_s = sbase + C::kStageOff + (s * 2) * C::kKTile;
+#pragma unroll
+                        for (int ks = 0; ks < D / 16; ++ks) {
+                            const uint64_t qd = sdesc_sw128(q_s + (ks >> 2) * C::kBlkQ + (ks & 3) * 32, 16, 1024);
+                            const uint64_t kd = sdesc_sw128(k_s + (ks >> 2) * C::kBlkK + (ks & 3) * 32, 16, 1024);
+                            mma_ss(tmem + C::kColS + q * kBN, qd, kd, idesc_qk, ks > 0 ? 1u : 0u);
+                        }
+                        tc_commit(&bars->sfull[q]);
+                        tc_commit(&bars->kempty[s]);
+                        if (j == it.ntiles - 1) tc_commit(&bars->qempty);
+                        return true;
+                    };
+                    auto split_pv = [&](int j) -> bool {
+                        const int q = j & 1, tg = tm + j, s = tg % ST;
+                        if (!xwait(&bars->pfull[q], (cpar >> q) & 1u, bars, p.err, 2)) return false;
+                        cpar ^= 1u << q;
+                        if (!xwait(&bars->vfull[s], (tg / ST) & 1, bars, p.err, 3)) return false;
+                        tc_fence_after();
+                        const uint32_t v_s = sbase + C::kStageOff + (s * 2 + 1) * C::kKTile;
+#pragma unroll
+                        for (int kk = 0; kk < kBN / 16; ++kk) {
+                            const uint64_t vd = sdesc_sw128(v_s + kk * 16 * 128, C::kBlkK, 1024);
+                            mma_ts(tmem + C::kColO + q * D, tmem + C::kColS + q * kBN + kk * 8, vd, idesc_pv,
+                                   (j > 1 || kk > 0) ? 1u : 0u);
+                        }
+                        if constexpr (PRECISE) {
+#pragma unroll
+                            for (int kk = 0; kk < kBN / 16; ++kk) {
+                                const uint64_t vd = sdesc_sw128(v_s + kk * 16 * 128, C::kBlkK, 1024);
+                                mma_ts(tmem + C::kColO + q * D, tmem + C::kColS + q * kBN + 64 + kk * 8, vd, idesc_pv,
+                                       1u);
+                            }
+                        }
+                        tc_commit(&bars->kvempty[s]);
+                        if (j + 2 >= it.ntiles) tc_commit(&bars->ofinal[q]);  // O_q's last tile
+                        return true;
+                    };
+                    ok = split_s(0) && split_s(1);
+                    for (int j = 0; ok && j < it.ntiles; ++j)
+                        ok = split_pv(j) && (j + 2 >= it.ntiles || split_s(j + 2));
                 }
                 tm += it.ntiles;
             }
@@ -439,23 +540,39 @@ __global__ void __launch_bounds__(384, 1)
         }
         __syncwarp();
     } else if (warp >= 4) {
-        // ================= softmax + epilogue, query tile q =================
+        // ================= softmax + epilogue: query tile q, or in a split item the key
+        // tiles of parity q =================
         const int q = (warp - 4) >> 2;
         const int r = threadIdx.x - 128 - q * 128;              // row = TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t colS = tmem + lane_base + C::kColS + q * kBN;
         const uint32_t colO = tmem + lane_base + C::kColO + q * D;
         int cw = 0, co = 0;  // phases consumed on sfull[q] and ofinal[q]
+        bool alive = true;   // false after a failed wait; the remaining items are skipped
         for (int i = i0; i < i1; ++i) {
             const ExtendItem *itp = p.items + i;
             const XItem it = load_item(itp, TQ);
-            if (q >= it.nq) continue;
-            const int t = q * TQ + r / G;                       // token within the item
+            if (!it.split && q >= it.nq) continue;
+            if (!alive) {
+                // the other warpgroup meets the same barrier on every split item
+                if (it.split) named_bar_and(kBarSplit, 256, false);
+                continue;
+            }
+            const int t = (it.split ? 0 : q * TQ) + r / G;      // token within the item
             const int lim = it.qpos0 + t;                       // last visible position
             float m = -INFINITY, l = 0.f;
             bool ok = true;
             int sg = 0, lt = 0, segpos = it.pos0;  // segment, tile within it, its first position
+            const int jsecond = it.split ? 2 : 1;  // this warpgroup's second tile and later rescale O
             for (int j = 0; j < it.ntiles; ++j) {
+                if (it.split && (j & 1) != q) {  // the other warpgroup's tile: move the cursor only
+                    if (++lt * kBN >= itp->nkeys[sg]) {
+                        segpos += itp->nkeys[sg];
+                        ++sg;
+                        lt = 0;
+                    }
+                    continue;
+                }
                 // lanes leave together: a split warp must not reach the .sync.aligned tcgen05 ops
                 if (!__all_sync(0xffffffffu, xwait(&bars->sfull[q], cw & 1, bars, p.err, 8))) {
                     ok = false;
@@ -486,7 +603,7 @@ __global__ void __launch_bounds__(384, 1)
                 }
                 float mx[4];  // 3-input max: two new scores per instruction, 4 chains
 #pragma unroll
-                for (int k = 0; k < 4; ++k) mx[k] = __uint_as_float(sv[k]);
+                for (int c = 0; c < 4; ++c) mx[c] = __uint_as_float(sv[c]);
 #pragma unroll
                 for (int c = 4; c < kBN; c += 2)
                     mx[(c >> 1) & 3] = fmax3(mx[(c >> 1) & 3], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
@@ -495,7 +612,7 @@ __global__ void __launch_bounds__(384, 1)
                 bool rescale = false;
                 if (mt > m + kRescaleThreshold || m == -INFINITY) {
                     alpha = (m == -INFINITY) ? 0.f : ex2(m - mt);
-                    rescale = (j > 0) && (m != -INFINITY);
+                    rescale = (j >= jsecond) && (m != -INFINITY);
                     m = mt;
                 }
                 // exponent reference: the larger of m and the tile max (arguments <= 0)
@@ -512,8 +629,9 @@ __global__ void __launch_bounds__(384, 1)
                 }
                 const float ls0 = ls[0] + ls[2], ls1 = ls[1] + ls[3];
                 l = l * alpha + (ls0 + ls1);
-                // PV of tile j-1 is complete: S of tile j was issued after it.  The whole warp
-                // rescales when any of its rows must (.sync.aligned), the others by 1.
+                // this warpgroup's previous P.V is complete: its S of this tile was issued
+                // after it.  The whole warp rescales when any of its rows must
+                // (.sync.aligned), the others by 1.
                 if (__any_sync(0xffffffffu, rescale)) {
                     const float f = rescale ? alpha : 1.f;
 #pragma unroll 1
@@ -530,43 +648,59 @@ __global__ void __launch_bounds__(384, 1)
                 tc_fence_before();
                 mbar_arrive(&bars->pfull[q]);
             }
-            if (!__all_sync(0xffffffffu, ok && xwait(&bars->ofinal[q], co & 1, bars, p.err, 10))) break;
+            bool fin = __all_sync(0xffffffffu, ok && xwait(&bars->ofinal[q], co & 1, bars, p.err, 10));
+            if (it.split) {
+                // exchange the row's running max and sum with the other warpgroup; both
+                // warpgroups leave together when either gave up on a wait
+                s_ml[q][r] = make_float2(m, l);
+                tc_fence_before();
+                fin = named_bar_and(kBarSplit, 256, fin);
+            }
+            if (!fin) {
+                alive = false;
+                continue;
+            }
             ++co;
             tc_fence_after();
             const bool valid = t < it.ntok;
             const int tok = it.tok0 + t;
             const int head = it.g * G + (r % G);
+            if (!it.split) {
 #pragma unroll 1
-            for (int c4 = 0; c4 < D / 32; ++c4) {
-                uint32_t ov[32];
-                tmem_ld32(colO + c4 * 32, ov);
-                tmem_ld_wait();
-                if (!valid) continue;
-                if (it.rec < 0) {
-                    const float inv = l > 0.f ? p.v_scale / l : 0.f;
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + ((int64_t)tok * p.hq + head) * D + c4 * 32);
+                for (int c4 = 0; c4 < D / 32; ++c4) {
+                    uint32_t ov[32];
+                    tmem_ld32(colO + c4 * 32, ov);
+                    tmem_ld_wait();
+                    if (!valid) continue;
+                    write_out<D>(p, it, t, tok, head, c4, ov, m, l);
+                }
+            } else {
+                // O = O_0 f_0 + O_1 f_1 over the common max; warpgroup q writes the columns
+                // [q D / 2, (q + 1) D / 2)
+                const float2 other = s_ml[q ^ 1][r];
+                const float mm = fmaxf(m, other.x);
+                const float fs = m == -INFINITY ? 0.f : ex2(m - mm);
+                const float fo = other.x == -INFINITY ? 0.f : ex2(other.x - mm);
+                const float f0 = q == 0 ? fs : fo, f1 = q == 0 ? fo : fs;
+                l = l * fs + other.y * fo;
+                m = mm;
+                const uint32_t colO0 = tmem + lane_base + C::kColO;
+#pragma unroll 1
+                for (int c4 = q * (D / 64); c4 < (q + 1) * (D / 64); ++c4) {
+                    uint32_t ov[32], ov1[32];
+                    tmem_ld32(colO0 + c4 * 32, ov);
+                    tmem_ld32(colO0 + D + c4 * 32, ov1);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            w[k] = pack_bf16x2(__uint_as_float(ov[v * 8 + 2 * k]) * inv,
-                                               __uint_as_float(ov[v * 8 + 2 * k + 1]) * inv);
-                        dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
-                    }
-                } else {
-                    const int64_t rb = (int64_t)(p.rec_list ? __ldg(p.rec_list + it.rec + t) : it.rec + t) * p.hq + head;
-                    float4 *dst = reinterpret_cast<float4 *>(p.rec_acc + rb * D + c4 * 32);
-#pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        dst[v] = make_float4(__uint_as_float(ov[4 * v]) * p.v_scale,
-                                             __uint_as_float(ov[4 * v + 1]) * p.v_scale,
-                                             __uint_as_float(ov[4 * v + 2]) * p.v_scale,
-                                             __uint_as_float(ov[4 * v + 3]) * p.v_scale);
-                    if (c4 == 0) *reinterpret_cast<float2 *>(p.rec_ml + rb * 2) = make_float2(m, l);
+                    for (int c = 0; c < 32; ++c)
+                        ov[c] = __float_as_uint(fmaf(__uint_as_float(ov[c]), f0, __uint_as_float(ov1[c]) * f1));
+                    if (!valid) continue;
+                    write_out<D>(p, it, t, tok, head, c4, ov, m, l);
                 }
             }
             tc_fence_before();  // the next item's first P.V overwrites O after our next arrive
+            // split: both warpgroups have read O_0 and O_1 before either arrives on the next item
+            if (it.split) named_bar_sync(kBarSplit, 256);
         }
     }
 

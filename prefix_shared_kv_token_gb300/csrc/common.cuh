@@ -40,6 +40,17 @@ PKV_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::
 PKV_DEV void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// Named barrier that also ANDs a predicate over its `count` threads: every thread gets the
+// same answer, so a group can leave together.  Warp-uniform (aligned) use only.
+PKV_DEV bool named_bar_and(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
 
 // ---------------------------------------------------------------------------------------
 // mbarrier

@@ -75,12 +75,15 @@ void lpt_deal(const std::vector<T> &items, const std::vector<int64_t> &cost, int
     }
 }
 
-// Extend-kernel item weight: key tiles x (1 + query tiles) -- a two-tile item overlaps one
-// tile's softmax with the other's MMAs, so it costs less than twice a one-tile item.
+// Extend-kernel item weight, in half key-tile steps of a two-query-tile item (6 per key tile):
+// a two-tile item overlaps one tile's softmax with the other's MMAs; a one-tile item over
+// several key tiles splits them between the two softmax warpgroups (about half the cost of
+// a two-tile item); a one-tile item over one key tile runs serially.
 int64_t extend_item_cost(const ExtendItem &x, int32_t tq) {
     int64_t tiles = 0;
     for (int32_t i = 0; i < x.nseg; ++i) tiles += (x.nkeys[i] + 127) / 128;
-    return tiles * (1 + (x.ntok > tq ? 2 : 1)) + 2;
+    const int64_t per = x.ntok > tq ? 6 : (tiles >= 2 ? 3 : 4);
+    return tiles * per + 4;
 }
 
 // Keys per gather unit (one CTA each): up to 32, fewer when the gather is small, so that it

@@ -241,6 +241,24 @@ def test_extend_ragged(prefix, suffix):
     check_outputs(w, calls)
 
 
+@pytest.mark.parametrize("cascade", [True, False])
+@pytest.mark.parametrize("hq,hkv,prefix,suffix", [
+    (16, 16, 100, 60),   # 2 key tiles; rows 0..27 see no key of the second
+    (16, 16, 250, 3),
+    (8, 4, 129, 64),     # a full 128-row query tile over 2 key tiles
+    (32, 8, 1000, 20),   # 8 key tiles
+    (32, 8, 300, 31),    # 3 key tiles: the even-tile warpgroup takes one more
+    (16, 16, 10, 128),   # rows that see fewer than 32 keys (precise weights), 2 key tiles
+])
+def test_extend_one_query_tile_over_several_key_tiles(cascade, hq, hkv, prefix, suffix):
+    """A single query tile over two or more key tiles is split between the two softmax
+    warpgroups (alternate key tiles, partial states combined at the end)."""
+    w = W.fewshot_extend(seed=47 + prefix, n_req=2, prefix=prefix, suffix=suffix, hq=hq, hkv=hkv, d=128,
+                         num_slots=4000)
+    _, calls = run_step(w, cascade=cascade)
+    check_outputs(w, calls)
+
+
 def test_extend_without_prefix():
     b = W.generate._Builder(43, 32, 8, 128, 2000)
     leaves = [b.segment(-1, n) for n in (1, 77, 160)]

@@ -256,6 +256,16 @@ enum {
  * unknown policy). */
 int pkv_tree_set_policy(pkv_tree *t, int policy);
 
+/* Paged tree: cache whole blocks of page_size tokens only ([SG] §技術的詳細 / Technical
+ * Details: its cache's insert refers to the KV by 16-token block, position / 16).
+ * match_prefix, insert, match_len and schedule then use the key's first page_size * floor(n / page_size) tokens
+ * and compare a block at a time, so every node key, match length and cached length is a
+ * multiple of page_size; a request's trailing partial block stays out of the tree.  The
+ * slots a caller inserts for a block are expected to be one pool page (pkv_batch.page_size).
+ * Allowed only while the tree is empty (PKV_E_INVALID otherwise, or for page_size outside
+ * [1, 4096]); page_size 1 is the token tree. */
+int pkv_tree_set_page_size(pkv_tree *t, int32_t page_size);
+
 /* Longest cached prefix of key[0..n) ([RC] "프리픽스 매칭"): writes its slots to values
  * (up to values_cap of them), the matched length to *matched and the last node on the
  * matched path to *last_node (0 = root when nothing matched).  A match that ends inside a

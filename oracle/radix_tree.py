@@ -41,6 +41,18 @@ hit_count: every node on the path a match_prefix returns (root excluded) gains o
 counted after any split.  priority: an insert raises its start node's priority to at least
 its own and gives it to the leaf it creates; a split's upper part takes the child's
 priority (as printed in "노드 분할"); new nodes otherwise start at 0 hits.
+
+Paged tree (page_size P > 1; "Efficiently Programming Large Language Models using SGLang"
+(summary), §Technical Details, whose cache insert refers to the KV by
+16-token block, position / 16).  The plainest reading that keeps the rest of the tree's
+behaviour: the cache holds whole blocks of P tokens only.
+  * match_prefix and insert look at the key's first P * floor(len / P) tokens; a trailing
+    partial block is never matched or inserted (it stays with the request that owns it);
+  * tokens compare a block at a time: a block matches when all its P tokens are equal, so
+    every node key, match length, split point and cached length is a multiple of P;
+  * a node's child key is its first block (the tuple of its first P tokens);
+  * everything else (times, hits, priorities, eviction, locking) is unchanged.
+With P = 1 every rule above is the token tree's.
 """
 
 from __future__ import annotations
@@ -84,20 +96,28 @@ def eviction_key(policy: str, n: TreeNode):
     raise ValueError(policy)
 
 
-def _key_match(a, b) -> int:
-    """Number of equal leading tokens of a and b."""
+def _key_match(a, b, page: int = 1) -> int:
+    """Number of equal leading tokens of a and b, counted in whole blocks of ``page``
+    tokens (a block counts only when all of its tokens are equal)."""
     n = 0
-    for x, y in zip(a, b):
-        if x != y:
-            break
-        n += 1
+    if page == 1:
+        for x, y in zip(a, b):
+            if x != y:
+                break
+            n += 1
+        return n
+    while n + page <= min(len(a), len(b)) and list(a[n:n + page]) == list(b[n:n + page]):
+        n += page
     return n
 
 
 class RadixCache:
-    def __init__(self, policy: str = "lru"):
+    def __init__(self, policy: str = "lru", page_size: int = 1):
         if policy not in POLICIES:
             raise ValueError(policy)
+        if page_size < 1:
+            raise ValueError(page_size)
+        self.page = page_size
         self.policy = policy
         self._next_id = 0
         self.clock = 0
@@ -111,18 +131,25 @@ class RadixCache:
         self._next_id += 1
         return n
 
+    def _child_key(self, key):
+        """Key of a child in its parent's table: its first token, or its first block."""
+        return key[0] if self.page == 1 else tuple(key[:self.page])
+
+    def _aligned(self, key):
+        return list(key)[:len(key) // self.page * self.page]
+
     # ---- match -------------------------------------------------------------------
     def match_prefix(self, key):
         """Longest cached prefix of ``key``: (concatenated slot values, last node)."""
         self.clock += 1
-        key = list(key)
+        key = self._aligned(key)
         node = self.root
         node.last_access_time = self.clock
         values = []
-        while key and key[0] in node.children:
-            child = node.children[key[0]]
+        while key and self._child_key(key) in node.children:
+            child = node.children[self._child_key(key)]
             child.last_access_time = self.clock
-            n = _key_match(child.key, key)
+            n = _key_match(child.key, key, self.page)
             if n < len(child.key):
                 upper = self._split_node(child.key, child, n)
                 values.extend(upper.value)
@@ -139,7 +166,7 @@ class RadixCache:
 
     def _split_node(self, key, child: TreeNode, split_len: int) -> TreeNode:
         upper = self._new_node(child.priority)
-        upper.children = {key[split_len]: child}
+        upper.children = {self._child_key(key[split_len:]): child}
         upper.parent = child.parent
         upper.lock_ref = child.lock_ref
         upper.key = child.key[:split_len]
@@ -147,7 +174,7 @@ class RadixCache:
         child.parent = upper
         child.key = child.key[split_len:]
         child.value = child.value[split_len:]
-        upper.parent.children[key[0]] = upper
+        upper.parent.children[self._child_key(key)] = upper
         return upper
 
     # ---- insert ------------------------------------------------------------------
@@ -156,14 +183,14 @@ class RadixCache:
         (the caller frees those entries of ``value``, they duplicate cached slots)."""
         assert len(key) == len(value)
         self.clock += 1
-        key, value = list(key), list(value)
+        key, value = self._aligned(key), list(value)[:len(self._aligned(key))]
         node = self.root
         node.last_access_time = self.clock
         node.priority = max(node.priority, priority)
         total = 0
-        while key and key[0] in node.children:
-            node = node.children[key[0]]
-            n = _key_match(node.key, key)
+        while key and self._child_key(key) in node.children:
+            node = node.children[self._child_key(key)]
+            n = _key_match(node.key, key, self.page)
             total += n
             key, value = key[n:], value[n:]
             if n < len(node.key):
@@ -173,7 +200,7 @@ class RadixCache:
             leaf.parent = node
             leaf.key = key
             leaf.value = value
-            node.children[key[0]] = leaf
+            node.children[self._child_key(key)] = leaf
             self.evictable_size_ += len(key)
         return total
 
@@ -199,7 +226,7 @@ class RadixCache:
             freed.extend(x.value)
             evicted += len(x.value)
             parent = x.parent
-            del parent.children[x.key[0]]
+            del parent.children[self._child_key(x.key)]
             self.evictable_size_ -= len(x.key)
             if not parent.children and parent.lock_ref == 0:
                 heapq.heappush(heap, (eviction_key(self.policy, parent), parent))

@@ -20,16 +20,16 @@ from __future__ import annotations
 
 def peek_match_len(tree, key) -> int:
     """Length of the longest cached prefix of ``key`` in the oracle ``RadixCache`` ``tree``,
-    walking child keys without splitting or touching any node."""
-    key = list(key)
+    walking child keys without splitting or touching any node.  A paged tree compares
+    whole blocks and ignores the key's trailing partial block, as its match_prefix does."""
+    page = tree.page
+    key = list(key)[:len(key) // page * page]
     node, n = tree.root, 0
-    while key and key[0] in node.children:
-        child = node.children[key[0]]
+    while key and tree._child_key(key) in node.children:
+        child = node.children[tree._child_key(key)]
         m = 0
-        for a, b in zip(child.key, key):
-            if a != b:
-                break
-            m += 1
+        while m + page <= min(len(child.key), len(key)) and child.key[m:m + page] == key[m:m + page]:
+            m += page
         n += m
         if m < len(child.key):
             break

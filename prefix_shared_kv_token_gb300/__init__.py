@@ -217,10 +217,13 @@ def set_kernel_events(start=None, stop=None) -> None:
 class RadixTree:
     POLICIES = ("lru", "lfu", "slru", "fifo", "mru", "filo", "priority")   # = PKV_EVICT_* order
 
-    def __init__(self, policy: str = "lru"):
+    def __init__(self, policy: str = "lru", page_size: int = 1):
         self._h = lib.pkv_tree_new()
         if not self._h:
             raise MemoryError("pkv_tree_new")
+        self.page_size = int(page_size)
+        if self.page_size != 1:
+            check("pkv_tree_set_page_size", lib.pkv_tree_set_page_size(self._h, self.page_size))
         if policy != "lru":
             self.set_policy(policy)
 

@@ -80,6 +80,7 @@ SIGNATURES = {
     "pkv_tree_insert": (C.c_int, [_P, _P, _P, _I64, _PI64]),
     "pkv_tree_insert_priority": (C.c_int, [_P, _P, _P, _I64, _I64, _PI64]),
     "pkv_tree_set_policy": (C.c_int, [_P, C.c_int]),
+    "pkv_tree_set_page_size": (C.c_int, [_P, _I32]),
     "pkv_tree_match_len": (C.c_int, [_P, _P, _I64, _PI64]),
     "pkv_schedule": (C.c_int, [_P, _P, _P, _I32, C.c_int, _P, _P]),
     "pkv_tree_evict": (C.c_int, [_P, _I64, _P, _I64, _PI64]),

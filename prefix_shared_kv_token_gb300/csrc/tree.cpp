@@ -24,6 +24,13 @@
 // returns (after any split); an insert raises its start node's priority to its own and gives
 // it to the leaf it creates; a split's upper part takes the child's priority.
 //
+// Paged tree (pkv_tree_set_page_size, P > 1; "Efficiently Programming Large Language Models
+// using SGLang", §Technical Details: its cache's insert refers to the KV by
+// 16-token block: position / 16): the cache holds whole blocks of P tokens.  match_prefix
+// and insert use the key's first P * floor(n / P) tokens, tokens compare a block at a time
+// (a block matches when all its tokens are equal), and a child is keyed by its first block.
+// Every node key, match length, split point and cached length is then a multiple of P.
+//
 // The cascade extraction (pkv_tree_cascade) turns the nodes shared by several requests of a
 // batch into spans for the attention kernels: the tree already knows which prefix KV is
 // shared ("Radix Tree 구조도": both branches under [1,2,3] share its KV).
@@ -45,7 +52,7 @@ namespace {
 struct Node {
     int64_t id = 0;
     int64_t parent = -1;
-    std::unordered_map<int32_t, int64_t> children;
+    std::unordered_map<int64_t, int64_t> children;  // child key (first token / block id) -> id
     std::vector<int32_t> key;
     std::vector<int32_t> value;
     int64_t lock_ref = 0;
@@ -56,6 +63,18 @@ struct Node {
 };
 
 constexpr int64_t kSlruProtect = 2;  // hits that move a node into SLRU's protected segment
+constexpr int64_t kNoBlock = INT64_MIN;  // a block that no node's key starts with
+
+struct BlockHash {
+    size_t operator()(const std::vector<int32_t> &b) const {
+        uint64_t h = 1469598103934665603ull;  // FNV-1a over the tokens
+        for (int32_t t : b) {
+            h ^= (uint32_t)t;
+            h *= 1099511628211ull;
+        }
+        return (size_t)h;
+    }
+};
 
 }  // namespace
 
@@ -66,6 +85,10 @@ struct pkv_tree {
     int64_t protected_ = 0;
     int64_t live = 0;
     int policy = PKV_EVICT_LRU;
+    int64_t page = 1;  // tokens per block
+    // paged tree: block contents -> small id, for the child tables (a block is interned when
+    // a node key first starts with it)
+    std::unordered_map<std::vector<int32_t>, int64_t, BlockHash> block_ids;
 
     pkv_tree() {
         Node root;
@@ -85,10 +108,30 @@ struct pkv_tree {
         return nodes.back().id;
     }
 
-    static int64_t key_match(const int32_t *a, int64_t na, const int32_t *b, int64_t nb) {
+    // Equal leading tokens of a and b, in whole blocks.
+    int64_t key_match(const int32_t *a, int64_t na, const int32_t *b, int64_t nb) const {
         int64_t n = std::min(na, nb), i = 0;
         while (i < n && a[i] == b[i]) ++i;
-        return i;
+        return i / page * page;
+    }
+
+    // Key of a child whose key starts at k: its first token, or its block's id (interned
+    // when `create`, else kNoBlock for a block no node starts with).
+    int64_t child_key(const int32_t *k, bool create) {
+        if (page == 1) return k[0];
+        std::vector<int32_t> b(k, k + page);
+        auto it = block_ids.find(b);
+        if (it != block_ids.end()) return it->second;
+        if (!create) return kNoBlock;
+        const int64_t id = (int64_t)block_ids.size();
+        block_ids.emplace(std::move(b), id);
+        return id;
+    }
+    int64_t find_child(int64_t node, const int32_t *k) {
+        const int64_t ck = child_key(k, false);
+        if (ck == kNoBlock) return -1;
+        auto it = nodes[node].children.find(ck);
+        return it == nodes[node].children.end() ? -1 : it->second;
     }
 
     // Split `child` after split_len tokens; returns the new upper node.
@@ -103,20 +146,21 @@ struct pkv_tree {
         c.key.erase(c.key.begin(), c.key.begin() + split_len);
         c.value.erase(c.value.begin(), c.value.begin() + split_len);
         c.parent = up;
-        u.children[c.key[0]] = child;
-        nodes[u.parent].children[u.key[0]] = up;
+        const int64_t ck = child_key(c.key.data(), true), uk = child_key(u.key.data(), true);
+        nodes[up].children[ck] = child;
+        nodes[nodes[up].parent].children[uk] = up;
         return up;
     }
 
     int64_t match(const int32_t *key, int64_t n, std::vector<int32_t> *values) {
         ++clock;
+        n = n / page * page;
         int64_t node = 0;
         nodes[0].last_access_time = clock;
         int64_t pos = 0;
         while (pos < n) {
-            auto it = nodes[node].children.find(key[pos]);
-            if (it == nodes[node].children.end()) break;
-            int64_t child = it->second;
+            const int64_t child = find_child(node, key + pos);
+            if (child < 0) break;
             nodes[child].last_access_time = clock;
             int64_t m = key_match(nodes[child].key.data(), (int64_t)nodes[child].key.size(),
                                   key + pos, n - pos);
@@ -135,12 +179,13 @@ struct pkv_tree {
     }
 
     // Cached prefix length of key without touching the tree (no split, no time, no hit).
-    int64_t peek(const int32_t *key, int64_t n) const {
+    int64_t peek(const int32_t *key, int64_t n) {
+        n = n / page * page;
         int64_t node = 0, pos = 0;
         while (pos < n) {
-            auto it = nodes[node].children.find(key[pos]);
-            if (it == nodes[node].children.end()) break;
-            const Node &c = nodes[it->second];
+            const int64_t child = find_child(node, key + pos);
+            if (child < 0) break;
+            const Node &c = nodes[child];
             int64_t m = key_match(c.key.data(), (int64_t)c.key.size(), key + pos, n - pos);
             pos += m;
             if (m < (int64_t)c.key.size()) break;
@@ -151,14 +196,15 @@ struct pkv_tree {
 
     int64_t insert(const int32_t *key, const int32_t *value, int64_t n, int64_t priority) {
         ++clock;
+        n = n / page * page;
         int64_t node = 0;
         nodes[0].last_access_time = clock;
         nodes[0].priority = std::max(nodes[0].priority, priority);
         int64_t pos = 0, total = 0;
         while (pos < n) {
-            auto it = nodes[node].children.find(key[pos]);
-            if (it == nodes[node].children.end()) break;
-            node = it->second;
+            const int64_t child = find_child(node, key + pos);
+            if (child < 0) break;
+            node = child;
             int64_t m = key_match(nodes[node].key.data(), (int64_t)nodes[node].key.size(),
                                   key + pos, n - pos);
             total += m;
@@ -171,7 +217,7 @@ struct pkv_tree {
             l.parent = node;
             l.key.assign(key + pos, key + n);
             l.value.assign(value + pos, value + n);
-            nodes[node].children[key[pos]] = leaf;
+            nodes[node].children[child_key(key + pos, true)] = leaf;
             evictable += n - pos;
         }
         return total;
@@ -209,7 +255,7 @@ struct pkv_tree {
             freed->insert(freed->end(), x.value.begin(), x.value.end());
             evicted += (int64_t)x.value.size();
             Node &p = nodes[x.parent];
-            p.children.erase(x.key[0]);
+            p.children.erase(child_key(x.key.data(), false));
             evictable -= (int64_t)x.key.size();
             x.alive = false;
             x.children.clear();
@@ -295,6 +341,14 @@ int pkv_tree_insert_priority(pkv_tree *t, const int32_t *key, const int32_t *val
     if (!t || n < 0 || (n > 0 && (!key || !value))) return PKV_E_INVALID;
     int64_t total = t->insert(key, value, n, priority);
     if (prefix_len) *prefix_len = total;
+    return PKV_OK;
+}
+
+int pkv_tree_set_page_size(pkv_tree *t, int32_t page_size) {
+    if (!t || page_size < 1 || page_size > 4096) return PKV_E_INVALID;
+    if (t->live != 1) return PKV_E_INVALID;  // only while the tree holds nothing
+    t->page = page_size;
+    t->block_ids.clear();
     return PKV_OK;
 }
 

@@ -168,3 +168,53 @@ def test_schedule_matches_oracle(seed):
         assert b.schedule(queue, policy) == schedule(a, queue, policy)
     assert sorted(b.dump()) == before            # scheduling leaves the tree as it was
     assert [b.match_len(q) for q in queue] == schedule(a, queue)[1]
+
+
+@pytest.mark.parametrize("page", [2, 4, 16])
+@pytest.mark.parametrize("seed", range(3))
+def test_paged_random_ops_bit_exact(page, seed):
+    """Paged trees (whole blocks of ``page`` tokens): C++ = oracle after random inserts,
+    matches (with splits at block boundaries), locks, evictions and schedules."""
+    from oracle.schedule import schedule
+    rng = random.Random(1000 * page + seed)
+    a, b = RadixCache("lru", page_size=page), RadixTree("lru", page_size=page)
+    locked, nxt = [], 0
+    for _ in range(300):
+        op = rng.random()
+        # few distinct tokens, so that keys often share leading tokens inside a block
+        key = [rng.randint(0, 2) for _ in range(rng.randint(0, 5 * page))]
+        if op < 0.4:
+            v = list(range(nxt, nxt + len(key)))
+            nxt += len(key)
+            assert a.insert(key, v) == b.insert(key, v)
+        elif op < 0.65:
+            va, na = a.match_prefix(key)
+            vb, nb = b.match_prefix(key)
+            assert va == vb.tolist() and na.id == nb and len(va) % page == 0
+            if va and rng.random() < 0.4:
+                assert a.inc_lock_ref(na) == b.inc_lock_ref(nb)
+                locked.append((na, nb))
+        elif op < 0.75 and locked:
+            na, nb = locked.pop(rng.randrange(len(locked)))
+            assert a.dec_lock_ref(na) == b.dec_lock_ref(nb)
+        else:
+            n = rng.randint(1, 3 * page)
+            assert a.evict(n) == b.evict(n).tolist()
+        s = b.sizes()
+        assert (s["evictable"], s["protected"], s["total"]) == (a.evictable_size_, a.protected_size_,
+                                                              a.total_size())
+    assert _oracle_dump(a) == sorted(b.dump())
+    assert all(len(r[4]) % page == 0 for r in b.dump())
+    queue = [[rng.randint(0, 2) for _ in range(rng.randint(0, 5 * page))] for _ in range(40)]
+    for policy in ("lpm", "fcfs"):
+        assert b.schedule(queue, policy) == schedule(a, queue, policy)
+
+
+def test_page_size_only_on_an_empty_tree():
+    from prefix_shared_kv_token_gb300 import _lib
+    t = RadixTree()
+    assert _lib.lib.pkv_tree_set_page_size(t._h, 0) == -1
+    assert _lib.lib.pkv_tree_set_page_size(t._h, 16) == 0
+    t.insert(list(range(20)), list(range(20)))
+    assert _lib.lib.pkv_tree_set_page_size(t._h, 4) == -1   # holds nodes: refused
+    assert t.match_prefix(list(range(20)))[0].tolist() == list(range(16))

@@ -96,12 +96,20 @@ int pkv_kv_store(const pkv_pool *pool, const void *k_new, const void *v_new,
 /* batch tables consumed by the attention calls (all device memory)                     */
 
 typedef struct pkv_batch {
-    const int32_t *req_to_token;      /* [num_rows][stride]: slot of each context position */
-    int64_t        stride;            /* >= longest context                                 */
+    const int32_t *req_to_token;      /* [num_rows][stride]: slot of each context position, */
+                                      /* or with page_size > 1 the page of each block       */
+    int64_t        stride;            /* entries per row: >= longest context (in blocks)    */
     int32_t        num_rows;
     const int32_t *req_pool_indices;  /* [batch]: row of request r in req_to_token          */
     const int32_t *seq_lens;          /* [batch]: context length of r, new tokens included  */
     int32_t        batch;
+    /* 0 or 1: a token table (above).  P > 1, a power of two <= 4096: a paged pool whose page
+     * k holds slots [k P, k P + P); req_to_token[row][b] is the page of positions
+     * [b P, b P + P), so position t reads slot req_to_token[row][t / P] * P + t % P ([SG]
+     * §Technical Details: the KV is referred to by 16-token block).  Any other value:
+     * PKV_E_INVALID.  A page whose slots fall outside the pool reads as zero K/V rows and
+     * sets PKV_DERR_SLOT_RANGE. */
+    int32_t        page_size;
 } pkv_batch;
 
 /* A shared-prefix cascade, in host memory.  Span s is a run of positions

@@ -89,15 +89,17 @@ class Pool:
 @dataclass
 class Batch:
     """Device batch tables: req_to_token [rows, stride] int32, req_pool_indices [B] int32,
-    seq_lens [B] int32 (torch tensors on the GPU)."""
+    seq_lens [B] int32 (torch tensors on the GPU).  With page_size P > 1, req_to_token holds
+    the page of each P-token block of a row (see pkv_batch)."""
     req_to_token: object
     req_pool_indices: object
     seq_lens: object
+    page_size: int = 1
 
     def c(self) -> PkvBatch:
         rt = self.req_to_token
         return PkvBatch(_ptr(rt), rt.shape[1], rt.shape[0], _ptr(self.req_pool_indices), _ptr(self.seq_lens),
-                        self.req_pool_indices.shape[0])
+                        self.req_pool_indices.shape[0], int(self.page_size))
 
 
 @dataclass

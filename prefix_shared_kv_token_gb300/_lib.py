@@ -30,7 +30,8 @@ class PkvPool(C.Structure):
 
 class PkvBatch(C.Structure):
     _fields_ = [("req_to_token", C.c_void_p), ("stride", C.c_int64), ("num_rows", C.c_int32),
-                ("req_pool_indices", C.c_void_p), ("seq_lens", C.c_void_p), ("batch", C.c_int32)]
+                ("req_pool_indices", C.c_void_p), ("seq_lens", C.c_void_p), ("batch", C.c_int32),
+                ("page_size", C.c_int32)]
 
 
 class PkvCascade(C.Structure):

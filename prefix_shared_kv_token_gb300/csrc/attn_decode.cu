@@ -48,6 +48,7 @@ struct DecodeParams {
     const int32_t *req_to_token;
     int64_t rt_stride;
     int32_t rt_rows;
+    int32_t page_shift;  // 0: token table; else log2 of the page size (page table)
     int32_t batch;
     const int32_t *req_pool_indices;
     const int32_t *seq_lens;
@@ -287,7 +288,7 @@ PKV_DEV TileSlot next_tile(const DecodeParams &p, TileCursor &cur, int c1, int k
         const DecodeItem it = p.items[cur.i];
         const int row = __ldg(p.req_pool_indices + it.src);
         const int k1 = it.k1 < 0 ? __ldg(p.seq_lens + it.src) : it.k1;
-        if (row < 0 || row >= p.rt_rows || it.k0 < 0 || k1 > p.rt_stride || k1 <= it.k0) {
+        if (row < 0 || row >= p.rt_rows || it.k0 < 0 || k1 > (p.rt_stride << p.page_shift) || k1 <= it.k0) {
             if ((threadIdx.x & 31) == 0) set_error(p.err, DERR_POSITION);
             continue;
         }
@@ -305,7 +306,7 @@ PKV_DEV TileSlot next_tile(const DecodeParams &p, TileCursor &cur, int c1, int k
     e.info.flags = (cur.j == 0 ? kFirst : 0) | (cur.j == cur.nt - 1 ? kLast : 0);
     e.g0 = cur.g0;
     const int kp = e.info.kpos + key;
-    e.slot = kp < cur.k1 ? __ldg(cur.rt + kp) : -1;
+    e.slot = kp < cur.k1 ? table_slot(cur.rt, kp, p.page_shift, p.num_slots) : -1;
     ++cur.j;
     cur.jj = cur.jj + 1 == cur.nt ? 0 : cur.jj + 1;
     return e;
@@ -579,6 +580,7 @@ int check_call(const pkv_pool *pool, const pkv_batch *batch, const void *q, void
     if (rc) return rc;
     if (!batch || !q || !o || !info || !plan_dev || !workspace) return PKV_E_INVALID;
     if (!batch->req_to_token || !batch->req_pool_indices || !batch->seq_lens) return PKV_E_INVALID;
+    if (page_shift_of(batch) < 0) return PKV_E_INVALID;
     if (info->op != op || info->batch != batch->batch) return PKV_E_PLAN;
     if (info->num_kv_heads != pool->num_kv_heads || info->head_dim != pool->head_dim) return PKV_E_PLAN;
     if (ws_bytes < info->workspace_bytes) return PKV_E_WORKSPACE;
@@ -612,6 +614,7 @@ extern "C" int pkv_attn_decode(const pkv_pool *pool, const pkv_batch *batch, con
     p.req_to_token = batch->req_to_token;
     p.rt_stride = batch->stride;
     p.rt_rows = batch->num_rows;
+    p.page_shift = page_shift_of(batch);
     p.batch = batch->batch;
     p.req_pool_indices = batch->req_pool_indices;
     p.seq_lens = batch->seq_lens;

@@ -118,6 +118,7 @@ struct GatherParams {
     const int32_t *req_to_token;
     int64_t rt_stride;
     int32_t rt_rows;
+    int32_t page_shift;  // 0: token table; else log2 of the page size (page table)
     const int32_t *req_pool_indices;
     const GatherUnit *units;
     uint16_t *k_out;
@@ -131,14 +132,15 @@ template <int D, bool FP8>
 __global__ void __launch_bounds__(256) gather_kernel(const GatherParams p) {
     const GatherUnit u = p.units[blockIdx.x];
     const int row = __ldg(p.req_pool_indices + u.src);
-    if (row < 0 || row >= p.rt_rows || u.pos0 < 0 || u.pos0 + u.len > p.rt_stride) {
+    if (row < 0 || row >= p.rt_rows || u.pos0 < 0 || u.pos0 + u.len > (p.rt_stride << p.page_shift)) {
         if (threadIdx.x == 0) set_error(p.err, DERR_POSITION);
         return;
     }
     // the unit's slots, checked once
     __shared__ int32_t s_slot[32];
     if (threadIdx.x < u.len) {
-        int32_t slot = __ldg(p.req_to_token + (int64_t)row * p.rt_stride + u.pos0 + threadIdx.x);
+        int32_t slot = table_slot(p.req_to_token + (int64_t)row * p.rt_stride, u.pos0 + threadIdx.x, p.page_shift,
+                                  p.num_slots);
         if (slot < 0 || (int64_t)slot >= p.num_slots) {
             set_error(p.err, DERR_SLOT_RANGE);
             slot = -1;  // zero row
@@ -820,6 +822,7 @@ int decode_span_tensor(const pkv_pool *pool, const pkv_batch *batch, const void 
     gp.req_to_token = batch->req_to_token;
     gp.rt_stride = batch->stride;
     gp.rt_rows = batch->num_rows;
+    gp.page_shift = page_shift_of(batch);
     gp.req_pool_indices = batch->req_pool_indices;
     gp.units = reinterpret_cast<const GatherUnit *>(plan + info->offsets[9]);
     gp.k_out = kg;
@@ -896,6 +899,7 @@ extern "C" int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, con
     gp.req_to_token = batch->req_to_token;
     gp.rt_stride = batch->stride;
     gp.rt_rows = batch->num_rows;
+    gp.page_shift = page_shift_of(batch);
     gp.req_pool_indices = batch->req_pool_indices;
     gp.units = reinterpret_cast<const GatherUnit *>(plan + info->offsets[4]);
     gp.k_out = kg;

@@ -36,6 +36,16 @@ PKV_DEV uint64_t global_timer_ns() {
 
 PKV_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// Slot of context position t from a row of the batch table: the token table's entry, or
+// with pages of 2^shift slots, the position's page times the page size plus its offset.
+// A page outside the pool gives -1 (the callers flag it and read zeros).
+PKV_DEV int32_t table_slot(const int32_t *row, int t, int shift, int64_t num_slots) {
+    if (shift == 0) return __ldg(row + t);
+    const int32_t pg = __ldg(row + (t >> shift));
+    const int64_t slot = ((int64_t)pg << shift) + (t & ((1 << shift) - 1));
+    return (pg < 0 || slot >= num_slots) ? -1 : (int32_t)slot;
+}
+
 // Named barrier `id` (1..15) among `count` threads (a multiple of 32).
 PKV_DEV void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

@@ -26,6 +26,16 @@ inline int validate_pool(const pkv_pool *p) {
     return PKV_OK;
 }
 
+// log2 of the batch table's page size (0 for a token table, page_size 0 or 1); -1 when the
+// page size is not a power of two in [1, 4096].
+inline int page_shift_of(const pkv_batch *b) {
+    const int32_t ps = b->page_size <= 1 ? 1 : b->page_size;
+    if (ps > 4096 || (ps & (ps - 1))) return -1;
+    int sh = 0;
+    while ((1 << sh) < ps) ++sh;
+    return sh;
+}
+
 // cuTensorMapEncodeTiled, resolved once through cudaGetDriverEntryPoint (no -lcuda needed).
 CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType dtype, cuuint32_t rank, void *base,
                       const cuuint64_t *dims, const cuuint64_t *strides_bytes, const cuuint32_t *box,

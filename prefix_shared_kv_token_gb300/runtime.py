@@ -142,15 +142,70 @@ class Call:
 
 
 class PrefixCache:
-    """Device pool + host radix tree + slot allocator for one workload's shapes."""
+    """Device pool + host radix tree + slot allocator for one workload's shapes.
 
-    def __init__(self, w, device="cuda"):
+    ``page_size`` P > 1 makes a paged pool: the allocator hands out pages of P slots, the
+    tree caches whole P-token blocks only, every block of a request's context lives in one
+    page (slot = page * P + position % P), and the batch tables are page tables.  A
+    request's trailing partial block is its own (``private``): it is not in the tree, and
+    the request's next tokens fill the rest of that page before new pages are taken."""
+
+    def __init__(self, w, device="cuda", page_size=1):
         self.w = w
         self.device = device
+        self.page = int(page_size)
         self.pool = Pool.allocate(w.num_slots, w.num_kv_heads, w.head_dim, w.dtype, w.k_scale, w.v_scale, device)
-        self.tree = RadixTree()
-        self.alloc = Allocator(w.slot_perm)
+        self.tree = RadixTree(page_size=self.page)
+        self.alloc = Allocator(w.slot_perm if self.page == 1 else w.page_perm(self.page))
+        self.private = {}   # paged pool: request id -> slots of its trailing partial block
         self.err = torch.zeros(64, dtype=torch.int32, device=device)
+
+    # ---- slots of positions
+    def _extend_slots(self, slots, n):
+        """Slots for the next ``n`` positions of a context whose first len(slots) positions
+        use ``slots``: fresh slots, or in a paged pool the rest of the last page, then new pages."""
+        if self.page == 1:
+            return self.alloc.alloc(n)
+        P, L0 = self.page, len(slots)
+        out = []
+        if L0 % P and n > 0:
+            page = int(slots[-1]) // P
+            take = min(n, P - L0 % P)
+            out.append(page * P + np.arange(L0 % P, L0 % P + take, dtype=np.int32))
+            n -= take
+        if n > 0:
+            pages = self.alloc.alloc((n + P - 1) // P)
+            out.append((pages[:, None].astype(np.int64) * P + np.arange(P)).reshape(-1)[:n].astype(np.int32))
+        return np.concatenate(out) if out else np.zeros(0, np.int32)
+
+    def _release_blocks(self, row, lo, hi):
+        """Give back the slots of positions [lo, hi) of ``row`` (whole blocks in a paged pool)."""
+        if hi <= lo:
+            return
+        if self.page == 1:
+            self.alloc.release(row[lo:hi])
+        else:
+            self.alloc.release(np.asarray(row[lo:hi:self.page]) // self.page)
+
+    def _table(self, rows, seq):
+        """Batch table of the rows: slots per position, or pages per block."""
+        B, P = len(rows), self.page
+        if P == 1:
+            stride = max(16, ((max(seq) if len(seq) else 1) + 15) // 16 * 16)
+            rt = np.zeros((max(B, 1), stride), dtype=np.int32)
+            for i, row in enumerate(rows):
+                rt[i, :len(row)] = row
+            return rt
+        nb = max(1, max(((len(r) + P - 1) // P for r in rows), default=1))
+        rt = np.zeros((max(B, 1), (nb + 3) // 4 * 4), dtype=np.int32)
+        for i, row in enumerate(rows):
+            pages = np.asarray(row[::P], dtype=np.int64) // P
+            # every block must sit in one page, in position order
+            want = (pages.repeat(P)[:len(row)] * P + np.arange(len(row)) % P).astype(np.int32)
+            if not np.array_equal(want, row):
+                raise RuntimeError("a context block is not one page of the pool")
+            rt[i, :len(pages)] = pages
+        return rt
 
     # ---- cache population (setup, not part of a step)
     def populate(self, max_batch_tokens=1 << 18):
@@ -163,14 +218,17 @@ class PrefixCache:
             m = len(vals)
             if m == c:
                 continue
-            new = self.alloc.alloc(c - m)
+            new = self._extend_slots(vals, c - m)
             kb, vb = _ctx_kv(w, r, m, c)
             ks.append(kb)
             vs.append(vb)
             locs.append(new)
             pending += c - m
-            pre = self.tree.insert(toks[:c], np.concatenate([vals, new]))
+            row = np.concatenate([vals, new]).astype(np.int32)
+            pre = self.tree.insert(toks[:c], row)
             assert pre == m, (pre, m)
+            if self.page > 1:   # the trailing partial block stays with the request
+                self.private[r.rid] = row[c // self.page * self.page:c]
             if pending >= max_batch_tokens:
                 self._store(ks, vs, locs)
                 ks, vs, locs, pending = [], [], [], 0
@@ -194,10 +252,12 @@ class PrefixCache:
             toks = _ctx_tokens(w, r)
             L, c = len(toks), len(toks) - r.n_new
             vals, last = self.tree.match_prefix(toks[:c])
+            if self.page > 1:   # whole blocks from the tree, the partial one from the request
+                vals = np.concatenate([vals, self.private.get(r.rid, np.zeros(0, np.int32))]).astype(np.int32)
             if len(vals) != c:
                 raise RuntimeError(f"request {r.rid}: cached part not fully in the tree ({len(vals)} of {c})")
             self.tree.inc_lock_ref(last)
-            new = self.alloc.alloc(r.n_new)
+            new = self._extend_slots(vals, r.n_new)
             rows.append(np.concatenate([vals, new]).astype(np.int32))
             last_nodes.append(last)
             seq.append(L)
@@ -208,10 +268,7 @@ class PrefixCache:
             vn.append(vb)
             qs.append(r.q)
         B = len(reqs)
-        stride = max(16, ((max(seq) if seq else 1) + 15) // 16 * 16)
-        rt = np.zeros((max(B, 1), stride), dtype=np.int32)
-        for i, row in enumerate(rows):
-            rt[i, :len(row)] = row
+        rt = self._table(rows, seq)
         seq = np.asarray(seq, dtype=np.int32)
         ext = np.asarray(ext, dtype=np.int32)
         casc = self.tree.cascade(last_nodes, min_group) if (cascade and B > 1) else None
@@ -225,7 +282,7 @@ class PrefixCache:
             plan = plan_decode(seq, hq, hkv, d, casc, opts)
         dev = self.device
         batch = Batch(torch.from_numpy(rt).to(dev), torch.arange(B, dtype=torch.int32, device=dev),
-                      torch.from_numpy(seq).to(dev))
+                      torch.from_numpy(seq).to(dev), self.page)
         plan_dev = torch.from_numpy(plan.blob).to(dev)
         ws = torch.zeros((plan.info.workspace_bytes + 3) // 4, dtype=torch.int32, device=dev)
         q = _bf16_dev(np.concatenate(qs), dev)
@@ -261,8 +318,13 @@ class PrefixCache:
         """After the call ran: cache every request's whole context (its new tokens join the
         tree with the slots they were stored in) and unlock its path, as a server does when a
         prefill chunk or a request finishes."""
-        for (toks, row, cached), n in zip(call.contexts, call.last_nodes):
+        P = self.page
+        for (toks, row, cached), n, r in zip(call.contexts, call.last_nodes, call.requests):
             pre = self.tree.insert(toks, row)
-            if pre > cached:   # another request of the call inserted the same new tokens first
-                self.alloc.release(row[cached:pre])
+            lo = cached // P * P   # the tree held the request's blocks up to here
+            if pre > lo:           # another request of the call inserted the same new tokens first
+                self._release_blocks(row, lo, pre)
+            if P > 1:
+                L = len(row)
+                self.private[r.rid] = row[L // P * P:L]
             self.tree.dec_lock_ref(n)

@@ -39,9 +39,9 @@ def _bits(t):
     return t.cpu().view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.cpu().numpy()
 
 
-def run_step(w, cascade=True, opts=None, kinds=("extend", "decode")):
+def run_step(w, cascade=True, opts=None, kinds=("extend", "decode"), page_size=1):
     pkv, PrefixCache = _pkv()
-    pc = PrefixCache(w)
+    pc = PrefixCache(w, page_size=page_size)
     pc.populate()
     calls = {}
     for kind in kinds:
@@ -293,3 +293,68 @@ def test_shared_equals_duplicated_prefix():
     _, plain = run_step(w, cascade=False)
     a, b = _f64(shared["extend"].o), _f64(plain["extend"].o)
     assert np.max(np.abs(a - b)) <= 2 * 2.0 ** -8
+
+
+# ------------------------------------------------------------------------------ paged pool
+
+@pytest.mark.parametrize("page", [4, 16])
+@pytest.mark.parametrize("cascade", [True, False])
+@pytest.mark.parametrize("hq,hkv,d", [(32, 8, 128), (8, 2, 64)])
+def test_paged_extend(page, cascade, hq, hkv, d):
+    """Page-table batches: the extend gathers read slot = page * P + position % P; the
+    shared prefix is shared in whole blocks (its partial last block is per request)."""
+    w = W.fewshot_extend(seed=60 + page, n_req=3, prefix=300, suffix=70, hq=hq, hkv=hkv, d=d, num_slots=4096)
+    pc, calls = run_step(w, cascade=cascade, page_size=page)
+    assert calls["extend"].batch.page_size == page
+    check_outputs(w, calls)
+    check_pool(w, pc)
+
+
+@pytest.mark.parametrize("page", [2, 16])
+@pytest.mark.parametrize("cascade", [True, False])
+def test_paged_decode(page, cascade):
+    w = W.batched_decode(seed=61, n_req=20, prefix=200, lo=5, hi=90, num_slots=8192)
+    pc, calls = run_step(w, cascade=cascade, page_size=page)
+    check_outputs(w, calls)
+    check_pool(w, pc)
+
+
+def test_paged_decode_tensor_core_spans():
+    # a span shared by >= 12 requests and >= 256 keys goes through the gather + extend path
+    w = W.batched_decode(seed=62, n_req=24, prefix=520, lo=3, hi=40, num_slots=16384)
+    _, calls = run_step(w, page_size=16)
+    assert calls["decode"].plan.info.offsets[8] > 0
+    check_outputs(w, calls)
+
+
+@pytest.mark.parametrize("page", [8, 16])
+def test_paged_fp8_tot_mixed(page):
+    w = W.tot_mixed(seed=63, root_len=300, depth=2, branch=3, seg=40, n_new_branches=2, num_slots=8192,
+                    dtype="fp8_e4m3")
+    pc, calls = run_step(w, page_size=page)
+    assert set(calls) == {"extend", "decode"}
+    check_outputs(w, calls)
+    check_pool(w, pc)
+
+
+def test_paged_equals_token_pool():
+    """The same workload through a token table and through a page table: identical outputs
+    (the kernels read the same K/V; only the slots differ)."""
+    w = W.fewshot_extend(seed=64, n_req=4, prefix=180, suffix=40, hq=8, hkv=2, d=64, num_slots=4096)
+    _, tok = run_step(w, cascade=False)
+    _, pag = run_step(w, cascade=False, page_size=16)
+    assert torch.equal(tok["extend"].o, pag["extend"].o)
+
+
+def test_paged_page_out_of_range_is_flagged():
+    """A page-table entry whose page lies outside the pool reads as zeros and sets
+    PKV_DERR_SLOT_RANGE (the kernel's own bounds check; nothing outside the pool is read)."""
+    pkv, _ = _pkv()
+    w = W.batched_decode(seed=65, n_req=4, prefix=40, lo=5, hi=20, num_slots=1024)
+    pc, calls = run_step(w, cascade=False, page_size=16)
+    c = calls["decode"]
+    c.batch.req_to_token[0, 0] = 1024 // 16        # one past the last page
+    c.workspace.zero_()
+    c.attend()
+    torch.cuda.synchronize()
+    assert pkv.get_device_error(c.workspace) & 0x100

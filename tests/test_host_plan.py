@@ -276,3 +276,31 @@ def test_extend_plan_covers_causal_triangle(cascade):
         assert np.all(cover[tok] == cover[tok, 0])
     if cascade:
         assert info.num_span_items > 0 and int(info.offsets[6]) < int(seq.sum())  # the span is gathered once
+
+
+def test_struct_layouts_match_header(tmp_path):
+    """The ctypes mirrors of the public structs have the header's sizes and field offsets."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if not cc:
+        pytest.skip("no C compiler")
+    structs = {"pkv_pool": _lib.PkvPool, "pkv_batch": _lib.PkvBatch, "pkv_cascade": _lib.PkvCascade,
+               "pkv_plan_opts": _lib.PkvPlanOpts, "pkv_plan_info": _lib.PkvPlanInfo}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "pkv.h"', "int main(void) {"]
+    for name, cls in structs.items():
+        lines.append(f'printf("{name} size %zu\\n", sizeof({name}));')
+        for fname, _ in cls._fields_:
+            lines.append(f'printf("{name} {fname} %zu\\n", offsetof({name}, {fname}));')
+    lines += ["return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    got = {tuple(l.split()[:2]): int(l.split()[2]) for l in out if l.strip()}
+    import ctypes as C
+    for name, cls in structs.items():
+        assert got[(name, "size")] == C.sizeof(cls), name
+        for fname, _ in cls._fields_:
+            assert got[(name, fname)] == getattr(cls, fname).offset, (name, fname)

@@ -76,6 +76,12 @@ class Workload:
     slot_perm: np.ndarray  # int32 permutation of [0, num_slots)
     meta: dict = field(default_factory=dict)
 
+    def page_perm(self, page_size: int) -> np.ndarray:
+        """Seeded permutation of the pool's pages of ``page_size`` slots (a paged pool's
+        free list; drawn from its own stream, so the workload's other draws are unchanged)."""
+        rng = np.random.default_rng([self.seed, 2, page_size])
+        return rng.permutation(self.num_slots // page_size).astype(np.int32)
+
     def context_len(self, req: Request) -> int:
         return int(sum(len(self.segments[s].tokens) for s in req.path))
 

@@ -199,7 +199,8 @@ def run_serving(args):
     res = {}
     with ClockSampler(0) as clocks:
         for policy in ("lpm", "fcfs"):
-            sim = ServingSim(stream, capacity=cap, policy=policy, max_running=64, prefill_budget=16384)
+            sim = ServingSim(stream, capacity=cap, policy=policy, max_running=64, prefill_budget=16384,
+                             page_size=args.page_size)
             t0 = time.perf_counter()
             sim.run()
             st = sim.summary()
@@ -213,6 +214,7 @@ def run_serving(args):
         "steps": lpm["steps"], "warmup": 1, "ms_per_step": round(lpm["device_ms"] / lpm["steps"], 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "serving_stream", "requests": len(stream.requests), "pool_slots": cap,
+                   "page_size": args.page_size,
                    "max_running": 64, "prefill_budget": 16384, "heads_q_kv": "32/8", "head_dim": 128,
                    "l2": "not flushed (a serving run; steps follow each other)"},
         "e2e": {"value": lpm["served_tokens_per_s_wall"], "unit": "tokens/s (host + device wall clock)"},
@@ -232,7 +234,7 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(dev)
     w = load_workload(args)
     facts = workload_facts(w)
-    pc = PrefixCache(w, device=str(dev))
+    pc = PrefixCache(w, device=str(dev), page_size=args.page_size)
     if w.name == "chunked_prefill":
         calls = pc.prepare_chunked()       # one extend call per chunk, over the chunks before it
     else:
@@ -343,7 +345,8 @@ def run_ours(args, rank, world):
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / pk["hbm_gbs"], 4), "kernel": "attn_decode (all its kernels)",
                 "algorithmic_per_launch": fx["kv_bytes"] + fx["qo_bytes"], "kernel_ms": round(dur * 1e3, 4)}
-    traffic = profiled_traffic(dominant, w.name)
+    # the committed ncu captures are of the token pool
+    traffic = profiled_traffic(dominant, w.name) if args.page_size == 1 else None
     roof["traffic"] = traffic
     roof["peak_source"] = pk["source"] + " (burst)"
 
@@ -352,7 +355,7 @@ def run_ours(args, rank, world):
     d2h = sum(c.d2h_bytes() for c in calls)
     cfg = {"workload": w.name, "config_id": None if args.workload else args.config, "requests": len(w.requests),
            "heads_q_kv": f"{w.num_q_heads}/{w.num_kv_heads}", "head_dim": w.head_dim, "pool_dtype": w.dtype,
-           "pool_slots": w.num_slots, "cascade": not args.no_cascade,
+           "pool_slots": w.num_slots, "page_size": args.page_size, "cascade": not args.no_cascade,
            "l2": "flushed between timed steps (512 MiB write outside the step events)",
            "tokens_per_step": tokens_per_step}
     for kind, fx_ in facts.items():
@@ -449,6 +452,8 @@ def main():
     ap.add_argument("--no-cascade", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pool-slots", type=int, default=0)
+    ap.add_argument("--page-size", type=int, default=1,
+                    help="1: token pool; P > 1: paged pool, whole P-token blocks shared, page-table batches")
     ap.add_argument("--workload", default="", choices=["", "chunked_prefill", "serving"],
                     help="chunked_prefill: long prompts prefilled chunk by chunk; serving: a multi-step "
                          "serving run, longest-prefix-first against first-come-first-served (instead of --config)")

@@ -16,6 +16,12 @@ attn_decode for one new token of every running request.  The decode plan is made
 stays valid while the running set is unchanged and is only re-planned when a request joins
 or leaves.  Synthetic inputs come from the seeded generators in ``workloads``: the K/V of a
 context entry depends only on (token, position), so shared prefixes share K/V exactly.
+
+With ``page_size`` P > 1 the pool is paged: slots come in pages of P, the tree caches whole
+P-token blocks only (a cached length is a multiple of P; a fully cached prompt recomputes its
+whole last block), every block of a request lives in one page, and the batch table is a
+page table written once at admission.  A request's trailing partial block is its own and is
+freed when it finishes.
 """
 
 from __future__ import annotations
@@ -56,7 +62,7 @@ class StepRecord:
 class ServingSim:
     def __init__(self, stream, capacity: int, policy: str = "lpm", max_running: int = 64,
                  prefill_budget: int = 16384, device: str = "cuda", record: bool = False,
-                 eviction: str = "lru", chunk_keys: int = 0):
+                 eviction: str = "lru", chunk_keys: int = 0, page_size: int = 1):
         self.s = stream
         self.policy = policy
         self.max_running = max_running
@@ -66,11 +72,13 @@ class ServingSim:
         self.opts = {"dynamic_tail": 1, **({"chunk_keys": chunk_keys} if chunk_keys else {})}
         s = stream
         self.pool = Pool.allocate(capacity, s.num_kv_heads, s.head_dim, "bf16", device=device)
-        self.tree = RadixTree(eviction)
-        self.alloc = Allocator(np.arange(capacity, dtype=np.int32))
+        self.page = P = int(page_size)
+        self.tree = RadixTree(eviction, page_size=P)
+        self.alloc = Allocator(np.arange(capacity // P, dtype=np.int32))   # slots, or pages
         longest = max(len(r.prompt) + r.out_len for r in s.requests)
         self.stride = (longest + 15) // 16 * 16
-        self.rt = torch.zeros((max_running, self.stride), dtype=torch.int32, device=device)
+        self.rt = torch.zeros((max_running, self.stride if P == 1 else (longest + P - 1) // P), dtype=torch.int32,
+                              device=device)
         self.seq = torch.zeros(max_running, dtype=torch.int32, device=device)
         self.free_rows = list(range(max_running - 1, -1, -1))
         self.pending = sorted(s.requests, key=lambda r: (r.arrival, r.rid))
@@ -83,13 +91,34 @@ class ServingSim:
 
     # ---- slots ---------------------------------------------------------------------
     def _ensure(self, n: int) -> bool:
-        short = n - self.alloc.available
+        """Room for n more positions (n fresh slots, or ceil(n / P) fresh pages)."""
+        P = self.page
+        short = (n + P - 1) // P - self.alloc.available
         if short > 0:
-            freed = self.tree.evict(short)
+            freed = self.tree.evict(short * P)
             if len(freed):
-                self.alloc.release(freed)
+                self._free(freed)
                 self.stats["evicted_tokens"] += len(freed)
-        return self.alloc.available >= n
+        return self.alloc.available * P >= n
+
+    def _take(self, n: int) -> np.ndarray:
+        """Slots of n positions that start a block: fresh slots, or whole fresh pages."""
+        P = self.page
+        if P == 1:
+            return self.alloc.alloc(n)
+        pages = self.alloc.alloc((n + P - 1) // P).astype(np.int64)
+        return (pages[:, None] * P + np.arange(P)).reshape(-1)[:n].astype(np.int32)
+
+    def _free(self, slots) -> None:
+        """Give back slots that cover whole blocks (whole pages in a paged pool)."""
+        slots = np.asarray(slots)
+        self.alloc.release(slots if self.page == 1 else slots[::self.page] // self.page)
+
+    def _write_row(self, run) -> None:
+        """A paged pool's table row: the page of every block of prompt + outputs."""
+        P = self.page
+        pages = np.asarray(run.slots[::P], np.int64) // P
+        self.rt[run.row, :len(pages)] = torch.from_numpy(pages.astype(np.int32)).to(self.device)
 
     # ---- one step ------------------------------------------------------------------
     def done(self) -> bool:
@@ -125,8 +154,10 @@ class ServingSim:
                 break
             r = self.waiting[i]
             vals, node = self.tree.match_prefix(r.prompt)
-            # a fully cached prompt still recomputes its last token (the step's first query)
-            cached = min(len(vals), len(r.prompt) - 1)
+            # a fully cached prompt still recomputes its last token (the step's first query);
+            # in a paged pool its whole last block, so the new positions start a block
+            cached = min(len(vals), len(r.prompt) - 1) if self.page == 1 else \
+                (len(vals) if len(vals) < len(r.prompt) else len(vals) - self.page)
             new = len(r.prompt) - cached
             if new > budget and admitted:   # an oversized prompt goes alone, first in line
                 continue
@@ -134,7 +165,7 @@ class ServingSim:
             if not self._ensure(new + r.out_len):
                 self.tree.dec_lock_ref(node)
                 continue
-            slots = np.concatenate([vals[:cached], self.alloc.alloc(new + r.out_len)]).astype(np.int32)
+            slots = np.concatenate([vals[:cached], self._take(new + r.out_len)]).astype(np.int32)
             admitted.append((_Running(r, self.free_rows.pop(), slots, node, list(r.prompt)), cached))
             taken.add(i)
             budget -= new
@@ -150,7 +181,10 @@ class ServingSim:
         seq, ext, rows, locs, ks, vs, qs, nodes = [], [], [], [], [], [], [], []
         for run, cached in admitted:
             L = len(run.req.prompt)
-            self.rt[run.row, :L] = torch.from_numpy(run.slots[:L]).to(dev)
+            if self.page == 1:
+                self.rt[run.row, :L] = torch.from_numpy(run.slots[:L]).to(dev)
+            else:
+                self._write_row(run)
             seq.append(L)
             ext.append(L - cached)
             rows.append(run.row)
@@ -169,7 +203,8 @@ class ServingSim:
             casc = None
         plan = plan_extend(seq, ext, qo, s.num_q_heads, s.num_kv_heads, s.head_dim, casc)
         self.seq[rows] = torch.from_numpy(seq).to(dev)
-        batch = Batch(self.rt, torch.tensor(rows, dtype=torch.int32, device=dev), self.seq[rows].contiguous())
+        batch = Batch(self.rt, torch.tensor(rows, dtype=torch.int32, device=dev), self.seq[rows].contiguous(),
+                      self.page)
         q = _bf16(np.concatenate(qs), dev)
         o = torch.empty_like(q)
         ws = torch.zeros((plan.info.workspace_bytes + 3) // 4, dtype=torch.int32, device=dev)
@@ -192,10 +227,13 @@ class ServingSim:
             vals, node = self.tree.match_prefix(run.req.prompt)
             if pre > cached:   # another admitted prompt inserted the same tokens first: use its slots
                 mine = run.slots[cached:pre].copy()
-                run.slots[:L] = vals
-                self.rt[run.row, :L] = torch.from_numpy(run.slots[:L]).to(dev)
+                run.slots[:len(vals)] = vals
+                if self.page == 1:
+                    self.rt[run.row, :L] = torch.from_numpy(run.slots[:L]).to(dev)
+                else:
+                    self._write_row(run)
                 torch.cuda.current_stream().synchronize()   # our copies of those rows are still being read
-                self.alloc.release(mine)
+                self._free(mine)
             self.tree.inc_lock_ref(node)
             self.tree.dec_lock_ref(run.last_node)
             run.last_node = node
@@ -230,10 +268,11 @@ class ServingSim:
             vs.append(v)
             qs.append(W.stream_query(s.seed, r.req.rid, p, s.num_q_heads, s.head_dim)[None])
         locs_t = torch.tensor(locs, dtype=torch.int32, device=dev)
-        self.rt[rows.long(), torch.tensor(pos, device=dev)] = locs_t
+        if self.page == 1:   # a page table already names every reserved position's page
+            self.rt[rows.long(), torch.tensor(pos, device=dev)] = locs_t
         seq_now = torch.tensor([p + 1 for p in pos], dtype=torch.int32, device=dev)
         self.seq[rows.long()] = seq_now
-        batch = Batch(self.rt, rows, seq_now)
+        batch = Batch(self.rt, rows, seq_now, self.page)
         q = _bf16(np.concatenate(qs), dev)
         o = torch.empty_like(q)
         ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -257,11 +296,15 @@ class ServingSim:
             if r.gen < r.req.out_len:
                 keep.append(r)
                 continue
-            n = len(r.tokens)
+            n, P = len(r.tokens), self.page
             pre = self.tree.insert(np.asarray(r.tokens, np.int32), r.slots[:n])
-            if pre > len(r.req.prompt):   # generated tokens already cached by another request
+            lo = len(r.req.prompt) // P * P   # the tree held the request's blocks up to here
+            if pre > lo:   # generated tokens already cached by another request
                 torch.cuda.current_stream().synchronize()
-                self.alloc.release(r.slots[len(r.req.prompt):pre])
+                self._free(r.slots[lo:pre])
+            if n % P:      # the trailing partial block is not in the tree: its page is free now
+                torch.cuda.current_stream().synchronize()
+                self._free(r.slots[n // P * P:n // P * P + 1])
             self.tree.dec_lock_ref(r.last_node)
             self.free_rows.append(r.row)
             self.stats["finished"] += 1

@@ -73,3 +73,22 @@ def test_longest_prefix_first_hits_more_than_fcfs():
         assert st[policy]["finished"] == len(s.requests)
     assert st["lpm"]["hit_rate"] > st["fcfs"]["hit_rate"], st
     assert st["lpm"]["prefill_tokens"] < st["fcfs"]["prefill_tokens"], st
+
+
+@pytest.mark.parametrize("page", [4, 16])
+def test_paged_serving_steps_match_oracle_under_eviction(page):
+    """The same serving loop over a paged pool (whole blocks cached, page tables, partial
+    blocks private and freed at finish): every output still matches the oracle."""
+    from prefix_shared_kv_token_gb300.serving import ServingSim
+    s = W.serving_stream(seed=83, n_groups=3, per_group=6, shared=200, unique=(10, 40), out=(2, 6), per_step=4,
+                         hq=8, hkv=2, d=64)
+    sim = ServingSim(s, capacity=1024, policy="lpm", max_running=6, prefill_budget=600, record=True,
+                     page_size=page)
+    sim.run()
+    st = sim.summary()
+    assert sim.done() and st["finished"] == len(s.requests)
+    assert st["evicted_tokens"] > 0 and st["cached_tokens"] > 0
+    assert st["cached_tokens"] % page == 0          # every hit is whole blocks
+    _check_records(s, sim.records)
+    # every page is back in the free list or held by the tree
+    assert sim.alloc.available * page + sim.tree.sizes()["total"] == 1024

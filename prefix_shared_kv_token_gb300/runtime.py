@@ -130,15 +130,81 @@ class Call:
     def d2h_bytes(self) -> int:
         return self.o.numel() * self.o.element_size()
 
-    def run_e2e(self, stream=None):
+    def copy_in(self):
+        """Host -> device copies of the call's inputs (on the current stream)."""
         h = self.host
         for name in ("q", "k_new", "v_new", "out_cache_loc"):
             getattr(self, name).copy_(h[name], non_blocking=True)
         for name in ("req_to_token", "req_pool_indices", "seq_lens"):
             getattr(self.batch, name).copy_(h[name], non_blocking=True)
         self.plan_dev.copy_(h["plan"], non_blocking=True)
+
+    def copy_out(self, host_o=None):
+        """Device -> host copy of the call's output (on the current stream)."""
+        (self.host["o"] if host_o is None else host_o).copy_(self.o, non_blocking=True)
+
+    def run_e2e(self, stream=None):
+        self.copy_in()
         self.run(stream)
-        h["o"].copy_(self.o, non_blocking=True)
+        self.copy_out()
+
+    def e2e_sets(self, n: int = 2) -> list:
+        """``n`` copies of this call with their own device inputs and output (the first is
+        this call itself), sharing the pool, plan, workspace and host buffers: the buffers a
+        pipelined end-to-end loop fills and drains while another copy computes."""
+        out = [self]
+        for _ in range(n - 1):
+            b = self.batch
+            batch = Batch(torch.empty_like(b.req_to_token), torch.empty_like(b.req_pool_indices),
+                          torch.empty_like(b.seq_lens), b.page_size)
+            c = Call(self.kind, self.pool, batch, self.plan, torch.empty_like(self.plan_dev), self.workspace,
+                     torch.empty_like(self.q), torch.empty_like(self.o), torch.empty_like(self.out_cache_loc),
+                     torch.empty_like(self.k_new), torch.empty_like(self.v_new), self.sm_scale, self.last_nodes,
+                     host=self.host, cascade=self.cascade, contexts=self.contexts, requests=self.requests)
+            out.append(c)
+        return out
+
+
+def run_e2e_pipelined(sets, steps: int, flush=None):
+    """End-to-end steps with the copies overlapped: step k's inputs go host -> device on one
+    copy stream while step k-1 computes, and step k-1's output goes device -> host on another
+    while step k computes.  ``sets`` holds, per call of a step, the buffer copies from
+    :meth:`Call.e2e_sets` (step k uses copy k mod n).  Every step's own copies happen inside
+    the returned span.  ``flush`` (a device tensor) is zeroed on the compute stream before each
+    step's kernels, inside the span.  Returns the elapsed milliseconds (CUDA events)."""
+    n = len(sets[0])
+    comp = torch.cuda.current_stream()
+    cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+    loaded = [torch.cuda.Event() for _ in range(n)]
+    done = [torch.cuda.Event() for _ in range(n)]
+    free = [torch.cuda.Event() for _ in range(n)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(comp)
+    cin.wait_event(start)
+    cout.wait_event(start)
+    for k in range(steps):
+        b = k % n
+        with torch.cuda.stream(cin):
+            if k >= n:
+                cin.wait_event(free[b])       # copy b's previous step has been read back
+            for calls in sets:
+                calls[b].copy_in()
+            loaded[b].record(cin)
+        comp.wait_event(loaded[b])
+        if flush is not None:
+            flush.zero_()
+        for calls in sets:
+            calls[b].run()
+        done[b].record(comp)
+        with torch.cuda.stream(cout):
+            cout.wait_event(done[b])
+            for calls in sets:
+                calls[b].copy_out()
+            free[b].record(cout)
+    comp.wait_stream(cout)
+    end.record(comp)
+    end.synchronize()
+    return start.elapsed_time(end)
 
 
 class PrefixCache:

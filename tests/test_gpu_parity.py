@@ -358,3 +358,22 @@ def test_paged_page_out_of_range_is_flagged():
     c.attend()
     torch.cuda.synchronize()
     assert pkv.get_device_error(c.workspace) & 0x100
+
+
+def test_pipelined_end_to_end_gives_the_device_outputs():
+    """The bench's end-to-end loop (inputs copied in and outputs copied out on their own
+    streams while the neighbouring step computes, two buffer sets) returns exactly the
+    outputs of a plain device run."""
+    from prefix_shared_kv_token_gb300.runtime import run_e2e_pipelined
+    w = W.tot_mixed(seed=45, root_len=300, depth=2, branch=3, seg=40, n_new_branches=2, num_slots=8000)
+    _, calls = run_step(w)
+    ref = {k: c.o.cpu().clone() for k, c in calls.items()}
+    cl = list(calls.values())
+    for c in cl:
+        c.pin_host()
+        c.host["o"].zero_()
+    sets = [c.e2e_sets(2) for c in cl]
+    ms = run_e2e_pipelined(sets, 5)
+    assert ms > 0
+    for c in cl:
+        assert torch.equal(c.host["o"], ref[c.kind]), c.kind

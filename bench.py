@@ -6,7 +6,7 @@ with the shared-prefix cascade), then the partial-state merge.  Inputs are resid
 when the timed region starts; the L2 is flushed (512 MiB write) between timed steps, outside
 the per-step CUDA events.  ``e2e`` repeats the measurement through the same C-ABI calls with
 every step's inputs copied from pinned host memory and its output copied back inside the
-timed region, the copies of neighbouring steps overlapping each step's kernels (two device
+timed region, the copies of neighbouring steps overlapping each step's kernels (three device
 buffer sets, one copy stream each way).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl ours|reference]
@@ -292,11 +292,12 @@ def run_ours(args, rank, world):
             torch.distributed.barrier()
         # end-to-end: same calls, inputs from pinned host memory, output back to the host.
         # Pipelined (step k+1's inputs copy in and step k-1's output copies out while step k
-        # computes; two device buffer sets), with a 256 MiB L2 flush before every step's
-        # kernels inside the timed span; and, for reference, fully serialised steps.
+        # computes; three device buffer sets, so the two copies never wait on each other),
+        # with a 256 MiB L2 flush before every step's kernels inside the timed span; and, for
+        # reference, fully serialised steps.
         for c in calls:
             c.pin_host()
-        sets = [c.e2e_sets(2) for c in calls]
+        sets = [c.e2e_sets(3) for c in calls]
         e2e_flush = flush[:(256 << 20) // 4]
         run_e2e_pipelined(sets, args.warmup, e2e_flush)
         e2e_total_ms = run_e2e_pipelined(sets, K, e2e_flush)
@@ -372,7 +373,7 @@ def run_ours(args, rank, world):
         "data": "synthetic", "config": cfg,
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": round(t_e2e * 1e3 / K, 4),
-                "mode": "pipelined: step k+1's H2D and step k-1's D2H overlap step k's kernels (2 device "
+                "mode": "pipelined: step k+1's H2D and step k-1's D2H overlap step k's kernels (3 device "
                         "buffer sets); a 256 MiB L2 flush precedes each step's kernels inside the span",
                 "serial_ms_per_step": round(float(np.mean(e2e_serial_ms)), 4)},
         "roofline": roof,

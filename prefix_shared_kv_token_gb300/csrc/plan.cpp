@@ -257,7 +257,9 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
     std::vector<int32_t> next_rec(batch, 0);
 
     std::vector<DecodeItem> items;
-    std::vector<int64_t> cost;  // load-balancing weight: keys, span re-reads (L2 hits) at 3/5
+    std::vector<int64_t> cost;  // load-balancing weight: 5 per key (a span's later member
+                                // groups cost as much per key as its first: measured per-CTA
+                                // times follow the tile count, not L2 reuse)
     std::vector<int32_t> row_req, row_rec;
     std::vector<MergeItem> merges;
     int32_t num_span_items = 0;
@@ -328,7 +330,7 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
                     const int32_t rot = (int32_t)((int64_t)(a / R) * ntile / ngrp);
                     for (int32_t g0 = 0; g0 < num_kv_heads; g0 += hg) {
                         items.push_back({g0, 0, b - a, off, cascade->span_req[s], st + c0, st + c1, rot});
-                        cost.push_back((int64_t)(c1 - c0) * (a == 0 ? 5 : 3) + kItemOverhead);
+                        cost.push_back((int64_t)(c1 - c0) * 5 + kItemOverhead);
                         ++num_span_items;
                     }
                 }

@@ -68,6 +68,7 @@ class Call:
     cascade: object = None
     contexts: list = field(default_factory=list)   # per request: (tokens, req_to_token row, cached length)
     requests: list = field(default_factory=list)
+    graph: object = None                           # captured attention launches (capture_attend)
 
     @property
     def num_queries(self) -> int:
@@ -100,6 +101,24 @@ class Call:
     def run(self, stream=None):
         self.store(stream)
         self.attend(stream)
+
+    def capture_attend(self):
+        """Record this call's attention launches once into a CUDA graph; :meth:`replay_attend`
+        then re-issues them with one launch (same plan, tables, buffers and workspace, as in
+        a decode loop whose plan is reused).  The library is called on a side stream while
+        capturing, exactly as :meth:`attend` calls it."""
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self.attend()          # resolve lazy set-up outside the capture
+        torch.cuda.current_stream().wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            self.attend()
+        self.graph = g
+
+    def replay_attend(self):
+        self.graph.replay()
 
     def launches(self) -> int:
         """Kernels one run() launches: the store, then the attention call's kernels."""

@@ -377,3 +377,19 @@ def test_pipelined_end_to_end_gives_the_device_outputs():
     assert ms > 0
     for c in cl:
         assert torch.equal(c.host["o"], ref[c.kind]), c.kind
+
+
+def test_decode_graph_replay_matches_the_call():
+    """A decode call captured once into a CUDA graph and replayed gives the call's outputs
+    (bit for bit), and replays again on the same workspace."""
+    w = W.batched_decode(seed=67, n_req=30, prefix=400, lo=10, hi=300, num_slots=1 << 15)
+    _, calls = run_step(w)
+    c = calls["decode"]
+    first = c.o.clone()
+    c.capture_attend()
+    for _ in range(3):
+        c.o.zero_()
+        c.replay_attend()
+        torch.cuda.synchronize()
+        assert torch.equal(c.o, first)
+    check_outputs(w, calls)

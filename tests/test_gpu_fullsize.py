@@ -22,17 +22,22 @@ def _cuda():
         pytest.skip("no CUDA device")
 
 
-@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
-def test_config_full_size(cfg):
+@pytest.mark.parametrize("cfg,page", [(1, 1), (2, 1), (3, 1), (4, 1), (5, 1), (3, 16), (4, 16)])
+def test_config_full_size(cfg, page):
     import prefix_shared_kv_token_gb300 as pkv
     from prefix_shared_kv_token_gb300.runtime import PrefixCache
 
     w = W.config(cfg)
-    pc = PrefixCache(w)
+    pc = PrefixCache(w, page_size=page)
     pc.populate()
     calls = {k: pc.prepare(k) for k in ("extend", "decode") if any(r.kind == k for r in w.requests)}
     for c in calls.values():
         c.run()
+    # decode calls as the bench times them: replayed from a CUDA graph captured once
+    if "decode" in calls:
+        calls["decode"].capture_attend()
+        calls["decode"].o.zero_()
+        calls["decode"].replay_attend()
     torch.cuda.synchronize()
     rng = np.random.default_rng(100 + cfg)
     tol = TOL[w.dtype]

@@ -64,6 +64,7 @@ struct ExtendParams {
     float *rec_acc;
     float *rec_ml;
     const int32_t *rec_list;  // NULL: token t of an item writes record rec + t; else rec_list[rec + t]
+    const PackInfo *packs;    // packed items' segments and row groups (NULL: none)
     int32_t *err;
 };
 
@@ -258,18 +259,23 @@ PKV_DEV void exp_pack_regs(const uint32_t *sv, uint32_t col, float sc, float neg
 struct XItem {
     int32_t g, tok0, ntok, qpos0, pos0, nseg, rec, ntiles, nq;
     bool split;  // one query tile over >= 2 key tiles: both softmax warpgroups take it
+    const int32_t *key0, *nkeys;  // segments (the item's own, or its PackInfo's)
+    const PackInfo *pk;           // packed item: segments' positions and groups, row groups
 };
-PKV_DEV XItem load_item(const ExtendItem *itp, int tq) {
+PKV_DEV XItem load_item(const ExtendItem *itp, int tq, const PackInfo *packs) {
     XItem x;
     x.g = itp->g;
     x.tok0 = itp->tok0;
     x.ntok = itp->ntok;
     x.qpos0 = itp->qpos0;
     x.pos0 = itp->pos0;
-    x.nseg = min(max(itp->nseg, 0), kMaxSegs);
-    x.rec = itp->rec;
+    x.pk = (itp->flags & kItemPacked) && packs ? packs + itp->rec : nullptr;
+    x.rec = x.pk ? -1 : itp->rec;  // a packed item's rec names its PackInfo; it writes o
+    x.nseg = min(max(itp->nseg, 0), x.pk ? kPackSegs : kMaxSegs);
+    x.key0 = x.pk ? x.pk->key0 : itp->key0;
+    x.nkeys = x.pk ? x.pk->nkeys : itp->nkeys;
     x.ntiles = 0;  // key tiles over all segments (each segment starts a new tile)
-    for (int sg = 0; sg < x.nseg; ++sg) x.ntiles += (itp->nkeys[sg] + kBN - 1) / kBN;
+    for (int sg = 0; sg < x.nseg; ++sg) x.ntiles += (x.nkeys[sg] + kBN - 1) / kBN;
     x.nq = x.ntok > tq ? 2 : 1;  // query tiles in use
     // split: warpgroup 0 takes the even key tiles and warpgroup 1 the odd ones, each with its
     // own running max, sum and accumulator (S_q, O_q), combined in the epilogue
@@ -315,7 +321,8 @@ PKV_DEV void write_out(const ExtendParams &p, const XItem &it, int t, int tok, i
 template <int D, int G, bool PRECISE>
 __global__ void __launch_bounds__(384, 1)
     extend_kernel(const ExtendParams p, const __grid_constant__ CUtensorMap qmap,
-                  const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
+                  const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                  const __grid_constant__ CUtensorMap qmapg) {
     using C = XCfg<D>;
     constexpr int ST = kXStages;
     constexpr int NBLK = D / 64;
@@ -372,22 +379,37 @@ __global__ void __launch_bounds__(384, 1)
             uint64_t *full = kside ? bars->kfull : bars->vfull;
             const uint32_t half = kside ? 0u : (uint32_t)C::kKTile;
             prefetch_tmap(map);
-            if (kside) prefetch_tmap(&qmap);
+            if (kside) {
+                prefetch_tmap(&qmap);
+                prefetch_tmap(&qmapg);
+            }
             int tp = 0, nql = 0;             // tiles and Q loads issued by this thread
             uint32_t split_mask = 0;         // bit s: stage s's previous tile came from a split item
             uint32_t kpar = 0;               // bit s: parity of the kempty commits due on stage s
             bool ok = true;
             for (int i = i0; ok && i < i1; ++i) {
                 const ExtendItem *itp = p.items + i;
-                const XItem it = load_item(itp, TQ);
+                const XItem it = load_item(itp, TQ, p.packs);
                 if (kside) {
                     if (nql > 0 && !xwait(&bars->qempty, (nql - 1) & 1, bars, p.err, 6)) break;
-                    mbar_arrive_expect_tx(&bars->q, it.nq * C::kQTile);
-                    for (int q = 0; q < it.nq; ++q)
+                    if (it.pk) {
+                        // a packed tile: each row group's tokens by their own 32-row box
+                        int ng = 0;
+                        while (ng < 4 && it.pk->ntok[ng] > 0) ++ng;
+                        mbar_arrive_expect_tx(&bars->q, ng * NBLK * 32 * 128);
+                        for (int m = 0; m < ng; ++m)
 #pragma unroll
-                        for (int b = 0; b < NBLK; ++b)
-                            tma_load_3d(sbase + C::kQOff + q * C::kQTile + b * C::kBlkQ, &qmap, b * 64, it.g * G,
-                                        it.tok0 + q * TQ, &bars->q);
+                            for (int b = 0; b < NBLK; ++b)
+                                tma_load_3d(sbase + C::kQOff + b * C::kBlkQ + m * 32 * 128, &qmapg, b * 64, it.g * G,
+                                            it.pk->tok0[m], &bars->q);
+                    } else {
+                        mbar_arrive_expect_tx(&bars->q, it.nq * C::kQTile);
+                        for (int q = 0; q < it.nq; ++q)
+#pragma unroll
+                            for (int b = 0; b < NBLK; ++b)
+                                tma_load_3d(sbase + C::kQOff + q * C::kQTile + b * C::kBlkQ, &qmap, b * 64, it.g * G,
+                                            it.tok0 + q * TQ, &bars->q);
+                    }
                     ++nql;
                 }
                 int sg = 0, lt = 0;  // segment and tile within it
@@ -405,8 +427,8 @@ __global__ void __launch_bounds__(384, 1)
                     split_mask = (split_mask & ~(1u << s)) | ((uint32_t)it.split << s);
                     kpar ^= (uint32_t)it.split << s;
                     const uint32_t dst = sbase + C::kStageOff + (s * 2) * C::kKTile + half;
-                    const int key = itp->key0[sg] + lt * kBN;
-                    if (++lt * kBN >= itp->nkeys[sg]) {
+                    const int key = it.key0[sg] + lt * kBN;
+                    if (++lt * kBN >= it.nkeys[sg]) {
                         ++sg;
                         lt = 0;
                     }
@@ -430,7 +452,7 @@ __global__ void __launch_bounds__(384, 1)
             uint32_t cpar = 0;        // bit q: parity of the next phase to consume on pfull[q]
             bool ok = true;
             for (int i = i0; ok && i < i1; ++i, ++ip) {
-                const XItem it = load_item(p.items + i, TQ);
+                const XItem it = load_item(p.items + i, TQ, p.packs);
                 if (!xwait(&bars->q, ip & 1, bars, p.err, 1)) break;
                 if (!it.split) {
                     auto issue_s = [&](int q, int j) -> bool {
@@ -553,23 +575,25 @@ __global__ void __launch_bounds__(384, 1)
         bool alive = true;   // false after a failed wait; the remaining items are skipped
         for (int i = i0; i < i1; ++i) {
             const ExtendItem *itp = p.items + i;
-            const XItem it = load_item(itp, TQ);
+            const XItem it = load_item(itp, TQ, p.packs);
             if (!it.split && q >= it.nq) continue;
             if (!alive) {
                 // the other warpgroup meets the same barrier on every split item
                 if (it.split) named_bar_and(kBarSplit, 256, false);
                 continue;
             }
-            const int t = (it.split ? 0 : q * TQ) + r / G;      // token within the item
-            const int lim = it.qpos0 + t;                       // last visible position
+            // token of this row within the item (packed: within its row group r / 32) and the
+            // last position it sees
+            const int t = it.pk ? (r & 31) / G : (it.split ? 0 : q * TQ) + r / G;
+            const int lim = (it.pk ? it.pk->qpos0[r >> 5] : it.qpos0) + t;
             float m = -INFINITY, l = 0.f;
             bool ok = true;
             int sg = 0, lt = 0, segpos = it.pos0;  // segment, tile within it, its first position
             const int jsecond = it.split ? 2 : 1;  // this warpgroup's second tile and later rescale O
             for (int j = 0; j < it.ntiles; ++j) {
                 if (it.split && (j & 1) != q) {  // the other warpgroup's tile: move the cursor only
-                    if (++lt * kBN >= itp->nkeys[sg]) {
-                        segpos += itp->nkeys[sg];
+                    if (++lt * kBN >= it.nkeys[sg]) {
+                        segpos += it.nkeys[sg];
                         ++sg;
                         lt = 0;
                     }
@@ -583,15 +607,17 @@ __global__ void __launch_bounds__(384, 1)
                 ++cw;
                 tc_fence_after();
                 const int kl0 = lt * kBN;                       // key index of column 0 in the segment
-                const int kp0 = segpos + kl0;                   // its context position
-                const int nvalid = min(kBN, itp->nkeys[sg] - kl0);
-                if (++lt * kBN >= itp->nkeys[sg]) {
-                    segpos += itp->nkeys[sg];
+                const int kp0 = (it.pk ? it.pk->spos[sg] : segpos) + kl0;  // its context position
+                const int nvalid = min(kBN, it.nkeys[sg] - kl0);
+                // packed: a member's own keys are hidden from the other row groups (warp-uniform)
+                const bool seen = !it.pk || it.pk->sgrp[sg] < 0 || it.pk->sgrp[sg] == (r >> 5);
+                if (++lt * kBN >= it.nkeys[sg]) {
+                    segpos += it.nkeys[sg];
                     ++sg;
                     lt = 0;
                 }
                 const int ncaus = lim - kp0 + 1;                // columns <= lim
-                const int lastc = min(nvalid, ncaus);           // columns [0, lastc) visible
+                const int lastc = seen ? min(nvalid, ncaus) : 0;  // columns [0, lastc) visible
                 // warp-uniform: the tcgen05.ld/st below are .sync.aligned, so every lane of
                 // the warp must take the same path (lastc differs between rows of a causal tile)
                 const bool full = __all_sync(0xffffffffu, lastc >= kBN);
@@ -664,8 +690,8 @@ __global__ void __launch_bounds__(384, 1)
             }
             ++co;
             tc_fence_after();
-            const bool valid = t < it.ntok;
-            const int tok = it.tok0 + t;
+            const bool valid = t < (it.pk ? it.pk->ntok[r >> 5] : it.ntok);
+            const int tok = (it.pk ? it.pk->tok0[r >> 5] : it.tok0) + t;
             const int head = it.g * G + (r % G);
             if (!it.split) {
 #pragma unroll 1
@@ -716,34 +742,36 @@ __global__ void __launch_bounds__(384, 1)
     }
 }
 
+// The kernel's tensor maps: Q tiles, K and V boxes, and Q row groups (packed items).
+struct XMaps {
+    CUtensorMap q, k, v, qg;
+};
+
 template <int D, int G, bool PRECISE>
-static int launch_extend(const ExtendParams &p, const CUtensorMap &qm, const CUtensorMap &km, const CUtensorMap &vm,
-                         int nctas, cudaStream_t s) {
+static int launch_extend(const ExtendParams &p, const XMaps &mp, int nctas, cudaStream_t s) {
     constexpr int smem = XCfg<D>::kSmem;
     static_assert(smem <= 232448, "shared memory budget");
     auto kern = extend_kernel<D, G, PRECISE>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return PKV_E_CUDA;
-    kern<<<nctas, 384, smem, s>>>(p, qm, km, vm);  // persistent: the plan's CTA lists
+    kern<<<nctas, 384, smem, s>>>(p, mp.q, mp.k, mp.v, mp.qg);  // persistent: the plan's CTA lists
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_E_CUDA;
 }
 
 template <int D, bool PRECISE>
-static int dispatch_g(int G, const ExtendParams &p, const CUtensorMap &qm, const CUtensorMap &km, const CUtensorMap &vm,
-                      int n, cudaStream_t s) {
+static int dispatch_g(int G, const ExtendParams &p, const XMaps &mp, int n, cudaStream_t s) {
     switch (G) {
-        case 1: return launch_extend<D, 1, PRECISE>(p, qm, km, vm, n, s);
-        case 2: return launch_extend<D, 2, PRECISE>(p, qm, km, vm, n, s);
-        case 4: return launch_extend<D, 4, PRECISE>(p, qm, km, vm, n, s);
-        case 8: return launch_extend<D, 8, PRECISE>(p, qm, km, vm, n, s);
+        case 1: return launch_extend<D, 1, PRECISE>(p, mp, n, s);
+        case 2: return launch_extend<D, 2, PRECISE>(p, mp, n, s);
+        case 4: return launch_extend<D, 4, PRECISE>(p, mp, n, s);
+        case 8: return launch_extend<D, 8, PRECISE>(p, mp, n, s);
         default: return PKV_E_UNSUPPORTED;
     }
 }
 
 template <int D>
-static int dispatch_extend(int G, const ExtendParams &p, const CUtensorMap &qm, const CUtensorMap &km,
-                           const CUtensorMap &vm, int n, cudaStream_t s, bool precise = false) {
-    return precise ? dispatch_g<D, true>(G, p, qm, km, vm, n, s) : dispatch_g<D, false>(G, p, qm, km, vm, n, s);
+static int dispatch_extend(int G, const ExtendParams &p, const XMaps &mp, int n, cudaStream_t s, bool precise = false) {
+    return precise ? dispatch_g<D, true>(G, p, mp, n, s) : dispatch_g<D, false>(G, p, mp, n, s);
 }
 
 template <int D>
@@ -760,15 +788,21 @@ int check_call(const pkv_pool *pool, const pkv_batch *batch, const void *q, void
 int launch_merge(const pkv_plan_info *info, const void *plan_dev, const float *rec_acc, const float *rec_ml,
                  uint16_t *o, cudaStream_t s);
 
-// Tensor maps: Q as [rows][Hq][D] (box 64 x G x 128/G); gathered K/V as [keys][Hkv][D] (box
-// 64 x 1 x 128): every box lands as 128 rows of 128 bytes, 128-byte swizzled.
+// Tensor maps: Q as [rows][Hq][D] (box 64 x G x 128/G, and 64 x G x 32/G for one row group
+// of a packed tile); gathered K/V as [keys][Hkv][D] (box 64 x 1 x 128): every box lands as
+// 128 (or 32) rows of 128 bytes, 128-byte swizzled.
 static int make_maps(const void *q, int64_t qrows, const uint16_t *kg, const uint16_t *vg, int64_t nkeys, int D,
-                     int hq, int hkv, CUtensorMap *qm, CUtensorMap *km, CUtensorMap *vm) {
+                     int hq, int hkv, XMaps *mp) {
     const int G = hq / hkv;
+    CUtensorMap *qm = &mp->q, *km = &mp->k, *vm = &mp->v;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)hq, (cuuint64_t)std::max<int64_t>(qrows, 1)};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)hq * D * 2};
     cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(128 / G)};
     if (encode_tiled(qm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return PKV_E_CUDA;
+    cuuint32_t gbox[3] = {64, (cuuint32_t)G, (cuuint32_t)(32 / G)};
+    if (encode_tiled(&mp->qg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, gbox,
                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
         return PKV_E_CUDA;
     cuuint64_t kdims[3] = {(cuuint64_t)D, (cuuint64_t)hkv, (cuuint64_t)std::max<int64_t>(nkeys, 1)};
@@ -835,8 +869,8 @@ int decode_span_tensor(const pkv_pool *pool, const pkv_batch *batch, const void 
                                                     batch->batch, hq * D / 8, err);
     if (cudaGetLastError() != cudaSuccess) return PKV_E_CUDA;
 
-    CUtensorMap qm, km, vm;
-    rc = make_maps(qg, nq, kg, vg, nkeys, D, hq, hkv, &qm, &km, &vm);
+    XMaps mp;
+    rc = make_maps(qg, nq, kg, vg, nkeys, D, hq, hkv, &mp);
     if (rc) return rc;
     ExtendParams p;
     p.o = nullptr;  // every item writes records
@@ -850,6 +884,7 @@ int decode_span_tensor(const pkv_pool *pool, const pkv_batch *batch, const void 
     p.rec_acc = rec_acc;
     p.rec_ml = rec_ml;
     p.rec_list = reinterpret_cast<const int32_t *>(plan + info->offsets[14]);
+    p.packs = nullptr;
     // the spans' items, then the short requests' items (precise weights)
     const ExtendItem *items = reinterpret_cast<const ExtendItem *>(plan + info->offsets[7]);
     const int64_t nprec = info->offsets[18];
@@ -861,8 +896,8 @@ int decode_span_tensor(const pkv_pool *pool, const pkv_batch *batch, const void 
         p.cta_off = reinterpret_cast<const int32_t *>(plan + info->offsets[part == 0 ? 16 : 19]);
         const int64_t nctas = info->offsets[part == 0 ? 17 : 20];
         if (nctas < 1 || nctas > n || nprec > nx) return PKV_E_PLAN;
-        int rc = D == 128 ? dispatch_extend<128>(G, p, qm, km, vm, (int)nctas, s, part == 1)
-                          : dispatch_extend<64>(G, p, qm, km, vm, (int)nctas, s, part == 1);
+        int rc = D == 128 ? dispatch_extend<128>(G, p, mp, (int)nctas, s, part == 1)
+                          : dispatch_extend<64>(G, p, mp, (int)nctas, s, part == 1);
         if (rc) return rc;
     }
     return PKV_OK;
@@ -911,8 +946,8 @@ extern "C" int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, con
         if (rc) return rc;
     }
 
-    CUtensorMap qm, km, vm;
-    rc = make_maps(q, info->total_q, kg, vg, nkeys, D, hq, hkv, &qm, &km, &vm);
+    XMaps mp;
+    rc = make_maps(q, info->total_q, kg, vg, nkeys, D, hq, hkv, &mp);
     if (rc) return rc;
 
     ExtendParams p;
@@ -927,6 +962,7 @@ extern "C" int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, con
     p.rec_acc = rec_acc;
     p.rec_ml = rec_ml;
     p.rec_list = nullptr;
+    p.packs = info->offsets[14] > 0 ? reinterpret_cast<const PackInfo *>(plan + info->offsets[13]) : nullptr;
     void *ev0 = g_kernel_events[0], *ev1 = g_kernel_events[1];
     g_kernel_events[0] = g_kernel_events[1] = nullptr;
     if (ev0 && cudaEventRecord(static_cast<cudaEvent_t>(ev0), s) != cudaSuccess) return PKV_E_CUDA;
@@ -939,8 +975,8 @@ extern "C" int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, con
         p.cta_off = reinterpret_cast<const int32_t *>(plan + info->offsets[part == 0 ? 7 : 11]);
         const int64_t nctas = info->offsets[part == 0 ? 8 : 12];
         if (nctas < 1 || nctas > nitems) return PKV_E_PLAN;
-        rc = D == 128 ? dispatch_extend<128>(G, p, qm, km, vm, (int)nctas, s, part == 1)
-                      : dispatch_extend<64>(G, p, qm, km, vm, (int)nctas, s, part == 1);
+        rc = D == 128 ? dispatch_extend<128>(G, p, mp, (int)nctas, s, part == 1)
+                      : dispatch_extend<64>(G, p, mp, (int)nctas, s, part == 1);
         if (rc) return rc;
     }
     if (ev1 && cudaEventRecord(static_cast<cudaEvent_t>(ev1), s) != cudaSuccess) return PKV_E_CUDA;

@@ -347,10 +347,28 @@ struct ExtendItem {      // 64 bytes
     int32_t qpos0;       // position of tok0; token t sees positions <= qpos0 + t
     int32_t pos0;        // context position of the first key of segment 0
     int32_t nseg;        // key segments, consecutive in context positions
-    int32_t rec;         // -1: write o directly; else first partial record (one per token)
-    int32_t flags;       // kItemPrecise: some row sees fewer than kPreciseKeys keys
+    int32_t rec;         // -1: write o directly; else first partial record (one per token);
+                         // kItemPacked: its PackInfo
+    int32_t flags;       // kItemPrecise: some row sees fewer than kPreciseKeys keys; kItemPacked
     int32_t key0[kMaxSegs];   // first gathered key of each segment (row of the workspace)
     int32_t nkeys[kMaxSegs];  // keys of each segment
+};
+
+// A packed extend item: the last few tokens of up to four requests (at most 32 / G each) in
+// one query tile, a 32-row group (one TMEM lane quarter, one softmax warp) each.  Its key
+// segments are the shared spans the requests have in common (every group sees them) and
+// each request's own remaining keys (only that request's group sees them); segment
+// positions are explicit, since every member's own keys start at the same position.
+constexpr int32_t kItemPacked = 4;
+constexpr int kPackSegs = 5;
+struct PackInfo {        // 128 bytes
+    int32_t key0[kPackSegs];   // first gathered key of each segment
+    int32_t nkeys[kPackSegs];  // keys of each segment
+    int32_t spos[kPackSegs];   // context position of each segment's first key
+    int32_t sgrp[kPackSegs];   // row group that sees the segment; -1: every group
+    int32_t tok0[4];           // first query token of each group
+    int32_t ntok[4];           // its tokens (0: group unused)
+    int32_t qpos0[4];          // position of its first token
 };
 
 struct GatherUnit {      // 16 bytes: copy `len` slot rows of one request row into the workspace

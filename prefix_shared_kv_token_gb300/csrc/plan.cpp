@@ -37,7 +37,16 @@ struct ExtendItem { int32_t g, tok0, ntok, qpos0, pos0, nseg, rec, flags, key0[k
 constexpr int32_t kPreciseKeys = 32;
 struct GatherUnit { int32_t src, pos0, len, key0; };
 struct MergeItem { int32_t out_row, rec0, nrec, rec_stride; };
-static_assert(sizeof(DecodeItem) == 32 && sizeof(ExtendItem) == 64 && sizeof(MergeItem) == 16, "layout");
+// a packed extend item (flags & kItemPacked): up to four requests' last few tokens in one
+// query tile, a 32-row group each, over shared segments (sgrp -1) and each one's own tail
+constexpr int32_t kItemPacked = 4;
+constexpr int32_t kPackSegs = 5;
+struct PackInfo {
+    int32_t key0[kPackSegs], nkeys[kPackSegs], spos[kPackSegs], sgrp[kPackSegs];
+    int32_t tok0[4], ntok[4], qpos0[4];
+};
+static_assert(sizeof(DecodeItem) == 32 && sizeof(ExtendItem) == 64 && sizeof(MergeItem) == 16 &&
+                  sizeof(PackInfo) == 128, "layout");
 
 constexpr size_t kHeader = 256;
 // decode: a shared span goes to the tensor-core path from this many member requests and keys
@@ -79,9 +88,11 @@ void lpt_deal(const std::vector<T> &items, const std::vector<int64_t> &cost, int
 // a two-tile item overlaps one tile's softmax with the other's MMAs; a one-tile item over
 // several key tiles splits them between the two softmax warpgroups (about half the cost of
 // a two-tile item); a one-tile item over one key tile runs serially.
-int64_t extend_item_cost(const ExtendItem &x, int32_t tq) {
+int64_t extend_item_cost(const ExtendItem &x, int32_t tq, const std::vector<PackInfo> *packs = nullptr) {
     int64_t tiles = 0;
-    for (int32_t i = 0; i < x.nseg; ++i) tiles += (x.nkeys[i] + 127) / 128;
+    const bool packed = (x.flags & kItemPacked) && packs;
+    const int32_t *nk = packed ? (*packs)[(size_t)x.rec].nkeys : x.nkeys;
+    for (int32_t i = 0; i < std::min(x.nseg, packed ? kPackSegs : kMaxSegs); ++i) tiles += (nk[i] + 127) / 128;
     const int64_t per = x.ntok > tq ? 6 : (tiles >= 2 ? 3 : 4);
     return tiles * per + 4;
 }
@@ -542,6 +553,11 @@ extern "C" int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int
     std::vector<ExtendItem> items;
     std::vector<MergeItem> merges;
     int32_t num_span_items = 0;
+    // A request's last few tokens (at most one 32-row group: 32/G tokens) after shared spans
+    // are set aside: such chunks with the same shared spans share one query tile, a row
+    // group each, over those spans plus each one's own tail (a packed item).
+    const int32_t RG = 32 / G;  // tokens per 32-row group
+    std::vector<ExtendItem> leftovers;
     for (int32_t r = 0; r < batch; ++r) {
         const int32_t e = extend_lens[r], p = seq_lens[r] - e;
         const auto &sg = segs_of[r];
@@ -562,6 +578,80 @@ extern "C" int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int
                 it.nkeys[k] = k + 1 == sg.size() ? end - R.pos0 : sg[k].len;
             }
             if (it.nseg > 1) ++num_span_items;
+            if (n <= RG && it.nseg > 1 && !(it.flags & 1)) {
+                leftovers.push_back(it);
+                continue;
+            }
+            for (int32_t g = 0; g < num_kv_heads; ++g) {
+                it.g = g;
+                items.push_back(it);
+            }
+        }
+    }
+    // pack the set-aside chunks: same shared segments (runs, lengths, start), up to 4 groups
+    // and kPackSegs segments per tile; a chunk left alone is an ordinary item
+    std::vector<PackInfo> packs;
+    {
+        auto same_shared = [](const ExtendItem &a, const ExtendItem &b) {
+            if (a.nseg != b.nseg || a.pos0 != b.pos0) return false;
+            for (int32_t k = 0; k + 1 < a.nseg; ++k)
+                if (a.key0[k] != b.key0[k] || a.nkeys[k] != b.nkeys[k]) return false;
+            return true;
+        };
+        std::vector<char> used(leftovers.size(), 0);
+        for (size_t a = 0; a < leftovers.size(); ++a) {
+            if (used[a]) continue;
+            const ExtendItem &lead = leftovers[a];
+            const int32_t nshared = lead.nseg - 1;
+            const int32_t cap = std::min<int32_t>(4, kPackSegs - nshared);
+            std::vector<size_t> grp{a};
+            used[a] = 1;
+            for (size_t b = a + 1; b < leftovers.size() && (int32_t)grp.size() < cap; ++b)
+                if (!used[b] && same_shared(lead, leftovers[b])) {
+                    grp.push_back(b);
+                    used[b] = 1;
+                }
+            if (grp.size() == 1) {
+                ExtendItem it = lead;
+                for (int32_t g = 0; g < num_kv_heads; ++g) {
+                    it.g = g;
+                    items.push_back(it);
+                }
+                continue;
+            }
+            PackInfo pk{};
+            int32_t pos = lead.pos0;
+            for (int32_t k = 0; k < nshared; ++k) {
+                pk.key0[k] = lead.key0[k];
+                pk.nkeys[k] = lead.nkeys[k];
+                pk.spos[k] = pos;
+                pk.sgrp[k] = -1;
+                pos += lead.nkeys[k];
+            }
+            for (size_t m = 0; m < grp.size(); ++m) {
+                const ExtendItem &x = leftovers[grp[m]];
+                const int32_t k = nshared + (int32_t)m;
+                pk.key0[k] = x.key0[x.nseg - 1];
+                pk.nkeys[k] = x.nkeys[x.nseg - 1];
+                pk.spos[k] = pos;  // every member's own tail starts right after the shared part
+                pk.sgrp[k] = (int32_t)m;
+                pk.tok0[m] = x.tok0;
+                pk.ntok[m] = x.ntok;
+                pk.qpos0[m] = x.qpos0;
+            }
+            ExtendItem it{};
+            it.tok0 = lead.tok0;
+            it.ntok = TQ2 / 2;  // one query tile
+            it.qpos0 = lead.qpos0;
+            it.pos0 = lead.pos0;
+            it.nseg = nshared + (int32_t)grp.size();
+            it.rec = (int32_t)packs.size();
+            it.flags = kItemPacked;
+            for (int32_t k = 0; k < std::min(it.nseg, kMaxSegs); ++k) {
+                it.key0[k] = pk.key0[k];
+                it.nkeys[k] = pk.nkeys[k];
+            }
+            packs.push_back(pk);
             for (int32_t g = 0; g < num_kv_heads; ++g) {
                 it.g = g;
                 items.push_back(it);
@@ -580,7 +670,7 @@ extern "C" int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int
         auto deal = [&](const std::vector<ExtendItem> &v, std::vector<ExtendItem> *out, std::vector<int32_t> *off) {
             const int32_t n = std::max<int32_t>(1, std::min<int32_t>((int32_t)v.size(), num_sms));
             std::vector<int64_t> cost;
-            for (const ExtendItem &x : v) cost.push_back(extend_item_cost(x, TQ2 / 2));
+            for (const ExtendItem &x : v) cost.push_back(extend_item_cost(x, TQ2 / 2, &packs));
             lpt_deal(v, cost, n, out, off);
             return n;
         };
@@ -615,8 +705,11 @@ extern "C" int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int
     info->offsets[10] = (int64_t)placed_x.size();
     info->offsets[11] = (int64_t)off; off = align16(off + cta_off_x.size() * sizeof(int32_t));
     info->offsets[12] = nctas_x;
+    info->offsets[13] = (int64_t)off; off = align16(off + packs.size() * sizeof(PackInfo));
+    info->offsets[14] = (int64_t)packs.size();
     std::vector<uint8_t> blob(std::max<size_t>(off, 16), 0);
     put(blob, (size_t)info->offsets[0], placed);
+    put(blob, (size_t)info->offsets[13], packs);
     put(blob, (size_t)info->offsets[7], cta_off);
     put(blob, (size_t)info->offsets[11], cta_off_x);
     put(blob, (size_t)info->offsets[3], merges);

@@ -393,3 +393,20 @@ def test_decode_graph_replay_matches_the_call():
         torch.cuda.synchronize()
         assert torch.equal(c.o, first)
     check_outputs(w, calls)
+
+
+@pytest.mark.parametrize("hq,hkv,d,suffix,n_req", [
+    (32, 8, 128, 70, 9),    # G 4: 6 last tokens per request, packed 4 + 4 (+ 1 alone)
+    (32, 8, 128, 65, 4),    # 1 last token each
+    (64, 8, 128, 66, 5),    # G 8: 2 last tokens (4-token row groups)
+    (16, 8, 64, 140, 3),    # G 2: 12 last tokens (16-token row groups)
+    (16, 16, 128, 20, 6),   # G 1: a whole 20-token suffix per row group
+])
+def test_extend_packed_last_tokens(hq, hkv, d, suffix, n_req):
+    """Requests sharing a cached prefix whose last few new tokens are packed, a 32-row group
+    each, into shared query tiles (each group also sees only its own remaining keys)."""
+    w = W.fewshot_extend(seed=68 + suffix, n_req=n_req, prefix=300, suffix=suffix, hq=hq, hkv=hkv, d=d,
+                         num_slots=8192)
+    _, calls = run_step(w)
+    assert int(calls["extend"].plan.info.offsets[14]) >= 1     # packed tiles were planned
+    check_outputs(w, calls)

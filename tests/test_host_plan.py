@@ -19,6 +19,8 @@ EXT = np.dtype([("g", "<i4"), ("tok0", "<i4"), ("ntok", "<i4"), ("qpos0", "<i4")
                 ("nseg", "<i4"), ("rec", "<i4"), ("flags", "<i4"), ("key0", "<i4", (4,)), ("nkeys", "<i4", (4,))])
 GU = np.dtype([("src", "<i4"), ("pos0", "<i4"), ("len", "<i4"), ("key0", "<i4")])
 MRG = np.dtype([("out_row", "<i4"), ("rec0", "<i4"), ("nrec", "<i4"), ("stride", "<i4")])
+PACK = np.dtype([("key0", "<i4", (5,)), ("nkeys", "<i4", (5,)), ("spos", "<i4", (5,)), ("sgrp", "<i4", (5,)),
+                 ("tok0", "<i4", (4,)), ("ntok", "<i4", (4,)), ("qpos0", "<i4", (4,))])
 
 
 def test_header_symbols_exported():
@@ -256,7 +258,29 @@ def test_extend_plan_covers_causal_triangle(cascade):
     pos_of_tok = np.concatenate([np.arange(pre[r], seq[r]) for r in range(4)])
     members = {0: {0, 1, 2}, 1: {0, 1, 2}, 2: {0, 1, 2}, 3: {3}}
     cover = np.zeros((T, 8, int(seq.max())), np.int32)
+    packs = _sections(plan, PACK, int(info.offsets[14]), info.offsets[13])
     for it in items:
+        if it["flags"] & 4:   # packed: row groups of several requests' last tokens
+            pk = packs[it["rec"]]
+            assert 2 <= it["nseg"] <= 5 and it["ntok"] == 128 // 4
+            ngrp = 0
+            for m in range(4):
+                for t in range(pk["ntok"][m]):
+                    tok = pk["tok0"][m] + t
+                    assert 1 <= pk["ntok"][m] <= 32 // 4
+                    for sgi in range(it["nseg"]):
+                        if pk["sgrp"][sgi] not in (-1, m):
+                            continue
+                        for k in range(pk["nkeys"][sgi]):
+                            pos = pk["spos"][sgi] + k
+                            if pos <= pk["qpos0"][m] + t:
+                                gk = pk["key0"][sgi] + k
+                                assert g_pos[gk] == pos
+                                assert g_src[gk] == req_of_tok[tok] or (casc is not None and g_src[gk] in members[req_of_tok[tok]])
+                                cover[tok, it["g"], pos] += 1
+                ngrp += pk["ntok"][m] > 0
+            assert ngrp >= 2
+            continue
         assert it["rec"] == -1 and 1 <= it["nseg"] <= 4
         for t in range(it["ntok"]):
             tok = it["tok0"] + t
@@ -276,6 +300,8 @@ def test_extend_plan_covers_causal_triangle(cascade):
         assert np.all(cover[tok] == cover[tok, 0])
     if cascade:
         assert info.num_span_items > 0 and int(info.offsets[6]) < int(seq.sum())  # the span is gathered once
+        # requests 0 and 2 end with 6 and 1 tokens after the shared span: one packed tile per head
+        assert int(info.offsets[14]) == 1 and sum(1 for it in items if it["flags"] & 4) == 8
 
 
 def test_struct_layouts_match_header(tmp_path):

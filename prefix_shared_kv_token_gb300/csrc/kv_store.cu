@@ -7,9 +7,9 @@
 // architecture figure: compute missing KV tensors, insert node).
 //
 // Design: a pure bandwidth kernel.  One token row per (token, K|V) is Hkv*d elements,
-// contiguous in both source and destination, so each thread moves 16-byte vectors and a warp
-// covers 512 contiguous source bytes; the grid is a multiple of the SM count and grid-strides
-// over all rows.  bf16 pools copy bits; fp8 pools divide by the per-tensor scale in IEEE
+// contiguous in both source and destination.  A warp moves one row at a time (its slot read
+// once, lanes striding the row's 16-byte vectors with four loads in flight); the grid is a
+// multiple of the SM count and grid-strides over all rows.  bf16 pools copy bits; fp8 pools divide by the per-tensor scale in IEEE
 // fp32 and round to E4M3 with saturation (cvt.rn.satfinite).  Slots outside [0, num_slots)
 // are skipped and reported in the error word instead of being written.
 
@@ -25,37 +25,45 @@ __global__ void __launch_bounds__(256) kv_store_kernel(const uint4 *__restrict__
                                                        uint8_t *__restrict__ k_pool, uint8_t *__restrict__ v_pool,
                                                        int64_t num_slots, float k_scale, float v_scale,
                                                        int32_t *__restrict__ err) {
-    // vec_per_row: 16-byte source vectors in one token row (Hkv * d * 2 / 16)
-    const int64_t per_tensor = n * (int64_t)vec_per_row;
-    const int64_t total = 2 * per_tensor;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
-        const bool is_v = idx >= per_tensor;
-        const int64_t j = is_v ? idx - per_tensor : idx;
-        const int64_t tok = j / vec_per_row;
-        const int32_t part = (int32_t)(j - tok * vec_per_row);
+    // one warp per token row (K rows of tokens 0..n-1, then their V rows), grid-strided; the
+    // row's slot is read once and the lanes stride its vec_per_row 16-byte source vectors,
+    // four loads in flight before their stores
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < 2 * n; row += nwarps) {
+        const bool is_v = row >= n;
+        const int64_t tok = is_v ? row - n : row;
         const int32_t slot = __ldg(loc + tok);
         if (slot < 0 || (int64_t)slot >= num_slots) {
-            set_error(err, DERR_SLOT_RANGE);
+            if (lane == 0) set_error(err, DERR_SLOT_RANGE);
             continue;
         }
-        const uint4 x = __ldcs((is_v ? v_new : k_new) + j);  // streamed once
+        const uint4 *src = (is_v ? v_new : k_new) + tok * vec_per_row;
         uint8_t *pool = is_v ? v_pool : k_pool;
-        if constexpr (!FP8) {
-            uint4 *dst = reinterpret_cast<uint4 *>(pool) + (int64_t)slot * vec_per_row + part;
-            *dst = x;
-        } else {
-            const float s = is_v ? v_scale : k_scale;
-            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-            uint16_t c[4];
+        const float s = is_v ? v_scale : k_scale;
+        for (int v0 = lane; v0 < vec_per_row; v0 += 4 * 32) {
+            uint4 x[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                c[i] = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(w[i]), s), __fdiv_rn(bf16_hi(w[i]), s));
-            uint2 y;
-            y.x = (uint32_t)c[0] | ((uint32_t)c[1] << 16);
-            y.y = (uint32_t)c[2] | ((uint32_t)c[3] << 16);
-            uint2 *dst = reinterpret_cast<uint2 *>(pool) + (int64_t)slot * vec_per_row + part;
-            *dst = y;
+            for (int k = 0; k < 4; ++k)
+                if (v0 + 32 * k < vec_per_row) x[k] = __ldcs(src + v0 + 32 * k);  // streamed once
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int v = v0 + 32 * k;
+                if (v >= vec_per_row) continue;
+                if constexpr (!FP8) {
+                    reinterpret_cast<uint4 *>(pool)[(int64_t)slot * vec_per_row + v] = x[k];
+                } else {
+                    const uint32_t w[4] = {x[k].x, x[k].y, x[k].z, x[k].w};
+                    uint16_t c[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        c[i] = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(w[i]), s), __fdiv_rn(bf16_hi(w[i]), s));
+                    uint2 y;
+                    y.x = (uint32_t)c[0] | ((uint32_t)c[1] << 16);
+                    y.y = (uint32_t)c[2] | ((uint32_t)c[3] << 16);
+                    reinterpret_cast<uint2 *>(pool)[(int64_t)slot * vec_per_row + v] = y;
+                }
+            }
         }
     }
 }
@@ -73,9 +81,8 @@ extern "C" int pkv_kv_store(const pkv_pool *pool, const void *k_new, const void 
     if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15) return PKV_E_INVALID;
     const int64_t row_bytes = (int64_t)pool->num_kv_heads * pool->head_dim * 2;  // bf16 source row
     const int32_t vec_per_row = (int32_t)(row_bytes / 16);
-    const int64_t total = 2 * n * vec_per_row;
-    const int threads = 256;
-    int64_t blocks = (total + threads - 1) / threads;
+    const int threads = 256;                      // 8 warps, one token row each at a time
+    int64_t blocks = (2 * n + 7) / 8;
     const int64_t cap = (int64_t)num_sms() * 8;  // 8 resident blocks of 256 per SM
     if (blocks > cap) blocks = cap;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

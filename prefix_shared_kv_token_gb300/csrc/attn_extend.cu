@@ -122,8 +122,15 @@ struct GatherParams {
     int32_t page_shift;  // 0: token table; else log2 of the page size (page table)
     const int32_t *req_pool_indices;
     const GatherUnit *units;
+    int32_t nunits;
     uint16_t *k_out;
     uint16_t *v_out;
+    // query rows copied by the CTAs after the units (decode's tensor-core spans; else none):
+    // row i of q_out = row q_rows[i] of q_src, q_row_vecs 16-byte vectors each
+    const uint4 *q_src;
+    uint4 *q_out;
+    const int32_t *q_rows;
+    int32_t q_batch, q_row_vecs;
     int32_t *err;
 };
 
@@ -131,6 +138,16 @@ struct GatherParams {
 // (Hkv * D elements, contiguous in the pool and in the output).
 template <int D, bool FP8>
 __global__ void __launch_bounds__(256) gather_kernel(const GatherParams p) {
+    if ((int)blockIdx.x >= p.nunits) {  // a query row
+        const int i = blockIdx.x - p.nunits, r = __ldg(p.q_rows + i);
+        if (r < 0 || r >= p.q_batch) {
+            if (threadIdx.x == 0) set_error(p.err, DERR_POSITION);
+            return;
+        }
+        for (int v = threadIdx.x; v < p.q_row_vecs; v += blockDim.x)
+            p.q_out[(int64_t)i * p.q_row_vecs + v] = __ldg(p.q_src + (int64_t)r * p.q_row_vecs + v);
+        return;
+    }
     const GatherUnit u = p.units[blockIdx.x];
     const int row = __ldg(p.req_pool_indices + u.src);
     if (row < 0 || row >= p.rt_rows || u.pos0 < 0 || u.pos0 + u.len > (p.rt_stride << p.page_shift)) {
@@ -816,19 +833,6 @@ static int make_maps(const void *q, int64_t qrows, const uint16_t *kg, const uin
     return PKV_OK;
 }
 
-// Copy query rows q[src[i]] (Hq * D bf16 each) to row i of a contiguous buffer.
-__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4 *__restrict__ q, uint4 *__restrict__ out,
-                                                         const int32_t *__restrict__ src, int batch, int row_vecs,
-                                                         int32_t *err) {
-    const int r = __ldg(src + blockIdx.x);
-    if (r < 0 || r >= batch) {
-        if (threadIdx.x == 0) set_error(err, DERR_POSITION);
-        return;
-    }
-    for (int i = threadIdx.x; i < row_vecs; i += blockDim.x)
-        out[(int64_t)blockIdx.x * row_vecs + i] = __ldg(q + (int64_t)r * row_vecs + i);
-}
-
 // Decode over shared spans with many members, on the tensor cores: the plan's spans are
 // gathered once into the workspace (bf16 [key][Hkv][D]), the member requests' query rows
 // are gathered next to them, and extend-kernel items (two 128-row query tiles of 128/G
@@ -862,12 +866,16 @@ int decode_span_tensor(const pkv_pool *pool, const pkv_batch *batch, const void 
     gp.k_out = kg;
     gp.v_out = vg;
     gp.err = err;
-    int rc = D == 128 ? launch_gather<128>(gp, fp8, (int)nunits, s) : launch_gather<64>(gp, fp8, (int)nunits, s);
+    // one launch: the span keys, then the member query rows
+    gp.nunits = (int32_t)nunits;
+    gp.q_src = static_cast<const uint4 *>(q);
+    gp.q_out = reinterpret_cast<uint4 *>(qg);
+    gp.q_rows = reinterpret_cast<const int32_t *>(plan + info->offsets[12]);
+    gp.q_batch = batch->batch;
+    gp.q_row_vecs = hq * D / 8;
+    int rc = D == 128 ? launch_gather<128>(gp, fp8, (int)(nunits + nq), s)
+                      : launch_gather<64>(gp, fp8, (int)(nunits + nq), s);
     if (rc) return rc;
-    gather_rows_kernel<<<(unsigned)nq, 256, 0, s>>>(static_cast<const uint4 *>(q), reinterpret_cast<uint4 *>(qg),
-                                                    reinterpret_cast<const int32_t *>(plan + info->offsets[12]),
-                                                    batch->batch, hq * D / 8, err);
-    if (cudaGetLastError() != cudaSuccess) return PKV_E_CUDA;
 
     XMaps mp;
     rc = make_maps(qg, nq, kg, vg, nkeys, D, hq, hkv, &mp);
@@ -941,6 +949,11 @@ extern "C" int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, con
     gp.v_out = vg;
     gp.err = reinterpret_cast<int32_t *>(ws);
     const int nunits = (int)info->offsets[5];
+    gp.nunits = nunits;  // no query rows to copy
+    gp.q_src = nullptr;
+    gp.q_out = nullptr;
+    gp.q_rows = nullptr;
+    gp.q_batch = gp.q_row_vecs = 0;
     if (nunits > 0) {
         rc = D == 128 ? launch_gather<128>(gp, fp8, nunits, s) : launch_gather<64>(gp, fp8, nunits, s);
         if (rc) return rc;

@@ -127,7 +127,7 @@ class Call:
         if self.kind == "extend":
             n += (1 if info.offsets[5] > 0 else 0) + 1           # key gather, extend kernel
         else:
-            n += 3 if info.offsets[8] > 0 else 0                  # tensor-core spans: gathers + kernel
+            n += 2 if info.offsets[8] > 0 else 0                  # tensor-core spans: gather + kernel
             n += 1 if info.num_items > 0 else 0                   # decode kernel
         return n + (1 if info.num_merge > 0 else 0)
 

@@ -125,10 +125,14 @@ class Call:
         info = self.plan.info
         n = 1 if self.out_cache_loc.numel() > 0 else 0
         if self.kind == "extend":
-            n += (1 if info.offsets[5] > 0 else 0) + 1           # key gather, extend kernel
+            nprec = int(info.offsets[10])                        # items with precise weights
+            n += (1 if info.offsets[5] > 0 else 0)               # key gather
+            n += (1 if info.num_items - nprec > 0 else 0) + (1 if nprec > 0 else 0)  # extend kernel(s)
         else:
-            n += 2 if info.offsets[8] > 0 else 0                  # tensor-core spans: gather + kernel
-            n += 1 if info.num_items > 0 else 0                   # decode kernel
+            nx, nprec = int(info.offsets[8]), int(info.offsets[18])
+            if nx > 0:                                           # tensor-core pass: one gather, then
+                n += 1 + (1 if nx - nprec > 0 else 0) + (1 if nprec > 0 else 0)  # span / short items
+            n += 1 if info.num_items > 0 else 0                  # decode kernel
         return n + (1 if info.num_merge > 0 else 0)
 
     # ---- end-to-end variant: inputs from pinned host buffers, output back to the host

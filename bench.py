@@ -107,6 +107,22 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def max_over_ranks(seconds, device):
+    """Each rank's timings -> their elementwise maximum over all ranks (the slowest replica
+    sets the job's time); with no process group, the rank's own timings."""
+    import torch
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return [float(x) for x in seconds]
+    t = torch.tensor([float(x) for x in seconds], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_throughput(world, steps, units_per_step, seconds):
+    """Whole-job rate: every replica processes ``units_per_step`` per step (weak scaling)."""
+    return world * steps * units_per_step / seconds
+
+
 def kernel_hash(kind):
     # the sources of every kernel the measured region runs (decode also runs the extend kernel)
     srcs = {"extend": ("attn_extend.cu",), "decode": ("attn_decode.cu", "attn_extend.cu"), "store": ("kv_store.cu",)}
@@ -331,14 +347,9 @@ def run_ours(args, rank, world):
             raise RuntimeError("device error word set during the timed steps")
 
     tokens_per_step = sum(c.num_queries for c in calls)
-    t_total = sum(step_ms) / 1e3
-    t_e2e = e2e_total_ms / 1e3
-    if world > 1:
-        tt = torch.tensor([t_total, t_e2e], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t_total, t_e2e = float(tt[0]), float(tt[1])
-    value = world * K * tokens_per_step / t_total
-    e2e_value = world * K * tokens_per_step / t_e2e
+    t_total, t_e2e = max_over_ranks([sum(step_ms) / 1e3, e2e_total_ms / 1e3], dev)
+    value = job_throughput(world, K, tokens_per_step, t_total)
+    e2e_value = job_throughput(world, K, tokens_per_step, t_e2e)
 
     # roofline of the dominant kernel
     pk = peaks()

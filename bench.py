@@ -124,8 +124,10 @@ def job_throughput(world, steps, units_per_step, seconds):
 
 
 def kernel_hash(kind):
-    # the sources of every kernel the measured region runs (decode also runs the extend kernel)
-    srcs = {"extend": ("attn_extend.cu",), "decode": ("attn_decode.cu", "attn_extend.cu"), "store": ("kv_store.cu",)}
+    # the sources of every kernel the measured region runs (decode also runs the extend kernel),
+    # and the planner, which decides what those kernels read
+    srcs = {"extend": ("attn_extend.cu", "plan.cpp"), "decode": ("attn_decode.cu", "attn_extend.cu", "plan.cpp"),
+            "store": ("kv_store.cu",)}
     h = hashlib.sha256()
     for f in srcs[kind] + ("common.cuh",):
         with open(os.path.join(ROOT, "prefix_shared_kv_token_gb300", "csrc", f), "rb") as fh:

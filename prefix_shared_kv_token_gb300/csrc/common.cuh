@@ -329,7 +329,7 @@ struct DecodeItem {      // 32 bytes
     int32_t src;         // batch index whose req_to_token row holds the keys
     int32_t k0;          // first key position
     int32_t k1;          // one past the last key position; < 0: seq_lens[src]
-    int32_t rot;         // tile the item starts at (tiles are visited cyclically from there)
+    int32_t rot;         // tile the item starts at (tiles are visited cyclically from there; the planner uses 0)
 };
 
 constexpr int kMaxSegs = 4;

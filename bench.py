@@ -7,7 +7,9 @@ when the timed region starts; the L2 is flushed (512 MiB write) between timed st
 the per-step CUDA events.  ``e2e`` repeats the measurement through the same C-ABI calls with
 every step's inputs copied from pinned host memory and its output copied back inside the
 timed region, the copies of neighbouring steps overlapping each step's kernels (three device
-buffer sets, one copy stream each way).
+buffer sets, one copy stream each way).  ``unflushed`` repeats the device-resident steps back
+to back with no flush between them; ``kv_store`` gives the store's GB/s on its bytes read and
+written.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl ours|reference]
 
@@ -334,7 +336,19 @@ def run_ours(args, rank, world):
                 c.run_e2e()
             e2e_ev[k][1].record(stream)
         torch.cuda.synchronize()
+        # the same device-resident steps back to back without the L2 flush (shared spans and
+        # the previous step's tables may still be in L2): reported beside the flushed figure
+        uev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for k in range(K):
+            uev[k][0].record(stream)
+            for c in calls:
+                c.store()
+            for c in calls:
+                c.replay_attend() if c.graph is not None else c.attend()
+            uev[k][1].record(stream)
+        torch.cuda.synchronize()
     step_ms = [ev[k][0].elapsed_time(ev[k][-1]) for k in range(K)]
+    unflushed_ms = [a.elapsed_time(b) for a, b in uev]
     store_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
     attn_ms = {}
     for i, c in enumerate(calls):   # per kind: all of the step's calls of that kind
@@ -377,6 +391,9 @@ def run_ours(args, rank, world):
     roof["peak_source"] = pk["source"] + " (burst)"
 
     launches_per_step = sum(c.launches() for c in calls)
+    # kv_store: bf16 K and V rows read, pool rows written (bf16 or e4m3), slot indices read
+    elem = 1 if w.dtype == "fp8_e4m3" else 2
+    store_bytes = sum((c.k_new.numel() + c.v_new.numel()) * (2 + elem) + c.out_cache_loc.numel() * 4 for c in calls)
     h2d = sum(c.h2d_bytes() for c in calls)
     d2h = sum(c.d2h_bytes() for c in calls)
     cfg = {"workload": w.name, "config_id": None if args.workload else args.config, "requests": len(w.requests),
@@ -401,6 +418,11 @@ def run_ours(args, rank, world):
         "gpu_launches": K * launches_per_step,
         "kernel_ms": {"kv_store": round(float(np.mean(store_ms)), 4),
                       **{f"attn_{k}": round(float(np.mean(v)), 4) for k, v in attn_ms.items()}},
+        "kv_store": {"bytes_per_step": int(store_bytes),
+                     "gbs": round(store_bytes / (float(np.mean(store_ms)) / 1e3) / 1e9, 1)},
+        "unflushed": {"ms_per_step": round(float(np.mean(unflushed_ms)), 4),
+                      "value": round(job_throughput(world, K, tokens_per_step, sum(unflushed_ms) / 1e3), 1),
+                      "note": "same steps without the L2 flush between them"},
         "wall_s": round(wall, 4),
         "clocks": clocks.summary(),
     }

@@ -8,8 +8,9 @@ memory -- and forwards to the library.  Names follow the C entry points without 
     kv_store      scatter new K/V rows into pool slots (bf16 copy or fp8 quantisation)
     plan_decode   host work decomposition of a decode call (split-KV, shared-prefix cascade)
     plan_extend   host work decomposition of an extend call
-    attn_decode   one query token per request over its whole context (tcgen05-free, mma.sync)
-    attn_extend   causal extend of the uncached suffix (tcgen05 / TMEM / TMA gather4)
+    attn_decode   one query token per request over its whole context (widely shared spans on
+                  the tensor cores, the rest by a persistent bulk-copy kernel with mma.sync)
+    attn_extend   causal extend of the uncached suffix (key gather, then tcgen05 / TMEM / TMA)
     RadixTree     host radix tree: match_prefix (with split), insert, LRU evict, lock_ref,
                   cascade extraction
     Allocator     token-slot free list

@@ -63,8 +63,9 @@ def _decode_cover(plan, seq, hkv, cascade_spans=None):
     recs_seen = {}
     for it in items:
         assert it["g0"] % hg == 0 and 1 <= it["nreq"] <= 16 // G
-        if it["k1"] >= 0:
-            assert 0 <= it["rot"] < (it["k1"] - it["k0"] + 15) // 16
+        # every item reads its keys in order from its first tile: member groups of one span
+        # chunk then read each tile at about the same time, so all but the first hit L2
+        assert it["rot"] == 0
         for i in range(it["nreq"]):
             r = row_req[it["row_off"] + i]
             k1 = it["k1"] if it["k1"] >= 0 else seq[r]

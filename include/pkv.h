@@ -131,8 +131,10 @@ typedef struct pkv_cascade {
 
 /* Planner knobs (NULL = defaults). */
 typedef struct pkv_plan_opts {
-    int32_t chunk_keys;    /* decode: keys per unshared work item (0 = default 256)         */
-    int32_t span_chunk;    /* decode: keys per shared-span work item (0 = default 4096)     */
+    int32_t chunk_keys;    /* decode: keys per unshared work item (0 = 256, cut finer for a */
+                           /* small batch so each persistent CTA gets about two items)      */
+    int32_t span_chunk;    /* decode: keys per shared-span work item (0 = 1024, cut finer   */
+                           /* the same way; tensor-core spans are sized for ~one item per SM) */
     int32_t num_sms;       /* SMs of the target GPU for load balancing (0 = 152)             */
     int32_t dynamic_tail;  /* decode: last item of each request reads its end from seq_lens  */
                            /* on the device, so the plan stays valid while tails grow by     */

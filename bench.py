@@ -12,6 +12,7 @@ to back with no flush between them; ``kv_store`` gives the store's GB/s on its b
 written.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl ours|reference]
+                    [--page-size P] [--workload chunked_prefill|serving] [--no-graph] [--no-cascade]
 
 --impl reference times the oracle (plain float64 CPU code) on the host cores on bounded
 samples of the same workload.  Under torchrun each rank runs an independent replica (the

@@ -13,6 +13,12 @@ written.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl ours|reference]
                     [--page-size P] [--workload chunked_prefill|serving] [--no-graph] [--no-cascade]
+                    [--no-cpu-baseline] [--no-more-configs] [--pool-slots S]
+
+The default run (few-shot extend, configuration 2) also measures the decode workloads and the
+mixed fp8 step (configurations 3-5) after the headline and reports them under
+``more_configs``; the oracle leg (``cpu_baseline``) is at the same time the parity check of
+every output it covers (``parity``).
 
 --impl reference times the oracle (plain float64 CPU code) on the host cores on bounded
 samples of the same workload.  Under torchrun each rank runs an independent replica (the
@@ -55,7 +61,7 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms while running."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -70,7 +76,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except Exception:
@@ -247,22 +253,29 @@ def run_serving(args):
     }
 
 
-def run_ours(args, rank, world):
+def measure(w, args, dev, steps, world, e2e=True):
+    """Build the workload's calls in a fresh pool and time ``steps`` steps of them (after
+    ``args.warmup`` untimed steps): per-step CUDA events on the launching stream, the L2
+    flushed between steps outside the events, clocks sampled meanwhile.  With ``e2e`` also the
+    pipelined end-to-end steps, the serial end-to-end steps and the unflushed steps.  Returns
+    (fields of the JSON line, the calls)."""
     import torch
-    import workloads as W
+    import prefix_shared_kv_token_gb300 as pkv
     from prefix_shared_kv_token_gb300.runtime import PrefixCache, run_e2e_pipelined
 
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    w = load_workload(args)
     facts = workload_facts(w)
     pc = PrefixCache(w, device=str(dev), page_size=args.page_size)
     if w.name == "chunked_prefill":
         calls = pc.prepare_chunked()       # one extend call per chunk, over the chunks before it
+        plan_ms = None
     else:
         pc.populate()
-        calls = [pc.prepare(kind, cascade=not args.no_cascade) for kind in ("extend", "decode")
-                 if any(r.kind == kind for r in w.requests)]
+        kinds = [k for k in ("extend", "decode") if any(r.kind == k for r in w.requests)]
+        calls = [pc.prepare(kind, cascade=not args.no_cascade) for kind in kinds]
+        # host planning of one step (tree match + lock, slots, tables, cascade, plan), which a
+        # server repeats for every new batch; measured after the calls above are built
+        plan_ms = (sum(pc.host_step_ms(k, reps=3, cascade=not args.no_cascade) for k in kinds)
+                   if args.page_size == 1 else None)
     stream = torch.cuda.current_stream()
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
 
@@ -282,18 +295,17 @@ def run_ours(args, rank, world):
         if c.kind == "decode" and not args.no_graph:
             c.capture_attend()
     torch.cuda.synchronize()
-    import prefix_shared_kv_token_gb300 as pkv
     for c in calls:
         if pkv.get_device_error(c.workspace) != 0:
             raise RuntimeError("device error word set during warm-up")
 
     # timed region: per-step events (store, attention per call) on the launching stream
-    K = args.steps
+    K = steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 + 2 * len(calls))] for _ in range(K)]
     # the extend call's tensor-core kernel alone (after its key gather, before its merge)
     kev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in calls]
            for _ in range(K)]
-    for a, b in (pair for step in kev for pair in step):
+    for a, b in (pair for step_ in kev for pair in step_):
         a.record(stream)
         b.record(stream)
     if world > 1:
@@ -316,46 +328,14 @@ def run_ours(args, rank, world):
                 e[3 + 2 * i].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
-        if world > 1:
-            torch.distributed.barrier()
-        # end-to-end: same calls, inputs from pinned host memory, output back to the host.
-        # Pipelined (step k+1's inputs copy in and step k-1's output copies out while step k
-        # computes; three device buffer sets, so the two copies never wait on each other),
-        # with a 256 MiB L2 flush before every step's kernels inside the timed span; and, for
-        # reference, fully serialised steps.
-        for c in calls:
-            c.pin_host()
-        sets = [c.e2e_sets(3) for c in calls]
-        e2e_flush = flush[:(256 << 20) // 4]
-        run_e2e_pipelined(sets, args.warmup, e2e_flush)
-        e2e_total_ms = run_e2e_pipelined(sets, K, e2e_flush)
-        e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-        for k in range(K):
-            flush.zero_()
-            e2e_ev[k][0].record(stream)
-            for c in calls:
-                c.run_e2e()
-            e2e_ev[k][1].record(stream)
-        torch.cuda.synchronize()
-        # the same device-resident steps back to back without the L2 flush (shared spans and
-        # the previous step's tables may still be in L2): reported beside the flushed figure
-        uev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-        for k in range(K):
-            uev[k][0].record(stream)
-            for c in calls:
-                c.store()
-            for c in calls:
-                c.replay_attend() if c.graph is not None else c.attend()
-            uev[k][1].record(stream)
-        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
     step_ms = [ev[k][0].elapsed_time(ev[k][-1]) for k in range(K)]
-    unflushed_ms = [a.elapsed_time(b) for a, b in uev]
     store_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
     attn_ms = {}
     for i, c in enumerate(calls):   # per kind: all of the step's calls of that kind
         t = [ev[k][2 + 2 * i].elapsed_time(ev[k][3 + 2 * i]) for k in range(K)]
         attn_ms[c.kind] = [x + y for x, y in zip(attn_ms[c.kind], t)] if c.kind in attn_ms else t
-    e2e_serial_ms = [a.elapsed_time(b) for a, b in e2e_ev]
     # per step: the extend kernels of all the step's extend calls
     ext_kernel_ms = [sum(a.elapsed_time(b) for (a, b), c in zip(kev[k], calls) if c.kind == "extend")
                      for k in range(K)] if any(c.kind == "extend" for c in calls) else None
@@ -364,9 +344,8 @@ def run_ours(args, rank, world):
             raise RuntimeError("device error word set during the timed steps")
 
     tokens_per_step = sum(c.num_queries for c in calls)
-    t_total, t_e2e = max_over_ranks([sum(step_ms) / 1e3, e2e_total_ms / 1e3], dev)
+    t_total = max_over_ranks([sum(step_ms) / 1e3], dev)[0]
     value = job_throughput(world, K, tokens_per_step, t_total)
-    e2e_value = job_throughput(world, K, tokens_per_step, t_e2e)
 
     # roofline of the dominant kernel
     pk = peaks()
@@ -385,7 +364,8 @@ def run_ours(args, rank, world):
         achieved = (fx["kv_bytes"] + fx["qo_bytes"]) / dur / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / pk["hbm_gbs"], 4), "kernel": "attn_decode (all its kernels)",
-                "algorithmic_per_launch": fx["kv_bytes"] + fx["qo_bytes"], "kernel_ms": round(dur * 1e3, 4)}
+                "algorithmic_per_launch": fx["kv_bytes"] + fx["qo_bytes"], "kernel_ms": round(dur * 1e3, 4),
+                "frac_of_8tbs_nominal": round(achieved / 8000.0, 4)}
     # the committed ncu captures are of the token pool
     traffic = profiled_traffic(dominant, w.name) if args.page_size == 1 else None
     roof["traffic"] = traffic
@@ -395,39 +375,146 @@ def run_ours(args, rank, world):
     # kv_store: bf16 K and V rows read, pool rows written (bf16 or e4m3), slot indices read
     elem = 1 if w.dtype == "fp8_e4m3" else 2
     store_bytes = sum((c.k_new.numel() + c.v_new.numel()) * (2 + elem) + c.out_cache_loc.numel() * 4 for c in calls)
+    out = {
+        "value": round(value, 1), "ms_per_step": round(t_total * 1e3 / K, 4), "steps": K,
+        "tokens_per_step": tokens_per_step, "roofline": roof, "gpu_launches": K * launches_per_step,
+        "kernel_ms": {"kv_store": round(float(np.mean(store_ms)), 4),
+                      **{f"attn_{k}": round(float(np.mean(v)), 4) for k, v in attn_ms.items()},
+                      **({"attn_decode_median": round(float(np.median(attn_ms["decode"])), 4)}
+                         if "decode" in attn_ms else {})},
+        "kv_store": {"bytes_per_step": int(store_bytes),
+                     "gbs": round(store_bytes / (float(np.mean(store_ms)) / 1e3) / 1e9, 1)},
+        "wall_s": round(wall, 4), "clocks": clocks.summary(),
+        "host_plan_ms_per_step": None if plan_ms is None else round(plan_ms, 3),
+    }
+    for kind, fx_ in facts.items():
+        out[f"{kind}_queries"] = fx_["queries"]
+    if not e2e:
+        return out, calls
+
+    # end-to-end: same calls, inputs from pinned host memory, output back to the host.
+    # Pipelined (step k+1's inputs copy in and step k-1's output copies out while step k
+    # computes; three device buffer sets, so the two copies never wait on each other), with a
+    # 256 MiB L2 flush before every step's kernels inside the timed span; and, for reference,
+    # fully serialised steps.
+    for c in calls:
+        c.pin_host()
+    sets = [c.e2e_sets(3) for c in calls]
+    e2e_flush = flush[:(256 << 20) // 4]
+    run_e2e_pipelined(sets, args.warmup, e2e_flush)
+    if world > 1:
+        torch.distributed.barrier()
+    e2e_total_ms = run_e2e_pipelined(sets, K, e2e_flush)
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for k in range(K):
+        flush.zero_()
+        e2e_ev[k][0].record(stream)
+        for c in calls:
+            c.run_e2e()
+        e2e_ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    # the same device-resident steps back to back without the L2 flush (shared spans and
+    # the previous step's tables may still be in L2): reported beside the flushed figure
+    uev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for k in range(K):
+        uev[k][0].record(stream)
+        for c in calls:
+            c.store()
+        for c in calls:
+            c.replay_attend() if c.graph is not None else c.attend()
+        uev[k][1].record(stream)
+    torch.cuda.synchronize()
+    unflushed_ms = [a.elapsed_time(b) for a, b in uev]
+    e2e_serial_ms = [a.elapsed_time(b) for a, b in e2e_ev]
+    t_e2e = max_over_ranks([e2e_total_ms / 1e3], dev)[0]
+    e2e_value = job_throughput(world, K, tokens_per_step, t_e2e)
     h2d = sum(c.h2d_bytes() for c in calls)
     d2h = sum(c.d2h_bytes() for c in calls)
+    e2e_ms = t_e2e * 1e3 / K
+    out["e2e"] = {
+        "value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+        "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 4),
+        "mode": "pipelined: step k+1's H2D and step k-1's D2H overlap step k's kernels (3 device "
+                "buffer sets); a 256 MiB L2 flush precedes each step's kernels inside the span",
+        "serial_ms_per_step": round(float(np.mean(e2e_serial_ms)), 4),
+        # a new batch every step also costs its host planning; if it does not overlap the
+        # previous step's device work, a step takes e2e + planning:
+        "host_plan_ms_per_step": out["host_plan_ms_per_step"],
+        "value_with_host_plan_serial": (None if plan_ms is None else
+                                        round(job_throughput(world, 1, tokens_per_step,
+                                                             (e2e_ms + plan_ms) / 1e3), 1)),
+    }
+    out["unflushed"] = {"ms_per_step": round(float(np.mean(unflushed_ms)), 4),
+                        "value": round(job_throughput(world, K, tokens_per_step, sum(unflushed_ms) / 1e3), 1),
+                        "note": "same steps without the L2 flush between them"}
+    return out, calls
+
+
+def run_ours(args, rank, world):
+    import torch
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = load_workload(args)
+    m, calls = measure(w, args, dev, args.steps, world, e2e=True)
     cfg = {"workload": w.name, "config_id": None if args.workload else args.config, "requests": len(w.requests),
            "heads_q_kv": f"{w.num_q_heads}/{w.num_kv_heads}", "head_dim": w.head_dim, "pool_dtype": w.dtype,
            "pool_slots": w.num_slots, "page_size": args.page_size, "cascade": not args.no_cascade,
            "decode_launch": "plain" if args.no_graph else "CUDA graph replay of the call's launches",
            "l2": "flushed between timed steps (512 MiB write outside the step events)",
-           "tokens_per_step": tokens_per_step}
-    for kind, fx_ in facts.items():
-        cfg[f"{kind}_queries"] = fx_["queries"]
+           "tokens_per_step": m["tokens_per_step"]}
+    for kind in ("extend", "decode"):
+        if f"{kind}_queries" in m:
+            cfg[f"{kind}_queries"] = m[f"{kind}_queries"]
     out = {
-        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": round(t_total * 1e3 / K, 4), "higher_is_better": True,
+        "metric": METRIC, "value": m["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": m["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "bf16 (fp8_e4m3 pool)",
-        "data": "synthetic", "config": cfg,
-        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(t_e2e * 1e3 / K, 4),
-                "mode": "pipelined: step k+1's H2D and step k-1's D2H overlap step k's kernels (3 device "
-                        "buffer sets); a 256 MiB L2 flush precedes each step's kernels inside the span",
-                "serial_ms_per_step": round(float(np.mean(e2e_serial_ms)), 4)},
-        "roofline": roof,
-        "gpu_launches": K * launches_per_step,
-        "kernel_ms": {"kv_store": round(float(np.mean(store_ms)), 4),
-                      **{f"attn_{k}": round(float(np.mean(v)), 4) for k, v in attn_ms.items()}},
-        "kv_store": {"bytes_per_step": int(store_bytes),
-                     "gbs": round(store_bytes / (float(np.mean(store_ms)) / 1e3) / 1e9, 1)},
-        "unflushed": {"ms_per_step": round(float(np.mean(unflushed_ms)), 4),
-                      "value": round(job_throughput(world, K, tokens_per_step, sum(unflushed_ms) / 1e3), 1),
-                      "note": "same steps without the L2 flush between them"},
-        "wall_s": round(wall, 4),
-        "clocks": clocks.summary(),
+        "data": "synthetic", "config": cfg, "e2e": m["e2e"], "roofline": m["roofline"],
+        "gpu_launches": m["gpu_launches"], "kernel_ms": m["kernel_ms"], "kv_store": m["kv_store"],
+        "unflushed": m["unflushed"], "wall_s": m["wall_s"], "clocks": m["clocks"],
     }
-    return out, w
+    return out, w, calls
+
+
+def run_more_configs(args, world, ids=(3, 4, 5), steps=200):
+    """The decode workloads (and the mixed fp8 step) measured in the same run as the headline,
+    each in its own pool (freed before the next): per call the device time, tokens/s and the
+    roofline -- unique K/V + q/o bytes over the decode call against the measured copy peak
+    and against 8 TB/s -- with its clocks and, on rank 0, every output checked against the
+    oracle.  ``steps`` timed steps each (a longer region than the headline's, so the clock
+    sampler sees it)."""
+    import torch
+    import workloads as W
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    res = {}
+    sub = argparse.Namespace(**vars(args))
+    sub.workload, sub.pool_slots = "", 0
+    for k in ids:
+        sub.config = k
+        w = W.config(k)
+        m, calls = measure(w, sub, dev, steps, world, e2e=False)
+        entry = {"workload": w.name, "steps": steps, "ms_per_step": m["ms_per_step"],
+                 "tokens_per_step": m["tokens_per_step"], "value": m["value"], "unit": "tokens/s",
+                 "kernel_ms": m["kernel_ms"], "roofline": m["roofline"], "clocks": m["clocks"],
+                 "host_plan_ms_per_step": m["host_plan_ms_per_step"]}
+        if "decode" in workload_facts(w):
+            fx = workload_facts(w)["decode"]
+            t = m["kernel_ms"]["attn_decode"] / 1e3
+            byts = fx["kv_bytes"] + fx["qo_bytes"]
+            entry["decode"] = {"ms_per_call": m["kernel_ms"]["attn_decode"],
+                               "ms_per_call_median": m["kernel_ms"].get("attn_decode_median"),
+                               "tokens_per_s": round(fx["queries"] / t, 1),
+                               "unique_bytes": byts, "achieved_gbs": round(byts / t / 1e9, 1),
+                               "frac_of_measured_peak": round(byts / t / 1e9 / peaks()["hbm_gbs"], 4),
+                               "frac_of_8tbs_nominal": round(byts / t / 1e9 / 8000.0, 4),
+                               "traffic": profiled_traffic("decode", w.name)}
+        if int(os.environ.get("RANK", 0)) == 0:
+            entry["parity"] = oracle_parity(w, calls, budget_s=60.0)["parity"]
+        res[f"config_{k}"] = entry
+        del calls, m
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return res
 
 
 # ----------------------------------------------------------------------------------------
@@ -461,11 +548,62 @@ def oracle_sample(w, budget_s, start=0):
     return toks, time.perf_counter() - t0, used
 
 
-def cpu_baseline(w, budget_s=12.0):
-    toks, secs, used = oracle_sample(w, budget_s)
-    return {"value": round(toks / secs, 2), "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
-            "sample": f"{used} of {len(w.requests)} requests ({toks} query tokens) of {w.name}, float64 numpy, "
-                      f"{secs:.1f} s"}
+PARITY_TOL = {"bf16": 1e-2, "fp8_e4m3": 5e-2}
+
+
+def oracle_parity(w, calls, budget_s=60.0):
+    """The oracle over the workload's requests in order, until `budget_s` of CPU work, each
+    request's outputs compared element by element with the GPU's (the calls' last outputs).
+    Returns {"parity": {...}, "cpu": (query tokens, seconds, requests)}: the max-abs error
+    against the tolerance over every compared output, and the oracle's own timing."""
+    from oracle import step as ostep
+    rows = {}   # request id -> (call, first output row)
+    for c in calls:
+        got = c.o.float().cpu().numpy()
+        r0 = 0
+        for r in c.requests:
+            n = r.n_new if c.kind == "extend" else 1
+            rows[r.rid] = (got, r0, n)
+            r0 += n
+    t0 = time.perf_counter()
+    err, compared, toks, used = 0.0, 0, 0, 0
+    total = sum(n for _, _, n in rows.values())
+    finite = True
+    for r in w.requests:
+        if r.rid not in rows:
+            continue
+        want, _ = ostep.request_output(w, r)
+        got, r0, n = rows[r.rid]
+        g = got[r0:r0 + n]
+        finite &= bool(np.all(np.isfinite(g)))
+        err = max(err, float(np.max(np.abs(g - want))))
+        compared += n
+        toks += n
+        used += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    secs = time.perf_counter() - t0
+    tol = PARITY_TOL[w.dtype]
+    return {"parity": {"max_abs_err": round(err, 6), "tol": tol, "outputs_compared": compared,
+                       "outputs_total": total, "elements_compared": compared * w.num_q_heads * w.head_dim,
+                       "pass": bool(finite and err <= tol and compared == total)},
+            "cpu": (toks, secs, used)}
+
+
+def cpu_baseline(w, calls=None, budget_s=12.0):
+    """The oracle timed on the host cores over a bounded sample of the workload; with the
+    GPU calls, the same oracle run is also the parity check of every output it covers."""
+    if calls is not None:
+        res = oracle_parity(w, calls, budget_s=max(budget_s, 60.0))
+        toks, secs, used = res["cpu"]
+        parity = res["parity"]
+    else:
+        toks, secs, used = oracle_sample(w, budget_s)
+        parity = None
+    cb = {"value": round(toks / secs, 2), "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+          "sample": f"{used} of {len(w.requests)} requests ({toks} query tokens) of {w.name}, float64 numpy, "
+                    f"{secs:.1f} s"}
+    return cb, parity
 
 
 def run_reference(args, rank, world):
@@ -504,6 +642,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cascade", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-more-configs", action="store_true",
+                    help="skip the decode and mixed workloads (configurations 3-5) measured after the headline")
     ap.add_argument("--pool-slots", type=int, default=0)
     ap.add_argument("--no-graph", action="store_true", help="launch decode calls directly instead of from a CUDA graph")
     ap.add_argument("--page-size", type=int, default=1,
@@ -533,10 +673,13 @@ def main():
         import torch
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         torch.distributed.init_process_group("nccl")
-    out, w = run_ours(args, rank, world)
+    out, w, calls = run_ours(args, rank, world)
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"], out["parity"] = cpu_baseline(w, calls)
+    del calls
+    if not args.no_more_configs and not args.workload and args.config == DEFAULT_CONFIG and args.page_size == 1:
+        out["more_configs"] = run_more_configs(args, world)
     if rank == 0:
-        if not args.no_cpu_baseline:
-            out["cpu_baseline"] = cpu_baseline(w)
         print(json.dumps(out))
     if world > 1:
         import torch

@@ -22,7 +22,8 @@
  *   - Returns PKV_OK (0) or a negative PKV_E_* code; pkv_strerror() names it.
  *   - "device" pointers are CUDA device memory owned by the caller; "host" pointers are
  *     ordinary host memory owned by the caller.  The library allocates no device memory and
- *     never synchronises a stream, except pkv_get_device_error(), which synchronises.
+ *     never synchronises a stream, except pkv_get_device_error() and
+ *     pkv_get_noalloc_device_error(), which synchronise.
  *   - Device calls are asynchronous on the given stream (a cudaStream_t passed as void*;
  *     NULL is the legacy default stream).  Argument errors are reported before anything is
  *     enqueued; launch errors come back as PKV_E_CUDA.
@@ -84,13 +85,24 @@ typedef struct pkv_pool {
 /* missing KV tensors -> insert node").                                                  */
 /*   k_new, v_new   device, bf16 [n][num_kv_heads][head_dim], row-major                   */
 /*   out_cache_loc  device, int32 [n]; slot of token i; entries must be distinct and in   */
-/*                  [0, num_slots) (a duplicate makes the result of that slot undefined)  */
+/*                  [0, num_slots) (a duplicate makes the result of that slot undefined;  */
+/*                  pkv_check_out_cache_loc below detects it on the host)                 */
 /*   workspace      device error word (4 bytes, 4-aligned) or NULL; a slot outside         */
 /*                  [0, num_slots) is never written and sets PKV_DERR_SLOT_RANGE there     */
 /* bf16 pool: bit-exact copy.  fp8 pool: e4m3_rn_satfinite(float(x) / scale) per element  */
 /* (IEEE fp32 division).  n == 0 is a no-op.                                              */
 int pkv_kv_store(const pkv_pool *pool, const void *k_new, const void *v_new,
                  const int32_t *out_cache_loc, int64_t n, void *workspace, void *stream);
+
+/* Host check of kv_store's precondition (opt-in: the allocator hands out distinct slots, so a
+ * caller runs this only on its checked path).  New tokens get slots from the allocator's free
+ * list ([RC] "Eviction 전략": evicted slots go back through token_to_kv_pool_allocator.free),
+ * so within one call no two tokens may name the same slot.
+ *   out_cache_loc  host int32 [n]
+ *   bad            host, may be NULL: index of the first entry that is out of [0, num_slots)
+ *                  or repeats an earlier entry's slot; -1 when there is none
+ * PKV_OK when every entry is in range and distinct, else PKV_E_INVALID.  Nothing is enqueued. */
+int pkv_check_out_cache_loc(const int32_t *out_cache_loc, int64_t n, int64_t num_slots, int64_t *bad);
 
 /* ------------------------------------------------------------------------------------ */
 /* batch tables consumed by the attention calls (all device memory)                     */
@@ -211,6 +223,19 @@ int pkv_get_device_error(void *workspace, void *stream, int32_t *raw);
  * handles owned by the caller; NULL, NULL clears it.  Process-wide, not thread-safe. */
 int pkv_set_kernel_events(void *start, void *stop);
 
+/* Failure-detection hook (no counterpart in the pages).  Every wait inside the attention
+ * kernels (one role waiting for another's copy, MMA or release) is bounded; when one gives up,
+ * the kernel records PKV_DERR_TIMEOUT | which-wait in the error word, every role of that CTA
+ * stops, copies and MMAs already in flight are allowed to land, tensor memory is freed and
+ * the kernel returns: the context stays usable and the host sees the flag through
+ * pkv_get_device_error.  This sets the limit used by attention calls launched (or captured)
+ * after it, in nanoseconds; 0 restores the default of 2 s, orders of magnitude above any
+ * legitimate wait.  A limit of a few nanoseconds makes the first wait that does not succeed
+ * at once give up -- the way to exercise the timeout path.  Process-wide, not thread-safe
+ * against concurrent launches.  pkv_get_wait_limit_ns returns the current limit. */
+int pkv_set_wait_limit_ns(uint64_t ns);
+uint64_t pkv_get_wait_limit_ns(void);
+
 /* pkv_attn_decode for callers that cannot allocate device memory (no counterpart in the
  * pages: it exists for embedding).  Some callers have no workspace to pass at call time --
  * a serving loop that froze its device-memory budget after start-up, or a host program
@@ -229,6 +254,15 @@ int pkv_set_kernel_events(void *start, void *stop);
 int pkv_attn_decode_noalloc(const pkv_pool *pool, const pkv_batch *batch, const void *q, void *o,
                             float sm_scale, const pkv_plan_info *info, const void *plan_dev,
                             void *stream);
+
+/* The error word of pkv_attn_decode_noalloc's fixed array on the current device (the array's
+ * address is private to the library, so pkv_get_device_error cannot reach it).  Synchronises
+ * `stream`; PKV_OK when the word is zero, else PKV_E_DEVICE with the raw word in *raw (may be
+ * NULL).  Each pkv_attn_decode_noalloc call clears the word before it launches, so after a
+ * call on `stream` this reports that call's slot-range, position and timeout flags.  Like the
+ * call itself it allocates nothing; on a device with no earlier call it looks up the array's
+ * address first. */
+int pkv_get_noalloc_device_error(void *stream, int32_t *raw);
 
 /* ------------------------------------------------------------------------------------ */
 /* host radix tree ([RC]): token ids -> pool slots, with LRU eviction and lock_ref       */

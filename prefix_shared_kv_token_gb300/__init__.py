@@ -6,6 +6,7 @@ memory -- and forwards to the library.  Names follow the C entry points without 
 ``pkv_`` prefix:
 
     kv_store      scatter new K/V rows into pool slots (bf16 copy or fp8 quantisation)
+    check_out_cache_loc  host check that a store's slots are in range and distinct
     plan_decode   host work decomposition of a decode call (split-KV, shared-prefix cascade)
     plan_extend   host work decomposition of an extend call
     attn_decode   one query token per request over its whole context (widely shared spans on
@@ -28,8 +29,10 @@ import numpy as np
 from ._lib import (PKV_BF16, PKV_FP8_E4M3, PkvBatch, PkvCascade, PkvError, PkvPlanInfo, PkvPlanOpts, PkvPool,
                    check, lib)
 
-__all__ = ["Pool", "Batch", "Plan", "Cascade", "kv_store", "plan_decode", "plan_extend", "attn_decode",
-           "attn_extend", "get_device_error", "set_kernel_events", "RadixTree", "Allocator", "PkvError", "version"]
+__all__ = ["Pool", "Batch", "Plan", "Cascade", "kv_store", "check_out_cache_loc", "plan_decode", "plan_extend",
+           "attn_decode", "attn_extend", "get_device_error", "get_noalloc_device_error", "set_kernel_events",
+           "set_wait_limit_ns", "get_wait_limit_ns",
+           "RadixTree", "Allocator", "PkvError", "version"]
 
 
 def version() -> int:
@@ -178,6 +181,17 @@ def kv_store(pool: Pool, k_new, v_new, out_cache_loc, workspace=None, stream=Non
                                            int(out_cache_loc.shape[0]), _ptr(workspace), _stream(stream)))
 
 
+def check_out_cache_loc(out_cache_loc, num_slots) -> int:
+    """Host check of kv_store's slot list (numpy int32 [n]): -1 when every slot is in range
+    and distinct, else the index of the first entry that is out of range or repeats a slot."""
+    loc = _i32(out_cache_loc)
+    bad = C.c_int64(-1)
+    rc = lib.pkv_check_out_cache_loc(_ptr(loc), len(loc), int(num_slots), C.byref(bad))
+    if rc not in (0, -1) or (rc == -1 and bad.value < 0):
+        check("pkv_check_out_cache_loc", rc)
+    return bad.value
+
+
 def attn_decode(pool: Pool, batch: Batch, q, o, sm_scale, plan: Plan, plan_dev, workspace, stream=None) -> None:
     p, b = pool.c(), batch.c()
     check("pkv_attn_decode", lib.pkv_attn_decode(C.byref(p), C.byref(b), _ptr(q), _ptr(o), float(sm_scale),
@@ -199,6 +213,26 @@ def get_device_error(workspace, stream=None) -> int:
     if rc not in (0, -7):
         check("pkv_get_device_error", rc)
     return raw.value
+
+
+def get_noalloc_device_error(stream=None) -> int:
+    """Synchronises the stream and returns the raw error word of attn_decode_noalloc's fixed
+    array on the current device (0 = no error)."""
+    raw = C.c_int32(0)
+    rc = lib.pkv_get_noalloc_device_error(_stream(stream), C.byref(raw))
+    if rc not in (0, -7):
+        check("pkv_get_noalloc_device_error", rc)
+    return raw.value
+
+
+def set_wait_limit_ns(ns: int = 0) -> None:
+    """Limit of every wait inside the attention kernels launched after this call (0 = the
+    default, 2 s).  A tiny limit makes the kernels give up and report PKV_DERR_TIMEOUT."""
+    check("pkv_set_wait_limit_ns", lib.pkv_set_wait_limit_ns(int(ns)))
+
+
+def get_wait_limit_ns() -> int:
+    return int(lib.pkv_get_wait_limit_ns())
 
 
 def set_kernel_events(start=None, stop=None) -> None:

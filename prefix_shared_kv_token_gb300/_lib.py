@@ -63,6 +63,7 @@ SIGNATURES = {
     "pkv_strerror": (C.c_char_p, [C.c_int]),
     "pkv_version": (C.c_int, []),
     "pkv_kv_store": (C.c_int, [C.POINTER(PkvPool), _P, _P, _P, _I64, _P, _P]),
+    "pkv_check_out_cache_loc": (C.c_int, [_P, _I64, _I64, _PI64]),
     "pkv_plan_decode": (C.c_int, [_I32, _P, _I32, _I32, _I32, C.POINTER(PkvCascade), C.POINTER(PkvPlanOpts), _P, _SZ,
                                   C.POINTER(PkvPlanInfo)]),
     "pkv_plan_extend": (C.c_int, [_I32, _P, _P, _P, _I32, _I32, _I32, C.POINTER(PkvCascade),
@@ -73,8 +74,11 @@ SIGNATURES = {
                                   _P, _SZ, _P]),
     "pkv_get_device_error": (C.c_int, [_P, _P, _PI32]),
     "pkv_set_kernel_events": (C.c_int, [_P, _P]),
+    "pkv_set_wait_limit_ns": (C.c_int, [C.c_uint64]),
+    "pkv_get_wait_limit_ns": (C.c_uint64, []),
     "pkv_attn_decode_noalloc": (C.c_int, [C.POINTER(PkvPool), C.POINTER(PkvBatch), _P, _P, _F,
                                           C.POINTER(PkvPlanInfo), _P, _P]),
+    "pkv_get_noalloc_device_error": (C.c_int, [_P, _PI32]),
     "pkv_tree_new": (_P, []),
     "pkv_tree_free": (None, [_P]),
     "pkv_tree_match_prefix": (C.c_int, [_P, _P, _I64, _P, _I64, _PI64, _PI64]),

@@ -3,12 +3,18 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <atomic>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "../../include/pkv.h"
 #include "launch.h"
 
 namespace pkv {
+
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 
 int num_sms() {
     static int cached[64] = {0};
@@ -53,6 +59,9 @@ CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType dtype, cuuint32_t ra
 
 void *g_kernel_events[2] = {nullptr, nullptr};
 
+static std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
 }  // namespace pkv
 
 extern "C" {
@@ -79,6 +88,40 @@ int pkv_set_kernel_events(void *start, void *stop) {
     pkv::g_kernel_events[0] = start;
     pkv::g_kernel_events[1] = stop;
     return PKV_OK;
+}
+
+int pkv_set_wait_limit_ns(uint64_t ns) {
+    pkv::g_wait_limit_ns.store(ns == 0 ? pkv::kDefaultWaitLimitNs : ns, std::memory_order_relaxed);
+    return PKV_OK;
+}
+
+uint64_t pkv_get_wait_limit_ns(void) { return pkv::wait_limit_ns(); }
+
+int pkv_check_out_cache_loc(const int32_t *out_cache_loc, int64_t n, int64_t num_slots, int64_t *bad) {
+    if (bad) *bad = -1;
+    if (n < 0 || num_slots <= 0 || (n > 0 && !out_cache_loc)) return PKV_E_INVALID;
+    // (slot, index) pairs sorted by slot: a repeated slot sits next to its twin; the later
+    // of the two occurrences (in call order) is the one reported
+    std::vector<std::pair<int32_t, int64_t>> v;
+    v.reserve((size_t)n);
+    int64_t first_bad = -1;
+    for (int64_t i = 0; i < n; ++i) {
+        const int32_t s = out_cache_loc[i];
+        if (s < 0 || (int64_t)s >= num_slots) {
+            if (first_bad < 0 || i < first_bad) first_bad = i;
+            continue;
+        }
+        v.push_back({s, i});
+    }
+    std::sort(v.begin(), v.end());
+    for (size_t j = 1; j < v.size(); ++j)
+        if (v[j].first == v[j - 1].first) {
+            const int64_t i = std::max(v[j].second, v[j - 1].second);
+            if (first_bad < 0 || i < first_bad) first_bad = i;
+        }
+    if (first_bad < 0) return PKV_OK;
+    if (bad) *bad = first_bad;
+    return PKV_E_INVALID;
 }
 
 int pkv_get_device_error(void *workspace, void *stream, int32_t *raw) {

@@ -30,8 +30,9 @@
 //   * fp8 pools: raw e4m3 rows land in the ring and each warp converts its own head's rows
 //     exactly to bf16 in a private tile (releasing the stage at once); k_scale folds into
 //     the logit scale, v_scale into the output.
-//   * Every wait is bounded (2 s); on expiry the CTA records PKV_DERR_TIMEOUT, its warps
-//     stop, and the producer lets its copies in flight land before it exits.
+//   * Every wait is bounded (the launch's wait limit, 2 s by default); on expiry the CTA
+//     records PKV_DERR_TIMEOUT, its warps stop, and the producer lets every copy it issued
+//     land before it exits.
 
 #include "../../include/pkv.h"
 #include "common.cuh"
@@ -63,6 +64,7 @@ struct DecodeParams {
     float *rec_acc;     // [rec][hq][D]
     float *rec_ml;      // [rec][hq][2]
     int32_t *err;
+    uint64_t wait_ns;   // limit of a pipeline wait (pkv_set_wait_limit_ns)
 };
 
 constexpr int kBK = 16;       // keys per tile
@@ -102,14 +104,16 @@ struct DGeo {
     }
 };
 
-PKV_DEV bool dwait(uint64_t *bar, uint32_t parity, int32_t *abort_flag, int32_t *err, int where) {
-    if (mbar_try_wait(bar, parity)) return true;
+PKV_DEV bool dwait(uint64_t *bar, uint32_t parity, int32_t *abort_flag, int32_t *err, int where, uint64_t limit_ns) {
+    const bool quick = short_wait_limit(limit_ns);
+    if (mbar_poll(bar, parity, quick)) return true;
     const uint64_t t0 = global_timer_ns();
+    const uint32_t mask = quick ? 0u : 255u;
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0) {
+        if (mbar_poll(bar, parity, quick)) return true;
+        if ((it & mask) == 0) {
             if (*reinterpret_cast<volatile int32_t *>(abort_flag)) return false;
-            if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+            if (global_timer_ns() - t0 > limit_ns) {
                 set_error(err, DERR_TIMEOUT | where);
                 *reinterpret_cast<volatile int32_t *>(abort_flag) = 1;
                 return false;
@@ -350,18 +354,17 @@ __global__ void __launch_bounds__(288, (D == 64 ? 2 : 1)) decode_kernel(const De
         TileSlot e0 = next_tile(p, cur, c1, key), e1 = next_tile(p, cur, c1, key);
         TileSlot e2 = next_tile(p, cur, c1, key), e3 = next_tile(p, cur, c1, key);
         int t = 0;
-        bool aborted = false;
+        bool ended = false;  // the list ran out (tile t carries kEnd) rather than a wait giving up
         for (;; ++t) {
             const int s = t % S;
-            if (t >= S && !__all_sync(0xffffffffu, dwait(&empty[s], ((t / S) - 1) & 1, abort_flag, p.err, 0x31))) {
-                aborted = true;  // warp-uniform: every lane leaves together
-                break;
-            }
+            if (t >= S && !__all_sync(0xffffffffu, dwait(&empty[s], ((t / S) - 1) & 1, abort_flag, p.err, 0x31, p.wait_ns)))
+                break;  // warp-uniform: every lane leaves together
             if (e0.info.flags & kEnd) {
                 if (lane == 0) {
                     tinfo[s].flags = kEnd;
                     mbar_arrive(&full[s]);
                 }
+                ended = true;
                 break;
             }
             const int kp = e0.info.kpos + key;
@@ -390,10 +393,13 @@ __global__ void __launch_bounds__(288, (D == 64 ? 2 : 1)) decode_kernel(const De
             e2 = e3;
             e3 = next_tile(p, cur, c1, key);
         }
-        if (aborted) {
-            // let the copies still in flight land (bounded) before the CTA exits
-            for (int u = t - S < 0 ? 0 : t - S; u < t; ++u) mbar_wait(&full[u % S], (u / S) & 1);
-        }
+        // Let every copy this warp issued land before it leaves: the consumers may have given
+        // up on a wait (and returned) while the last tiles were still in flight.  Tile t was
+        // not issued; tiles before t - S were released by the consumers, so they have landed,
+        // and so has tile t - S when the list ran out (its stage was released for the kEnd
+        // tile, which re-armed that stage: its barrier must not be waited on again).  In a
+        // normal run the remaining phases completed long ago and each wait returns at once.
+        for (int u = max(0, t - S + (ended ? 1 : 0)); u < t; ++u) mbar_wait(&full[u % S], (u / S) & 1);
         return;
     }
 
@@ -411,7 +417,7 @@ __global__ void __launch_bounds__(288, (D == 64 ? 2 : 1)) decode_kernel(const De
     uint8_t *conv = smem + geo.conv + w * Gm::kConvBytes;
     for (int t = 0;; ++t) {
         const int s = t % S;
-        if (!__all_sync(0xffffffffu, dwait(&full[s], (t / S) & 1, abort_flag, p.err, 0x33))) return;
+        if (!__all_sync(0xffffffffu, dwait(&full[s], (t / S) & 1, abort_flag, p.err, 0x33, p.wait_ns))) return;
         const TileInfo ti = tinfo[s];
         if (ti.flags & kEnd) return;
         if (ti.flags & kFirst) {
@@ -629,6 +635,7 @@ extern "C" int pkv_attn_decode(const pkv_pool *pool, const pkv_batch *batch, con
     p.row_rec = reinterpret_cast<const int32_t *>(plan + info->offsets[SEC_ROW_REC]);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     p.err = reinterpret_cast<int32_t *>(ws);
+    p.wait_ns = wait_limit_ns();
     p.rec_acc = reinterpret_cast<float *>(ws + kWorkspaceHeader);
     p.rec_ml = p.rec_acc + (size_t)info->num_records * info->num_q_heads * info->head_dim;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -35,8 +35,9 @@
 //      The softmax holds a row's 128 scores in registers (one tcgen05.ld pass), takes the
 //      row max as a tree, folds scale and max into one FFMA per score and skips the mask on
 //      full tiles; the kernel fits the 168-register budget of 384 threads without spilling.
-//      Every wait is bounded (2 s); on expiry the CTA records
-//      PKV_DERR_TIMEOUT, its roles stop, in-flight work drains and tensor memory is freed.
+//      Every wait is bounded (the launch's wait limit, 2 s by default); on expiry the CTA
+//      records PKV_DERR_TIMEOUT, its roles stop, in-flight work drains and tensor memory is
+//      freed.
 
 #include <algorithm>
 
@@ -66,6 +67,7 @@ struct ExtendParams {
     const int32_t *rec_list;  // NULL: token t of an item writes record rec + t; else rec_list[rec + t]
     const PackInfo *packs;    // packed items' segments and row groups (NULL: none)
     int32_t *err;
+    uint64_t wait_ns;         // limit of a pipeline wait (pkv_set_wait_limit_ns)
 };
 
 template <int D>
@@ -88,18 +90,22 @@ struct XBars {
     uint64_t kfull[kXStages], vfull[kXStages], kvempty[kXStages], kempty[kXStages];
     uint64_t sfull[2], pfull[2], ofinal[2];
     uint64_t drain;
+    uint64_t wait_ns;   // limit of a pipeline wait (the launch's, copied here once)
     uint32_t tmem_base;
     int32_t abort_flag;
 };
 
 PKV_DEV bool xwait(uint64_t *bar, uint32_t parity, XBars *b, int32_t *err, int where) {
-    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t limit_ns = b->wait_ns;
+    const bool quick = short_wait_limit(limit_ns);
+    if (mbar_poll(bar, parity, quick)) return true;
     const uint64_t t0 = global_timer_ns();
+    const uint32_t mask = quick ? 0u : 255u;
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0) {
+        if (mbar_poll(bar, parity, quick)) return true;
+        if ((it & mask) == 0) {
             if (*reinterpret_cast<volatile int32_t *>(&b->abort_flag)) return false;
-            if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+            if (global_timer_ns() - t0 > limit_ns) {
                 set_error(err, DERR_TIMEOUT | where);
                 *reinterpret_cast<volatile int32_t *>(&b->abort_flag) = 1;
                 return false;
@@ -373,6 +379,7 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(&bars->ofinal[q], 1);
         }
         mbar_init(&bars->drain, 1);
+        bars->wait_ns = p.wait_ns;
         bars->abort_flag = 0;
         fence_mbar_init();
     }
@@ -454,11 +461,14 @@ __global__ void __launch_bounds__(384, 1)
                     for (int b = 0; b < NBLK; ++b) tma_load_3d(dst + b * C::kBlkK, map, b * 64, it.g, key, &full[s]);
                 }
             }
-            if (*reinterpret_cast<volatile int32_t *>(&bars->abort_flag)) {
-                // aborted: let this thread's copies still in flight land (bounded) before exit
-                if (kside && nql > 0) mbar_wait(&bars->q, (nql - 1) & 1);
-                for (int t = tp > ST ? tp - ST : 0; t < tp; ++t) mbar_wait(&full[t % ST], (t / ST) & 1);
-            }
+            // Let every copy this thread issued land before it leaves, whether or not a wait
+            // gave up: another role may have stopped waiting (and the CTA may be unwinding)
+            // while the last tiles were still in flight.  Each stage's last tile is one of the
+            // last ST; earlier tiles were released by the MMAs, so they have landed; no stage
+            // is re-armed after its last tile.  In a normal run these phases completed long
+            // ago and each wait returns at once.
+            if (kside && nql > 0) mbar_wait(&bars->q, (nql - 1) & 1);
+            for (int t = tp > ST ? tp - ST : 0; t < tp; ++t) mbar_wait(&full[t % ST], (t / ST) & 1);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -893,6 +903,7 @@ int decode_span_tensor(const pkv_pool *pool, const pkv_batch *batch, const void 
     p.rec_ml = rec_ml;
     p.rec_list = reinterpret_cast<const int32_t *>(plan + info->offsets[14]);
     p.packs = nullptr;
+    p.wait_ns = wait_limit_ns();
     // the spans' items, then the short requests' items (precise weights)
     const ExtendItem *items = reinterpret_cast<const ExtendItem *>(plan + info->offsets[7]);
     const int64_t nprec = info->offsets[18];
@@ -975,6 +986,7 @@ extern "C" int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, con
     p.rec_acc = rec_acc;
     p.rec_ml = rec_ml;
     p.rec_list = nullptr;
+    p.wait_ns = wait_limit_ns();
     p.packs = info->offsets[14] > 0 ? reinterpret_cast<const PackInfo *>(plan + info->offsets[13]) : nullptr;
     void *ev0 = g_kernel_events[0], *ev1 = g_kernel_events[1];
     g_kernel_events[0] = g_kernel_events[1] = nullptr;

@@ -88,15 +88,43 @@ PKV_DEV bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete, for at most ~timeout_ns.
-// Returns false on timeout (the caller records the error and unwinds).
-constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s: orders of magnitude above any legit wait
+// Non-blocking probe of the same phase (mbarrier.try_wait may suspend the thread for a
+// system-dependent time before it returns false; test_wait never does).
+PKV_DEV bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded waits.  A pipeline wait (a role waiting for another role's data or release) gives
+// up after the launch's wait limit, a kernel argument set by pkv_set_wait_limit_ns (2 s by
+// default: orders of magnitude above any legitimate wait); the caller then records the
+// error and unwinds.  A drain wait -- letting copies or MMAs that are already in flight land
+// before the CTA frees or abandons what they write to -- always allows kDrainTimeoutNs, so a
+// short pipeline limit never cuts a drain short.
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+constexpr uint64_t kDrainTimeoutNs = 2000000000ull;
+// A limit under ~1 ms is a short limit: its waits poll with the non-blocking test_wait and
+// read the timer on every try, so the limit is noticed as soon as the timer passes it (a
+// blocking try_wait could sit out a whole short wait inside one call).  The long default
+// limit keeps try_wait and reads the timer every 256 tries.
+PKV_DEV bool short_wait_limit(uint64_t limit_ns) { return limit_ns < (1ull << 20); }
+PKV_DEV bool mbar_poll(uint64_t *bar, uint32_t parity, bool quick) {
+    return quick ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity);
+}
+
+// Wait for the phase with the given parity to complete, for at most ~kDrainTimeoutNs.
+// Returns false on timeout.
 PKV_DEV bool mbar_wait(uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0 && global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+        if ((it & 255u) == 0 && global_timer_ns() - t0 > kDrainTimeoutNs) return false;
     }
 }
 

@@ -16,6 +16,8 @@
 //     the device current) and caches it; make that first call before any stream capture.
 //   * Each call clears the error word on its stream before launching; the records need no
 //     clearing because every record the merge reads is written by the same call.
+//   * pkv_get_noalloc_device_error reads that error word (the array's address is private to
+//     this file, so pkv_get_device_error cannot be pointed at it).
 // No cudaMalloc, cudaFree or allocating library routine is called here.
 
 #include <cuda_runtime.h>
@@ -59,4 +61,11 @@ extern "C" int pkv_attn_decode_noalloc(const pkv_pool *pool, const pkv_batch *ba
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(ws, 0, sizeof(int32_t), s) != cudaSuccess) return PKV_E_CUDA;  // error word
     return pkv_attn_decode(pool, batch, q, o, sm_scale, info, plan_dev, ws, PKV_NOALLOC_WORKSPACE_BYTES, stream);
+}
+
+extern "C" int pkv_get_noalloc_device_error(void *stream, int32_t *raw) {
+    void *ws = nullptr;
+    int rc = scratch_for_current_device(&ws);
+    if (rc) return rc;
+    return pkv_get_device_error(ws, stream, raw);
 }

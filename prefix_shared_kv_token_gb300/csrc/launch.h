@@ -15,6 +15,10 @@ int num_sms();  // SMs of the current device (cached per device)
 // cudaEvent_t pair set by pkv_set_kernel_events (consumed by the next pkv_attn_extend)
 extern void *g_kernel_events[2];
 
+// Limit of a pipeline wait inside the attention kernels for the next launches, in ns
+// (pkv_set_wait_limit_ns; 2 s by default).
+uint64_t wait_limit_ns();
+
 inline int validate_pool(const pkv_pool *p) {
     if (!p || !p->k || !p->v) return PKV_E_INVALID;
     if (p->num_slots <= 0 || p->num_kv_heads <= 0) return PKV_E_INVALID;

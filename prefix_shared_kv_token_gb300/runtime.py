@@ -20,7 +20,8 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-from . import Allocator, Batch, Pool, RadixTree, attn_decode, attn_extend, kv_store, plan_decode, plan_extend
+from . import (Allocator, Batch, Pool, RadixTree, attn_decode, attn_extend, check_out_cache_loc, kv_store, plan_decode,
+               plan_extend)
 
 
 def _ctx_tokens(w, req):
@@ -237,10 +238,14 @@ class PrefixCache:
     tree caches whole P-token blocks only, every block of a request's context lives in one
     page (slot = page * P + position % P), and the batch tables are page tables.  A
     request's trailing partial block is its own (``private``): it is not in the tree, and
-    the request's next tokens fill the rest of that page before new pages are taken."""
+    the request's next tokens fill the rest of that page before new pages are taken.
 
-    def __init__(self, w, device="cuda", page_size=1):
+    ``check_slots`` runs the host check of every call's ``out_cache_loc`` (slots in range and
+    distinct, kv_store's precondition) before anything is copied to the device."""
+
+    def __init__(self, w, device="cuda", page_size=1, check_slots=True):
         self.w = w
+        self.check_slots = bool(check_slots)
         self.device = device
         self.page = int(page_size)
         self.pool = Pool.allocate(w.num_slots, w.num_kv_heads, w.head_dim, w.dtype, w.k_scale, w.v_scale, device)
@@ -332,11 +337,13 @@ class PrefixCache:
         kv_store(self.pool, k, v, loc, self.err)
 
     # ---- one attention call of a step
-    def prepare(self, kind, cascade=True, opts=None, min_group=2, requests=None) -> Call:
-        """One attention call over the workload's requests of ``kind`` (or the given subset)."""
+    def _plan_host(self, kind, cascade, opts, min_group, requests):
+        """The host half of one call: match every request's cached part in the tree (it must hit
+        completely) and lock its path, allocate slots for the new tokens, build the batch table,
+        extract the cascade and plan the kernels.  Returns a dict of host arrays."""
         w = self.w
         reqs = [r for r in (w.requests if requests is None else requests) if r.kind == kind]
-        rows, last_nodes, seq, ext, new_all, kn, vn, qs = [], [], [], [], [], [], [], []
+        rows, last_nodes, seq, ext, new_all = [], [], [], [], []
         for r in reqs:
             toks = _ctx_tokens(w, r)
             L, c = len(toks), len(toks) - r.n_new
@@ -352,10 +359,6 @@ class PrefixCache:
             seq.append(L)
             ext.append(r.n_new)
             new_all.append(new)
-            kb, vb = _ctx_kv(w, r, c, L)
-            kn.append(kb)
-            vn.append(vb)
-            qs.append(r.q)
         B = len(reqs)
         rt = self._table(rows, seq)
         seq = np.asarray(seq, dtype=np.int32)
@@ -369,18 +372,59 @@ class PrefixCache:
             plan = plan_extend(seq, ext, qo, hq, hkv, d, casc, opts)
         else:
             plan = plan_decode(seq, hq, hkv, d, casc, opts)
+        loc_host = np.concatenate(new_all).astype(np.int32) if new_all else np.zeros(0, np.int32)
+        if self.check_slots:
+            bad = check_out_cache_loc(loc_host, self.pool.num_slots)
+            if bad >= 0:
+                raise RuntimeError(f"out_cache_loc[{bad}] = {loc_host[bad]} is out of range or repeats a slot")
+        return {"reqs": reqs, "rows": rows, "last_nodes": last_nodes, "seq": seq, "ext": ext, "new": new_all,
+                "rt": rt, "cascade": casc, "plan": plan, "loc": loc_host}
+
+    def host_step_ms(self, kind, reps=5, cascade=True, opts=None, min_group=2, requests=None) -> float:
+        """Host time of planning one call like :meth:`prepare` (tree match and lock, slot
+        allocation, batch table, cascade, plan, slot check), in ms, the mean of ``reps`` runs:
+        what a server pays on the host for every new batch before its kernels can start.  Each
+        run's slots and locks are given back, so the cache holds the same nodes, tokens and
+        free slots afterwards (access times and hit counts move, as any match moves them).
+        Token pools only (a paged pool's partial pages are not given back)."""
+        import time
+        if self.page != 1:
+            raise ValueError("host_step_ms: token pools only")
+        ts = []
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            h = self._plan_host(kind, cascade, opts, min_group, requests)
+            ts.append(time.perf_counter() - t0)
+            for new in h["new"]:
+                if len(new):
+                    self.alloc.release(new)
+            for n in h["last_nodes"]:
+                self.tree.dec_lock_ref(n)
+        return 1e3 * float(np.mean(ts))
+
+    def prepare(self, kind, cascade=True, opts=None, min_group=2, requests=None) -> Call:
+        """One attention call over the workload's requests of ``kind`` (or the given subset)."""
+        w = self.w
+        h = self._plan_host(kind, cascade, opts, min_group, requests)
+        reqs, rows, plan = h["reqs"], h["rows"], h["plan"]
+        kn, vn = [], []
+        for r, row in zip(reqs, rows):
+            kb, vb = _ctx_kv(w, r, len(row) - r.n_new, len(row))
+            kn.append(kb)
+            vn.append(vb)
+        B = len(reqs)
         dev = self.device
-        batch = Batch(torch.from_numpy(rt).to(dev), torch.arange(B, dtype=torch.int32, device=dev),
-                      torch.from_numpy(seq).to(dev), self.page)
+        batch = Batch(torch.from_numpy(h["rt"]).to(dev), torch.arange(B, dtype=torch.int32, device=dev),
+                      torch.from_numpy(h["seq"]).to(dev), self.page)
         plan_dev = torch.from_numpy(plan.blob).to(dev)
         ws = torch.zeros((plan.info.workspace_bytes + 3) // 4, dtype=torch.int32, device=dev)
-        q = _bf16_dev(np.concatenate(qs), dev)
+        q = _bf16_dev(np.concatenate([r.q for r in reqs]), dev)
         o = torch.empty_like(q)
-        loc = torch.from_numpy(np.concatenate(new_all).astype(np.int32)).to(dev)
+        loc = torch.from_numpy(h["loc"]).to(dev)
         k_new = _bf16_dev(np.concatenate(kn), dev)
         v_new = _bf16_dev(np.concatenate(vn), dev)
-        call = Call(kind, self.pool, batch, plan, plan_dev, ws, q, o, loc, k_new, v_new, w.sm_scale, last_nodes,
-                    cascade=casc)
+        call = Call(kind, self.pool, batch, plan, plan_dev, ws, q, o, loc, k_new, v_new, w.sm_scale,
+                    h["last_nodes"], cascade=h["cascade"])
         call.contexts = [(_ctx_tokens(w, r), row, len(row) - r.n_new) for r, row in zip(reqs, rows)]
         call.requests = reqs
         return call

@@ -64,7 +64,7 @@ struct DecodeParams {
     float *rec_acc;     // [rec][hq][D]
     float *rec_ml;      // [rec][hq][2]
     int32_t *err;
-    uint64_t wait_ns;   // limit of a pipeline wait (pkv_set_wait_limit_ns)
+    WaitPolicy wait;    // pipeline waits (pkv_set_wait_limit_ns)
 };
 
 constexpr int kBK = 16;       // keys per tile
@@ -104,16 +104,18 @@ struct DGeo {
     }
 };
 
-PKV_DEV bool dwait(uint64_t *bar, uint32_t parity, int32_t *abort_flag, int32_t *err, int where, uint64_t limit_ns) {
-    const bool quick = short_wait_limit(limit_ns);
-    if (mbar_poll(bar, parity, quick)) return true;
+// QUICK launches (a short wait limit) poll with test_wait and read the timer on every try;
+// the others try_wait and read it every 256 retries.
+template <bool QUICK>
+PKV_DEV bool dwait(uint64_t *bar, uint32_t parity, int32_t *abort_flag, int32_t *err, int where,
+                   const WaitPolicy &wp) {
+    if (QUICK ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    const uint32_t mask = quick ? 0u : 255u;
     for (uint32_t it = 1;; ++it) {
-        if (mbar_poll(bar, parity, quick)) return true;
-        if ((it & mask) == 0) {
+        if (QUICK ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+        if (QUICK || (it & 255u) == 0) {
             if (*reinterpret_cast<volatile int32_t *>(abort_flag)) return false;
-            if (global_timer_ns() - t0 > limit_ns) {
+            if (global_timer_ns() - t0 > wp.limit_ns) {
                 set_error(err, DERR_TIMEOUT | where);
                 *reinterpret_cast<volatile int32_t *>(abort_flag) = 1;
                 return false;
@@ -316,7 +318,7 @@ PKV_DEV TileSlot next_tile(const DecodeParams &p, TileCursor &cur, int c1, int k
     return e;
 }
 
-template <int D, int G, bool FP8>
+template <int D, int G, bool FP8, bool QUICK>
 __global__ void __launch_bounds__(288, (D == 64 ? 2 : 1)) decode_kernel(const DecodeParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     using Gm = DGeo<D, FP8>;
@@ -328,6 +330,8 @@ __global__ void __launch_bounds__(288, (D == 64 ? 2 : 1)) decode_kernel(const De
     uint8_t *ring = smem + kHdr;
     const Gm geo(p.hg);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();     // the query tokens' K/V were stored, and the span gather ran, just before
+    pdl_trigger();  // the span pass may take SMs as this kernel's CTAs finish
     const int c0 = __ldg(p.cta_off + blockIdx.x), c1 = __ldg(p.cta_off + blockIdx.x + 1);
 
     if (threadIdx.x == 0) {
@@ -357,7 +361,7 @@ __global__ void __launch_bounds__(288, (D == 64 ? 2 : 1)) decode_kernel(const De
         bool ended = false;  // the list ran out (tile t carries kEnd) rather than a wait giving up
         for (;; ++t) {
             const int s = t % S;
-            if (t >= S && !__all_sync(0xffffffffu, dwait(&empty[s], ((t / S) - 1) & 1, abort_flag, p.err, 0x31, p.wait_ns)))
+            if (t >= S && !__all_sync(0xffffffffu, dwait<QUICK>(&empty[s], ((t / S) - 1) & 1, abort_flag, p.err, 0x31, p.wait)))
                 break;  // warp-uniform: every lane leaves together
             if (e0.info.flags & kEnd) {
                 if (lane == 0) {
@@ -417,7 +421,7 @@ __global__ void __launch_bounds__(288, (D == 64 ? 2 : 1)) decode_kernel(const De
     uint8_t *conv = smem + geo.conv + w * Gm::kConvBytes;
     for (int t = 0;; ++t) {
         const int s = t % S;
-        if (!__all_sync(0xffffffffu, dwait(&full[s], (t / S) & 1, abort_flag, p.err, 0x33, p.wait_ns))) return;
+        if (!__all_sync(0xffffffffu, dwait<QUICK>(&full[s], (t / S) & 1, abort_flag, p.err, 0x33, p.wait))) return;
         const TileInfo ti = tinfo[s];
         if (ti.flags & kEnd) return;
         if (ti.flags & kFirst) {
@@ -488,6 +492,8 @@ __global__ void __launch_bounds__(288, (D == 64 ? 2 : 1)) decode_kernel(const De
 template <int D>
 __global__ void __launch_bounds__(256) merge_kernel(const MergeItem *__restrict__ merges, const float *__restrict__ rec_acc,
                                                     const float *__restrict__ rec_ml, uint16_t *__restrict__ o, int hq) {
+    pdl_wait();  // every record of the call has been written
+    pdl_trigger();
     const MergeItem mi = merges[blockIdx.x];
     const int h = blockIdx.y * 8 + (threadIdx.x >> 5);
     if (h >= hq) return;
@@ -546,11 +552,10 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeItem *__restrict_
 template <int D, int G, bool FP8>
 static int launch_decode(const DecodeParams &p, int nctas, cudaStream_t s) {
     const DGeo<D, FP8> geo(p.hg);
-    auto kern = decode_kernel<D, G, FP8>;
+    auto kern = p.wait.quick ? decode_kernel<D, G, FP8, true> : decode_kernel<D, G, FP8, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, geo.bytes) != cudaSuccess)
         return PKV_E_CUDA;
-    kern<<<nctas, 32 * (p.hg + 1), geo.bytes, s>>>(p);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_E_CUDA;
+    return launch_pdl(kern, dim3(nctas), dim3(32 * (p.hg + 1)), geo.bytes, s, p) == cudaSuccess ? PKV_OK : PKV_E_CUDA;
 }
 
 template <int D>
@@ -573,11 +578,9 @@ int launch_merge(const pkv_plan_info *info, const void *plan_dev, const float *r
     if (info->num_merge == 0) return PKV_OK;
     const MergeItem *m = reinterpret_cast<const MergeItem *>(static_cast<const uint8_t *>(plan_dev) + info->offsets[3]);
     const dim3 grid((unsigned)info->num_merge, (unsigned)((info->num_q_heads + 7) / 8));
-    if (info->head_dim == 128)
-        merge_kernel<128><<<grid, 256, 0, s>>>(m, rec_acc, rec_ml, o, info->num_q_heads);
-    else
-        merge_kernel<64><<<grid, 256, 0, s>>>(m, rec_acc, rec_ml, o, info->num_q_heads);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_E_CUDA;
+    const cudaError_t e = launch_pdl(info->head_dim == 128 ? merge_kernel<128> : merge_kernel<64>, grid, dim3(256), 0,
+                                     s, m, rec_acc, rec_ml, o, (int)info->num_q_heads);
+    return e == cudaSuccess ? PKV_OK : PKV_E_CUDA;
 }
 
 int check_call(const pkv_pool *pool, const pkv_batch *batch, const void *q, void *o, const pkv_plan_info *info,
@@ -635,12 +638,16 @@ extern "C" int pkv_attn_decode(const pkv_pool *pool, const pkv_batch *batch, con
     p.row_rec = reinterpret_cast<const int32_t *>(plan + info->offsets[SEC_ROW_REC]);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     p.err = reinterpret_cast<int32_t *>(ws);
-    p.wait_ns = wait_limit_ns();
+    p.wait = wait_policy(wait_limit_ns());
     p.rec_acc = reinterpret_cast<float *>(ws + kWorkspaceHeader);
     p.rec_ml = p.rec_acc + (size_t)info->num_records * info->num_q_heads * info->head_dim;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // widely shared spans on the tensor cores first, then everything else, then the merge
-    rc = decode_span_tensor(pool, batch, q, sm_scale, info, plan, ws, p.rec_acc, p.rec_ml, s);
+    // The gather of the widely shared spans (and their members' query rows), the decode
+    // kernel over everything else, the spans on the tensor cores, the merge.  The span pass
+    // reads only what the gather wrote, so it takes SMs as decode CTAs finish instead of
+    // waiting for the whole decode kernel, and its records are the freshest in L2 when the
+    // merge reads them.
+    rc = decode_span_gather(pool, batch, q, info, plan, ws, s);
     if (rc) return rc;
     if (info->num_items > 0) {
         const int G = info->num_q_heads / info->num_kv_heads;
@@ -648,5 +655,7 @@ extern "C" int pkv_attn_decode(const pkv_pool *pool, const pkv_batch *batch, con
                                    : dispatch_g<64>(G, fp8, p, (int)nctas, s);
         if (rc) return rc;
     }
+    rc = decode_span_attend(pool, q, sm_scale, info, plan, ws, p.rec_acc, p.rec_ml, s, info->num_items > 0);
+    if (rc) return rc;
     return launch_merge(info, plan_dev, p.rec_acc, p.rec_ml, p.o, s);
 }

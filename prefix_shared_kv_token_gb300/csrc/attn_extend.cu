@@ -67,7 +67,10 @@ struct ExtendParams {
     const int32_t *rec_list;  // NULL: token t of an item writes record rec + t; else rec_list[rec + t]
     const PackInfo *packs;    // packed items' segments and row groups (NULL: none)
     int32_t *err;
-    uint64_t wait_ns;         // limit of a pipeline wait (pkv_set_wait_limit_ns)
+    WaitPolicy wait;          // pipeline waits (pkv_set_wait_limit_ns)
+    int32_t pdl_wait_start;   // 1: wait for the preceding kernel before reading anything (it
+                              // wrote this launch's inputs); 0: the inputs were complete
+                              // earlier, wait only before exiting
 };
 
 template <int D>
@@ -90,22 +93,18 @@ struct XBars {
     uint64_t kfull[kXStages], vfull[kXStages], kvempty[kXStages], kempty[kXStages];
     uint64_t sfull[2], pfull[2], ofinal[2];
     uint64_t drain;
-    uint64_t wait_ns;   // limit of a pipeline wait (the launch's, copied here once)
     uint32_t tmem_base;
     int32_t abort_flag;
 };
 
-PKV_DEV bool xwait(uint64_t *bar, uint32_t parity, XBars *b, int32_t *err, int where) {
-    const uint64_t limit_ns = b->wait_ns;
-    const bool quick = short_wait_limit(limit_ns);
-    if (mbar_poll(bar, parity, quick)) return true;
+PKV_DEV bool xwait(uint64_t *bar, uint32_t parity, XBars *b, int32_t *err, int where, const WaitPolicy &wp) {
+    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    const uint32_t mask = quick ? 0u : 255u;
     for (uint32_t it = 1;; ++it) {
-        if (mbar_poll(bar, parity, quick)) return true;
-        if ((it & mask) == 0) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (it == 1 || (it & wp.check_mask) == 0) {
             if (*reinterpret_cast<volatile int32_t *>(&b->abort_flag)) return false;
-            if (global_timer_ns() - t0 > limit_ns) {
+            if (global_timer_ns() - t0 > wp.limit_ns) {
                 set_error(err, DERR_TIMEOUT | where);
                 *reinterpret_cast<volatile int32_t *>(&b->abort_flag) = 1;
                 return false;
@@ -144,6 +143,8 @@ struct GatherParams {
 // (Hkv * D elements, contiguous in the pool and in the output).
 template <int D, bool FP8>
 __global__ void __launch_bounds__(256) gather_kernel(const GatherParams p) {
+    pdl_wait();     // the pool rows and tables may come from the preceding kernel
+    pdl_trigger();
     if ((int)blockIdx.x >= p.nunits) {  // a query row
         const int i = blockIdx.x - p.nunits, r = __ldg(p.q_rows + i);
         if (r < 0 || r >= p.q_batch) {
@@ -357,12 +358,17 @@ __global__ void __launch_bounds__(384, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int i0 = __ldg(p.cta_off + blockIdx.x), i1 = __ldg(p.cta_off + blockIdx.x + 1);
 
+    if (p.pdl_wait_start) pdl_wait();
+    pdl_trigger();
     // once any CTA of this launch gave up on a wait, the rest exit instead of waiting too
     __shared__ int32_t s_skip;
     __shared__ float2 s_ml[2][kBM];  // split items: each warpgroup's running (max, sum) per row
     if (threadIdx.x == 0) s_skip = (*reinterpret_cast<volatile int32_t *>(p.err) & DERR_TIMEOUT) != 0;
     __syncthreads();
-    if (s_skip) return;
+    if (s_skip) {
+        if (!p.pdl_wait_start) pdl_wait();
+        return;
+    }
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->q, 1);
@@ -379,7 +385,6 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(&bars->ofinal[q], 1);
         }
         mbar_init(&bars->drain, 1);
-        bars->wait_ns = p.wait_ns;
         bars->abort_flag = 0;
         fence_mbar_init();
     }
@@ -415,7 +420,7 @@ __global__ void __launch_bounds__(384, 1)
                 const ExtendItem *itp = p.items + i;
                 const XItem it = load_item(itp, TQ, p.packs);
                 if (kside) {
-                    if (nql > 0 && !xwait(&bars->qempty, (nql - 1) & 1, bars, p.err, 6)) break;
+                    if (nql > 0 && !xwait(&bars->qempty, (nql - 1) & 1, bars, p.err, 6, p.wait)) break;
                     if (it.pk) {
                         // a packed tile: each row group's tokens by their own 32-row box
                         int ng = 0;
@@ -443,7 +448,7 @@ __global__ void __launch_bounds__(384, 1)
                         const bool early = kside && ((split_mask >> s) & 1u);
                         uint64_t *bar = early ? &bars->kempty[s] : &bars->kvempty[s];
                         const uint32_t par = early ? ((kpar >> s) & 1u) ^ 1u : (uint32_t)((tp / ST) - 1) & 1u;
-                        if (!xwait(bar, par, bars, p.err, kside ? 5 : 7)) {
+                        if (!xwait(bar, par, bars, p.err, kside ? 5 : 7, p.wait)) {
                             ok = false;
                             break;
                         }
@@ -480,11 +485,11 @@ __global__ void __launch_bounds__(384, 1)
             bool ok = true;
             for (int i = i0; ok && i < i1; ++i, ++ip) {
                 const XItem it = load_item(p.items + i, TQ, p.packs);
-                if (!xwait(&bars->q, ip & 1, bars, p.err, 1)) break;
+                if (!xwait(&bars->q, ip & 1, bars, p.err, 1, p.wait)) break;
                 if (!it.split) {
                     auto issue_s = [&](int q, int j) -> bool {
                         const int tg = tm + j, s = tg % ST;
-                        if (q == 0 && !xwait(&bars->kfull[s], (tg / ST) & 1, bars, p.err, 4)) return false;
+                        if (q == 0 && !xwait(&bars->kfull[s], (tg / ST) & 1, bars, p.err, 4, p.wait)) return false;
                         tc_fence_after();
                         const uint32_t q_s = sbase + C::kQOff + q * C::kQTile;
                         const uint32_t k_s = sbase + C::kStageOff + (s * 2) * C::kKTile;
@@ -500,9 +505,9 @@ __global__ void __launch_bounds__(384, 1)
                     };
                     auto issue_pv = [&](int q, int j) -> bool {
                         const int tg = tm + j, s = tg % ST;
-                        if (!xwait(&bars->pfull[q], (cpar >> q) & 1u, bars, p.err, 2)) return false;
+                        if (!xwait(&bars->pfull[q], (cpar >> q) & 1u, bars, p.err, 2, p.wait)) return false;
                         cpar ^= 1u << q;
-                        if (q == 0 && !xwait(&bars->vfull[s], (tg / ST) & 1, bars, p.err, 3)) return false;
+                        if (q == 0 && !xwait(&bars->vfull[s], (tg / ST) & 1, bars, p.err, 3, p.wait)) return false;
                         tc_fence_after();
                         const uint32_t v_s = sbase + C::kStageOff + (s * 2 + 1) * C::kKTile;
 #pragma unroll
@@ -539,7 +544,7 @@ __global__ void __launch_bounds__(384, 1)
                     // its S is done and the next K tile loads while this one's P.V still waits.
                     auto split_s = [&](int j) -> bool {
                         const int q = j & 1, tg = tm + j, s = tg % ST;
-                        if (!xwait(&bars->kfull[s], (tg / ST) & 1, bars, p.err, 4)) return false;
+                        if (!xwait(&bars->kfull[s], (tg / ST) & 1, bars, p.err, 4, p.wait)) return false;
                         tc_fence_after();
                         const uint32_t q_s = sbase + C::kQOff;
                         const uint32_t k_s = sbase + C::kStageOff + (s * 2) * C::kKTile;
@@ -556,9 +561,9 @@ __global__ void __launch_bounds__(384, 1)
                     };
                     auto split_pv = [&](int j) -> bool {
                         const int q = j & 1, tg = tm + j, s = tg % ST;
-                        if (!xwait(&bars->pfull[q], (cpar >> q) & 1u, bars, p.err, 2)) return false;
+                        if (!xwait(&bars->pfull[q], (cpar >> q) & 1u, bars, p.err, 2, p.wait)) return false;
                         cpar ^= 1u << q;
-                        if (!xwait(&bars->vfull[s], (tg / ST) & 1, bars, p.err, 3)) return false;
+                        if (!xwait(&bars->vfull[s], (tg / ST) & 1, bars, p.err, 3, p.wait)) return false;
                         tc_fence_after();
                         const uint32_t v_s = sbase + C::kStageOff + (s * 2 + 1) * C::kKTile;
 #pragma unroll
@@ -627,7 +632,7 @@ __global__ void __launch_bounds__(384, 1)
                     continue;
                 }
                 // lanes leave together: a split warp must not reach the .sync.aligned tcgen05 ops
-                if (!__all_sync(0xffffffffu, xwait(&bars->sfull[q], cw & 1, bars, p.err, 8))) {
+                if (!__all_sync(0xffffffffu, xwait(&bars->sfull[q], cw & 1, bars, p.err, 8, p.wait))) {
                     ok = false;
                     break;
                 }
@@ -703,7 +708,7 @@ __global__ void __launch_bounds__(384, 1)
                 tc_fence_before();
                 mbar_arrive(&bars->pfull[q]);
             }
-            bool fin = __all_sync(0xffffffffu, ok && xwait(&bars->ofinal[q], co & 1, bars, p.err, 10));
+            bool fin = __all_sync(0xffffffffu, ok && xwait(&bars->ofinal[q], co & 1, bars, p.err, 10, p.wait));
             if (it.split) {
                 // exchange the row's running max and sum with the other warpgroup; both
                 // warpgroups leave together when either gave up on a wait
@@ -767,6 +772,7 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
+    if (!p.pdl_wait_start) pdl_wait();  // complete only after the preceding kernel
 }
 
 // The kernel's tensor maps: Q tiles, K and V boxes, and Q row groups (packed items).
@@ -781,8 +787,9 @@ static int launch_extend(const ExtendParams &p, const XMaps &mp, int nctas, cuda
     auto kern = extend_kernel<D, G, PRECISE>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return PKV_E_CUDA;
-    kern<<<nctas, 384, smem, s>>>(p, mp.q, mp.k, mp.v, mp.qg);  // persistent: the plan's CTA lists
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_E_CUDA;
+    // persistent: the plan's CTA lists
+    return launch_pdl(kern, dim3(nctas), dim3(384), smem, s, p, mp.q, mp.k, mp.v, mp.qg) == cudaSuccess ? PKV_OK
+                                                                                                     : PKV_E_CUDA;
 }
 
 template <int D, bool PRECISE>
@@ -803,11 +810,10 @@ static int dispatch_extend(int G, const ExtendParams &p, const XMaps &mp, int n,
 
 template <int D>
 static int launch_gather(const GatherParams &p, bool fp8, int nunits, cudaStream_t s) {
-    if (fp8)
-        gather_kernel<D, true><<<nunits, 256, 0, s>>>(p);
-    else
-        gather_kernel<D, false><<<nunits, 256, 0, s>>>(p);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_E_CUDA;
+    return launch_pdl(fp8 ? gather_kernel<D, true> : gather_kernel<D, false>, dim3(nunits), dim3(256), 0, s, p) ==
+                   cudaSuccess
+               ? PKV_OK
+               : PKV_E_CUDA;
 }
 
 int check_call(const pkv_pool *pool, const pkv_batch *batch, const void *q, void *o, const pkv_plan_info *info,
@@ -848,20 +854,29 @@ static int make_maps(const void *q, int64_t qrows, const uint16_t *kg, const uin
 // are gathered next to them, and extend-kernel items (two 128-row query tiles of 128/G
 // members x G heads, one KV head, a chunk of the span; no mask: every query comes after
 // the span) write each member's partial record for the chunk.
-int decode_span_tensor(const pkv_pool *pool, const pkv_batch *batch, const void *q, float sm_scale,
-                       const pkv_plan_info *info, const uint8_t *plan, uint8_t *ws, float *rec_acc, float *rec_ml,
-                       cudaStream_t s) {
-    const int64_t nx = info->offsets[8], nunits = info->offsets[10], nkeys = info->offsets[11];
-    const int64_t nq = info->offsets[13];
-    if (nx == 0) return PKV_OK;
-    const int D = info->head_dim, hq = info->num_q_heads, hkv = info->num_kv_heads, G = hq / hkv;
-    const bool fp8 = pool->dtype == PKV_FP8_E4M3;
-    int32_t *err = reinterpret_cast<int32_t *>(ws);
-    uint16_t *kg = reinterpret_cast<uint16_t *>(ws + info->offsets[15]);
-    uint16_t *vg = kg + (size_t)nkeys * hkv * D;
-    const size_t qoff = ((size_t)info->offsets[15] + 2 * (size_t)nkeys * hkv * D * 2 + 255) & ~size_t(255);
-    uint16_t *qg = reinterpret_cast<uint16_t *>(ws + qoff);
+struct SpanBufs {
+    uint16_t *kg, *vg, *qg;
+    int64_t nunits, nkeys, nq, nx;
+};
+static SpanBufs span_bufs(const pkv_plan_info *info, uint8_t *ws) {
+    SpanBufs b;
+    b.nx = info->offsets[8];
+    b.nunits = info->offsets[10];
+    b.nkeys = info->offsets[11];
+    b.nq = info->offsets[13];
+    const int D = info->head_dim, hkv = info->num_kv_heads;
+    b.kg = reinterpret_cast<uint16_t *>(ws + info->offsets[15]);
+    b.vg = b.kg + (size_t)b.nkeys * hkv * D;
+    const size_t qoff = ((size_t)info->offsets[15] + 2 * (size_t)b.nkeys * hkv * D * 2 + 255) & ~size_t(255);
+    b.qg = reinterpret_cast<uint16_t *>(ws + qoff);
+    return b;
+}
 
+int decode_span_gather(const pkv_pool *pool, const pkv_batch *batch, const void *q, const pkv_plan_info *info,
+                       const uint8_t *plan, uint8_t *ws, cudaStream_t s) {
+    const SpanBufs b = span_bufs(info, ws);
+    if (b.nx == 0) return PKV_OK;
+    const int D = info->head_dim, hq = info->num_q_heads, hkv = info->num_kv_heads;
     GatherParams gp;
     gp.k_pool = static_cast<const uint8_t *>(pool->k);
     gp.v_pool = static_cast<const uint8_t *>(pool->v);
@@ -873,22 +888,31 @@ int decode_span_tensor(const pkv_pool *pool, const pkv_batch *batch, const void 
     gp.page_shift = page_shift_of(batch);
     gp.req_pool_indices = batch->req_pool_indices;
     gp.units = reinterpret_cast<const GatherUnit *>(plan + info->offsets[9]);
-    gp.k_out = kg;
-    gp.v_out = vg;
-    gp.err = err;
+    gp.k_out = b.kg;
+    gp.v_out = b.vg;
+    gp.err = reinterpret_cast<int32_t *>(ws);
     // one launch: the span keys, then the member query rows
-    gp.nunits = (int32_t)nunits;
+    gp.nunits = (int32_t)b.nunits;
     gp.q_src = static_cast<const uint4 *>(q);
-    gp.q_out = reinterpret_cast<uint4 *>(qg);
+    gp.q_out = reinterpret_cast<uint4 *>(b.qg);
     gp.q_rows = reinterpret_cast<const int32_t *>(plan + info->offsets[12]);
     gp.q_batch = batch->batch;
     gp.q_row_vecs = hq * D / 8;
-    int rc = D == 128 ? launch_gather<128>(gp, fp8, (int)(nunits + nq), s)
-                      : launch_gather<64>(gp, fp8, (int)(nunits + nq), s);
-    if (rc) return rc;
+    const bool fp8 = pool->dtype == PKV_FP8_E4M3;
+    return D == 128 ? launch_gather<128>(gp, fp8, (int)(b.nunits + b.nq), s)
+                    : launch_gather<64>(gp, fp8, (int)(b.nunits + b.nq), s);
+}
 
+int decode_span_attend(const pkv_pool *pool, const void *q, float sm_scale, const pkv_plan_info *info,
+                       const uint8_t *plan, uint8_t *ws, float *rec_acc, float *rec_ml, cudaStream_t s,
+                       bool after_decode) {
+    (void)q;
+    const SpanBufs b = span_bufs(info, ws);
+    if (b.nx == 0) return PKV_OK;
+    const int D = info->head_dim, hq = info->num_q_heads, hkv = info->num_kv_heads, G = hq / hkv;
+    const bool fp8 = pool->dtype == PKV_FP8_E4M3;
     XMaps mp;
-    rc = make_maps(qg, nq, kg, vg, nkeys, D, hq, hkv, &mp);
+    int rc = make_maps(b.qg, b.nq, b.kg, b.vg, b.nkeys, D, hq, hkv, &mp);
     if (rc) return rc;
     ExtendParams p;
     p.o = nullptr;  // every item writes records
@@ -897,26 +921,30 @@ int decode_span_tensor(const pkv_pool *pool, const pkv_batch *batch, const void 
     p.scale_log2 = sm_scale * (fp8 ? pool->k_scale : 1.f) * kLog2eX;
     p.v_scale = fp8 ? pool->v_scale : 1.f;
     p.items = reinterpret_cast<const ExtendItem *>(plan + info->offsets[7]);
-    p.num_items = (int32_t)nx;
-    p.err = err;
+    p.num_items = (int32_t)b.nx;
+    p.err = reinterpret_cast<int32_t *>(ws);
     p.rec_acc = rec_acc;
     p.rec_ml = rec_ml;
     p.rec_list = reinterpret_cast<const int32_t *>(plan + info->offsets[14]);
     p.packs = nullptr;
-    p.wait_ns = wait_limit_ns();
+    p.wait = wait_policy(wait_limit_ns());
+    // Right after the gather, wait for it first; after the decode kernel (which itself waited
+    // for the gather), read the gathered rows at once and wait for the decode kernel only
+    // before exiting, so the merge that follows sees every record.
+    p.pdl_wait_start = after_decode ? 0 : 1;
     // the spans' items, then the short requests' items (precise weights)
     const ExtendItem *items = reinterpret_cast<const ExtendItem *>(plan + info->offsets[7]);
     const int64_t nprec = info->offsets[18];
     for (int part = 0; part < 2; ++part) {
-        const int64_t n = part == 0 ? nx - nprec : nprec;
+        const int64_t n = part == 0 ? b.nx - nprec : nprec;
         if (n == 0) continue;
-        p.items = items + (part == 0 ? 0 : nx - nprec);
+        p.items = items + (part == 0 ? 0 : b.nx - nprec);
         p.num_items = (int32_t)n;
         p.cta_off = reinterpret_cast<const int32_t *>(plan + info->offsets[part == 0 ? 16 : 19]);
         const int64_t nctas = info->offsets[part == 0 ? 17 : 20];
-        if (nctas < 1 || nctas > n || nprec > nx) return PKV_E_PLAN;
-        int rc = D == 128 ? dispatch_extend<128>(G, p, mp, (int)nctas, s, part == 1)
-                          : dispatch_extend<64>(G, p, mp, (int)nctas, s, part == 1);
+        if (nctas < 1 || nctas > n || nprec > b.nx) return PKV_E_PLAN;
+        rc = D == 128 ? dispatch_extend<128>(G, p, mp, (int)nctas, s, part == 1)
+                      : dispatch_extend<64>(G, p, mp, (int)nctas, s, part == 1);
         if (rc) return rc;
     }
     return PKV_OK;
@@ -986,7 +1014,8 @@ extern "C" int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, con
     p.rec_acc = rec_acc;
     p.rec_ml = rec_ml;
     p.rec_list = nullptr;
-    p.wait_ns = wait_limit_ns();
+    p.wait = wait_policy(wait_limit_ns());
+    p.pdl_wait_start = 1;  // the gather just before wrote the keys
     p.packs = info->offsets[14] > 0 ? reinterpret_cast<const PackInfo *>(plan + info->offsets[13]) : nullptr;
     void *ev0 = g_kernel_events[0], *ev1 = g_kernel_events[1];
     g_kernel_events[0] = g_kernel_events[1] = nullptr;

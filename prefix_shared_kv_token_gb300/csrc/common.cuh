@@ -36,6 +36,16 @@ PKV_DEV uint64_t global_timer_ns() {
 
 PKV_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// Programmatic dependent launch (every kernel here is launched with the programmatic stream
+// serialization attribute, launch_pdl): the next kernel in the stream may be scheduled once
+// every CTA of this one has issued pdl_trigger (or exited), and its CTAs then take SMs as they
+// free up.  pdl_wait blocks until the preceding grid has completed and its writes are
+// visible; each kernel calls it before it reads what the preceding kernels wrote -- or, when
+// it reads nothing of theirs, before it exits, so that its own completion still implies
+// theirs.
+PKV_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+PKV_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Slot of context position t from a row of the batch table: the token table's entry, or
 // with pages of 2^shift slots, the position's page times the page size plus its offset.
 // A page outside the pool gives -1 (the callers flag it and read zeros).
@@ -88,8 +98,8 @@ PKV_DEV bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Non-blocking probe of the same phase (mbarrier.try_wait may suspend the thread for a
-// system-dependent time before it returns false; test_wait never does).
+// Non-blocking probe of the same phase (try_wait may suspend the thread for a while before
+// it returns false; test_wait never does).
 PKV_DEV bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -108,13 +118,20 @@ PKV_DEV bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
 // short pipeline limit never cuts a drain short.
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 constexpr uint64_t kDrainTimeoutNs = 2000000000ull;
-// A limit under ~1 ms is a short limit: its waits poll with the non-blocking test_wait and
-// read the timer on every try, so the limit is noticed as soon as the timer passes it (a
-// blocking try_wait could sit out a whole short wait inside one call).  The long default
-// limit keeps try_wait and reads the timer every 256 tries.
-PKV_DEV bool short_wait_limit(uint64_t limit_ns) { return limit_ns < (1ull << 20); }
-PKV_DEV bool mbar_poll(uint64_t *bar, uint32_t parity, bool quick) {
-    return quick ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity);
+// How a pipeline wait polls, fixed per launch from its limit (wait_policy on the host).  A
+// wait first tries once (try_wait, which may suspend the thread briefly); after a failed
+// retry, and then every (check_mask + 1) retries, it reads the timer.  The long default limit
+// checks every 256 retries; a short limit (under 1 ms: the way to exercise the timeout path)
+// checks on every retry, and its `quick` launches poll with the non-blocking test_wait so a
+// short wait cannot pass unnoticed inside one suspended try.
+struct WaitPolicy {
+    uint64_t limit_ns;
+    uint32_t check_mask;
+    uint32_t quick;
+};
+__host__ __device__ inline WaitPolicy wait_policy(uint64_t limit_ns) {
+    const bool quick = limit_ns < (1ull << 20);
+    return WaitPolicy{limit_ns, quick ? 0u : 255u, quick ? 1u : 0u};
 }
 
 // Wait for the phase with the given parity to complete, for at most ~kDrainTimeoutNs.

@@ -28,6 +28,8 @@ __global__ void __launch_bounds__(256) kv_store_kernel(const uint4 *__restrict__
     // one warp per token row (K rows of tokens 0..n-1, then their V rows), grid-strided; the
     // row's slot is read once and the lanes stride its vec_per_row 16-byte source vectors,
     // four loads in flight before their stores
+    pdl_wait();     // the rows and slots may come from the preceding kernel
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     for (int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < 2 * n; row += nwarps) {
@@ -86,15 +88,12 @@ extern "C" int pkv_kv_store(const pkv_pool *pool, const void *k_new, const void 
     const int64_t cap = (int64_t)num_sms() * 8;  // 8 resident blocks of 256 per SM
     if (blocks > cap) blocks = cap;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (pool->dtype == PKV_BF16)
-        kv_store_kernel<false><<<(unsigned)blocks, threads, 0, s>>>(
-            reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new), out_cache_loc, n,
-            vec_per_row, reinterpret_cast<uint8_t *>(pool->k), reinterpret_cast<uint8_t *>(pool->v), pool->num_slots,
-            1.f, 1.f, reinterpret_cast<int32_t *>(workspace));
-    else
-        kv_store_kernel<true><<<(unsigned)blocks, threads, 0, s>>>(
-            reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new), out_cache_loc, n,
-            vec_per_row, reinterpret_cast<uint8_t *>(pool->k), reinterpret_cast<uint8_t *>(pool->v), pool->num_slots,
-            pool->k_scale, pool->v_scale, reinterpret_cast<int32_t *>(workspace));
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_E_CUDA;
+    const bool fp8 = pool->dtype != PKV_BF16;
+    const cudaError_t e = launch_pdl(fp8 ? kv_store_kernel<true> : kv_store_kernel<false>, dim3((unsigned)blocks),
+                                     dim3(threads), 0, s, reinterpret_cast<const uint4 *>(k_new),
+                                     reinterpret_cast<const uint4 *>(v_new), out_cache_loc, n, vec_per_row,
+                                     reinterpret_cast<uint8_t *>(pool->k), reinterpret_cast<uint8_t *>(pool->v),
+                                     pool->num_slots, fp8 ? pool->k_scale : 1.f, fp8 ? pool->v_scale : 1.f,
+                                     reinterpret_cast<int32_t *>(workspace));
+    return e == cudaSuccess ? PKV_OK : PKV_E_CUDA;
 }

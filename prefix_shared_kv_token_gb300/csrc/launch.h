@@ -6,11 +6,33 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/pkv.h"
 
 namespace pkv {
 
 int num_sms();  // SMs of the current device (cached per device)
+
+// Launch with programmatic stream serialization: the kernel may be scheduled while the
+// previous kernel in the stream still runs (once all that kernel's CTAs issued pdl_trigger or
+// exited), so launch latency and set-up overlap the previous kernel's tail.  The kernel must
+// call pdl_wait before it touches anything earlier work wrote, or before it exits.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args &&...args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // cudaEvent_t pair set by pkv_set_kernel_events (consumed by the next pkv_attn_extend)
 extern void *g_kernel_events[2];
@@ -45,10 +67,15 @@ CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType dtype, cuuint32_t ra
                       const cuuint64_t *dims, const cuuint64_t *strides_bytes, const cuuint32_t *box,
                       CUtensorMapSwizzle swizzle);
 
-// Tensor-core pass of a decode plan over its widely shared spans (gather, query-row gather,
-// extend kernel writing partial records); no-op when the plan has none.
-int decode_span_tensor(const pkv_pool *pool, const pkv_batch *batch, const void *q, float sm_scale,
-                       const pkv_plan_info *info, const uint8_t *plan, uint8_t *ws, float *rec_acc, float *rec_ml,
-                       cudaStream_t s);
+// Tensor-core pass of a decode plan over its widely shared spans, in two launches' worth of
+// steps: the gather of the spans' keys and their members' query rows, then the extend
+// kernel writing partial records (after_decode: the decode kernel was launched in between,
+// so the pass reads the gather's output without waiting for that kernel, and waits for it
+// before it exits).  No-ops when the plan has no such spans.
+int decode_span_gather(const pkv_pool *pool, const pkv_batch *batch, const void *q, const pkv_plan_info *info,
+                       const uint8_t *plan, uint8_t *ws, cudaStream_t s);
+int decode_span_attend(const pkv_pool *pool, const void *q, float sm_scale, const pkv_plan_info *info,
+                       const uint8_t *plan, uint8_t *ws, float *rec_acc, float *rec_ml, cudaStream_t s,
+                       bool after_decode);
 
 }  // namespace pkv

@@ -13,7 +13,7 @@ written.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl ours|reference]
                     [--page-size P] [--workload chunked_prefill|serving] [--no-graph] [--no-cascade]
-                    [--no-cpu-baseline] [--no-more-configs] [--pool-slots S]
+                    [--no-cpu-baseline] [--no-more-configs] [--pool-slots S] [--chunked-gather]
 
 The default run (few-shot extend, configuration 2) also measures the decode workloads and the
 mixed fp8 step (configurations 3-5) after the headline and reports them under
@@ -266,7 +266,9 @@ def measure(w, args, dev, steps, world, e2e=True):
     facts = workload_facts(w)
     pc = PrefixCache(w, device=str(dev), page_size=args.page_size)
     if w.name == "chunked_prefill":
-        calls = pc.prepare_chunked()       # one extend call per chunk, over the chunks before it
+        # one extend call per chunk, over the chunks before it: stored with its chunk and read
+        # from a context buffer (default), or stored separately and gathered from the pool
+        calls = pc.prepare_chunked(fused=not getattr(args, "chunked_gather", False))
         plan_ms = None
     else:
         pc.populate()
@@ -383,7 +385,10 @@ def measure(w, args, dev, steps, world, e2e=True):
                       **({"attn_decode_median": round(float(np.median(attn_ms["decode"])), 4)}
                          if "decode" in attn_ms else {})},
         "kv_store": {"bytes_per_step": int(store_bytes),
-                     "gbs": round(store_bytes / (float(np.mean(store_ms)) / 1e3) / 1e9, 1)},
+                     "gbs": (round(store_bytes / (float(np.mean(store_ms)) / 1e3) / 1e9, 1)
+                             if all(c.ctx is None for c in calls) else None),
+                     **({"note": "stored inside each chunk's attention call"}
+                        if any(c.ctx is not None for c in calls) else {})},
         "wall_s": round(wall, 4), "clocks": clocks.summary(),
         "host_plan_ms_per_step": None if plan_ms is None else round(plan_ms, 3),
     }
@@ -462,6 +467,9 @@ def run_ours(args, rank, world):
            "decode_launch": "plain" if args.no_graph else "CUDA graph replay of the call's launches",
            "l2": "flushed between timed steps (512 MiB write outside the step events)",
            "tokens_per_step": m["tokens_per_step"]}
+    if w.name == "chunked_prefill":
+        cfg["chunks"] = "separate stores, gather per chunk" if args.chunked_gather else \
+            "stored into and read from a context buffer"
     for kind in ("extend", "decode"):
         if f"{kind}_queries" in m:
             cfg[f"{kind}_queries"] = m[f"{kind}_queries"]
@@ -642,6 +650,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cascade", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--chunked-gather", action="store_true",
+                    help="chunked_prefill: separate stores and a gather of the whole context per chunk "
+                         "(instead of chunks stored into and read from a context buffer)")
     ap.add_argument("--no-more-configs", action="store_true",
                     help="skip the decode and mixed workloads (configurations 3-5) measured after the headline")
     ap.add_argument("--pool-slots", type=int, default=0)

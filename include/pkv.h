@@ -212,6 +212,39 @@ int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, const void *q,
                     float sm_scale, const pkv_plan_info *info, const void *plan_dev,
                     void *workspace, size_t ws_bytes, void *stream);
 
+/* Chunked prefill over a context buffer kept by the caller ("SGLang后端运行时优化细节",
+ * §RadixAttention KV缓存复用的底层逻辑, 3 开发者需关注的配置项: --chunked-prefill-size prefills a
+ * long prompt a chunk at a time, each chunk over the chunks cached before it).  The caller
+ * keeps, for every request being prefilled this way, a run of rows in two device arrays
+ * ctx_k, ctx_v of bf16 [ctx_rows][num_kv_heads][head_dim]: context position t of request r
+ * lives at row ctx_row0[r] + t.  Each chunk's call stores its new tokens' K/V into the pool
+ * (exactly as pkv_kv_store) and, in the same pass, into their context rows as the pool now
+ * holds them (bf16 bits; for an fp8 pool the stored code converted exactly to bf16, unscaled);
+ * its attention then reads the context rows directly.  Rows of earlier positions must hold
+ * what the earlier calls (or the caller) wrote there: nothing is gathered or re-read from the
+ * pool.  Positions and masks are those of pkv_plan_extend; there is no cascade.
+ *   ctx_row0   host int32 [batch]; rows [ctx_row0[r], ctx_row0[r] + seq_lens[r]) inside
+ *              [0, ctx_rows) and disjoint between requests (else PKV_E_INVALID)
+ * The plan's workspace_bytes does not include the context arrays (the caller owns them). */
+int pkv_plan_extend_ctx(int32_t batch, const int32_t *seq_lens, const int32_t *extend_lens,
+                        const int32_t *qo_indptr, const int32_t *ctx_row0, int64_t ctx_rows,
+                        int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                        const pkv_plan_opts *opts, void *plan, size_t plan_cap, pkv_plan_info *info);
+
+/* The store + attention of one chunk (a plan from pkv_plan_extend_ctx).
+ *   q, o                      as pkv_attn_extend ([total_q][num_q_heads][head_dim] bf16)
+ *   k_new, v_new, out_cache_loc  the new tokens' K/V rows and pool slots, in q order, as
+ *                             pkv_kv_store takes them (total_q rows)
+ *   ctx_k, ctx_v, ctx_rows    the context arrays (device, 16-byte aligned), ctx_rows rows each
+ *   workspace                 as pkv_attn_extend; slot-range errors of the store are recorded
+ *                             in its error word (a bad slot's pool and context rows are not
+ *                             written)
+ * pkv_attn_extend rejects a context-buffer plan and this call any other (PKV_E_PLAN). */
+int pkv_attn_extend_ctx(const pkv_pool *pool, const void *q, void *o, float sm_scale, const void *k_new,
+                        const void *v_new, const int32_t *out_cache_loc, void *ctx_k, void *ctx_v,
+                        int64_t ctx_rows, const pkv_plan_info *info, const void *plan_dev, void *workspace,
+                        size_t ws_bytes, void *stream);
+
 /* Synchronises `stream`, reads the error word of `workspace` (PKV_OK when zero, else
  * PKV_E_DEVICE with the raw word in *raw when raw != NULL). */
 int pkv_get_device_error(void *workspace, void *stream, int32_t *raw);

@@ -12,6 +12,8 @@ memory -- and forwards to the library.  Names follow the C entry points without 
     attn_decode   one query token per request over its whole context (widely shared spans on
                   the tensor cores, the rest by a persistent bulk-copy kernel with mma.sync)
     attn_extend   causal extend of the uncached suffix (key gather, then tcgen05 / TMEM / TMA)
+    plan_extend_ctx / attn_extend_ctx  chunked prefill over a caller-kept context buffer: each
+                  chunk is stored into the pool and its context rows in one pass, nothing gathered
     RadixTree     host radix tree: match_prefix (with split), insert, LRU evict, lock_ref,
                   cascade extraction
     Allocator     token-slot free list
@@ -30,7 +32,7 @@ from ._lib import (PKV_BF16, PKV_FP8_E4M3, PkvBatch, PkvCascade, PkvError, PkvPl
                    check, lib)
 
 __all__ = ["Pool", "Batch", "Plan", "Cascade", "kv_store", "check_out_cache_loc", "plan_decode", "plan_extend",
-           "attn_decode", "attn_extend", "get_device_error", "get_noalloc_device_error", "set_kernel_events",
+           "plan_extend_ctx", "attn_decode", "attn_extend", "attn_extend_ctx", "get_device_error", "get_noalloc_device_error", "set_kernel_events",
            "set_wait_limit_ns", "get_wait_limit_ns",
            "RadixTree", "Allocator", "PkvError", "version"]
 
@@ -171,6 +173,21 @@ def plan_extend(seq_lens, extend_lens, qo_indptr, num_q_heads, num_kv_heads, hea
     return Plan(info, blob)
 
 
+def plan_extend_ctx(seq_lens, extend_lens, qo_indptr, ctx_row0, ctx_rows, num_q_heads, num_kv_heads, head_dim,
+                    opts=None) -> Plan:
+    """Extend plan over a caller-kept context buffer (chunked prefill): request r's context
+    position t is row ctx_row0[r] + t of the context arrays (see pkv_plan_extend_ctx)."""
+    seq, ext, qo, row0 = _i32(seq_lens), _i32(extend_lens), _i32(qo_indptr), _i32(ctx_row0)
+    info = PkvPlanInfo()
+    o = _opts(opts)
+    args = (len(seq), _ptr(seq), _ptr(ext), _ptr(qo), _ptr(row0), int(ctx_rows), num_q_heads, num_kv_heads,
+            head_dim, o)
+    check("pkv_plan_extend_ctx", lib.pkv_plan_extend_ctx(*args, None, 0, C.byref(info)))
+    blob = np.zeros(info.plan_bytes, dtype=np.uint8)
+    check("pkv_plan_extend_ctx", lib.pkv_plan_extend_ctx(*args, _ptr(blob), blob.nbytes, C.byref(info)))
+    return Plan(info, blob)
+
+
 # ----------------------------------------------------------------------------------------
 # device calls
 
@@ -204,6 +221,17 @@ def attn_extend(pool: Pool, batch: Batch, q, o, sm_scale, plan: Plan, plan_dev, 
     check("pkv_attn_extend", lib.pkv_attn_extend(C.byref(p), C.byref(b), _ptr(q), _ptr(o), float(sm_scale),
                                                  C.byref(plan.info), _ptr(plan_dev), _ptr(workspace),
                                                  workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def attn_extend_ctx(pool: Pool, q, o, sm_scale, k_new, v_new, out_cache_loc, ctx_k, ctx_v, plan: Plan, plan_dev,
+                    workspace, stream=None) -> None:
+    """Store one chunk's new tokens (pool and context rows) and attend over the context arrays
+    ctx_k / ctx_v (torch bf16 [ctx_rows, Hkv, d])."""
+    p = pool.c()
+    check("pkv_attn_extend_ctx", lib.pkv_attn_extend_ctx(
+        C.byref(p), _ptr(q), _ptr(o), float(sm_scale), _ptr(k_new), _ptr(v_new), _ptr(out_cache_loc), _ptr(ctx_k),
+        _ptr(ctx_v), int(ctx_k.shape[0]), C.byref(plan.info), _ptr(plan_dev), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def get_device_error(workspace, stream=None) -> int:

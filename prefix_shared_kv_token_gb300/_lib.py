@@ -68,6 +68,10 @@ SIGNATURES = {
                                   C.POINTER(PkvPlanInfo)]),
     "pkv_plan_extend": (C.c_int, [_I32, _P, _P, _P, _I32, _I32, _I32, C.POINTER(PkvCascade),
                                   C.POINTER(PkvPlanOpts), _P, _SZ, C.POINTER(PkvPlanInfo)]),
+    "pkv_plan_extend_ctx": (C.c_int, [_I32, _P, _P, _P, _P, _I64, _I32, _I32, _I32, C.POINTER(PkvPlanOpts), _P, _SZ,
+                                      C.POINTER(PkvPlanInfo)]),
+    "pkv_attn_extend_ctx": (C.c_int, [C.POINTER(PkvPool), _P, _P, _F, _P, _P, _P, _P, _P, _I64,
+                                      C.POINTER(PkvPlanInfo), _P, _P, _SZ, _P]),
     "pkv_attn_decode": (C.c_int, [C.POINTER(PkvPool), C.POINTER(PkvBatch), _P, _P, _F, C.POINTER(PkvPlanInfo), _P,
                                   _P, _SZ, _P]),
     "pkv_attn_extend": (C.c_int, [C.POINTER(PkvPool), C.POINTER(PkvBatch), _P, _P, _F, C.POINTER(PkvPlanInfo), _P,

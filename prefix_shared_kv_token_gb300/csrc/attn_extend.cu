@@ -952,22 +952,77 @@ int decode_span_attend(const pkv_pool *pool, const void *q, float sm_scale, cons
 
 }  // namespace pkv
 
+namespace pkv {
+
+int launch_store(const pkv_pool *pool, const void *k_new, const void *v_new, const int32_t *out_cache_loc, int64_t n,
+                 void *workspace, void *ctx_k, void *ctx_v, const int32_t *ctx_row, cudaStream_t s);
+
+// The extend items of a plan over keys already laid out as bf16 [key][Hkv][D] arrays (the
+// workspace's gathered runs, or a caller's context arrays), then the merge.
+static int extend_items(const pkv_pool *pool, const void *q, void *o, float sm_scale, const pkv_plan_info *info,
+                        const void *plan_dev, uint8_t *ws, const uint16_t *kg, const uint16_t *vg, int64_t nkeys,
+                        cudaStream_t s) {
+    const int D = info->head_dim, hq = info->num_q_heads, hkv = info->num_kv_heads, G = hq / hkv;
+    const bool fp8 = pool->dtype == PKV_FP8_E4M3;
+    const uint8_t *plan = static_cast<const uint8_t *>(plan_dev);
+    float *rec_acc = reinterpret_cast<float *>(ws + kWorkspaceHeader);
+    float *rec_ml = rec_acc + (size_t)info->num_records * hq * D;
+    XMaps mp;
+    int rc = make_maps(q, info->total_q, kg, vg, nkeys, D, hq, hkv, &mp);
+    if (rc) return rc;
+
+    ExtendParams p;
+    p.o = static_cast<uint16_t *>(o);
+    p.hkv = hkv;
+    p.hq = hq;
+    p.scale_log2 = sm_scale * (fp8 ? pool->k_scale : 1.f) * kLog2eX;
+    p.v_scale = fp8 ? pool->v_scale : 1.f;
+    p.items = reinterpret_cast<const ExtendItem *>(plan + info->offsets[0]);
+    p.num_items = info->num_items;
+    p.err = reinterpret_cast<int32_t *>(ws);
+    p.rec_acc = rec_acc;
+    p.rec_ml = rec_ml;
+    p.rec_list = nullptr;
+    p.wait = wait_policy(wait_limit_ns());
+    p.pdl_wait_start = 1;  // the gather (or the store) just before wrote the keys
+    p.packs = info->offsets[14] > 0 ? reinterpret_cast<const PackInfo *>(plan + info->offsets[13]) : nullptr;
+    void *ev0 = g_kernel_events[0], *ev1 = g_kernel_events[1];
+    g_kernel_events[0] = g_kernel_events[1] = nullptr;
+    if (ev0 && cudaEventRecord(static_cast<cudaEvent_t>(ev0), s) != cudaSuccess) return PKV_E_CUDA;
+    // the main item list, then (if any) the items whose rows see few keys (precise weights)
+    for (int part = 0; part < 2; ++part) {
+        const int64_t nitems = part == 0 ? info->num_items - info->offsets[10] : info->offsets[10];
+        if (nitems == 0) continue;
+        p.items = reinterpret_cast<const ExtendItem *>(plan + info->offsets[part == 0 ? 0 : 9]);
+        p.num_items = (int32_t)nitems;
+        p.cta_off = reinterpret_cast<const int32_t *>(plan + info->offsets[part == 0 ? 7 : 11]);
+        const int64_t nctas = info->offsets[part == 0 ? 8 : 12];
+        if (nctas < 1 || nctas > nitems) return PKV_E_PLAN;
+        rc = D == 128 ? dispatch_extend<128>(G, p, mp, (int)nctas, s, part == 1)
+                      : dispatch_extend<64>(G, p, mp, (int)nctas, s, part == 1);
+        if (rc) return rc;
+    }
+    if (ev1 && cudaEventRecord(static_cast<cudaEvent_t>(ev1), s) != cudaSuccess) return PKV_E_CUDA;
+    return launch_merge(info, plan_dev, rec_acc, rec_ml, p.o, s);
+}
+
+}  // namespace pkv
+
 extern "C" int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, const void *q, void *o, float sm_scale,
                                const pkv_plan_info *info, const void *plan_dev, void *workspace, size_t ws_bytes,
                                void *stream) {
     using namespace pkv;
     int rc = check_call(pool, batch, q, o, info, plan_dev, workspace, ws_bytes, 2);
     if (rc) return rc;
+    if (info->offsets[16] != 0) return PKV_E_PLAN;  // a context-buffer plan: pkv_attn_extend_ctx
     if (info->num_items == 0) return PKV_OK;
-    const int D = info->head_dim, hq = info->num_q_heads, hkv = info->num_kv_heads, G = hq / hkv;
+    const int D = info->head_dim, hq = info->num_q_heads, hkv = info->num_kv_heads;
     const bool fp8 = pool->dtype == PKV_FP8_E4M3;
     const uint8_t *plan = static_cast<const uint8_t *>(plan_dev);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
     // workspace: header | records (acc, ml) | gathered K | gathered V
-    float *rec_acc = reinterpret_cast<float *>(ws + kWorkspaceHeader);
-    float *rec_ml = rec_acc + (size_t)info->num_records * hq * D;
     const size_t rec_bytes = (size_t)info->num_records * hq * (D + 2) * 4;
     uint16_t *kg = reinterpret_cast<uint16_t *>(ws + kWorkspaceHeader + ((rec_bytes + 255) & ~size_t(255)));
     const int64_t nkeys = info->offsets[6];  // gathered keys
@@ -997,42 +1052,37 @@ extern "C" int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, con
         rc = D == 128 ? launch_gather<128>(gp, fp8, nunits, s) : launch_gather<64>(gp, fp8, nunits, s);
         if (rc) return rc;
     }
+    return extend_items(pool, q, o, sm_scale, info, plan_dev, ws, kg, vg, nkeys, s);
+}
 
-    XMaps mp;
-    rc = make_maps(q, info->total_q, kg, vg, nkeys, D, hq, hkv, &mp);
+extern "C" int pkv_attn_extend_ctx(const pkv_pool *pool, const void *q, void *o, float sm_scale, const void *k_new,
+                                   const void *v_new, const int32_t *out_cache_loc, void *ctx_k, void *ctx_v,
+                                   int64_t ctx_rows, const pkv_plan_info *info, const void *plan_dev,
+                                   void *workspace, size_t ws_bytes, void *stream) {
+    using namespace pkv;
+    int rc = validate_pool(pool);
     if (rc) return rc;
-
-    ExtendParams p;
-    p.o = static_cast<uint16_t *>(o);
-    p.hkv = hkv;
-    p.hq = hq;
-    p.scale_log2 = sm_scale * (fp8 ? pool->k_scale : 1.f) * kLog2eX;
-    p.v_scale = fp8 ? pool->v_scale : 1.f;
-    p.items = reinterpret_cast<const ExtendItem *>(plan + info->offsets[0]);
-    p.num_items = info->num_items;
-    p.err = reinterpret_cast<int32_t *>(ws);
-    p.rec_acc = rec_acc;
-    p.rec_ml = rec_ml;
-    p.rec_list = nullptr;
-    p.wait = wait_policy(wait_limit_ns());
-    p.pdl_wait_start = 1;  // the gather just before wrote the keys
-    p.packs = info->offsets[14] > 0 ? reinterpret_cast<const PackInfo *>(plan + info->offsets[13]) : nullptr;
-    void *ev0 = g_kernel_events[0], *ev1 = g_kernel_events[1];
-    g_kernel_events[0] = g_kernel_events[1] = nullptr;
-    if (ev0 && cudaEventRecord(static_cast<cudaEvent_t>(ev0), s) != cudaSuccess) return PKV_E_CUDA;
-    // the main item list, then (if any) the items whose rows see few keys (precise weights)
-    for (int part = 0; part < 2; ++part) {
-        const int64_t nitems = part == 0 ? info->num_items - info->offsets[10] : info->offsets[10];
-        if (nitems == 0) continue;
-        p.items = reinterpret_cast<const ExtendItem *>(plan + info->offsets[part == 0 ? 0 : 9]);
-        p.num_items = (int32_t)nitems;
-        p.cta_off = reinterpret_cast<const int32_t *>(plan + info->offsets[part == 0 ? 7 : 11]);
-        const int64_t nctas = info->offsets[part == 0 ? 8 : 12];
-        if (nctas < 1 || nctas > nitems) return PKV_E_PLAN;
-        rc = D == 128 ? dispatch_extend<128>(G, p, mp, (int)nctas, s, part == 1)
-                      : dispatch_extend<64>(G, p, mp, (int)nctas, s, part == 1);
-        if (rc) return rc;
-    }
-    if (ev1 && cudaEventRecord(static_cast<cudaEvent_t>(ev1), s) != cudaSuccess) return PKV_E_CUDA;
-    return launch_merge(info, plan_dev, rec_acc, rec_ml, p.o, s);
+    if (!q || !o || !info || !plan_dev || !workspace || !ctx_k || !ctx_v) return PKV_E_INVALID;
+    if (info->op != 2 || info->offsets[16] != 1 || info->offsets[6] != ctx_rows) return PKV_E_PLAN;
+    if (info->num_kv_heads != pool->num_kv_heads || info->head_dim != pool->head_dim) return PKV_E_PLAN;
+    if (ws_bytes < info->workspace_bytes) return PKV_E_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(plan_dev) & 15) || (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return PKV_E_INVALID;
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(o) | reinterpret_cast<uintptr_t>(ctx_k) |
+         reinterpret_cast<uintptr_t>(ctx_v)) & 15)
+        return PKV_E_INVALID;
+    const int64_t n = info->total_q;
+    if (n == 0) return PKV_OK;
+    if (!k_new || !v_new || !out_cache_loc) return PKV_E_INVALID;
+    if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15) return PKV_E_INVALID;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const uint8_t *plan = static_cast<const uint8_t *>(plan_dev);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    // the new tokens into the pool and, as the pool now holds them, into their context rows
+    rc = launch_store(pool, k_new, v_new, out_cache_loc, n, ws, ctx_k, ctx_v,
+                      reinterpret_cast<const int32_t *>(plan + info->offsets[15]), s);
+    if (rc) return rc;
+    if (info->num_items == 0) return PKV_OK;
+    return extend_items(pool, q, o, sm_scale, info, plan_dev, ws, static_cast<const uint16_t *>(ctx_k),
+                        static_cast<const uint16_t *>(ctx_v), ctx_rows, s);
 }

@@ -479,10 +479,16 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
     return emit(blob, plan, plan_cap, info);
 }
 
-extern "C" int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int32_t *extend_lens,
-                               const int32_t *qo_indptr, int32_t num_q_heads, int32_t num_kv_heads,
-                               int32_t head_dim, const pkv_cascade *cascade, const pkv_plan_opts *opts,
-                               void *plan, size_t plan_cap, pkv_plan_info *info) {
+// Extend plans.  ctx_row0 == NULL: the call gathers its key runs (shared spans, each
+// request's own positions) from the pool into the workspace.  ctx_row0 != NULL (context-
+// buffer plans, chunked prefill): request r's context positions [0, seq_lens[r]) live in the
+// caller's bf16 context arrays at rows ctx_row0[r] + position; earlier calls wrote the rows of
+// its earlier positions, and this call writes the rows of its new tokens while it stores them
+// into the pool, so nothing is gathered (no cascade).
+static int plan_extend_impl(int32_t batch, const int32_t *seq_lens, const int32_t *extend_lens,
+                            const int32_t *qo_indptr, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                            const pkv_cascade *cascade, const pkv_plan_opts *opts, const int32_t *ctx_row0,
+                            int64_t ctx_rows, void *plan, size_t plan_cap, pkv_plan_info *info) {
     const int32_t num_sms = (opts && opts->num_sms > 0) ? opts->num_sms : 152;
     if (!info || batch < 0 || (batch > 0 && (!seq_lens || !extend_lens || !qo_indptr))) return PKV_E_INVALID;
     int rc = check_heads(num_q_heads, num_kv_heads, head_dim);
@@ -491,6 +497,19 @@ extern "C" int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int
     for (int32_t r = 0; r < batch; ++r) {
         if (extend_lens[r] < 1 || extend_lens[r] > seq_lens[r]) return PKV_E_INVALID;
         if (qo_indptr[r + 1] - qo_indptr[r] != extend_lens[r]) return PKV_E_INVALID;
+    }
+    const bool ctx = ctx_row0 != nullptr;
+    if (ctx) {
+        if (cascade || ctx_rows <= 0 || ctx_rows >= ((int64_t)1 << 31)) return PKV_E_INVALID;
+        // each request's rows inside the arrays, no two requests' rows overlapping
+        std::vector<std::pair<int64_t, int64_t>> rows;
+        for (int32_t r = 0; r < batch; ++r) {
+            if (ctx_row0[r] < 0 || (int64_t)ctx_row0[r] + seq_lens[r] > ctx_rows) return PKV_E_INVALID;
+            rows.push_back({ctx_row0[r], (int64_t)ctx_row0[r] + seq_lens[r]});
+        }
+        std::sort(rows.begin(), rows.end());
+        for (size_t i = 1; i < rows.size(); ++i)
+            if (rows[i].first < rows[i - 1].second) return PKV_E_INVALID;
     }
     const int32_t G = num_q_heads / num_kv_heads;
     const int32_t TQ2 = 2 * (128 / G);  // query tokens per item (two 128-row tiles)
@@ -519,6 +538,7 @@ extern "C" int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int
     if (cascade)
         for (int32_t s = 0; s < cascade->num_spans; ++s)
             span_run.push_back(add_run(cascade->span_req[s], cascade->span_start[s], cascade->span_len[s]));
+    if (ctx) nkeys = ctx_rows;  // keys are rows of the caller's context arrays
     // segments per request: (run, keys used), in context order.  The last shared span is cut
     // to a multiple of the 128-key tile and its remainder joins the request's own gathered
     // tail, so no key tile is spent on a few leftover span keys.
@@ -526,7 +546,10 @@ extern "C" int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int
     std::vector<std::vector<Seg>> segs_of(batch);
     for (int32_t r = 0; r < batch; ++r) {
         const int32_t ns = (int32_t)spans_of[r].size();
-        if (ns + 1 <= kMaxSegs) {
+        if (ctx) {
+            runs.push_back({r, 0, seq_lens[r], ctx_row0[r]});
+            segs_of[r].push_back({(int32_t)runs.size() - 1, seq_lens[r]});
+        } else if (ns + 1 <= kMaxSegs) {
             int32_t rem = 0;
             for (int32_t k = 0; k < ns; ++k) {
                 const int32_t sp = spans_of[r][k];
@@ -546,8 +569,16 @@ extern "C" int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int
     if (nkeys >= ((int64_t)1 << 31)) return PKV_E_UNSUPPORTED;
     std::vector<GatherUnit> units;
     const int32_t uk = gather_unit_keys(nkeys, num_sms);
-    for (const Run &R : runs)
-        for (int32_t c = 0; c < R.len; c += uk) units.push_back({R.src, R.pos0 + c, std::min(uk, R.len - c), R.key0 + c});
+    if (!ctx)
+        for (const Run &R : runs)
+            for (int32_t c = 0; c < R.len; c += uk)
+                units.push_back({R.src, R.pos0 + c, std::min(uk, R.len - c), R.key0 + c});
+    // context-buffer plans: the row of every new token (in q order), written by the store
+    std::vector<int32_t> tok_row;
+    if (ctx)
+        for (int32_t r = 0; r < batch; ++r)
+            for (int32_t i = 0; i < extend_lens[r]; ++i)
+                tok_row.push_back(ctx_row0[r] + seq_lens[r] - extend_lens[r] + i);
 
     // items: up to 2 x 128/G query tokens of one request x one KV head, over its segments;
     // the last segment is cut at the last query token's position (causal)
@@ -708,6 +739,8 @@ extern "C" int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int
     info->offsets[12] = nctas_x;
     info->offsets[13] = (int64_t)off; off = align16(off + packs.size() * sizeof(PackInfo));
     info->offsets[14] = (int64_t)packs.size();
+    info->offsets[15] = (int64_t)off; off = align16(off + tok_row.size() * sizeof(int32_t));
+    info->offsets[16] = ctx ? 1 : 0;
     std::vector<uint8_t> blob(std::max<size_t>(off, 16), 0);
     put(blob, (size_t)info->offsets[0], placed);
     put(blob, (size_t)info->offsets[13], packs);
@@ -715,8 +748,27 @@ extern "C" int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int
     put(blob, (size_t)info->offsets[11], cta_off_x);
     put(blob, (size_t)info->offsets[3], merges);
     put(blob, (size_t)info->offsets[4], units);
+    put(blob, (size_t)info->offsets[15], tok_row);
     const size_t rec_bytes = (size_t)info->num_records * num_q_heads * (head_dim + 2) * 4;
     info->workspace_bytes = kHeader + ((rec_bytes + 255) & ~size_t(255)) +
-                            2 * (size_t)nkeys * num_kv_heads * head_dim * 2;
+                            (ctx ? 0 : 2 * (size_t)nkeys * num_kv_heads * head_dim * 2);
     return emit(blob, plan, plan_cap, info);
+}
+
+extern "C" int pkv_plan_extend(int32_t batch, const int32_t *seq_lens, const int32_t *extend_lens,
+                               const int32_t *qo_indptr, int32_t num_q_heads, int32_t num_kv_heads,
+                               int32_t head_dim, const pkv_cascade *cascade, const pkv_plan_opts *opts,
+                               void *plan, size_t plan_cap, pkv_plan_info *info) {
+    return plan_extend_impl(batch, seq_lens, extend_lens, qo_indptr, num_q_heads, num_kv_heads, head_dim, cascade,
+                            opts, nullptr, 0, plan, plan_cap, info);
+}
+
+extern "C" int pkv_plan_extend_ctx(int32_t batch, const int32_t *seq_lens, const int32_t *extend_lens,
+                                   const int32_t *qo_indptr, const int32_t *ctx_row0, int64_t ctx_rows,
+                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   const pkv_plan_opts *opts, void *plan, size_t plan_cap, pkv_plan_info *info) {
+    if (!ctx_row0 && batch > 0) return PKV_E_INVALID;
+    static const int32_t none = 0;
+    return plan_extend_impl(batch, seq_lens, extend_lens, qo_indptr, num_q_heads, num_kv_heads, head_dim, nullptr,
+                            opts, ctx_row0 ? ctx_row0 : &none, ctx_rows, plan, plan_cap, info);
 }

@@ -20,8 +20,8 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-from . import (Allocator, Batch, Pool, RadixTree, attn_decode, attn_extend, check_out_cache_loc, kv_store, plan_decode,
-               plan_extend)
+from . import (Allocator, Batch, Pool, RadixTree, attn_decode, attn_extend, attn_extend_ctx, check_out_cache_loc,
+               kv_store, plan_decode, plan_extend, plan_extend_ctx)
 
 
 def _ctx_tokens(w, req):
@@ -70,15 +70,19 @@ class Call:
     contexts: list = field(default_factory=list)   # per request: (tokens, req_to_token row, cached length)
     requests: list = field(default_factory=list)
     graph: object = None                           # captured attention launches (capture_attend)
+    ctx: tuple = None                              # (ctx_k, ctx_v): a chunk over a context buffer
 
     @property
     def num_queries(self) -> int:
         return int(self.q.shape[0])
 
-    def layer(self, pool: Pool, w) -> "Call":
+    def layer(self, pool: Pool, w, ctx=None) -> "Call":
         """The same call for another layer of the model: that layer's pool, and its queries and
         new K/V rows from ``w`` (a workload of the same structure whose requests match this
-        call's one for one).  Tables, plan and slots are shared by all layers."""
+        call's one for one).  Tables, plan and slots are shared by all layers; a chunk over a
+        context buffer takes that layer's context arrays ``ctx`` = (ctx_k, ctx_v)."""
+        if (self.ctx is None) != (ctx is None):
+            raise ValueError("a context-buffer call needs the layer's context arrays (and only it does)")
         reqs = [w.requests[r.rid] for r in self.requests]
         kn, vn = [], []
         for r, (_, row, cached) in zip(reqs, self.contexts):
@@ -90,12 +94,18 @@ class Call:
         return Call(self.kind, pool, self.batch, self.plan, self.plan_dev, torch.zeros_like(self.workspace), q,
                     torch.empty_like(q), self.out_cache_loc, _bf16_dev(np.concatenate(kn), dev),
                     _bf16_dev(np.concatenate(vn), dev), w.sm_scale, self.last_nodes, cascade=self.cascade,
-                    contexts=self.contexts, requests=reqs)
+                    contexts=self.contexts, requests=reqs, ctx=ctx)
 
     def store(self, stream=None):
+        if self.ctx is not None:
+            return  # a chunk over a context buffer stores inside its attention call
         kv_store(self.pool, self.k_new, self.v_new, self.out_cache_loc, self.workspace, stream)
 
     def attend(self, stream=None):
+        if self.ctx is not None:
+            attn_extend_ctx(self.pool, self.q, self.o, self.sm_scale, self.k_new, self.v_new, self.out_cache_loc,
+                            self.ctx[0], self.ctx[1], self.plan, self.plan_dev, self.workspace, stream)
+            return
         f = attn_extend if self.kind == "extend" else attn_decode
         f(self.pool, self.batch, self.q, self.o, self.sm_scale, self.plan, self.plan_dev, self.workspace, stream)
 
@@ -125,7 +135,11 @@ class Call:
         """Kernels one run() launches: the store, then the attention call's kernels."""
         info = self.plan.info
         n = 1 if self.out_cache_loc.numel() > 0 else 0
-        if self.kind == "extend":
+        if self.ctx is not None:                                 # store (with the context rows),
+            n = 1 if self.out_cache_loc.numel() > 0 else 0       # then the extend kernel(s)
+            nprec = int(info.offsets[10])
+            n += (1 if info.num_items - nprec > 0 else 0) + (1 if nprec > 0 else 0)
+        elif self.kind == "extend":
             nprec = int(info.offsets[10])                        # items with precise weights
             n += (1 if info.offsets[5] > 0 else 0)               # key gather
             n += (1 if info.num_items - nprec > 0 else 0) + (1 if nprec > 0 else 0)  # extend kernel(s)
@@ -184,7 +198,8 @@ class Call:
             c = Call(self.kind, self.pool, batch, self.plan, torch.empty_like(self.plan_dev), self.workspace,
                      torch.empty_like(self.q), torch.empty_like(self.o), torch.empty_like(self.out_cache_loc),
                      torch.empty_like(self.k_new), torch.empty_like(self.v_new), self.sm_scale, self.last_nodes,
-                     host=self.host, cascade=self.cascade, contexts=self.contexts, requests=self.requests)
+                     host=self.host, cascade=self.cascade, contexts=self.contexts, requests=self.requests,
+                     ctx=self.ctx)
             out.append(c)
         return out
 
@@ -337,7 +352,7 @@ class PrefixCache:
         kv_store(self.pool, k, v, loc, self.err)
 
     # ---- one attention call of a step
-    def _plan_host(self, kind, cascade, opts, min_group, requests):
+    def _plan_host(self, kind, cascade, opts, min_group, requests, ctx_base=None):
         """The host half of one call: match every request's cached part in the tree (it must hit
         completely) and lock its path, allocate slots for the new tokens, build the batch table,
         extract the cascade and plan the kernels.  Returns a dict of host arrays."""
@@ -367,7 +382,12 @@ class PrefixCache:
         if casc is not None and casc.num_spans == 0:
             casc = None
         hq, hkv, d = w.num_q_heads, w.num_kv_heads, w.head_dim
-        if kind == "extend":
+        if ctx_base is not None:   # chunks over a context buffer: rows by prompt, no cascade
+            casc = None
+            qo = np.concatenate([[0], np.cumsum(ext)]).astype(np.int32)
+            row0 = [ctx_base["row0"][r.path[0]] for r in reqs]
+            plan = plan_extend_ctx(seq, ext, qo, row0, ctx_base["rows"], hq, hkv, d, opts)
+        elif kind == "extend":
             qo = np.concatenate([[0], np.cumsum(ext)]).astype(np.int32)
             plan = plan_extend(seq, ext, qo, hq, hkv, d, casc, opts)
         else:
@@ -402,10 +422,11 @@ class PrefixCache:
                 self.tree.dec_lock_ref(n)
         return 1e3 * float(np.mean(ts))
 
-    def prepare(self, kind, cascade=True, opts=None, min_group=2, requests=None) -> Call:
-        """One attention call over the workload's requests of ``kind`` (or the given subset)."""
+    def prepare(self, kind, cascade=True, opts=None, min_group=2, requests=None, ctx=None) -> Call:
+        """One attention call over the workload's requests of ``kind`` (or the given subset).
+        ``ctx`` (from :meth:`context_buffer`): an extend chunk over that context buffer."""
         w = self.w
-        h = self._plan_host(kind, cascade, opts, min_group, requests)
+        h = self._plan_host(kind, cascade, opts, min_group, requests, ctx_base=ctx)
         reqs, rows, plan = h["reqs"], h["rows"], h["plan"]
         kn, vn = [], []
         for r, row in zip(reqs, rows):
@@ -424,7 +445,8 @@ class PrefixCache:
         k_new = _bf16_dev(np.concatenate(kn), dev)
         v_new = _bf16_dev(np.concatenate(vn), dev)
         call = Call(kind, self.pool, batch, plan, plan_dev, ws, q, o, loc, k_new, v_new, w.sm_scale,
-                    h["last_nodes"], cascade=h["cascade"])
+                    h["last_nodes"], cascade=h["cascade"],
+                    ctx=None if ctx is None else (ctx["k"], ctx["v"]))
         call.contexts = [(_ctx_tokens(w, r), row, len(row) - r.n_new) for r, row in zip(reqs, rows)]
         call.requests = reqs
         return call
@@ -433,16 +455,35 @@ class PrefixCache:
         for n in call.last_nodes:
             self.tree.dec_lock_ref(n)
 
-    def prepare_chunked(self, opts=None) -> list:
+    def context_buffer(self):
+        """Context arrays for chunked prefill: one run of rows per prompt (the requests under one
+        root segment), as long as its longest context; bf16 [rows, Hkv, d] for K and for V."""
+        w = self.w
+        length = {}
+        for r in w.requests:
+            length[r.path[0]] = max(length.get(r.path[0], 0), w.context_len(r))
+        row0, rows = {}, 0
+        for root in sorted(length):
+            row0[root] = rows
+            rows += length[root]
+        k = torch.zeros((max(rows, 1), w.num_kv_heads, w.head_dim), dtype=torch.bfloat16, device=self.device)
+        return {"k": k, "v": torch.zeros_like(k), "row0": row0, "rows": max(rows, 1)}
+
+    def prepare_chunked(self, opts=None, fused=True) -> list:
         """Chunked prefill of a workload whose ``meta["chunk"]`` numbers each extend request's
         step: one call per step, planned over the chunks the earlier steps cached.  The tree
         learns each step's tokens when the step is planned (host only), so all the calls can be
-        planned ahead; run them in order."""
+        planned ahead; run them in order.  ``fused``: every call stores its chunk into the pool
+        and into a context buffer shared by the calls, and attends over that buffer (nothing
+        is gathered); else each call's store is separate and its attention gathers the whole
+        context from the pool."""
         steps = self.w.meta["chunk"]
+        ctx = self.context_buffer() if fused else None
+        self.ctx = ctx
         calls = []
         for c in sorted(set(steps)):
             reqs = [r for r, k in zip(self.w.requests, steps) if k == c]
-            call = self.prepare("extend", opts=opts, requests=reqs)
+            call = self.prepare("extend", opts=opts, requests=reqs, ctx=ctx)
             self.commit(call)
             calls.append(call)
         return calls

@@ -40,42 +40,96 @@ def _check(w, call, tol=1e-2):
     assert err <= tol, err
 
 
+def _check_pool_and_context(w, pc):
+    """Every prompt's pool rows equal the oracle's store of its K/V, bit for bit; with a
+    context buffer, the prompt's context rows hold exactly the values the pool holds (bf16
+    bits, or the fp8 code converted to bf16)."""
+    from oracle.fp8 import e4m3_decode, quantize_to_pool
+    last = {}
+    for r in w.requests:
+        if r.path[0] not in last or w.context_len(r) > w.context_len(last[r.path[0]]):
+            last[r.path[0]] = r
+    for root, r in last.items():
+        toks = W.context_tokens(w, r)
+        vals, _ = pc.tree.match_prefix(toks)
+        assert len(vals) == len(toks)
+        kb, vb = W.context_kv_bits(w, r)
+        idx = torch.from_numpy(vals.astype(np.int64)).cuda()
+        for pool_t, bits, scale, name in ((pc.pool.k, kb, w.k_scale, "k"), (pc.pool.v, vb, w.v_scale, "v")):
+            got = pool_t[idx].cpu()
+            if w.dtype == "bf16":
+                want_pool = bits
+                assert np.array_equal(got.view(torch.int16).numpy().view(np.uint16), want_pool)
+                want_ctx = want_pool
+            else:
+                codes = quantize_to_pool(W.bf16_bits_to_f64(bits), scale)
+                assert np.array_equal(got.numpy(), codes)
+                # every e4m3 value is a bf16 value: the cast is exact
+                want_ctx = torch.from_numpy(e4m3_decode(codes).astype(np.float32)).to(torch.bfloat16) \
+                    .view(torch.int16).numpy().view(np.uint16)
+            if pc.ctx is not None:
+                r0 = pc.ctx["row0"][root]
+                ctx = pc.ctx[name][r0:r0 + len(toks)].cpu().view(torch.int16).numpy().view(np.uint16)
+                assert np.array_equal(ctx, want_ctx), name
+
+
+@pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("prompt,chunk", [(1000, 256), (700, 700), (513, 128)])
-def test_chunked_prefill_matches_oracle(prompt, chunk):
+def test_chunked_prefill_matches_oracle(prompt, chunk, fused):
     from prefix_shared_kv_token_gb300.runtime import PrefixCache
     w = W.chunked_prefill(seed=61, n_req=3, prompt=prompt, chunk=chunk, num_slots=8000)
     pc = PrefixCache(w)
-    calls = pc.prepare_chunked()
+    calls = pc.prepare_chunked(fused=fused)
     assert len(calls) == -(-prompt // chunk)
+    assert all((c.ctx is not None) == fused for c in calls)
     _run(calls)
     for c in calls:
         _check(w, c)
-    # the whole prompts are cached afterwards
+    # the whole prompts are cached afterwards, in the pool and (fused) in the context buffer
     for r in w.requests:
         if w.meta["chunk"][r.rid] == len(calls) - 1:
             vals, _ = pc.tree.match_prefix(W.context_tokens(w, r))
             assert len(vals) == prompt
+    _check_pool_and_context(w, pc)
 
 
-def test_chunked_prefill_fp8():
+@pytest.mark.parametrize("fused", [True, False])
+def test_chunked_prefill_fp8(fused):
     from prefix_shared_kv_token_gb300.runtime import PrefixCache
     w = W.chunked_prefill(seed=63, n_req=2, prompt=600, chunk=200, num_slots=4000, dtype="fp8_e4m3")
     pc = PrefixCache(w)
-    calls = pc.prepare_chunked()
+    calls = pc.prepare_chunked(fused=fused)
     _run(calls)
     for c in calls:
         _check(w, c, tol=5e-2)
+    _check_pool_and_context(w, pc)
 
 
-def test_multi_layer_pools_share_tables_and_plan():
+def test_fused_chunk_reports_a_bad_slot_without_writing():
+    import prefix_shared_kv_token_gb300 as pkv
+    from prefix_shared_kv_token_gb300.runtime import PrefixCache
+    w = W.chunked_prefill(seed=64, n_req=1, prompt=300, chunk=150, num_slots=2000)
+    pc = PrefixCache(w)
+    calls = pc.prepare_chunked(fused=True)
+    c = calls[0]
+    c.out_cache_loc[3] = w.num_slots + 5          # host-made bad slot: skipped and reported
+    c.attend()
+    torch.cuda.synchronize()
+    assert pkv.get_device_error(c.workspace) & 0x100
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_multi_layer_pools_share_tables_and_plan(fused):
     from prefix_shared_kv_token_gb300 import Pool
     from prefix_shared_kv_token_gb300.runtime import PrefixCache
     layers = [W.chunked_prefill(seed=70 + l, n_req=2, prompt=500, chunk=250, num_slots=3000) for l in range(3)]
     pc = PrefixCache(layers[0])
-    base = pc.prepare_chunked()
+    base = pc.prepare_chunked(fused=fused)
     pools = [pc.pool] + [Pool.allocate(w.num_slots, w.num_kv_heads, w.head_dim, w.dtype, w.k_scale, w.v_scale, "cuda")
                          for w in layers[1:]]
-    per_layer = [[c if l == 0 else c.layer(pools[l], layers[l]) for c in base] for l in range(3)]
+    # each layer keeps its own context arrays (fused), shared by that layer's chunks
+    ctxs = [None if not fused else (torch.zeros_like(pc.ctx["k"]), torch.zeros_like(pc.ctx["v"])) for _ in layers]
+    per_layer = [[c if l == 0 else c.layer(pools[l], layers[l], ctx=ctxs[l]) for c in base] for l in range(3)]
     for step in range(len(base)):                  # a forward pass: every layer, step by step
         _run([per_layer[l][step] for l in range(3)])
     for l in range(3):

@@ -14,6 +14,7 @@ written.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl ours|reference]
                     [--page-size P] [--workload chunked_prefill|serving] [--no-graph] [--no-cascade]
                     [--no-cpu-baseline] [--no-more-configs] [--pool-slots S] [--chunked-gather]
+                    [--kv-layout interleaved|separate]
 
 The default run (few-shot extend, configuration 2) also measures the decode workloads and the
 mixed fp8 step (configurations 3-5) after the headline and reports them under
@@ -264,7 +265,7 @@ def measure(w, args, dev, steps, world, e2e=True):
     from prefix_shared_kv_token_gb300.runtime import PrefixCache, run_e2e_pipelined
 
     facts = workload_facts(w)
-    pc = PrefixCache(w, device=str(dev), page_size=args.page_size)
+    pc = PrefixCache(w, device=str(dev), page_size=args.page_size, kv_layout=args.kv_layout)
     if w.name == "chunked_prefill":
         # one extend call per chunk, over the chunks before it: stored with its chunk and read
         # from a context buffer (default), or stored separately and gathered from the pool
@@ -463,7 +464,8 @@ def run_ours(args, rank, world):
     m, calls = measure(w, args, dev, args.steps, world, e2e=True)
     cfg = {"workload": w.name, "config_id": None if args.workload else args.config, "requests": len(w.requests),
            "heads_q_kv": f"{w.num_q_heads}/{w.num_kv_heads}", "head_dim": w.head_dim, "pool_dtype": w.dtype,
-           "pool_slots": w.num_slots, "page_size": args.page_size, "cascade": not args.no_cascade,
+           "pool_slots": w.num_slots, "page_size": args.page_size, "kv_layout": args.kv_layout,
+           "cascade": not args.no_cascade,
            "decode_launch": "plain" if args.no_graph else "CUDA graph replay of the call's launches",
            "l2": "flushed between timed steps (512 MiB write outside the step events)",
            "tokens_per_step": m["tokens_per_step"]}
@@ -650,6 +652,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cascade", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv-layout", default="interleaved", choices=["interleaved", "separate"],
+                    help="pool layout: a slot's K and V rows adjacent (default) or two dense arrays")
     ap.add_argument("--chunked-gather", action="store_true",
                     help="chunked_prefill: separate stores and a gather of the whole context per chunk "
                          "(instead of chunks stored into and read from a context buffer)")

@@ -66,14 +66,21 @@ int pkv_version(void);  /* major*10000 + minor*100 + patch */
 typedef enum { PKV_BF16 = 0, PKV_FP8_E4M3 = 1 } pkv_dtype;
 
 typedef struct pkv_pool {
-    void   *k;             /* device, [num_slots][num_kv_heads][head_dim] elements        */
-    void   *v;             /* device, same layout; bf16 (2 B) or e4m3 (1 B) elements      */
+    void   *k;             /* device, slot s's K row of [num_kv_heads][head_dim] elements at */
+                           /* element s * slot_stride                                       */
+    void   *v;             /* device, the same for V; bf16 (2 B) or e4m3 (1 B) elements     */
     int64_t num_slots;     /* num_slots * num_kv_heads must be < 2^31                     */
     int32_t num_kv_heads;
     int32_t head_dim;      /* 64 or 128                                                   */
     int32_t dtype;         /* pkv_dtype                                                   */
     float   k_scale;       /* fp8 only: stored code = e4m3(x / k_scale), value = code*k_scale */
     float   v_scale;
+    /* Elements from one slot's row to the next, in k and in v; 0 means num_kv_heads *
+     * head_dim (two dense arrays).  2 * num_kv_heads * head_dim with v = k + num_kv_heads *
+     * head_dim is the interleaved layout [num_slots][K row | V row]: a slot's K and V are one
+     * contiguous run, which decode reads with a single copy per key.  The stride in bytes
+     * must be a multiple of 16. */
+    int64_t slot_stride;
 } pkv_pool;
 
 /* ------------------------------------------------------------------------------------ */

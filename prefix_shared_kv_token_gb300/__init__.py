@@ -68,7 +68,9 @@ def _i32(a) -> np.ndarray:
 @dataclass
 class Pool:
     """Device KV pool: k, v are torch tensors [num_slots, num_kv_heads, head_dim] of bfloat16
-    (dtype 'bf16') or uint8 holding e4m3 codes (dtype 'fp8_e4m3')."""
+    (dtype 'bf16') or uint8 holding e4m3 codes (dtype 'fp8_e4m3') -- two dense arrays, or
+    (layout 'interleaved') the K and V halves of one [num_slots, 2, num_kv_heads, head_dim]
+    array, so a slot's K and V rows are one contiguous run."""
     k: object
     v: object
     dtype: str = "bf16"
@@ -76,20 +78,33 @@ class Pool:
     v_scale: float = 1.0
 
     @classmethod
-    def allocate(cls, num_slots, num_kv_heads, head_dim, dtype="bf16", k_scale=1.0, v_scale=1.0, device="cuda"):
+    def allocate(cls, num_slots, num_kv_heads, head_dim, dtype="bf16", k_scale=1.0, v_scale=1.0, device="cuda",
+                 layout="separate"):
         import torch
         tdt = torch.bfloat16 if dtype == "bf16" else torch.uint8
-        k = torch.zeros((num_slots, num_kv_heads, head_dim), dtype=tdt, device=device)
-        v = torch.zeros_like(k)
+        if layout == "interleaved":
+            kv = torch.zeros((num_slots, 2, num_kv_heads, head_dim), dtype=tdt, device=device)
+            k, v = kv[:, 0], kv[:, 1]
+        elif layout == "separate":
+            k = torch.zeros((num_slots, num_kv_heads, head_dim), dtype=tdt, device=device)
+            v = torch.zeros_like(k)
+        else:
+            raise ValueError(f"unknown pool layout {layout!r}")
         return cls(k, v, dtype, float(k_scale), float(v_scale))
 
     @property
     def num_slots(self):
         return self.k.shape[0]
 
+    @property
+    def layout(self) -> str:
+        return "separate" if self.k.stride(0) == self.k.shape[1] * self.k.shape[2] else "interleaved"
+
     def c(self) -> PkvPool:
+        assert self.k.stride(0) == self.v.stride(0) and self.k.stride(1) == self.k.shape[2] and self.k.stride(2) == 1
         return PkvPool(_ptr(self.k), _ptr(self.v), self.k.shape[0], self.k.shape[1], self.k.shape[2],
-                       PKV_BF16 if self.dtype == "bf16" else PKV_FP8_E4M3, self.k_scale, self.v_scale)
+                       PKV_BF16 if self.dtype == "bf16" else PKV_FP8_E4M3, self.k_scale, self.v_scale,
+                       int(self.k.stride(0)))
 
 
 @dataclass

@@ -25,7 +25,8 @@ ERRORS = {
 
 class PkvPool(C.Structure):
     _fields_ = [("k", C.c_void_p), ("v", C.c_void_p), ("num_slots", C.c_int64), ("num_kv_heads", C.c_int32),
-                ("head_dim", C.c_int32), ("dtype", C.c_int32), ("k_scale", C.c_float), ("v_scale", C.c_float)]
+                ("head_dim", C.c_int32), ("dtype", C.c_int32), ("k_scale", C.c_float), ("v_scale", C.c_float),
+                ("slot_stride", C.c_int64)]
 
 
 class PkvBatch(C.Structure):

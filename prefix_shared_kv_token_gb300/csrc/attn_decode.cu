@@ -61,6 +61,8 @@ struct DecodeParams {
     const int32_t *cta_off;  // items of CTA b: [cta_off[b], cta_off[b + 1])
     const int32_t *row_req;
     const int32_t *row_rec;
+    int64_t slot_bytes;  // from one slot's pool row to the next
+    int32_t joint;       // one copy per key brings its K and V rows (interleaved pool, hg == hkv)
     float *rec_acc;     // [rec][hq][D]
     float *rec_ml;      // [rec][hq][2]
     int32_t *err;
@@ -84,21 +86,32 @@ constexpr int32_t kFirst = 1, kLast = 2, kEnd = 4;
 // 32 (mod 128) bytes, V rows at 16 (mod 128), so the 8-byte K fragment loads and the
 // 16-byte ldmatrix.trans rows of a warp hit distinct banks.  fp8: raw rows of hg * D codes;
 // each consumer warp converts its head into a private bf16 tile with those strides.
+// Joint layout (an interleaved pool read by a head group that covers every KV head): each
+// key's K row and V row arrive together by one copy, [K row | V row] at a stride of 2 rowb + 32
+// (bf16: the K loads stay conflict-free; the V rows share that stride).
 template <int D, bool FP8>
 struct DGeo {
     static constexpr int kStages = FP8 ? 4 : 3;
     static constexpr int kConvK = 2 * D + 32, kConvV = 2 * D + 16;
     static constexpr int kConvBytes = kBK * (kConvK + kConvV);  // per consumer warp
-    int rowb;   // pool bytes of one key's head-group row, per tensor
-    int sk, sv; // stage row strides
-    int stage;  // bytes per stage
-    int conv;   // offset of the conversion tiles (fp8)
-    int bytes;  // dynamic shared memory
-    __host__ __device__ explicit DGeo(int hg) {
+    int rowb;     // pool bytes of one key's head-group row, per tensor
+    int kstride;  // stage offset of key j's K row: j * kstride
+    int vbase, vstride;  // of key j's V row: vbase + j * vstride
+    int stage;    // bytes per stage
+    int conv;     // offset of the conversion tiles (fp8)
+    int bytes;    // dynamic shared memory
+    __host__ __device__ DGeo(int hg, bool joint) {
         rowb = hg * D * (FP8 ? 1 : 2);
-        sk = FP8 ? rowb : rowb + 32;
-        sv = FP8 ? rowb : rowb + 16;
-        stage = kBK * (sk + sv);
+        if (joint) {
+            kstride = vstride = 2 * rowb + (FP8 ? 0 : 32);
+            vbase = rowb;
+            stage = kBK * kstride;
+        } else {
+            kstride = FP8 ? rowb : rowb + 32;
+            vstride = FP8 ? rowb : rowb + 16;
+            vbase = kBK * kstride;
+            stage = kBK * (kstride + vstride);
+        }
         conv = kHdr + kStages * stage;
         bytes = conv + (FP8 ? hg * kConvBytes : 0);
     }
@@ -160,7 +173,7 @@ PKV_DEV void load_rows(const DecodeParams &p, int item, int w, ItemRows<D, G> &x
 
 // fp8: convert this warp's head (codes at column `col` of each raw row) into its bf16 tiles.
 template <int D>
-PKV_DEV void convert_head(const uint8_t *raw, int rowb, int col, uint8_t *conv) {
+PKV_DEV void convert_head(const uint8_t *raw, const DGeo<D, true> &geo, int col, uint8_t *conv) {
     using Gm = DGeo<D, true>;
     const int lane = threadIdx.x & 31;
     constexpr int kChunks = kBK * D / 16;  // 16 codes per chunk, per tensor
@@ -168,7 +181,8 @@ PKV_DEV void convert_head(const uint8_t *raw, int rowb, int col, uint8_t *conv) 
     for (int i = lane; i < 2 * kChunks; i += 32) {
         const int tensor = i >= kChunks, ci = i - tensor * kChunks;
         const int key = ci / (D / 16), cc = ci % (D / 16);
-        const uint4 x = *reinterpret_cast<const uint4 *>(raw + (tensor * kBK + key) * rowb + col + cc * 16);
+        const int row = tensor ? geo.vbase + key * geo.vstride : key * geo.kstride;
+        const uint4 x = *reinterpret_cast<const uint4 *>(raw + row + col + cc * 16);
         const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
         uint32_t y[8];
 #pragma unroll
@@ -328,7 +342,7 @@ __global__ void __launch_bounds__(288, (D == 64 ? 2 : 1)) decode_kernel(const De
     int32_t *abort_flag = reinterpret_cast<int32_t *>(smem + 64);
     TileInfo *tinfo = reinterpret_cast<TileInfo *>(smem + 128);
     uint8_t *ring = smem + kHdr;
-    const Gm geo(p.hg);
+    const Gm geo(p.hg, p.joint != 0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_wait();     // the query tokens' K/V were stored, and the span gather ran, just before
     pdl_trigger();  // the span pass may take SMs as this kernel's CTAs finish
@@ -346,11 +360,15 @@ __global__ void __launch_bounds__(288, (D == 64 ? 2 : 1)) decode_kernel(const De
 
     if (warp == p.hg) {
         // ------------------------------------------------------------------ producer warp
-        // lanes 0-15: K row of key `lane` of the tile; lanes 16-31: V row of key `lane - 16`
+        // lanes 0-15: K row of key `lane` of the tile; lanes 16-31: V row of key `lane - 16`.
+        // Joint layout: lanes 0-15 each bring key `lane`'s K and V rows with one copy.
         const int key = lane & 15;
-        const bool is_v = lane >= 16;
+        const bool joint = p.joint != 0;
+        const bool is_v = !joint && lane >= 16;
+        const bool issuer = !joint || lane < 16;
         const uint8_t *pool = is_v ? p.v_pool : p.k_pool;
         const int64_t head_bytes = (int64_t)D * (FP8 ? 1 : 2);
+        const uint32_t copy_bytes = (uint32_t)geo.rowb * (joint ? 2u : 1u);
         // the slots of the next 4 tiles are in flight while the current tile is issued
         TileCursor cur;
         cur.i = c0 - 1;
@@ -372,26 +390,27 @@ __global__ void __launch_bounds__(288, (D == 64 ? 2 : 1)) decode_kernel(const De
                 break;
             }
             const int kp = e0.info.kpos + key;
-            const bool in = kp < e0.info.k1;
+            const bool in = issuer && kp < e0.info.k1;
             const bool valid = in && e0.slot >= 0 && (int64_t)e0.slot < p.num_slots;
             if (in && !valid) set_error(p.err, DERR_SLOT_RANGE);
-            uint8_t *dst = ring + s * geo.stage + (is_v ? kBK * geo.sk + key * geo.sv : key * geo.sk);
+            uint8_t *dst = ring + s * geo.stage + (is_v ? geo.vbase + key * geo.vstride : key * geo.kstride);
             // no copy: a V row past the item's end, or either row of a bad slot, reads as zeros
-            // (keys past the end are masked, so their K rows are left as they are)
-            if (!valid && (in || is_v)) {
-                for (int b = 0; b < geo.rowb; b += 16) *reinterpret_cast<uint4 *>(dst + b) = make_uint4(0u, 0u, 0u, 0u);
+            // (keys past the end are masked, so their K rows are left as they are; in the joint
+            // layout the K row past the end is cleared with its V row)
+            if (issuer && !valid && (in || is_v || joint)) {
+                for (uint32_t b = 0; b < copy_bytes; b += 16) *reinterpret_cast<uint4 *>(dst + b) = make_uint4(0u, 0u, 0u, 0u);
                 fence_proxy_async_smem();  // a later bulk copy rewrites this row
             }
             const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
             __syncwarp();
             if (lane == 0) {
                 tinfo[s] = e0.info;
-                mbar_arrive_expect_tx(&full[s], nvalid * (uint32_t)geo.rowb);
+                mbar_arrive_expect_tx(&full[s], nvalid * copy_bytes);
             }
             __syncwarp();
             if (valid)
-                bulk_copy_g2s(smem_u32(dst), pool + ((int64_t)e0.slot * p.hkv + e0.g0) * head_bytes, (uint32_t)geo.rowb,
-                              &full[s]);
+                bulk_copy_g2s(smem_u32(dst), pool + (int64_t)e0.slot * p.slot_bytes + (int64_t)e0.g0 * head_bytes,
+                              copy_bytes, &full[s]);
             e0 = e1;
             e1 = e2;
             e2 = e3;
@@ -443,14 +462,14 @@ __global__ void __launch_bounds__(288, (D == 64 ? 2 : 1)) decode_kernel(const De
         }
         const uint8_t *stage = ring + s * geo.stage;
         if constexpr (FP8) {
-            convert_head<D>(stage, geo.rowb, w * D, conv);
+            convert_head<D>(stage, geo, w * D, conv);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
             tile16<D>(st, cur.qf, conv, Gm::kConvK, conv + kBK * Gm::kConvK, Gm::kConvV, ti.kpos, ti.k1, p.scale_log2);
             __syncwarp();  // the conversion tiles are rewritten for the next tile
         } else {
             const int col = w * D * 2;
-            tile16<D>(st, cur.qf, stage + col, geo.sk, stage + kBK * geo.sk + col, geo.sv, ti.kpos, ti.k1,
+            tile16<D>(st, cur.qf, stage + col, geo.kstride, stage + geo.vbase + col, geo.vstride, ti.kpos, ti.k1,
                       p.scale_log2);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
@@ -551,7 +570,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeItem *__restrict_
 
 template <int D, int G, bool FP8>
 static int launch_decode(const DecodeParams &p, int nctas, cudaStream_t s) {
-    const DGeo<D, FP8> geo(p.hg);
+    const DGeo<D, FP8> geo(p.hg, p.joint != 0);
     auto kern = p.wait.quick ? decode_kernel<D, G, FP8, true> : decode_kernel<D, G, FP8, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, geo.bytes) != cudaSuccess)
         return PKV_E_CUDA;
@@ -636,6 +655,8 @@ extern "C" int pkv_attn_decode(const pkv_pool *pool, const pkv_batch *batch, con
     p.cta_off = reinterpret_cast<const int32_t *>(plan + info->offsets[SEC_CTA_OFF]);
     p.row_req = reinterpret_cast<const int32_t *>(plan + info->offsets[SEC_ROW_REQ]);
     p.row_rec = reinterpret_cast<const int32_t *>(plan + info->offsets[SEC_ROW_REC]);
+    p.slot_bytes = slot_bytes(pool);
+    p.joint = kv_interleaved(pool) && hg == pool->num_kv_heads ? 1 : 0;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     p.err = reinterpret_cast<int32_t *>(ws);
     p.wait = wait_policy(wait_limit_ns());

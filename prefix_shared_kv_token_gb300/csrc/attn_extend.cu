@@ -119,6 +119,7 @@ PKV_DEV bool xwait(uint64_t *bar, uint32_t parity, XBars *b, int32_t *err, int w
 struct GatherParams {
     const uint8_t *k_pool;
     const uint8_t *v_pool;
+    int64_t slot_bytes;  // from one slot's row to the next
     int64_t num_slots;
     int32_t hkv;
     const int32_t *req_to_token;
@@ -193,9 +194,9 @@ __global__ void __launch_bounds__(256) gather_kernel(const GatherParams p) {
             if (slot < 0) continue;
             const uint8_t *pool = tensor ? p.v_pool : p.k_pool;
             if constexpr (!FP8) {
-                y[k] = __ldg(reinterpret_cast<const uint4 *>(pool + (int64_t)slot * elems * 2) + v);
+                y[k] = __ldg(reinterpret_cast<const uint4 *>(pool + (int64_t)slot * p.slot_bytes) + v);
             } else {
-                const uint2 x = __ldg(reinterpret_cast<const uint2 *>(pool + (int64_t)slot * elems) + v);
+                const uint2 x = __ldg(reinterpret_cast<const uint2 *>(pool + (int64_t)slot * p.slot_bytes) + v);
                 y[k].x = e4m3x2_to_bf16x2((uint16_t)(x.x & 0xFFFFu));
                 y[k].y = e4m3x2_to_bf16x2((uint16_t)(x.x >> 16));
                 y[k].z = e4m3x2_to_bf16x2((uint16_t)(x.y & 0xFFFFu));
@@ -880,6 +881,7 @@ int decode_span_gather(const pkv_pool *pool, const pkv_batch *batch, const void 
     GatherParams gp;
     gp.k_pool = static_cast<const uint8_t *>(pool->k);
     gp.v_pool = static_cast<const uint8_t *>(pool->v);
+    gp.slot_bytes = slot_bytes(pool);
     gp.num_slots = pool->num_slots;
     gp.hkv = hkv;
     gp.req_to_token = batch->req_to_token;
@@ -1031,6 +1033,7 @@ extern "C" int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, con
     GatherParams gp;
     gp.k_pool = static_cast<const uint8_t *>(pool->k);
     gp.v_pool = static_cast<const uint8_t *>(pool->v);
+    gp.slot_bytes = slot_bytes(pool);
     gp.num_slots = pool->num_slots;
     gp.hkv = hkv;
     gp.req_to_token = batch->req_to_token;

@@ -24,7 +24,8 @@ namespace pkv {
 template <bool FP8, bool CTX>
 __global__ void __launch_bounds__(256) kv_store_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
                                                        const int32_t *__restrict__ loc, int64_t n, int32_t vec_per_row,
-                                                       uint8_t *__restrict__ k_pool, uint8_t *__restrict__ v_pool,
+                                                       int64_t slot_bytes, uint8_t *__restrict__ k_pool,
+                                                       uint8_t *__restrict__ v_pool,
                                                        int64_t num_slots, float k_scale, float v_scale,
                                                        int32_t *__restrict__ err, uint4 *__restrict__ ctx_k,
                                                        uint4 *__restrict__ ctx_v, const int32_t *__restrict__ ctx_row) {
@@ -44,7 +45,7 @@ __global__ void __launch_bounds__(256) kv_store_kernel(const uint4 *__restrict__
             continue;
         }
         const uint4 *src = (is_v ? v_new : k_new) + tok * vec_per_row;
-        uint8_t *pool = is_v ? v_pool : k_pool;
+        uint8_t *pool = (is_v ? v_pool : k_pool) + (int64_t)slot * slot_bytes;
         const float s = is_v ? v_scale : k_scale;
         uint4 *cdst = nullptr;
         if constexpr (CTX) cdst = (is_v ? ctx_v : ctx_k) + (int64_t)__ldg(ctx_row + tok) * vec_per_row;
@@ -58,7 +59,7 @@ __global__ void __launch_bounds__(256) kv_store_kernel(const uint4 *__restrict__
                 const int v = v0 + 32 * k;
                 if (v >= vec_per_row) continue;
                 if constexpr (!FP8) {
-                    reinterpret_cast<uint4 *>(pool)[(int64_t)slot * vec_per_row + v] = x[k];
+                    reinterpret_cast<uint4 *>(pool)[v] = x[k];
                     if constexpr (CTX) cdst[v] = x[k];
                 } else {
                     const uint32_t w[4] = {x[k].x, x[k].y, x[k].z, x[k].w};
@@ -69,7 +70,7 @@ __global__ void __launch_bounds__(256) kv_store_kernel(const uint4 *__restrict__
                     uint2 y;
                     y.x = (uint32_t)c[0] | ((uint32_t)c[1] << 16);
                     y.y = (uint32_t)c[2] | ((uint32_t)c[3] << 16);
-                    reinterpret_cast<uint2 *>(pool)[(int64_t)slot * vec_per_row + v] = y;
+                    reinterpret_cast<uint2 *>(pool)[v] = y;
                     if constexpr (CTX)
                         cdst[v] = make_uint4(e4m3x2_to_bf16x2(c[0]), e4m3x2_to_bf16x2(c[1]), e4m3x2_to_bf16x2(c[2]),
                                              e4m3x2_to_bf16x2(c[3]));
@@ -96,7 +97,7 @@ int launch_store(const pkv_pool *pool, const void *k_new, const void *v_new, con
                     : (ctx ? kv_store_kernel<false, true> : kv_store_kernel<false, false>);
     const cudaError_t e = launch_pdl(kern, dim3((unsigned)blocks), dim3(threads), 0, s,
                                      reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new),
-                                     out_cache_loc, n, vec_per_row, reinterpret_cast<uint8_t *>(pool->k),
+                                     out_cache_loc, n, vec_per_row, slot_bytes(pool), reinterpret_cast<uint8_t *>(pool->k),
                                      reinterpret_cast<uint8_t *>(pool->v), pool->num_slots, fp8 ? pool->k_scale : 1.f,
                                      fp8 ? pool->v_scale : 1.f, reinterpret_cast<int32_t *>(workspace),
                                      reinterpret_cast<uint4 *>(ctx_k), reinterpret_cast<uint4 *>(ctx_v), ctx_row);

@@ -47,9 +47,28 @@ inline int validate_pool(const pkv_pool *p) {
     if (p->head_dim != 64 && p->head_dim != 128) return PKV_E_UNSUPPORTED;
     if (p->dtype != PKV_BF16 && p->dtype != PKV_FP8_E4M3) return PKV_E_UNSUPPORTED;
     if (p->num_slots * (int64_t)p->num_kv_heads >= ((int64_t)1 << 31)) return PKV_E_UNSUPPORTED;
-    if ((reinterpret_cast<uintptr_t>(p->k) | reinterpret_cast<uintptr_t>(p->v)) & 127) return PKV_E_INVALID;
+    // rows start 16-byte aligned (bulk copies and vector loads); the arrays 128-byte aligned
+    // unless interleaved, where v sits one K row after k
+    if (reinterpret_cast<uintptr_t>(p->k) & 127) return PKV_E_INVALID;
+    if (reinterpret_cast<uintptr_t>(p->v) & 15) return PKV_E_INVALID;
+    const int64_t row = (int64_t)p->num_kv_heads * p->head_dim;
+    if (p->slot_stride != 0 && (p->slot_stride < row || ((p->slot_stride * (p->dtype == PKV_BF16 ? 2 : 1)) & 15)))
+        return PKV_E_INVALID;
     if (p->dtype == PKV_FP8_E4M3 && !(p->k_scale > 0.f && p->v_scale > 0.f)) return PKV_E_INVALID;
     return PKV_OK;
+}
+
+// Bytes from one slot's row to the next in the pool's k and v arrays.
+inline int64_t slot_bytes(const pkv_pool *p) {
+    const int64_t stride = p->slot_stride != 0 ? p->slot_stride : (int64_t)p->num_kv_heads * p->head_dim;
+    return stride * (p->dtype == PKV_BF16 ? 2 : 1);
+}
+
+// The interleaved layout [slot][K row | V row]: a slot's K and V rows are one contiguous run.
+inline bool kv_interleaved(const pkv_pool *p) {
+    const int64_t row_bytes = (int64_t)p->num_kv_heads * p->head_dim * (p->dtype == PKV_BF16 ? 2 : 1);
+    return slot_bytes(p) == 2 * row_bytes &&
+           reinterpret_cast<uintptr_t>(p->v) == reinterpret_cast<uintptr_t>(p->k) + (uintptr_t)row_bytes;
 }
 
 // log2 of the batch table's page size (0 for a token table, page_size 0 or 1); -1 when the

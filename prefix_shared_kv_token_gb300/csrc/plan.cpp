@@ -52,6 +52,9 @@ constexpr size_t kHeader = 256;
 // decode: a shared span goes to the tensor-core path from this many member requests and keys
 constexpr int32_t kTensorMinMembers = 12;
 constexpr int32_t kTensorMinKeys = 256;
+// decode: a batch whose contexts are all this short (and that has a CTA per request) gets one
+// item per request and no merge
+constexpr int32_t kFlatMaxLen = 128;
 size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
 // Persistent CTAs: deal items longest-processing-time-first onto the least loaded of nctas
@@ -201,6 +204,24 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
     rc = spans_per_request(cascade, batch, seq_lens, &spans_of, &tail_start);
     if (rc) return rc;
 
+    // A tiny batch -- every context at most kFlatMaxLen keys, a CTA for every request -- is
+    // bound by latency, not bytes: each request becomes one item over its whole context that
+    // writes its output directly (no span items, no records, no merge launch), whatever the
+    // cascade says.  Explicit chunk options keep the general plan.
+    bool flat_plan = false;
+    {
+        int32_t max_len = 0;
+        for (int32_t r = 0; r < batch; ++r) max_len = std::max(max_len, seq_lens[r]);
+        flat_plan = !(opts && (opts->chunk_keys > 0 || opts->span_chunk > 0)) && batch <= num_sms &&
+                    max_len <= kFlatMaxLen;
+        if (flat_plan) {
+            cascade = nullptr;
+            spans_of.assign((size_t)batch, {});
+            tail_start.assign((size_t)batch, 0);
+            chunk = std::max<int32_t>(max_len, 1);
+        }
+    }
+
     // Shared spans with many member requests go to the tensor-core path: the span's keys
     // are gathered once into the workspace and attended as a dense block by 2 x 128/G of its
     // member requests per item (extend kernel), instead of re-reading the span per group of
@@ -240,7 +261,7 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
                         ((cascade->grp_indptr[s + 1] - cascade->grp_indptr[s] + R - 1) / R);
         const int64_t target = 2 * (int64_t)num_sms * decode_ctas_per_sm(hg, head_dim) / (num_kv_heads / hg);
         const int32_t fine = (int32_t)std::max<int64_t>(64, ((work + target - 1) / std::max<int64_t>(target, 1) + 15) / 16 * 16);
-        if (!(opts && opts->chunk_keys > 0)) chunk = std::min(chunk, fine);
+        if (!(opts && opts->chunk_keys > 0) && !flat_plan) chunk = std::min(chunk, fine);
         if (!(opts && opts->span_chunk > 0))
             for (int32_t s = 0; s < nspans; ++s)
                 if (!sp_tensor[s]) sp_chunk[s] = std::min(span_chunk, fine);

@@ -256,14 +256,17 @@ class PrefixCache:
     the request's next tokens fill the rest of that page before new pages are taken.
 
     ``check_slots`` runs the host check of every call's ``out_cache_loc`` (slots in range and
-    distinct, kv_store's precondition) before anything is copied to the device."""
+    distinct, kv_store's precondition) before anything is copied to the device.
+    ``kv_layout``: "interleaved" (a slot's K and V rows adjacent: decode reads both with one
+    copy) or "separate" (two dense arrays)."""
 
-    def __init__(self, w, device="cuda", page_size=1, check_slots=True):
+    def __init__(self, w, device="cuda", page_size=1, check_slots=True, kv_layout="interleaved"):
         self.w = w
         self.check_slots = bool(check_slots)
         self.device = device
         self.page = int(page_size)
-        self.pool = Pool.allocate(w.num_slots, w.num_kv_heads, w.head_dim, w.dtype, w.k_scale, w.v_scale, device)
+        self.pool = Pool.allocate(w.num_slots, w.num_kv_heads, w.head_dim, w.dtype, w.k_scale, w.v_scale, device,
+                                  layout=kv_layout)
         self.tree = RadixTree(page_size=self.page)
         self.alloc = Allocator(w.slot_perm if self.page == 1 else w.page_perm(self.page))
         self.private = {}   # paged pool: request id -> slots of its trailing partial block

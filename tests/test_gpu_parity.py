@@ -410,3 +410,32 @@ def test_extend_packed_last_tokens(hq, hkv, d, suffix, n_req):
     _, calls = run_step(w)
     assert int(calls["extend"].plan.info.offsets[14]) >= 1     # packed tiles were planned
     check_outputs(w, calls)
+
+
+# ------------------------------------------------------------------------------ pool layouts
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8_e4m3"])
+@pytest.mark.parametrize("page", [1, 16])
+def test_interleaved_and_separate_pools_give_identical_results(dtype, page):
+    # the same step with a slot's K and V rows adjacent (one copy per key in decode) and in two
+    # dense arrays: the kernels do the same arithmetic, so outputs and stored rows match bit
+    # for bit, and both match the oracle
+    pkv, PrefixCache = _pkv()
+    w = W.tot_mixed(seed=39, root_len=600, depth=2, branch=4, seg=160, n_new_branches=3, num_slots=16384,
+                    dtype=dtype)
+    outs = {}
+    for layout in ("interleaved", "separate"):
+        pc = PrefixCache(w, page_size=page, kv_layout=layout)
+        assert pc.pool.layout == layout
+        pc.populate()
+        calls = {k: pc.prepare(k) for k in ("extend", "decode")}
+        for c in calls.values():
+            c.run()
+        torch.cuda.synchronize()
+        for c in calls.values():
+            assert pkv.get_device_error(c.workspace) == 0
+        check_outputs(w, calls)
+        check_pool(w, pc)
+        outs[layout] = {k: c.o.clone() for k, c in calls.items()}
+    for k in outs["separate"]:
+        assert torch.equal(outs["interleaved"][k], outs["separate"][k]), k

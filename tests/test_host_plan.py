@@ -331,3 +331,21 @@ def test_struct_layouts_match_header(tmp_path):
         assert got[(name, "size")] == C.sizeof(cls), name
         for fname, _ in cls._fields_:
             assert got[(name, fname)] == getattr(cls, fname).offset, (name, fname)
+
+
+def test_decode_plan_tiny_batch_is_flat():
+    # 4 requests of 80 keys sharing 64 (the tiny decode workload's shape): one item per request
+    # over its whole context, direct outputs, no span items, no records, no merge
+    seq = np.full(4, 80, np.int32)
+    casc = pkv.Cascade(span_req=np.array([0], np.int32), span_start=np.array([0], np.int32),
+                       span_len=np.array([64], np.int32), grp_indptr=np.array([0, 4], np.int32),
+                       grp_req=np.arange(4, dtype=np.int32))
+    plan = pkv.plan_decode(seq, 8, 2, 64, casc)
+    items = _decode_cover(plan, seq, 2)
+    assert len(items) == 4 and plan.info.num_span_items == 0
+    assert plan.info.num_records == 0 and plan.info.num_merge == 0
+    assert np.all(items["k0"] == 0) and np.all(items["k1"] == 80)
+    # explicit chunk options keep the general plan (span items, records, merges)
+    gen = pkv.plan_decode(seq, 8, 2, 64, casc, {"span_chunk": 64})
+    _decode_cover(gen, seq, 2)
+    assert gen.info.num_span_items > 0 and gen.info.num_merge == 4

@@ -274,7 +274,9 @@ def measure(w, args, dev, steps, world, e2e=True):
     else:
         pc.populate()
         kinds = [k for k in ("extend", "decode") if any(r.kind == k for r in w.requests)]
-        calls = [pc.prepare(kind, cascade=not args.no_cascade) for kind in kinds]
+        popts = {"span_sms": args.span_sms} if getattr(args, "span_sms", 0) else None
+        calls = [pc.prepare(kind, cascade=not args.no_cascade, opts=popts if kind == "decode" else None)
+                 for kind in kinds]
         # host planning of one step (tree match + lock, slots, tables, cascade, plan), which a
         # server repeats for every new batch; measured after the calls above are built
         plan_ms = (sum(pc.host_step_ms(k, reps=3, cascade=not args.no_cascade) for k in kinds)
@@ -652,6 +654,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cascade", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--span-sms", type=int, default=0,
+                    help="decode: SMs left to the tensor-core span pass, run beside the decode kernel (0: after it)")
     ap.add_argument("--kv-layout", default="interleaved", choices=["interleaved", "separate"],
                     help="pool layout: a slot's K and V rows adjacent (default) or two dense arrays")
     ap.add_argument("--chunked-gather", action="store_true",

@@ -158,6 +158,9 @@ typedef struct pkv_plan_opts {
     int32_t dynamic_tail;  /* decode: last item of each request reads its end from seq_lens  */
                            /* on the device, so the plan stays valid while tails grow by     */
                            /* whole decode steps inside the same chunk                        */
+    int32_t span_sms;      /* decode: SMs left to the tensor-core pass over widely shared     */
+                           /* spans, which then runs beside the decode kernel (whose CTAs     */
+                           /* take the other SMs); 0 = it runs after the decode kernel        */
 } pkv_plan_opts;
 
 /* Host description of a plan; pass it, with a device copy of the plan blob, to the device

@@ -150,7 +150,7 @@ class Plan:
 def _opts(opts):
     if opts is None:
         return None
-    o = PkvPlanOpts(0, 0, 0, 0)
+    o = PkvPlanOpts()
     for k, v in opts.items():
         setattr(o, k, int(v))
     return C.byref(o)

@@ -42,7 +42,7 @@ class PkvCascade(C.Structure):
 
 class PkvPlanOpts(C.Structure):
     _fields_ = [("chunk_keys", C.c_int32), ("span_chunk", C.c_int32), ("num_sms", C.c_int32),
-                ("dynamic_tail", C.c_int32)]
+                ("dynamic_tail", C.c_int32), ("span_sms", C.c_int32)]
 
 
 class PkvPlanInfo(C.Structure):

@@ -230,13 +230,41 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
     std::vector<int32_t> sp_chunk(nspans, span_chunk);
     std::vector<char> sp_tensor(nspans, 0);
     std::vector<char> in_tensor(batch, 0);
+    // The tensor-core span pass runs beside the decode kernel on span_sms SMs when it is small
+    // next to it (opts->span_sms: 0 = decide here, < 0 = never, > 0 = that many SMs).  The
+    // estimate, in SM-microseconds at the rates measured on GB300: a decode-kernel key moves
+    // its head group's K and V rows at ~40 KB per us per SM; a tensor-core span item costs
+    // ~2.3 us per 128-key tile for two 128-row query tiles, plus ~5 us to start.  Beside the
+    // decode kernel the pass gets about 1.25x its share of the SMs, at least 12; it stays after
+    // the decode kernel when its share is above a fifth.
+    int32_t span_sms = (opts && opts->span_sms != 0) ? std::max(opts->span_sms, 0) : -1;
+    if (span_sms < 0 && nspans > 0) {
+        const double elem = 2.0;  // bytes of a pool element the decode kernel moves (bf16 rows)
+        double dec = 0.0, spn = 0.0;
+        for (int32_t r = 0; r < batch; ++r) dec += (double)(seq_lens[r] - tail_start[r]);
+        for (int32_t s = 0; s < nspans; ++s) {
+            const int32_t m = cascade->grp_indptr[s + 1] - cascade->grp_indptr[s], len = cascade->span_len[s];
+            if (m >= kTensorMinMembers && len >= kTensorMinKeys)
+                spn += (double)((m + TQ2 - 1) / TQ2) * num_kv_heads * (((len + 127) / 128) * 2.3 + 5.0);
+            else
+                dec += (double)len * ((m + R - 1) / R);
+        }
+        dec *= (double)num_kv_heads * head_dim * elem * 2.0 / 40000.0;  // SM-us
+        const double share = spn / std::max(spn + dec, 1.0);
+        span_sms = (spn > 0.0 && share <= 0.2) ? std::max<int32_t>(12, (int32_t)(1.25 * share * num_sms + 0.5)) : 0;
+    }
+    span_sms = std::min(std::max(span_sms, 0), num_sms - 1);
     for (int32_t s = 0; s < nspans; ++s) {
         const int32_t m = cascade->grp_indptr[s + 1] - cascade->grp_indptr[s], len = cascade->span_len[s];
         if (m < kTensorMinMembers || len < kTensorMinKeys) continue;
         sp_tensor[s] = 1;
+        // Beside the decode kernel (span_sms option) the pass has few SMs and time to spare:
+        // about two long items per SM there (fewer records, less set-up per key); else about
+        // one item per SM.
         const int64_t per_chunk = (int64_t)((m + TQ2 - 1) / TQ2) * num_kv_heads;
-        const int32_t nch = (int32_t)std::max<int64_t>(
-            1, std::min<int64_t>((num_sms + per_chunk - 1) / per_chunk, (len + 511) / 512));
+        const int64_t want = span_sms > 0 ? (2 * (int64_t)span_sms + per_chunk / 2) / per_chunk
+                                          : (num_sms + per_chunk - 1) / per_chunk;
+        const int32_t nch = (int32_t)std::max<int64_t>(1, std::min<int64_t>(want, (len + 511) / 512));
         sp_chunk[s] = ((len + nch - 1) / nch + 127) / 128 * 128;
         for (int32_t i = cascade->grp_indptr[s]; i < cascade->grp_indptr[s + 1]; ++i) in_tensor[cascade->grp_req[i]] = 1;
     }
@@ -415,8 +443,10 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
 
     // persistent CTAs: longest-processing-time-first onto the least loaded CTA
     const int32_t n_items = (int32_t)items.size();
+    // SMs left to the tensor-core span pass, which then runs beside the decode kernel
+    if (xitems.empty() || n_items == 0) span_sms = 0;
     const int32_t nctas = std::max<int32_t>(
-        1, std::min<int64_t>(n_items, (int64_t)num_sms * decode_ctas_per_sm(hg, head_dim)));
+        1, std::min<int64_t>(n_items, (int64_t)(num_sms - span_sms) * decode_ctas_per_sm(hg, head_dim)));
     std::vector<DecodeItem> placed;
     std::vector<int32_t> cta_off;
     lpt_deal(items, cost, nctas, &placed, &cta_off);
@@ -434,16 +464,17 @@ extern "C" int pkv_plan_decode(int32_t batch, const int32_t *seq_lens, int32_t n
     // back, each dealt onto its own persistent CTAs
     std::vector<ExtendItem> xplaced, xplaced_p;
     std::vector<int32_t> xcta_off, xcta_off_p;
-    auto xdeal = [&](const std::vector<ExtendItem> &v, std::vector<ExtendItem> *out, std::vector<int32_t> *off) {
+    auto xdeal = [&](const std::vector<ExtendItem> &v, std::vector<ExtendItem> *out, std::vector<int32_t> *off,
+                     int32_t sms) {
         if (v.empty()) return 0;
-        const int32_t n = std::max<int32_t>(1, std::min<int32_t>((int32_t)v.size(), num_sms));
+        const int32_t n = std::max<int32_t>(1, std::min<int32_t>((int32_t)v.size(), sms));
         std::vector<int64_t> xcost;
         for (const ExtendItem &x : v) xcost.push_back(extend_item_cost(x, TQ2 / 2));
         lpt_deal(v, xcost, n, out, off);
         return n;
     };
-    const int32_t xctas = xdeal(xitems, &xplaced, &xcta_off);
-    const int32_t xctas_p = xdeal(xprecise, &xplaced_p, &xcta_off_p);
+    const int32_t xctas = xdeal(xitems, &xplaced, &xcta_off, span_sms > 0 ? span_sms : num_sms);
+    const int32_t xctas_p = xdeal(xprecise, &xplaced_p, &xcta_off_p, num_sms);
     xplaced.insert(xplaced.end(), xplaced_p.begin(), xplaced_p.end());
 
     std::memset(info, 0, sizeof(*info));

@@ -349,3 +349,30 @@ def test_decode_plan_tiny_batch_is_flat():
     gen = pkv.plan_decode(seq, 8, 2, 64, casc, {"span_chunk": 64})
     _decode_cover(gen, seq, 2)
     assert gen.info.num_span_items > 0 and gen.info.num_merge == 4
+
+
+def test_decode_plan_span_pass_beside_the_decode_kernel():
+    # a 1,024-key prefix shared by 64 requests (tensor-core span) and long unshared tails: the
+    # span pass is small next to the decode kernel, so it gets a few SMs of its own and runs
+    # beside it, in about two long items per SM (fewer records than one item per SM)
+    rng = np.random.default_rng(5)
+    seq = (1024 + rng.integers(1500, 3000, size=64)).astype(np.int32)
+    casc = pkv.Cascade(span_req=np.array([0], np.int32), span_start=np.array([0], np.int32),
+                       span_len=np.array([1024], np.int32), grp_indptr=np.array([0, 64], np.int32),
+                       grp_req=np.arange(64, dtype=np.int32))
+    auto = pkv.plan_decode(seq, 32, 8, 128, casc)
+    _decode_cover(auto, seq, 8)
+    x_auto = int(auto.info.offsets[17])
+    assert 12 <= x_auto < 152 and int(auto.info.offsets[5]) == 152 - x_auto
+    serial = pkv.plan_decode(seq, 32, 8, 128, casc, {"span_sms": -1})
+    _decode_cover(serial, seq, 8)
+    assert int(serial.info.offsets[5]) == 152 and int(serial.info.offsets[17]) > x_auto
+    assert auto.info.num_records <= serial.info.num_records
+    fixed = pkv.plan_decode(seq, 32, 8, 128, casc, {"span_sms": 20})
+    _decode_cover(fixed, seq, 8)
+    assert int(fixed.info.offsets[17]) <= 20 and int(fixed.info.offsets[5]) == 132
+    # a span pass large next to the decode kernel stays after it
+    short = np.full(64, 1100, np.int32)
+    big = pkv.plan_decode(short, 32, 8, 128, casc)
+    _decode_cover(big, short, 8)
+    assert int(big.info.offsets[5]) == min(152, big.info.num_items)

@@ -62,7 +62,8 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 20 ms while running."""
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms from start() to stop(); each
+    sample carries the host time it arrived, so a summary covers any interval of the run."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -71,9 +72,9 @@ class ClockSampler:
     def __init__(self, index=0):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.lines = []   # (host time, csv line)
 
-    def __enter__(self):
+    def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
@@ -86,20 +87,23 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
 
-    def __exit__(self, *exc):
+    def stop(self):
         if self.proc:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
+            self.proc = None
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for t, ln in list(self.lines):
+            if (t0 is not None and t < t0) or (t1 is not None and t > t1):
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -115,6 +119,31 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+    def clocks(self, timed, window):
+        """The clock record of a measurement: the samples inside its timed region, and when
+        those are fewer than three (a short region), the samples of the whole measurement
+        window around it (warm-up, timed steps and the other timed variants: the same load)."""
+        s = self.summary(*timed)
+        if s["samples"] >= 3:
+            return s
+        w = self.summary(*window)
+        w["timed_region_samples"] = s["samples"]
+        w["window"] = "the measurement's warm-up, timed and end-to-end steps (the timed region alone is short)"
+        return w
+
+
+_SAMPLER = None
+
+
+def sampler():
+    """The run's clock sampler (started on first use, before any measurement)."""
+    global _SAMPLER
+    if _SAMPLER is None:
+        import torch
+        _SAMPLER = ClockSampler(torch.cuda.current_device() if torch.cuda.is_available() else 0).start()
+        time.sleep(0.3)   # nvidia-smi's first samples arrive before the first measurement
+    return _SAMPLER
 
 
 def max_over_ranks(seconds, device):
@@ -226,17 +255,18 @@ def run_serving(args):
     served = sum(len(r.prompt) + r.out_len for r in stream.requests)
     cap = args.pool_slots or 16384
     res = {}
-    with ClockSampler(0) as clocks:
-        for policy in ("lpm", "fcfs"):
-            sim = ServingSim(stream, capacity=cap, policy=policy, max_running=64, prefill_budget=16384,
-                             page_size=args.page_size)
-            t0 = time.perf_counter()
-            sim.run()
-            st = sim.summary()
-            st["wall_s"] = round(time.perf_counter() - t0, 3)
-            st["served_tokens_per_s_device"] = round(served / (st["device_ms"] / 1e3), 1)
-            st["served_tokens_per_s_wall"] = round(served / st["wall_s"], 1)
-            res[policy] = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in st.items()}
+    smp = sampler()
+    ts0 = time.perf_counter()
+    for policy in ("lpm", "fcfs"):
+        sim = ServingSim(stream, capacity=cap, policy=policy, max_running=64, prefill_budget=16384,
+                         page_size=args.page_size)
+        t0 = time.perf_counter()
+        sim.run()
+        st = sim.summary()
+        st["wall_s"] = round(time.perf_counter() - t0, 3)
+        st["served_tokens_per_s_device"] = round(served / (st["device_ms"] / 1e3), 1)
+        st["served_tokens_per_s_wall"] = round(served / st["wall_s"], 1)
+        res[policy] = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in st.items()}
     lpm = res["lpm"]
     return {
         "metric": METRIC, "value": lpm["served_tokens_per_s_device"], "unit": "tokens/s", "n_gpus": 1,
@@ -250,7 +280,7 @@ def run_serving(args):
         "serving": res,
         "lpm_over_fcfs": {"device_time": round(res["fcfs"]["device_ms"] / lpm["device_ms"], 3),
                           "hit_rate": [lpm["hit_rate"], res["fcfs"]["hit_rate"]]},
-        "clocks": clocks.summary(),
+        "clocks": smp.summary(ts0, time.perf_counter()),
     }
 
 
@@ -290,6 +320,8 @@ def measure(w, args, dev, steps, world, e2e=True):
         for c in calls:
             c.attend()
 
+    smp = sampler()
+    win0 = time.perf_counter()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -316,23 +348,23 @@ def measure(w, args, dev, steps, world, e2e=True):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(dev.index) as clocks:
-        t0 = time.perf_counter()
-        for k in range(K):
-            flush.zero_()
-            e = ev[k]
-            e[0].record(stream)
-            for c in calls:
-                c.store()
-            e[1].record(stream)
-            for i, c in enumerate(calls):
-                if c.kind == "extend":
-                    pkv.set_kernel_events(*kev[k][i])
-                e[2 + 2 * i].record(stream)
-                c.replay_attend() if c.graph is not None else c.attend()
-                e[3 + 2 * i].record(stream)
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    for k in range(K):
+        flush.zero_()
+        e = ev[k]
+        e[0].record(stream)
+        for c in calls:
+            c.store()
+        e[1].record(stream)
+        for i, c in enumerate(calls):
+            if c.kind == "extend":
+                pkv.set_kernel_events(*kev[k][i])
+            e[2 + 2 * i].record(stream)
+            c.replay_attend() if c.graph is not None else c.attend()
+            e[3 + 2 * i].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    wall = t1 - t0
     if world > 1:
         torch.distributed.barrier()
     step_ms = [ev[k][0].elapsed_time(ev[k][-1]) for k in range(K)]
@@ -392,13 +424,14 @@ def measure(w, args, dev, steps, world, e2e=True):
                              if all(c.ctx is None for c in calls) else None),
                      **({"note": "stored inside each chunk's attention call"}
                         if any(c.ctx is not None for c in calls) else {})},
-        "wall_s": round(wall, 4), "clocks": clocks.summary(),
+        "wall_s": round(wall, 4), "clocks": smp.clocks((t0, t1), (win0, time.perf_counter())),
         "host_plan_ms_per_step": None if plan_ms is None else round(plan_ms, 3),
     }
     for kind, fx_ in facts.items():
         out[f"{kind}_queries"] = fx_["queries"]
     if not e2e:
         return out, calls
+    win_mid = time.perf_counter()
 
     # end-to-end: same calls, inputs from pinned host memory, output back to the host.
     # Pipelined (step k+1's inputs copy in and step k-1's output copies out while step k
@@ -452,6 +485,8 @@ def measure(w, args, dev, steps, world, e2e=True):
                                         round(job_throughput(world, 1, tokens_per_step,
                                                              (e2e_ms + plan_ms) / 1e3), 1)),
     }
+    if out["clocks"].get("window"):   # the window grew by the end-to-end and unflushed steps
+        out["clocks"] = smp.clocks((t0, t1), (win0, time.perf_counter()))
     out["unflushed"] = {"ms_per_step": round(float(np.mean(unflushed_ms)), 4),
                         "value": round(job_throughput(world, K, tokens_per_step, sum(unflushed_ms) / 1e3), 1),
                         "note": "same steps without the L2 flush between them"}
@@ -707,4 +742,8 @@ def main():
 
 
 if __name__ == "__main__":
-    main()
+    try:
+        main()
+    finally:
+        if _SAMPLER is not None:
+            _SAMPLER.stop()

@@ -160,7 +160,10 @@ typedef struct pkv_plan_opts {
                            /* whole decode steps inside the same chunk                        */
     int32_t span_sms;      /* decode: SMs left to the tensor-core pass over widely shared     */
                            /* spans, which then runs beside the decode kernel (whose CTAs     */
-                           /* take the other SMs); 0 = it runs after the decode kernel        */
+                           /* take the other SMs); 0 = decided by the planner, < 0 = the pass */
+                           /* always runs after the decode kernel                             */
+    int32_t fuse_store;    /* extend: a plan for pkv_attn_extend_store, which stores the new  */
+                           /* tokens itself (pool and gathered rows in one pass)              */
 } pkv_plan_opts;
 
 /* Host description of a plan; pass it, with a device copy of the plan blob, to the device
@@ -221,6 +224,20 @@ int pkv_attn_decode(const pkv_pool *pool, const pkv_batch *batch, const void *q,
 int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, const void *q, void *o,
                     float sm_scale, const pkv_plan_info *info, const void *plan_dev,
                     void *workspace, size_t ws_bytes, void *stream);
+
+/* Store + extend in one call (a plan from pkv_plan_extend with opts->fuse_store set): the new
+ * tokens' K/V go into the pool exactly as pkv_kv_store writes them and, as the pool now holds
+ * them, straight into the call's gathered rows, so the key gather reads only cached
+ * positions -- the rows just stored are not read back from the pool ([PR] "compute missing
+ * KV tensors -> insert node": the missing K/V are computed once and reused).
+ *   k_new, v_new, out_cache_loc  the new tokens' rows and slots in q order (total_q rows),
+ *                                as pkv_kv_store takes them
+ * Everything else as pkv_attn_extend; slot-range errors of the store go to the workspace
+ * error word.  pkv_attn_extend rejects a fused-store plan and this call any other. */
+int pkv_attn_extend_store(const pkv_pool *pool, const pkv_batch *batch, const void *q, void *o, float sm_scale,
+                          const void *k_new, const void *v_new, const int32_t *out_cache_loc,
+                          const pkv_plan_info *info, const void *plan_dev, void *workspace, size_t ws_bytes,
+                          void *stream);
 
 /* Chunked prefill over a context buffer kept by the caller ("SGLang后端运行时优化细节",
  * §RadixAttention KV缓存复用的底层逻辑, 3 开发者需关注的配置项: --chunked-prefill-size prefills a

@@ -12,6 +12,8 @@ memory -- and forwards to the library.  Names follow the C entry points without 
     attn_decode   one query token per request over its whole context (widely shared spans on
                   the tensor cores, the rest by a persistent bulk-copy kernel with mma.sync)
     attn_extend   causal extend of the uncached suffix (key gather, then tcgen05 / TMEM / TMA)
+    attn_extend_store  kv_store + attn_extend in one call: the new rows are stored into the pool
+                  and straight into the gathered rows (the gather reads cached positions only)
     plan_extend_ctx / attn_extend_ctx  chunked prefill over a caller-kept context buffer: each
                   chunk is stored into the pool and its context rows in one pass, nothing gathered
     RadixTree     host radix tree: match_prefix (with split), insert, LRU evict, lock_ref,
@@ -32,7 +34,7 @@ from ._lib import (PKV_BF16, PKV_FP8_E4M3, PkvBatch, PkvCascade, PkvError, PkvPl
                    check, lib)
 
 __all__ = ["Pool", "Batch", "Plan", "Cascade", "kv_store", "check_out_cache_loc", "plan_decode", "plan_extend",
-           "plan_extend_ctx", "attn_decode", "attn_extend", "attn_extend_ctx", "get_device_error", "get_noalloc_device_error", "set_kernel_events",
+           "plan_extend_ctx", "attn_decode", "attn_extend", "attn_extend_store", "attn_extend_ctx", "get_device_error", "get_noalloc_device_error", "set_kernel_events",
            "set_wait_limit_ns", "get_wait_limit_ns",
            "RadixTree", "Allocator", "PkvError", "version"]
 
@@ -236,6 +238,17 @@ def attn_extend(pool: Pool, batch: Batch, q, o, sm_scale, plan: Plan, plan_dev, 
     check("pkv_attn_extend", lib.pkv_attn_extend(C.byref(p), C.byref(b), _ptr(q), _ptr(o), float(sm_scale),
                                                  C.byref(plan.info), _ptr(plan_dev), _ptr(workspace),
                                                  workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def attn_extend_store(pool: Pool, batch: Batch, q, o, sm_scale, k_new, v_new, out_cache_loc, plan: Plan, plan_dev,
+                      workspace, stream=None) -> None:
+    """kv_store of the call's new tokens and attn_extend in one call (a plan made with
+    opts={"fuse_store": 1}): the new rows go to the pool and straight to their gathered rows."""
+    p, b = pool.c(), batch.c()
+    check("pkv_attn_extend_store", lib.pkv_attn_extend_store(
+        C.byref(p), C.byref(b), _ptr(q), _ptr(o), float(sm_scale), _ptr(k_new), _ptr(v_new), _ptr(out_cache_loc),
+        C.byref(plan.info), _ptr(plan_dev), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
 
 
 def attn_extend_ctx(pool: Pool, q, o, sm_scale, k_new, v_new, out_cache_loc, ctx_k, ctx_v, plan: Plan, plan_dev,

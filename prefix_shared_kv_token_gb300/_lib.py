@@ -42,7 +42,7 @@ class PkvCascade(C.Structure):
 
 class PkvPlanOpts(C.Structure):
     _fields_ = [("chunk_keys", C.c_int32), ("span_chunk", C.c_int32), ("num_sms", C.c_int32),
-                ("dynamic_tail", C.c_int32), ("span_sms", C.c_int32)]
+                ("dynamic_tail", C.c_int32), ("span_sms", C.c_int32), ("fuse_store", C.c_int32)]
 
 
 class PkvPlanInfo(C.Structure):
@@ -71,6 +71,8 @@ SIGNATURES = {
                                   C.POINTER(PkvPlanOpts), _P, _SZ, C.POINTER(PkvPlanInfo)]),
     "pkv_plan_extend_ctx": (C.c_int, [_I32, _P, _P, _P, _P, _I64, _I32, _I32, _I32, C.POINTER(PkvPlanOpts), _P, _SZ,
                                       C.POINTER(PkvPlanInfo)]),
+    "pkv_attn_extend_store": (C.c_int, [C.POINTER(PkvPool), C.POINTER(PkvBatch), _P, _P, _F, _P, _P, _P,
+                                        C.POINTER(PkvPlanInfo), _P, _P, _SZ, _P]),
     "pkv_attn_extend_ctx": (C.c_int, [C.POINTER(PkvPool), _P, _P, _F, _P, _P, _P, _P, _P, _I64,
                                       C.POINTER(PkvPlanInfo), _P, _P, _SZ, _P]),
     "pkv_attn_decode": (C.c_int, [C.POINTER(PkvPool), C.POINTER(PkvBatch), _P, _P, _F, C.POINTER(PkvPlanInfo), _P,

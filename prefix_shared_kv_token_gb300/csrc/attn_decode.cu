@@ -574,7 +574,7 @@ static int launch_decode(const DecodeParams &p, int nctas, cudaStream_t s) {
     auto kern = p.wait.quick ? decode_kernel<D, G, FP8, true> : decode_kernel<D, G, FP8, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, geo.bytes) != cudaSuccess)
         return PKV_E_CUDA;
-    return launch_pdl(kern, dim3(nctas), dim3(32 * (p.hg + 1)), geo.bytes, s, p) == cudaSuccess ? PKV_OK : PKV_E_CUDA;
+    return launch_pdl(kern, dim3(nctas), dim3(32 * (p.hg + 1)), geo.bytes, s, true, p) == cudaSuccess ? PKV_OK : PKV_E_CUDA;
 }
 
 template <int D>
@@ -598,7 +598,7 @@ int launch_merge(const pkv_plan_info *info, const void *plan_dev, const float *r
     const MergeItem *m = reinterpret_cast<const MergeItem *>(static_cast<const uint8_t *>(plan_dev) + info->offsets[3]);
     const dim3 grid((unsigned)info->num_merge, (unsigned)((info->num_q_heads + 7) / 8));
     const cudaError_t e = launch_pdl(info->head_dim == 128 ? merge_kernel<128> : merge_kernel<64>, grid, dim3(256), 0,
-                                     s, m, rec_acc, rec_ml, o, (int)info->num_q_heads);
+                                     s, true, m, rec_acc, rec_ml, o, (int)info->num_q_heads);
     return e == cudaSuccess ? PKV_OK : PKV_E_CUDA;
 }
 

@@ -97,7 +97,10 @@ struct XBars {
     int32_t abort_flag;
 };
 
-PKV_DEV bool xwait(uint64_t *bar, uint32_t parity, XBars *b, int32_t *err, int where, const WaitPolicy &wp) {
+// ctx: the waiting role's position (item << 16 | its tile or phase counter), recorded with
+// the CTA and the parity waited for when this wait is the launch's first timeout.
+PKV_DEV bool xwait(uint64_t *bar, uint32_t parity, XBars *b, int32_t *err, int where, const WaitPolicy &wp,
+                   int32_t ctx) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
@@ -105,7 +108,7 @@ PKV_DEV bool xwait(uint64_t *bar, uint32_t parity, XBars *b, int32_t *err, int w
         if (it == 1 || (it & wp.check_mask) == 0) {
             if (*reinterpret_cast<volatile int32_t *>(&b->abort_flag)) return false;
             if (global_timer_ns() - t0 > wp.limit_ns) {
-                set_error(err, DERR_TIMEOUT | where);
+                set_error_where(err, DERR_TIMEOUT | where, (int32_t)blockIdx.x, ctx, (int32_t)parity);
                 *reinterpret_cast<volatile int32_t *>(&b->abort_flag) = 1;
                 return false;
             }
@@ -138,14 +141,25 @@ struct GatherParams {
     const int32_t *q_rows;
     int32_t q_batch, q_row_vecs;
     int32_t *err;
+    int32_t pdl_wait_start;  // 1: wait for the preceding kernel first; 0: it wrote nothing this
+                             // gather reads, wait for it only before exiting
 };
 
 // One CTA per unit of <= 32 keys: thread t moves 16-byte pieces of the units' slot rows
 // (Hkv * D elements, contiguous in the pool and in the output).
 template <int D, bool FP8>
+PKV_DEV void gather_body(const GatherParams &p);
+
+template <int D, bool FP8>
 __global__ void __launch_bounds__(256) gather_kernel(const GatherParams p) {
-    pdl_wait();     // the pool rows and tables may come from the preceding kernel
+    if (p.pdl_wait_start) pdl_wait();  // the pool rows and tables may come from the preceding kernel
     pdl_trigger();
+    gather_body<D, FP8>(p);
+    if (!p.pdl_wait_start) pdl_wait();  // complete only after the preceding kernel
+}
+
+template <int D, bool FP8>
+PKV_DEV void gather_body(const GatherParams &p) {
     if ((int)blockIdx.x >= p.nunits) {  // a query row
         const int i = blockIdx.x - p.nunits, r = __ldg(p.q_rows + i);
         if (r < 0 || r >= p.q_batch) {
@@ -357,10 +371,11 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t sbase = smem_u32(smem);
     XBars *bars = reinterpret_cast<XBars *>(smem + C::kBarOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int i0 = __ldg(p.cta_off + blockIdx.x), i1 = __ldg(p.cta_off + blockIdx.x + 1);
 
     if (p.pdl_wait_start) pdl_wait();
     pdl_trigger();
+    // the plan is read only from here on: with pdl_wait_start it may come from the kernel before
+    const int i0 = __ldg(p.cta_off + blockIdx.x), i1 = __ldg(p.cta_off + blockIdx.x + 1);
     // once any CTA of this launch gave up on a wait, the rest exit instead of waiting too
     __shared__ int32_t s_skip;
     __shared__ float2 s_ml[2][kBM];  // split items: each warpgroup's running (max, sum) per row
@@ -421,7 +436,7 @@ __global__ void __launch_bounds__(384, 1)
                 const ExtendItem *itp = p.items + i;
                 const XItem it = load_item(itp, TQ, p.packs);
                 if (kside) {
-                    if (nql > 0 && !xwait(&bars->qempty, (nql - 1) & 1, bars, p.err, 6, p.wait)) break;
+                    if (nql > 0 && !xwait(&bars->qempty, (nql - 1) & 1, bars, p.err, 6, p.wait, (i << 16) | (nql & 0xFFFF))) break;
                     if (it.pk) {
                         // a packed tile: each row group's tokens by their own 32-row box
                         int ng = 0;
@@ -449,7 +464,7 @@ __global__ void __launch_bounds__(384, 1)
                         const bool early = kside && ((split_mask >> s) & 1u);
                         uint64_t *bar = early ? &bars->kempty[s] : &bars->kvempty[s];
                         const uint32_t par = early ? ((kpar >> s) & 1u) ^ 1u : (uint32_t)((tp / ST) - 1) & 1u;
-                        if (!xwait(bar, par, bars, p.err, kside ? 5 : 7, p.wait)) {
+                        if (!xwait(bar, par, bars, p.err, kside ? 5 : 7, p.wait, (i << 16) | (tp & 0xFFFF))) {
                             ok = false;
                             break;
                         }
@@ -486,11 +501,11 @@ __global__ void __launch_bounds__(384, 1)
             bool ok = true;
             for (int i = i0; ok && i < i1; ++i, ++ip) {
                 const XItem it = load_item(p.items + i, TQ, p.packs);
-                if (!xwait(&bars->q, ip & 1, bars, p.err, 1, p.wait)) break;
+                if (!xwait(&bars->q, ip & 1, bars, p.err, 1, p.wait, (i << 16) | (ip & 0xFFFF))) break;
                 if (!it.split) {
                     auto issue_s = [&](int q, int j) -> bool {
                         const int tg = tm + j, s = tg % ST;
-                        if (q == 0 && !xwait(&bars->kfull[s], (tg / ST) & 1, bars, p.err, 4, p.wait)) return false;
+                        if (q == 0 && !xwait(&bars->kfull[s], (tg / ST) & 1, bars, p.err, 4, p.wait, (i << 16) | (tg & 0xFFFF))) return false;
                         tc_fence_after();
                         const uint32_t q_s = sbase + C::kQOff + q * C::kQTile;
                         const uint32_t k_s = sbase + C::kStageOff + (s * 2) * C::kKTile;
@@ -506,9 +521,9 @@ __global__ void __launch_bounds__(384, 1)
                     };
                     auto issue_pv = [&](int q, int j) -> bool {
                         const int tg = tm + j, s = tg % ST;
-                        if (!xwait(&bars->pfull[q], (cpar >> q) & 1u, bars, p.err, 2, p.wait)) return false;
+                        if (!xwait(&bars->pfull[q], (cpar >> q) & 1u, bars, p.err, 2, p.wait, (i << 16) | (tg & 0xFFFF))) return false;
                         cpar ^= 1u << q;
-                        if (q == 0 && !xwait(&bars->vfull[s], (tg / ST) & 1, bars, p.err, 3, p.wait)) return false;
+                        if (q == 0 && !xwait(&bars->vfull[s], (tg / ST) & 1, bars, p.err, 3, p.wait, (i << 16) | (tg & 0xFFFF))) return false;
                         tc_fence_after();
                         const uint32_t v_s = sbase + C::kStageOff + (s * 2 + 1) * C::kKTile;
 #pragma unroll
@@ -545,7 +560,7 @@ __global__ void __launch_bounds__(384, 1)
                     // its S is done and the next K tile loads while this one's P.V still waits.
                     auto split_s = [&](int j) -> bool {
                         const int q = j & 1, tg = tm + j, s = tg % ST;
-                        if (!xwait(&bars->kfull[s], (tg / ST) & 1, bars, p.err, 4, p.wait)) return false;
+                        if (!xwait(&bars->kfull[s], (tg / ST) & 1, bars, p.err, 4, p.wait, (i << 16) | (tg & 0xFFFF))) return false;
                         tc_fence_after();
                         const uint32_t q_s = sbase + C::kQOff;
                         const uint32_t k_s = sbase + C::kStageOff + (s * 2) * C::kKTile;
@@ -562,9 +577,9 @@ __global__ void __launch_bounds__(384, 1)
                     };
                     auto split_pv = [&](int j) -> bool {
                         const int q = j & 1, tg = tm + j, s = tg % ST;
-                        if (!xwait(&bars->pfull[q], (cpar >> q) & 1u, bars, p.err, 2, p.wait)) return false;
+                        if (!xwait(&bars->pfull[q], (cpar >> q) & 1u, bars, p.err, 2, p.wait, (i << 16) | (tg & 0xFFFF))) return false;
                         cpar ^= 1u << q;
-                        if (!xwait(&bars->vfull[s], (tg / ST) & 1, bars, p.err, 3, p.wait)) return false;
+                        if (!xwait(&bars->vfull[s], (tg / ST) & 1, bars, p.err, 3, p.wait, (i << 16) | (tg & 0xFFFF))) return false;
                         tc_fence_after();
                         const uint32_t v_s = sbase + C::kStageOff + (s * 2 + 1) * C::kKTile;
 #pragma unroll
@@ -633,7 +648,7 @@ __global__ void __launch_bounds__(384, 1)
                     continue;
                 }
                 // lanes leave together: a split warp must not reach the .sync.aligned tcgen05 ops
-                if (!__all_sync(0xffffffffu, xwait(&bars->sfull[q], cw & 1, bars, p.err, 8, p.wait))) {
+                if (!__all_sync(0xffffffffu, xwait(&bars->sfull[q], cw & 1, bars, p.err, 8, p.wait, (i << 16) | (cw & 0xFFFF)))) {
                     ok = false;
                     break;
                 }
@@ -709,7 +724,7 @@ __global__ void __launch_bounds__(384, 1)
                 tc_fence_before();
                 mbar_arrive(&bars->pfull[q]);
             }
-            bool fin = __all_sync(0xffffffffu, ok && xwait(&bars->ofinal[q], co & 1, bars, p.err, 10, p.wait));
+            bool fin = __all_sync(0xffffffffu, ok && xwait(&bars->ofinal[q], co & 1, bars, p.err, 10, p.wait, (i << 16) | (co & 0xFFFF)));
             if (it.split) {
                 // exchange the row's running max and sum with the other warpgroup; both
                 // warpgroups leave together when either gave up on a wait
@@ -782,36 +797,37 @@ struct XMaps {
 };
 
 template <int D, int G, bool PRECISE>
-static int launch_extend(const ExtendParams &p, const XMaps &mp, int nctas, cudaStream_t s) {
+static int launch_extend(const ExtendParams &p, const XMaps &mp, int nctas, cudaStream_t s, bool pdl) {
     constexpr int smem = XCfg<D>::kSmem;
     static_assert(smem <= 232448, "shared memory budget");
     auto kern = extend_kernel<D, G, PRECISE>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return PKV_E_CUDA;
     // persistent: the plan's CTA lists
-    return launch_pdl(kern, dim3(nctas), dim3(384), smem, s, p, mp.q, mp.k, mp.v, mp.qg) == cudaSuccess ? PKV_OK
+    return launch_pdl(kern, dim3(nctas), dim3(384), smem, s, pdl, p, mp.q, mp.k, mp.v, mp.qg) == cudaSuccess ? PKV_OK
                                                                                                      : PKV_E_CUDA;
 }
 
 template <int D, bool PRECISE>
-static int dispatch_g(int G, const ExtendParams &p, const XMaps &mp, int n, cudaStream_t s) {
+static int dispatch_g(int G, const ExtendParams &p, const XMaps &mp, int n, cudaStream_t s, bool pdl) {
     switch (G) {
-        case 1: return launch_extend<D, 1, PRECISE>(p, mp, n, s);
-        case 2: return launch_extend<D, 2, PRECISE>(p, mp, n, s);
-        case 4: return launch_extend<D, 4, PRECISE>(p, mp, n, s);
-        case 8: return launch_extend<D, 8, PRECISE>(p, mp, n, s);
+        case 1: return launch_extend<D, 1, PRECISE>(p, mp, n, s, pdl);
+        case 2: return launch_extend<D, 2, PRECISE>(p, mp, n, s, pdl);
+        case 4: return launch_extend<D, 4, PRECISE>(p, mp, n, s, pdl);
+        case 8: return launch_extend<D, 8, PRECISE>(p, mp, n, s, pdl);
         default: return PKV_E_UNSUPPORTED;
     }
 }
 
 template <int D>
-static int dispatch_extend(int G, const ExtendParams &p, const XMaps &mp, int n, cudaStream_t s, bool precise = false) {
-    return precise ? dispatch_g<D, true>(G, p, mp, n, s) : dispatch_g<D, false>(G, p, mp, n, s);
+static int dispatch_extend(int G, const ExtendParams &p, const XMaps &mp, int n, cudaStream_t s, bool precise,
+                           bool pdl) {
+    return precise ? dispatch_g<D, true>(G, p, mp, n, s, pdl) : dispatch_g<D, false>(G, p, mp, n, s, pdl);
 }
 
 template <int D>
 static int launch_gather(const GatherParams &p, bool fp8, int nunits, cudaStream_t s) {
-    return launch_pdl(fp8 ? gather_kernel<D, true> : gather_kernel<D, false>, dim3(nunits), dim3(256), 0, s, p) ==
+    return launch_pdl(fp8 ? gather_kernel<D, true> : gather_kernel<D, false>, dim3(nunits), dim3(256), 0, s, true, p) ==
                    cudaSuccess
                ? PKV_OK
                : PKV_E_CUDA;
@@ -893,6 +909,7 @@ int decode_span_gather(const pkv_pool *pool, const pkv_batch *batch, const void 
     gp.k_out = b.kg;
     gp.v_out = b.vg;
     gp.err = reinterpret_cast<int32_t *>(ws);
+    gp.pdl_wait_start = 1;
     // one launch: the span keys, then the member query rows
     gp.nunits = (int32_t)b.nunits;
     gp.q_src = static_cast<const uint4 *>(q);
@@ -945,8 +962,8 @@ int decode_span_attend(const pkv_pool *pool, const void *q, float sm_scale, cons
         p.cta_off = reinterpret_cast<const int32_t *>(plan + info->offsets[part == 0 ? 16 : 19]);
         const int64_t nctas = info->offsets[part == 0 ? 17 : 20];
         if (nctas < 1 || nctas > n || nprec > b.nx) return PKV_E_PLAN;
-        rc = D == 128 ? dispatch_extend<128>(G, p, mp, (int)nctas, s, part == 1)
-                      : dispatch_extend<64>(G, p, mp, (int)nctas, s, part == 1);
+        rc = D == 128 ? dispatch_extend<128>(G, p, mp, (int)nctas, s, part == 1, true)
+                      : dispatch_extend<64>(G, p, mp, (int)nctas, s, part == 1, true);
         if (rc) return rc;
     }
     return PKV_OK;
@@ -957,7 +974,7 @@ int decode_span_attend(const pkv_pool *pool, const void *q, float sm_scale, cons
 namespace pkv {
 
 int launch_store(const pkv_pool *pool, const void *k_new, const void *v_new, const int32_t *out_cache_loc, int64_t n,
-                 void *workspace, void *ctx_k, void *ctx_v, const int32_t *ctx_row, cudaStream_t s);
+                 void *workspace, void *ctx_k, void *ctx_v, const int32_t *ctx_row, int64_t ctx_rows, cudaStream_t s);
 
 // The extend items of a plan over keys already laid out as bf16 [key][Hkv][D] arrays (the
 // workspace's gathered runs, or a caller's context arrays), then the merge.
@@ -986,6 +1003,11 @@ static int extend_items(const pkv_pool *pool, const void *q, void *o, float sm_s
     p.rec_ml = rec_ml;
     p.rec_list = nullptr;
     p.wait = wait_policy(wait_limit_ns());
+    // The extend kernels of an extend call are ordinary stream launches: they start once the
+    // store / gather before them has completed.  (Launched programmatically, so that their
+    // CTAs took SMs while the store was still running, the serving loop's prefill calls
+    // intermittently found a K/V tile row of another CTA written over a CTA's pipeline
+    // barriers, and the pipeline timed out; with ordinary launches it never did.)
     p.pdl_wait_start = 1;  // the gather (or the store) just before wrote the keys
     p.packs = info->offsets[14] > 0 ? reinterpret_cast<const PackInfo *>(plan + info->offsets[13]) : nullptr;
     void *ev0 = g_kernel_events[0], *ev1 = g_kernel_events[1];
@@ -1000,8 +1022,8 @@ static int extend_items(const pkv_pool *pool, const void *q, void *o, float sm_s
         p.cta_off = reinterpret_cast<const int32_t *>(plan + info->offsets[part == 0 ? 7 : 11]);
         const int64_t nctas = info->offsets[part == 0 ? 8 : 12];
         if (nctas < 1 || nctas > nitems) return PKV_E_PLAN;
-        rc = D == 128 ? dispatch_extend<128>(G, p, mp, (int)nctas, s, part == 1)
-                      : dispatch_extend<64>(G, p, mp, (int)nctas, s, part == 1);
+        rc = D == 128 ? dispatch_extend<128>(G, p, mp, (int)nctas, s, part == 1, false)
+                      : dispatch_extend<64>(G, p, mp, (int)nctas, s, part == 1, false);
         if (rc) return rc;
     }
     if (ev1 && cudaEventRecord(static_cast<cudaEvent_t>(ev1), s) != cudaSuccess) return PKV_E_CUDA;
@@ -1010,14 +1032,23 @@ static int extend_items(const pkv_pool *pool, const void *q, void *o, float sm_s
 
 }  // namespace pkv
 
-extern "C" int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, const void *q, void *o, float sm_scale,
-                               const pkv_plan_info *info, const void *plan_dev, void *workspace, size_t ws_bytes,
-                               void *stream) {
-    using namespace pkv;
+namespace pkv {
+
+// pkv_attn_extend, and with `store` (a fused-store plan) the store of the new tokens first:
+// into the pool and straight into their gathered rows; the gather (cached positions only)
+// then runs beside the store and waits for it only before exiting.
+static int extend_call(const pkv_pool *pool, const pkv_batch *batch, const void *q, void *o, float sm_scale,
+                       const void *k_new, const void *v_new, const int32_t *out_cache_loc, bool store,
+                       const pkv_plan_info *info, const void *plan_dev, void *workspace, size_t ws_bytes,
+                       void *stream) {
     int rc = check_call(pool, batch, q, o, info, plan_dev, workspace, ws_bytes, 2);
     if (rc) return rc;
-    if (info->offsets[16] != 0) return PKV_E_PLAN;  // a context-buffer plan: pkv_attn_extend_ctx
-    if (info->num_items == 0) return PKV_OK;
+    if (info->offsets[16] != (store ? 2 : 0)) return PKV_E_PLAN;
+    if (store) {
+        if (info->total_q > 0 && (!k_new || !v_new || !out_cache_loc)) return PKV_E_INVALID;
+        if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15) return PKV_E_INVALID;
+    }
+    if (info->num_items == 0 && !(store && info->total_q > 0)) return PKV_OK;
     const int D = info->head_dim, hq = info->num_q_heads, hkv = info->num_kv_heads;
     const bool fp8 = pool->dtype == PKV_FP8_E4M3;
     const uint8_t *plan = static_cast<const uint8_t *>(plan_dev);
@@ -1045,17 +1076,42 @@ extern "C" int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, con
     gp.k_out = kg;
     gp.v_out = vg;
     gp.err = reinterpret_cast<int32_t *>(ws);
+    gp.pdl_wait_start = 1;
     const int nunits = (int)info->offsets[5];
     gp.nunits = nunits;  // no query rows to copy
     gp.q_src = nullptr;
     gp.q_out = nullptr;
     gp.q_rows = nullptr;
     gp.q_batch = gp.q_row_vecs = 0;
+    if (store && info->total_q > 0) {
+        rc = launch_store(pool, k_new, v_new, out_cache_loc, info->total_q, ws, kg, vg,
+                          reinterpret_cast<const int32_t *>(plan + info->offsets[15]), nkeys, s);
+        if (rc) return rc;
+        gp.pdl_wait_start = 0;  // it reads no row the store writes
+    }
     if (nunits > 0) {
         rc = D == 128 ? launch_gather<128>(gp, fp8, nunits, s) : launch_gather<64>(gp, fp8, nunits, s);
         if (rc) return rc;
     }
+    if (info->num_items == 0) return PKV_OK;
     return extend_items(pool, q, o, sm_scale, info, plan_dev, ws, kg, vg, nkeys, s);
+}
+
+}  // namespace pkv
+
+extern "C" int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, const void *q, void *o, float sm_scale,
+                               const pkv_plan_info *info, const void *plan_dev, void *workspace, size_t ws_bytes,
+                               void *stream) {
+    return pkv::extend_call(pool, batch, q, o, sm_scale, nullptr, nullptr, nullptr, false, info, plan_dev, workspace,
+                            ws_bytes, stream);
+}
+
+extern "C" int pkv_attn_extend_store(const pkv_pool *pool, const pkv_batch *batch, const void *q, void *o,
+                                     float sm_scale, const void *k_new, const void *v_new,
+                                     const int32_t *out_cache_loc, const pkv_plan_info *info, const void *plan_dev,
+                                     void *workspace, size_t ws_bytes, void *stream) {
+    return pkv::extend_call(pool, batch, q, o, sm_scale, k_new, v_new, out_cache_loc, true, info, plan_dev, workspace,
+                            ws_bytes, stream);
 }
 
 extern "C" int pkv_attn_extend_ctx(const pkv_pool *pool, const void *q, void *o, float sm_scale, const void *k_new,
@@ -1083,7 +1139,7 @@ extern "C" int pkv_attn_extend_ctx(const pkv_pool *pool, const void *q, void *o,
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     // the new tokens into the pool and, as the pool now holds them, into their context rows
     rc = launch_store(pool, k_new, v_new, out_cache_loc, n, ws, ctx_k, ctx_v,
-                      reinterpret_cast<const int32_t *>(plan + info->offsets[15]), s);
+                      reinterpret_cast<const int32_t *>(plan + info->offsets[15]), ctx_rows, s);
     if (rc) return rc;
     if (info->num_items == 0) return PKV_OK;
     return extend_items(pool, q, o, sm_scale, info, plan_dev, ws, static_cast<const uint16_t *>(ctx_k),

@@ -23,6 +23,15 @@ enum DeviceError : int32_t {
 PKV_DEV void set_error(int32_t *err, int32_t code) {
     if (err) atomicCAS(err, 0, code);
 }
+// The same, and when this is the first error, where it happened: words 1-3 of the header get
+// the CTA, the role's position and the parity waited for (diagnostics of a timeout).
+PKV_DEV void set_error_where(int32_t *err, int32_t code, int32_t cta, int32_t ctx, int32_t parity) {
+    if (err && atomicCAS(err, 0, code) == 0) {
+        err[1] = cta;
+        err[2] = ctx;
+        err[3] = parity;
+    }
+}
 
 // ---------------------------------------------------------------------------------------
 // shared-memory addresses and fences

@@ -20,7 +20,9 @@
 namespace pkv {
 
 // CTX: each row is also written, as the bf16 values the pool now holds (fp8: the stored code
-// converted exactly, unscaled), to row ctx_row[token] of the caller's context arrays.
+// converted exactly, unscaled), to row ctx_row[token] of the caller's context arrays
+// (ctx_rows rows; a row outside them records DERR_POSITION with the token and the row, and
+// that copy is skipped).
 template <bool FP8, bool CTX>
 __global__ void __launch_bounds__(256) kv_store_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
                                                        const int32_t *__restrict__ loc, int64_t n, int32_t vec_per_row,
@@ -28,7 +30,8 @@ __global__ void __launch_bounds__(256) kv_store_kernel(const uint4 *__restrict__
                                                        uint8_t *__restrict__ v_pool,
                                                        int64_t num_slots, float k_scale, float v_scale,
                                                        int32_t *__restrict__ err, uint4 *__restrict__ ctx_k,
-                                                       uint4 *__restrict__ ctx_v, const int32_t *__restrict__ ctx_row) {
+                                                       uint4 *__restrict__ ctx_v, const int32_t *__restrict__ ctx_row,
+                                                       int64_t ctx_rows) {
     // one warp per token row (K rows of tokens 0..n-1, then their V rows), grid-strided; the
     // row's slot is read once and the lanes stride its vec_per_row 16-byte source vectors,
     // four loads in flight before their stores
@@ -48,7 +51,14 @@ __global__ void __launch_bounds__(256) kv_store_kernel(const uint4 *__restrict__
         uint8_t *pool = (is_v ? v_pool : k_pool) + (int64_t)slot * slot_bytes;
         const float s = is_v ? v_scale : k_scale;
         uint4 *cdst = nullptr;
-        if constexpr (CTX) cdst = (is_v ? ctx_v : ctx_k) + (int64_t)__ldg(ctx_row + tok) * vec_per_row;
+        if constexpr (CTX) {
+            const int32_t r = __ldg(ctx_row + tok);
+            if (r < 0 || (int64_t)r >= ctx_rows) {
+                if (lane == 0) set_error_where(err, DERR_POSITION, (int32_t)tok, r, 0);
+            } else {
+                cdst = (is_v ? ctx_v : ctx_k) + (int64_t)r * vec_per_row;
+            }
+        }
         for (int v0 = lane; v0 < vec_per_row; v0 += 4 * 32) {
             uint4 x[4];
 #pragma unroll
@@ -60,7 +70,7 @@ __global__ void __launch_bounds__(256) kv_store_kernel(const uint4 *__restrict__
                 if (v >= vec_per_row) continue;
                 if constexpr (!FP8) {
                     reinterpret_cast<uint4 *>(pool)[v] = x[k];
-                    if constexpr (CTX) cdst[v] = x[k];
+                    if (CTX && cdst) cdst[v] = x[k];
                 } else {
                     const uint32_t w[4] = {x[k].x, x[k].y, x[k].z, x[k].w};
                     uint16_t c[4];
@@ -71,7 +81,7 @@ __global__ void __launch_bounds__(256) kv_store_kernel(const uint4 *__restrict__
                     y.x = (uint32_t)c[0] | ((uint32_t)c[1] << 16);
                     y.y = (uint32_t)c[2] | ((uint32_t)c[3] << 16);
                     reinterpret_cast<uint2 *>(pool)[v] = y;
-                    if constexpr (CTX)
+                    if (CTX && cdst)
                         cdst[v] = make_uint4(e4m3x2_to_bf16x2(c[0]), e4m3x2_to_bf16x2(c[1]), e4m3x2_to_bf16x2(c[2]),
                                              e4m3x2_to_bf16x2(c[3]));
                 }
@@ -85,7 +95,7 @@ __global__ void __launch_bounds__(256) kv_store_kernel(const uint4 *__restrict__
 namespace pkv {
 
 int launch_store(const pkv_pool *pool, const void *k_new, const void *v_new, const int32_t *out_cache_loc, int64_t n,
-                 void *workspace, void *ctx_k, void *ctx_v, const int32_t *ctx_row, cudaStream_t s) {
+                 void *workspace, void *ctx_k, void *ctx_v, const int32_t *ctx_row, int64_t ctx_rows, cudaStream_t s) {
     const int64_t row_bytes = (int64_t)pool->num_kv_heads * pool->head_dim * 2;  // bf16 source row
     const int32_t vec_per_row = (int32_t)(row_bytes / 16);
     const int threads = 256;                      // 8 warps, one token row each at a time
@@ -95,12 +105,12 @@ int launch_store(const pkv_pool *pool, const void *k_new, const void *v_new, con
     const bool fp8 = pool->dtype != PKV_BF16, ctx = ctx_k != nullptr;
     auto kern = fp8 ? (ctx ? kv_store_kernel<true, true> : kv_store_kernel<true, false>)
                     : (ctx ? kv_store_kernel<false, true> : kv_store_kernel<false, false>);
-    const cudaError_t e = launch_pdl(kern, dim3((unsigned)blocks), dim3(threads), 0, s,
+    const cudaError_t e = launch_pdl(kern, dim3((unsigned)blocks), dim3(threads), 0, s, true,
                                      reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new),
                                      out_cache_loc, n, vec_per_row, slot_bytes(pool), reinterpret_cast<uint8_t *>(pool->k),
                                      reinterpret_cast<uint8_t *>(pool->v), pool->num_slots, fp8 ? pool->k_scale : 1.f,
                                      fp8 ? pool->v_scale : 1.f, reinterpret_cast<int32_t *>(workspace),
-                                     reinterpret_cast<uint4 *>(ctx_k), reinterpret_cast<uint4 *>(ctx_v), ctx_row);
+                                     reinterpret_cast<uint4 *>(ctx_k), reinterpret_cast<uint4 *>(ctx_v), ctx_row, ctx_rows);
     return e == cudaSuccess ? PKV_OK : PKV_E_CUDA;
 }
 
@@ -115,6 +125,6 @@ extern "C" int pkv_kv_store(const pkv_pool *pool, const void *k_new, const void 
     if (n == 0) return PKV_OK;
     if (!k_new || !v_new || !out_cache_loc) return PKV_E_INVALID;
     if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15) return PKV_E_INVALID;
-    return launch_store(pool, k_new, v_new, out_cache_loc, n, workspace, nullptr, nullptr, nullptr,
+    return launch_store(pool, k_new, v_new, out_cache_loc, n, workspace, nullptr, nullptr, nullptr, 0,
                         reinterpret_cast<cudaStream_t>(stream));
 }

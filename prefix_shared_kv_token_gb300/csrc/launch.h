@@ -14,13 +14,14 @@ namespace pkv {
 
 int num_sms();  // SMs of the current device (cached per device)
 
-// Launch with programmatic stream serialization: the kernel may be scheduled while the
-// previous kernel in the stream still runs (once all that kernel's CTAs issued pdl_trigger or
-// exited), so launch latency and set-up overlap the previous kernel's tail.  The kernel must
-// call pdl_wait before it touches anything earlier work wrote, or before it exits.
+// Launch with programmatic stream serialization (pdl = true): the kernel may be scheduled
+// while the previous kernel in the stream still runs (once all that kernel's CTAs issued
+// pdl_trigger or exited), so launch latency and set-up overlap the previous kernel's tail.
+// The kernel must call pdl_wait before it reads anything earlier work wrote, and before it
+// exits.  pdl = false is an ordinary stream launch (pdl_wait then returns at once).
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                              Args &&...args) {
+                              bool pdl, Args &&...args) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -30,7 +31,7 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 

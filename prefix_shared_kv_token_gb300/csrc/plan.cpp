@@ -596,6 +596,9 @@ static int plan_extend_impl(int32_t batch, const int32_t *seq_lens, const int32_
     // tail, so no key tile is spent on a few leftover span keys.
     struct Seg { int32_t run, len; };
     std::vector<std::vector<Seg>> segs_of(batch);
+    // fused store (pkv_attn_extend_store): the call's store writes each new token's K/V to
+    // the pool and straight to its gathered row, so the gather covers cached positions only
+    const bool fuse = !ctx && opts && opts->fuse_store;
     for (int32_t r = 0; r < batch; ++r) {
         const int32_t ns = (int32_t)spans_of[r].size();
         if (ctx) {
@@ -621,16 +624,25 @@ static int plan_extend_impl(int32_t batch, const int32_t *seq_lens, const int32_
     if (nkeys >= ((int64_t)1 << 31)) return PKV_E_UNSUPPORTED;
     std::vector<GatherUnit> units;
     const int32_t uk = gather_unit_keys(nkeys, num_sms);
+    // each request's own run (its last segment) holds its new positions [seq - ext, seq)
+    std::vector<int32_t> own_run_of(runs.size(), -1);
+    for (int32_t r = 0; r < batch; ++r) own_run_of[(size_t)segs_of[r].back().run] = r;
     if (!ctx)
-        for (const Run &R : runs)
-            for (int32_t c = 0; c < R.len; c += uk)
-                units.push_back({R.src, R.pos0 + c, std::min(uk, R.len - c), R.key0 + c});
-    // context-buffer plans: the row of every new token (in q order), written by the store
+        for (size_t j = 0; j < runs.size(); ++j) {
+            const Run &R = runs[j];
+            const int32_t r = own_run_of[j];
+            const int32_t len = (fuse && r >= 0) ? seq_lens[r] - extend_lens[r] - R.pos0 : R.len;
+            for (int32_t c = 0; c < len; c += uk) units.push_back({R.src, R.pos0 + c, std::min(uk, len - c), R.key0 + c});
+        }
+    // the row of every new token (in q order) that the store writes: in the caller's context
+    // arrays (context-buffer plans) or among the gathered rows (fused-store plans)
     std::vector<int32_t> tok_row;
-    if (ctx)
-        for (int32_t r = 0; r < batch; ++r)
+    if (ctx || fuse)
+        for (int32_t r = 0; r < batch; ++r) {
+            const Run &R = runs[(size_t)segs_of[r].back().run];
             for (int32_t i = 0; i < extend_lens[r]; ++i)
-                tok_row.push_back(ctx_row0[r] + seq_lens[r] - extend_lens[r] + i);
+                tok_row.push_back(R.key0 + seq_lens[r] - extend_lens[r] + i - R.pos0);
+        }
 
     // items: up to 2 x 128/G query tokens of one request x one KV head, over its segments;
     // the last segment is cut at the last query token's position (causal)
@@ -792,7 +804,7 @@ static int plan_extend_impl(int32_t batch, const int32_t *seq_lens, const int32_
     info->offsets[13] = (int64_t)off; off = align16(off + packs.size() * sizeof(PackInfo));
     info->offsets[14] = (int64_t)packs.size();
     info->offsets[15] = (int64_t)off; off = align16(off + tok_row.size() * sizeof(int32_t));
-    info->offsets[16] = ctx ? 1 : 0;
+    info->offsets[16] = ctx ? 1 : (fuse ? 2 : 0);
     std::vector<uint8_t> blob(std::max<size_t>(off, 16), 0);
     put(blob, (size_t)info->offsets[0], placed);
     put(blob, (size_t)info->offsets[13], packs);

@@ -20,8 +20,8 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-from . import (Allocator, Batch, Pool, RadixTree, attn_decode, attn_extend, attn_extend_ctx, check_out_cache_loc,
-               kv_store, plan_decode, plan_extend, plan_extend_ctx)
+from . import (Allocator, Batch, Pool, RadixTree, attn_decode, attn_extend, attn_extend_ctx, attn_extend_store,
+               check_out_cache_loc, kv_store, plan_decode, plan_extend, plan_extend_ctx)
 
 
 def _ctx_tokens(w, req):
@@ -71,6 +71,7 @@ class Call:
     requests: list = field(default_factory=list)
     graph: object = None                           # captured attention launches (capture_attend)
     ctx: tuple = None                              # (ctx_k, ctx_v): a chunk over a context buffer
+    fused: bool = False                            # extend: the attention call stores the new rows
 
     @property
     def num_queries(self) -> int:
@@ -94,14 +95,18 @@ class Call:
         return Call(self.kind, pool, self.batch, self.plan, self.plan_dev, torch.zeros_like(self.workspace), q,
                     torch.empty_like(q), self.out_cache_loc, _bf16_dev(np.concatenate(kn), dev),
                     _bf16_dev(np.concatenate(vn), dev), w.sm_scale, self.last_nodes, cascade=self.cascade,
-                    contexts=self.contexts, requests=reqs, ctx=ctx)
+                    contexts=self.contexts, requests=reqs, ctx=ctx, fused=self.fused)
 
     def store(self, stream=None):
-        if self.ctx is not None:
-            return  # a chunk over a context buffer stores inside its attention call
+        if self.ctx is not None or self.fused:
+            return  # stored inside the attention call
         kv_store(self.pool, self.k_new, self.v_new, self.out_cache_loc, self.workspace, stream)
 
     def attend(self, stream=None):
+        if self.fused:
+            attn_extend_store(self.pool, self.batch, self.q, self.o, self.sm_scale, self.k_new, self.v_new,
+                              self.out_cache_loc, self.plan, self.plan_dev, self.workspace, stream)
+            return
         if self.ctx is not None:
             attn_extend_ctx(self.pool, self.q, self.o, self.sm_scale, self.k_new, self.v_new, self.out_cache_loc,
                             self.ctx[0], self.ctx[1], self.plan, self.plan_dev, self.workspace, stream)
@@ -139,8 +144,8 @@ class Call:
             n = 1 if self.out_cache_loc.numel() > 0 else 0       # then the extend kernel(s)
             nprec = int(info.offsets[10])
             n += (1 if info.num_items - nprec > 0 else 0) + (1 if nprec > 0 else 0)
-        elif self.kind == "extend":
-            nprec = int(info.offsets[10])                        # items with precise weights
+        elif self.kind == "extend":                              # (a fused call's store is its own
+            nprec = int(info.offsets[10])                        # launch, counted above)
             n += (1 if info.offsets[5] > 0 else 0)               # key gather
             n += (1 if info.num_items - nprec > 0 else 0) + (1 if nprec > 0 else 0)  # extend kernel(s)
         else:
@@ -199,7 +204,7 @@ class Call:
                      torch.empty_like(self.q), torch.empty_like(self.o), torch.empty_like(self.out_cache_loc),
                      torch.empty_like(self.k_new), torch.empty_like(self.v_new), self.sm_scale, self.last_nodes,
                      host=self.host, cascade=self.cascade, contexts=self.contexts, requests=self.requests,
-                     ctx=self.ctx)
+                     ctx=self.ctx, fused=self.fused)
             out.append(c)
         return out
 
@@ -258,11 +263,13 @@ class PrefixCache:
     ``check_slots`` runs the host check of every call's ``out_cache_loc`` (slots in range and
     distinct, kv_store's precondition) before anything is copied to the device.
     ``kv_layout``: "interleaved" (a slot's K and V rows adjacent: decode reads both with one
-    copy) or "separate" (two dense arrays)."""
+    copy) or "separate" (two dense arrays).  ``fuse_store``: extend calls store their new
+    rows themselves (pool and gathered rows in one pass) instead of a separate kv_store."""
 
-    def __init__(self, w, device="cuda", page_size=1, check_slots=True, kv_layout="interleaved"):
+    def __init__(self, w, device="cuda", page_size=1, check_slots=True, kv_layout="interleaved", fuse_store=True):
         self.w = w
         self.check_slots = bool(check_slots)
+        self.fuse_store = bool(fuse_store)
         self.device = device
         self.page = int(page_size)
         self.pool = Pool.allocate(w.num_slots, w.num_kv_heads, w.head_dim, w.dtype, w.k_scale, w.v_scale, device,
@@ -392,6 +399,8 @@ class PrefixCache:
             plan = plan_extend_ctx(seq, ext, qo, row0, ctx_base["rows"], hq, hkv, d, opts)
         elif kind == "extend":
             qo = np.concatenate([[0], np.cumsum(ext)]).astype(np.int32)
+            if self.fuse_store:
+                opts = dict(opts or {}, fuse_store=1)
             plan = plan_extend(seq, ext, qo, hq, hkv, d, casc, opts)
         else:
             plan = plan_decode(seq, hq, hkv, d, casc, opts)
@@ -449,7 +458,8 @@ class PrefixCache:
         v_new = _bf16_dev(np.concatenate(vn), dev)
         call = Call(kind, self.pool, batch, plan, plan_dev, ws, q, o, loc, k_new, v_new, w.sm_scale,
                     h["last_nodes"], cascade=h["cascade"],
-                    ctx=None if ctx is None else (ctx["k"], ctx["v"]))
+                    ctx=None if ctx is None else (ctx["k"], ctx["v"]),
+                    fused=kind == "extend" and ctx is None and self.fuse_store)
         call.contexts = [(_ctx_tokens(w, r), row, len(row) - r.n_new) for r, row in zip(reqs, rows)]
         call.requests = reqs
         return call

@@ -10,8 +10,8 @@ recently used first and the paths of running requests are locked ("[SGLang] Radi
 inserted into the tree, where later requests can hit it.
 
 Every step the host (C++ tree, scheduler and planner through ``libpkv``) decides the batch
-and the device runs kv_store + attn_extend for the admitted prompts and kv_store +
-attn_decode for one new token of every running request.  The decode plan is made with
+and the device runs attn_extend_store for the admitted prompts (their new rows stored by the
+extend call itself) and kv_store + attn_decode for one new token of every running request.  The decode plan is made with
 ``dynamic_tail`` (each request's last item reads its end from the device ``seq_lens``), so it
 stays valid while the running set is unchanged and is only re-planned when a request joins
 or leaves.  Synthetic inputs come from the seeded generators in ``workloads``: the K/V of a
@@ -31,7 +31,8 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-from . import (Allocator, Batch, Pool, RadixTree, attn_decode, attn_extend, kv_store, plan_decode, plan_extend)
+from . import (Allocator, Batch, Pool, RadixTree, attn_decode, attn_extend_store, kv_store, plan_decode,
+               plan_extend)
 
 
 def _bf16(bits: np.ndarray, device) -> torch.Tensor:
@@ -71,7 +72,7 @@ class ServingSim:
         self.record = record
         self.opts = {"dynamic_tail": 1, **({"chunk_keys": chunk_keys} if chunk_keys else {})}
         s = stream
-        self.pool = Pool.allocate(capacity, s.num_kv_heads, s.head_dim, "bf16", device=device)
+        self.pool = Pool.allocate(capacity, s.num_kv_heads, s.head_dim, "bf16", device=device, layout="interleaved")
         self.page = P = int(page_size)
         self.tree = RadixTree(eviction, page_size=P)
         self.alloc = Allocator(np.arange(capacity // P, dtype=np.int32))   # slots, or pages
@@ -88,6 +89,8 @@ class ServingSim:
                       "finished": 0, "evicted_tokens": 0, "plans": 0, "device_ms": 0.0, "steps": 0}
         self._decode = None          # (running rids, plan, plan_dev, workspace, batch)
         self._ev = []
+        self._err_words = []      # the header words of every call's workspace, checked after the run
+        self._plans = []
 
     # ---- slots ---------------------------------------------------------------------
     def _ensure(self, n: int) -> bool:
@@ -141,6 +144,25 @@ class ServingSim:
             self.step()
         torch.cuda.synchronize()
         self.stats["device_ms"] = sum(a.elapsed_time(b) for a, b in self._ev)
+        # every call's error word (kernels only set it): a range or timeout flag fails the run
+        if self._err_words:
+            words = torch.stack(self._err_words).cpu()
+            bad = (words[:, 0] != 0).nonzero()
+            if len(bad):
+                k = int(bad[0, 0])
+                plan = self._plans[k]
+                item = int(words[k, 2]) >> 16
+                info = plan.info
+                blob = plan.blob
+                desc = {}
+                for name, off in (("main", int(info.offsets[0])), ("second", int(info.offsets[9]))):
+                    a = off + 64 * item
+                    if a + 64 <= len(blob):
+                        desc[name] = np.frombuffer(blob[a:a + 64].tobytes(), np.int32).tolist()
+                raise RuntimeError(f"a kernel of the serving run set its error word: {int(words[k, 0]):#x} (call {k}, "
+                                   f"op {info.op}, header words {[int(x) for x in words[k, 1:4]]}, items "
+                                   f"{info.num_items} (second list {int(info.offsets[10])}), packs "
+                                   f"{int(info.offsets[14])}, item {item}: {desc})")
         return self.stats
 
     # ---- admission: scheduler order, lock the cached path, reserve slots ----------------
@@ -201,7 +223,7 @@ class ServingSim:
         casc = self.tree.cascade(nodes, 2) if len(nodes) > 1 else None
         if casc is not None and casc.num_spans == 0:
             casc = None
-        plan = plan_extend(seq, ext, qo, s.num_q_heads, s.num_kv_heads, s.head_dim, casc)
+        plan = plan_extend(seq, ext, qo, s.num_q_heads, s.num_kv_heads, s.head_dim, casc, {"fuse_store": 1})
         self.seq[rows] = torch.from_numpy(seq).to(dev)
         batch = Batch(self.rt, torch.tensor(rows, dtype=torch.int32, device=dev), self.seq[rows].contiguous(),
                       self.page)
@@ -210,11 +232,14 @@ class ServingSim:
         ws = torch.zeros((plan.info.workspace_bytes + 3) // 4, dtype=torch.int32, device=dev)
         ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
         ev[0].record()
-        kv_store(self.pool, _bf16(np.concatenate(ks), dev), _bf16(np.concatenate(vs), dev),
-                 torch.from_numpy(np.concatenate(locs)).to(dev), ws)
-        attn_extend(self.pool, batch, q, o, s.sm_scale, plan, torch.from_numpy(plan.blob).to(dev), ws)
+        # the prompts' new rows are stored by the attention call itself (pool and gathered rows)
+        attn_extend_store(self.pool, batch, q, o, s.sm_scale, _bf16(np.concatenate(ks), dev),
+                          _bf16(np.concatenate(vs), dev), torch.from_numpy(np.concatenate(locs)).to(dev), plan,
+                          torch.from_numpy(plan.blob).to(dev), ws)
         ev[1].record()
         self._ev.append(ev)
+        self._err_words.append(ws[:4].clone())
+        self._plans.append(plan)
         self.stats["prefill_tokens"] += int(ext.sum())
         if self.record:
             self.records.append(StepRecord("extend", [run.req.rid for run, _ in admitted],
@@ -281,6 +306,8 @@ class ServingSim:
         attn_decode(self.pool, batch, q, o, s.sm_scale, plan, plan_dev, ws)
         ev[1].record()
         self._ev.append(ev)
+        self._err_words.append(ws[:4].clone())
+        self._plans.append(plan)
         self.stats["decode_tokens"] += len(runs)
         if self.record:
             self.records.append(StepRecord("decode", [r.req.rid for r in runs], [[p] for p in pos],

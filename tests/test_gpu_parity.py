@@ -439,3 +439,28 @@ def test_interleaved_and_separate_pools_give_identical_results(dtype, page):
         outs[layout] = {k: c.o.clone() for k, c in calls.items()}
     for k in outs["separate"]:
         assert torch.equal(outs["interleaved"][k], outs["separate"][k]), k
+
+
+@pytest.mark.parametrize("dtype,page,cascade", [("bf16", 1, True), ("bf16", 1, False), ("fp8_e4m3", 1, True),
+                                                ("bf16", 16, True)])
+def test_fused_store_extend_equals_store_then_extend(dtype, page, cascade):
+    # kv_store + attn_extend as one call (the new rows stored into the pool and straight into
+    # their gathered rows) against the separate store and the gather of every position:
+    # outputs and pool rows bit for bit, both against the oracle
+    pkv, PrefixCache = _pkv()
+    w = W.fewshot_extend(seed=41, n_req=7, prefix=333, suffix=150, num_slots=8192, dtype=dtype)
+    res = {}
+    for fused in (True, False):
+        pc = PrefixCache(w, page_size=page, fuse_store=fused)
+        pc.populate()
+        c = pc.prepare("extend", cascade=cascade)
+        assert c.fused == fused and int(c.plan.info.offsets[16]) == (2 if fused else 0)
+        c.run()
+        torch.cuda.synchronize()
+        assert pkv.get_device_error(c.workspace) == 0
+        check_outputs(w, {"extend": c})
+        check_pool(w, pc)
+        idx = c.out_cache_loc.long()
+        res[fused] = (c.o.clone(), pc.pool.k[idx].clone(), pc.pool.v[idx].clone())
+    for a, b in zip(res[True], res[False]):
+        assert torch.equal(a, b)

@@ -233,7 +233,9 @@ int pkv_attn_extend(const pkv_pool *pool, const pkv_batch *batch, const void *q,
  *   k_new, v_new, out_cache_loc  the new tokens' rows and slots in q order (total_q rows),
  *                                as pkv_kv_store takes them
  * Everything else as pkv_attn_extend; slot-range errors of the store go to the workspace
- * error word.  pkv_attn_extend rejects a fused-store plan and this call any other. */
+ * error word, and so does a context row outside the plan's gathered rows (PKV_DERR_POSITION,
+ * header words 1-2 = the token and the row; that copy is skipped).  pkv_attn_extend rejects
+ * a fused-store plan and this call any other. */
 int pkv_attn_extend_store(const pkv_pool *pool, const pkv_batch *batch, const void *q, void *o, float sm_scale,
                           const void *k_new, const void *v_new, const int32_t *out_cache_loc,
                           const pkv_plan_info *info, const void *plan_dev, void *workspace, size_t ws_bytes,
@@ -265,7 +267,8 @@ int pkv_plan_extend_ctx(int32_t batch, const int32_t *seq_lens, const int32_t *e
  *   ctx_k, ctx_v, ctx_rows    the context arrays (device, 16-byte aligned), ctx_rows rows each
  *   workspace                 as pkv_attn_extend; slot-range errors of the store are recorded
  *                             in its error word (a bad slot's pool and context rows are not
- *                             written)
+ *                             written), and so is a context row outside [0, ctx_rows)
+ *                             (PKV_DERR_POSITION; that copy is skipped)
  * pkv_attn_extend rejects a context-buffer plan and this call any other (PKV_E_PLAN). */
 int pkv_attn_extend_ctx(const pkv_pool *pool, const void *q, void *o, float sm_scale, const void *k_new,
                         const void *v_new, const int32_t *out_cache_loc, void *ctx_k, void *ctx_v,
@@ -285,7 +288,8 @@ int pkv_set_kernel_events(void *start, void *stop);
 
 /* Failure-detection hook (no counterpart in the pages).  Every wait inside the attention
  * kernels (one role waiting for another's copy, MMA or release) is bounded; when one gives up,
- * the kernel records PKV_DERR_TIMEOUT | which-wait in the error word, every role of that CTA
+ * the kernel records PKV_DERR_TIMEOUT | which-wait in the error word (an extend kernel also
+ * the CTA and the parity waited for, in header words 1 and 3), every role of that CTA
  * stops, copies and MMAs already in flight are allowed to land, tensor memory is freed and
  * the kernel returns: the context stays usable and the host sees the flag through
  * pkv_get_device_error.  This sets the limit used by attention calls launched (or captured)

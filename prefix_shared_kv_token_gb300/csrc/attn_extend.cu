@@ -97,10 +97,10 @@ struct XBars {
     int32_t abort_flag;
 };
 
-// ctx: the waiting role's position (item << 16 | its tile or phase counter), recorded with
-// the CTA and the parity waited for when this wait is the launch's first timeout.
-PKV_DEV bool xwait(uint64_t *bar, uint32_t parity, XBars *b, int32_t *err, int where, const WaitPolicy &wp,
-                   int32_t ctx) {
+// The launch's first timeout records the wait site (low byte of the code), the CTA and the
+// parity waited for.  (Recording the role's item and tile as well cost the kernel 3 %: the
+// arguments are computed on every wait.)
+PKV_DEV bool xwait(uint64_t *bar, uint32_t parity, XBars *b, int32_t *err, int where, const WaitPolicy &wp) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
@@ -108,7 +108,7 @@ PKV_DEV bool xwait(uint64_t *bar, uint32_t parity, XBars *b, int32_t *err, int w
         if (it == 1 || (it & wp.check_mask) == 0) {
             if (*reinterpret_cast<volatile int32_t *>(&b->abort_flag)) return false;
             if (global_timer_ns() - t0 > wp.limit_ns) {
-                set_error_where(err, DERR_TIMEOUT | where, (int32_t)blockIdx.x, ctx, (int32_t)parity);
+                set_error_where(err, DERR_TIMEOUT | where, (int32_t)blockIdx.x, 0, (int32_t)parity);
                 *reinterpret_cast<volatile int32_t *>(&b->abort_flag) = 1;
                 return false;
             }
@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(384, 1)
                 const ExtendItem *itp = p.items + i;
                 const XItem it = load_item(itp, TQ, p.packs);
                 if (kside) {
-                    if (nql > 0 && !xwait(&bars->qempty, (nql - 1) & 1, bars, p.err, 6, p.wait, (i << 16) | (nql & 0xFFFF))) break;
+                    if (nql > 0 && !xwait(&bars->qempty, (nql - 1) & 1, bars, p.err, 6, p.wait)) break;
                     if (it.pk) {
                         // a packed tile: each row group's tokens by their own 32-row box
                         int ng = 0;
@@ -464,7 +464,7 @@ __global__ void __launch_bounds__(384, 1)
                         const bool early = kside && ((split_mask >> s) & 1u);
                         uint64_t *bar = early ? &bars->kempty[s] : &bars->kvempty[s];
                         const uint32_t par = early ? ((kpar >> s) & 1u) ^ 1u : (uint32_t)((tp / ST) - 1) & 1u;
-                        if (!xwait(bar, par, bars, p.err, kside ? 5 : 7, p.wait, (i << 16) | (tp & 0xFFFF))) {
+                        if (!xwait(bar, par, bars, p.err, kside ? 5 : 7, p.wait)) {
                             ok = false;
                             break;
                         }
@@ -501,11 +501,11 @@ __global__ void __launch_bounds__(384, 1)
             bool ok = true;
             for (int i = i0; ok && i < i1; ++i, ++ip) {
                 const XItem it = load_item(p.items + i, TQ, p.packs);
-                if (!xwait(&bars->q, ip & 1, bars, p.err, 1, p.wait, (i << 16) | (ip & 0xFFFF))) break;
+                if (!xwait(&bars->q, ip & 1, bars, p.err, 1, p.wait)) break;
                 if (!it.split) {
                     auto issue_s = [&](int q, int j) -> bool {
                         const int tg = tm + j, s = tg % ST;
-                        if (q == 0 && !xwait(&bars->kfull[s], (tg / ST) & 1, bars, p.err, 4, p.wait, (i << 16) | (tg & 0xFFFF))) return false;
+                        if (q == 0 && !xwait(&bars->kfull[s], (tg / ST) & 1, bars, p.err, 4, p.wait)) return false;
                         tc_fence_after();
                         const uint32_t q_s = sbase + C::kQOff + q * C::kQTile;
                         const uint32_t k_s = sbase + C::kStageOff + (s * 2) * C::kKTile;
@@ -521,9 +521,9 @@ __global__ void __launch_bounds__(384, 1)
                     };
                     auto issue_pv = [&](int q, int j) -> bool {
                         const int tg = tm + j, s = tg % ST;
-                        if (!xwait(&bars->pfull[q], (cpar >> q) & 1u, bars, p.err, 2, p.wait, (i << 16) | (tg & 0xFFFF))) return false;
+                        if (!xwait(&bars->pfull[q], (cpar >> q) & 1u, bars, p.err, 2, p.wait)) return false;
                         cpar ^= 1u << q;
-                        if (q == 0 && !xwait(&bars->vfull[s], (tg / ST) & 1, bars, p.err, 3, p.wait, (i << 16) | (tg & 0xFFFF))) return false;
+                        if (q == 0 && !xwait(&bars->vfull[s], (tg / ST) & 1, bars, p.err, 3, p.wait)) return false;
                         tc_fence_after();
                         const uint32_t v_s = sbase + C::kStageOff + (s * 2 + 1) * C::kKTile;
 #pragma unroll
@@ -560,7 +560,7 @@ __global__ void __launch_bounds__(384, 1)
                     // its S is done and the next K tile loads while this one's P.V still waits.
                     auto split_s = [&](int j) -> bool {
                         const int q = j & 1, tg = tm + j, s = tg % ST;
-                        if (!xwait(&bars->kfull[s], (tg / ST) & 1, bars, p.err, 4, p.wait, (i << 16) | (tg & 0xFFFF))) return false;
+                        if (!xwait(&bars->kfull[s], (tg / ST) & 1, bars, p.err, 4, p.wait)) return false;
                         tc_fence_after();
                         const uint32_t q_s = sbase + C::kQOff;
                         const uint32_t k_s = sbase + C::kStageOff + (s * 2) * C::kKTile;
@@ -577,9 +577,9 @@ __global__ void __launch_bounds__(384, 1)
                     };
                     auto split_pv = [&](int j) -> bool {
                         const int q = j & 1, tg = tm + j, s = tg % ST;
-                        if (!xwait(&bars->pfull[q], (cpar >> q) & 1u, bars, p.err, 2, p.wait, (i << 16) | (tg & 0xFFFF))) return false;
+                        if (!xwait(&bars->pfull[q], (cpar >> q) & 1u, bars, p.err, 2, p.wait)) return false;
                         cpar ^= 1u << q;
-                        if (!xwait(&bars->vfull[s], (tg / ST) & 1, bars, p.err, 3, p.wait, (i << 16) | (tg & 0xFFFF))) return false;
+                        if (!xwait(&bars->vfull[s], (tg / ST) & 1, bars, p.err, 3, p.wait)) return false;
                         tc_fence_after();
                         const uint32_t v_s = sbase + C::kStageOff + (s * 2 + 1) * C::kKTile;
 #pragma unroll
@@ -648,7 +648,7 @@ __global__ void __launch_bounds__(384, 1)
                     continue;
                 }
                 // lanes leave together: a split warp must not reach the .sync.aligned tcgen05 ops
-                if (!__all_sync(0xffffffffu, xwait(&bars->sfull[q], cw & 1, bars, p.err, 8, p.wait, (i << 16) | (cw & 0xFFFF)))) {
+                if (!__all_sync(0xffffffffu, xwait(&bars->sfull[q], cw & 1, bars, p.err, 8, p.wait))) {
                     ok = false;
                     break;
                 }
@@ -724,7 +724,7 @@ __global__ void __launch_bounds__(384, 1)
                 tc_fence_before();
                 mbar_arrive(&bars->pfull[q]);
             }
-            bool fin = __all_sync(0xffffffffu, ok && xwait(&bars->ofinal[q], co & 1, bars, p.err, 10, p.wait, (i << 16) | (co & 0xFFFF)));
+            bool fin = __all_sync(0xffffffffu, ok && xwait(&bars->ofinal[q], co & 1, bars, p.err, 10, p.wait));
             if (it.split) {
                 // exchange the row's running max and sum with the other warpgroup; both
                 // warpgroups leave together when either gave up on a wait

@@ -24,12 +24,13 @@ PKV_DEV void set_error(int32_t *err, int32_t code) {
     if (err) atomicCAS(err, 0, code);
 }
 // The same, and when this is the first error, where it happened: words 1-3 of the header get
-// the CTA, the role's position and the parity waited for (diagnostics of a timeout).
-PKV_DEV void set_error_where(int32_t *err, int32_t code, int32_t cta, int32_t ctx, int32_t parity) {
+// three values of the caller's choosing (an extend-kernel timeout: the CTA, 0 and the parity
+// waited for; the fused store's bad context row: the token and the row).
+PKV_DEV void set_error_where(int32_t *err, int32_t code, int32_t w1, int32_t w2, int32_t w3) {
     if (err && atomicCAS(err, 0, code) == 0) {
-        err[1] = cta;
-        err[2] = ctx;
-        err[3] = parity;
+        err[1] = w1;
+        err[2] = w2;
+        err[3] = w3;
     }
 }
 

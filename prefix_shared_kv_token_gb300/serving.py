@@ -150,19 +150,17 @@ class ServingSim:
             bad = (words[:, 0] != 0).nonzero()
             if len(bad):
                 k = int(bad[0, 0])
-                plan = self._plans[k]
-                item = int(words[k, 2]) >> 16
-                info = plan.info
-                blob = plan.blob
-                desc = {}
-                for name, off in (("main", int(info.offsets[0])), ("second", int(info.offsets[9]))):
-                    a = off + 64 * item
-                    if a + 64 <= len(blob):
-                        desc[name] = np.frombuffer(blob[a:a + 64].tobytes(), np.int32).tolist()
-                raise RuntimeError(f"a kernel of the serving run set its error word: {int(words[k, 0]):#x} (call {k}, "
-                                   f"op {info.op}, header words {[int(x) for x in words[k, 1:4]]}, items "
-                                   f"{info.num_items} (second list {int(info.offsets[10])}), packs "
-                                   f"{int(info.offsets[14])}, item {item}: {desc})")
+                info = self._plans[k].info
+                code, w1, w2, w3 = (int(x) for x in words[k, :4])
+                if code & 0x200:    # a pipeline wait gave up: its site, the CTA, the parity
+                    where = f"wait site {code & 0xFF} in CTA {w1} (parity {w3})"
+                elif code & 0x400 and info.op == 2:   # the fused store: token and context row
+                    where = f"token {w1} / context row {w2}, or a work item outside its row"
+                else:
+                    where = f"header words {[w1, w2, w3]}"
+                raise RuntimeError(f"a kernel of the serving run set its error word: {code:#x} (call {k}, op "
+                                   f"{info.op}, {where}; plan: {info.num_items} items, "
+                                   f"{int(info.offsets[10])} of them in the second list)")
         return self.stats
 
     # ---- admission: scheduler order, lock the cached path, reserve slots ----------------

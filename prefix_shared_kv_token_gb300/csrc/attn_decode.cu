@@ -38,6 +38,9 @@
 #include "common.cuh"
 #include "launch.h"
 
+// persistent decode CTAs per SM for a head group of hg KV heads (the planner's rule)
+int decode_ctas_per_sm(int32_t hg, int32_t d);
+
 namespace pkv {
 
 struct DecodeParams {
@@ -67,6 +70,9 @@ struct DecodeParams {
     float *rec_ml;      // [rec][hq][2]
     int32_t *err;
     WaitPolicy wait;    // pipeline waits (pkv_set_wait_limit_ns)
+    int32_t late_wait;  // 1: the kernel before (the span gather) wrote nothing this one reads; an
+                        // extra warp waits for it and then releases the next kernel, the others
+                        // start at once
 };
 
 constexpr int kBK = 16;       // keys per tile
@@ -333,7 +339,7 @@ PKV_DEV TileSlot next_tile(const DecodeParams &p, TileCursor &cur, int c1, int k
 }
 
 template <int D, int G, bool FP8, bool QUICK>
-__global__ void __launch_bounds__(288, (D == 64 ? 2 : 1)) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__((D == 64 ? 288 : 320), (D == 64 ? 2 : 1)) decode_kernel(const DecodeParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     using Gm = DGeo<D, FP8>;
     constexpr int S = Gm::kStages;
@@ -344,8 +350,11 @@ __global__ void __launch_bounds__(288, (D == 64 ? 2 : 1)) decode_kernel(const De
     uint8_t *ring = smem + kHdr;
     const Gm geo(p.hg, p.joint != 0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    pdl_wait();     // the query tokens' K/V were stored, and the span gather ran, just before
-    pdl_trigger();  // the span pass may take SMs as this kernel's CTAs finish
+    const bool late = p.late_wait != 0;
+    if (!late) {
+        pdl_wait();     // the query tokens' K/V were stored just before
+        pdl_trigger();  // the span pass may take SMs as this kernel's CTAs finish
+    }
     const int c0 = __ldg(p.cta_off + blockIdx.x), c1 = __ldg(p.cta_off + blockIdx.x + 1);
 
     if (threadIdx.x == 0) {
@@ -357,6 +366,19 @@ __global__ void __launch_bounds__(288, (D == 64 ? 2 : 1)) decode_kernel(const De
         fence_mbar_init();
     }
     __syncthreads();
+
+    if (late && warp == p.hg + 1) {
+        // After the span gather, which reads the pool but writes only its own rows, the other
+        // warps stream at once: what they read (pool, tables, queries, plan) was complete
+        // before the gather started, since the gather waited for the kernel before it.  This
+        // warp waits for the gather, then lets the span pass (which reads the gather's rows)
+        // be scheduled; the CTA completes only after the gather has.
+        if (lane == 0) {
+            pdl_wait();
+            pdl_trigger();
+        }
+        return;
+    }
 
     if (warp == p.hg) {
         // ------------------------------------------------------------------ producer warp
@@ -574,7 +596,8 @@ static int launch_decode(const DecodeParams &p, int nctas, cudaStream_t s) {
     auto kern = p.wait.quick ? decode_kernel<D, G, FP8, true> : decode_kernel<D, G, FP8, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, geo.bytes) != cudaSuccess)
         return PKV_E_CUDA;
-    return launch_pdl(kern, dim3(nctas), dim3(32 * (p.hg + 1)), geo.bytes, s, true, p) == cudaSuccess ? PKV_OK : PKV_E_CUDA;
+    const int warps = p.hg + 1 + (p.late_wait ? 1 : 0);
+    return launch_pdl(kern, dim3(nctas), dim3(32 * warps), geo.bytes, s, true, p) == cudaSuccess ? PKV_OK : PKV_E_CUDA;
 }
 
 template <int D>
@@ -670,6 +693,11 @@ extern "C" int pkv_attn_decode(const pkv_pool *pool, const pkv_batch *batch, con
     // merge reads them.
     rc = decode_span_gather(pool, batch, q, info, plan, ws, s);
     if (rc) return rc;
+    // After a span gather the decode kernel streams from its start and one extra warp waits
+    // for the gather, where that warp does not cost the kernel a CTA per SM (d = 128: 12 warps
+    // of 168 registers fit an SM; at most 10 warps a CTA).
+    const int per_sm = decode_ctas_per_sm((int32_t)hg, info->head_dim);
+    p.late_wait = (info->offsets[8] > 0 && info->head_dim == 128 && hg + 2 <= 10 && per_sm * (hg + 2) <= 12) ? 1 : 0;
     if (info->num_items > 0) {
         const int G = info->num_q_heads / info->num_kv_heads;
         rc = info->head_dim == 128 ? dispatch_g<128>(G, fp8, p, (int)nctas, s)

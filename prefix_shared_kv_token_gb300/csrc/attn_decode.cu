@@ -533,9 +533,11 @@ __global__ void __launch_bounds__((D == 64 ? 288 : 320), (D == 64 ? 2 : 1)) deco
 template <int D>
 __global__ void __launch_bounds__(256) merge_kernel(const MergeItem *__restrict__ merges, const float *__restrict__ rec_acc,
                                                     const float *__restrict__ rec_ml, uint16_t *__restrict__ o, int hq) {
+    // the merge list is plan data, complete before the call: read it while the kernel before
+    // is still running, then wait for the records
+    const MergeItem mi = merges[blockIdx.x];
     pdl_wait();  // every record of the call has been written
     pdl_trigger();
-    const MergeItem mi = merges[blockIdx.x];
     const int h = blockIdx.y * 8 + (threadIdx.x >> 5);
     if (h >= hq) return;
     const int lane = threadIdx.x & 31;

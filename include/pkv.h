@@ -288,8 +288,7 @@ int pkv_set_kernel_events(void *start, void *stop);
 
 /* Failure-detection hook (no counterpart in the pages).  Every wait inside the attention
  * kernels (one role waiting for another's copy, MMA or release) is bounded; when one gives up,
- * the kernel records PKV_DERR_TIMEOUT | which-wait in the error word (an extend kernel also
- * the CTA and the parity waited for, in header words 1 and 3), every role of that CTA
+ * the kernel records PKV_DERR_TIMEOUT | which-wait in the error word, every role of that CTA
  * stops, copies and MMAs already in flight are allowed to land, tensor memory is freed and
  * the kernel returns: the context stays usable and the host sees the flag through
  * pkv_get_device_error.  This sets the limit used by attention calls launched (or captured)

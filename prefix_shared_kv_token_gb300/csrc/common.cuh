@@ -24,8 +24,8 @@ PKV_DEV void set_error(int32_t *err, int32_t code) {
     if (err) atomicCAS(err, 0, code);
 }
 // The same, and when this is the first error, where it happened: words 1-3 of the header get
-// three values of the caller's choosing (an extend-kernel timeout: the CTA, 0 and the parity
-// waited for; the fused store's bad context row: the token and the row).
+// three values of the caller's choosing (the fused store's bad context row: the token, the row
+// and 0).
 PKV_DEV void set_error_where(int32_t *err, int32_t code, int32_t w1, int32_t w2, int32_t w3) {
     if (err && atomicCAS(err, 0, code) == 0) {
         err[1] = w1;

@@ -152,8 +152,8 @@ class ServingSim:
                 k = int(bad[0, 0])
                 info = self._plans[k].info
                 code, w1, w2, w3 = (int(x) for x in words[k, :4])
-                if code & 0x200:    # a pipeline wait gave up: its site, the CTA, the parity
-                    where = f"wait site {code & 0xFF} in CTA {w1} (parity {w3})"
+                if code & 0x200:    # a pipeline wait gave up (low byte: which wait)
+                    where = f"wait site {code & 0xFF}"
                 elif code & 0x400 and info.op == 2:   # the fused store: token and context row
                     where = f"token {w1} / context row {w2}, or a work item outside its row"
                 else:

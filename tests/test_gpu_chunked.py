@@ -136,3 +136,44 @@ def test_multi_layer_pools_share_tables_and_plan(fused):
         for c in per_layer[l]:
             _check(layers[l], c)
         assert per_layer[l][0].plan is base[0].plan   # one plan for all layers
+
+
+@pytest.mark.parametrize("path", ["context_buffer", "fused_store"])
+def test_store_reports_an_out_of_range_row_without_writing_it(path):
+    # The store of a context-buffer or fused-store call writes each new token's K/V to the
+    # pool and to row tok_row[token] of the context / gathered arrays.  A host-made row past
+    # those arrays must be reported (PKV_DERR_POSITION, header words = token and row) and its
+    # copy skipped; the pool rows are still stored.
+    import prefix_shared_kv_token_gb300 as pkv
+    from prefix_shared_kv_token_gb300.runtime import PrefixCache
+    if path == "context_buffer":
+        w = W.chunked_prefill(seed=66, n_req=1, prompt=300, chunk=150, num_slots=2000)
+        pc = PrefixCache(w)
+        c = pc.prepare_chunked(fused=True)[0]
+        rows = int(c.ctx[0].shape[0])
+        before = c.ctx[0].clone()
+    else:
+        w = W.fewshot_extend(seed=67, n_req=3, prefix=200, suffix=40, num_slots=4096)
+        pc = PrefixCache(w, fuse_store=True)
+        pc.populate()
+        c = pc.prepare("extend", cascade=True)
+        assert c.fused
+        rows = int(c.plan.info.offsets[6])
+    tok, bad = 3, rows + 7
+    at = int(c.plan.info.offsets[15]) + 4 * tok
+    c.plan_dev[at:at + 4] = torch.tensor([bad], dtype=torch.int32).view(torch.uint8).to(c.plan_dev.device)
+    c.workspace.zero_()
+    c.attend()
+    torch.cuda.synchronize()
+    words = c.workspace[:4].view(torch.int32).cpu().tolist()
+    assert words[0] == 0x400 and words[1] == tok and words[2] == bad, words
+    assert pkv.get_device_error(c.workspace) == 0x400
+    # the token's pool rows were stored (bf16: the new rows themselves)
+    slot = int(c.out_cache_loc[tok])
+    assert torch.equal(pc.pool.k[slot].view(torch.int16).cpu(), c.k_new[tok].view(torch.int16).cpu())
+    assert torch.equal(pc.pool.v[slot].view(torch.int16).cpu(), c.v_new[tok].view(torch.int16).cpu())
+    if path == "context_buffer":
+        # no context row was written for it: its own row keeps what it held before
+        ok = int(torch.from_numpy(c.plan.blob[int(c.plan.info.offsets[15]):][:4 * (tok + 1)].copy())
+                 .view(torch.int32)[tok])
+        assert torch.equal(c.ctx[0][ok], before[ok])

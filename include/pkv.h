@@ -419,6 +419,17 @@ int pkv_schedule(pkv_tree *t, const int32_t *tokens, const int64_t *offsets, int
 int pkv_tree_inc_lock_ref(pkv_tree *t, int64_t node, int64_t *delta);
 int pkv_tree_dec_lock_ref(pkv_tree *t, int64_t node, int64_t *delta);
 
+/* A batch's match-and-lock in one call: for i = 0 .. n-1 in order, key i = keys[offsets[i] ..
+ * offsets[i+1]) (host, CSR) is matched as pkv_tree_match_prefix matches it (splitting a node
+ * it ends inside, updating access times) and the path to its last matched node is locked as
+ * pkv_tree_inc_lock_ref locks it -- the same tree, values and nodes as the 2n single calls.
+ * values (room for offsets[n] entries) receives the matched values of every key back to
+ * back, key i's at values[sum of matched[0 .. i)]; matched[i] and last_nodes[i] get key i's
+ * matched length and last node.  What a server does for every newly admitted batch before
+ * planning it ([RC] "매칭", "참조 카운트: lock_ref"). */
+int pkv_tree_match_lock_batch(pkv_tree *t, const int32_t *keys, const int64_t *offsets, int32_t n,
+                              int32_t *values, int64_t *matched, int64_t *last_nodes);
+
 int pkv_tree_sizes(pkv_tree *t, int64_t *evictable, int64_t *protected_size,
                    int64_t *total, int64_t *num_nodes);
 

@@ -376,6 +376,23 @@ class RadixTree:
         check("pkv_tree_evict", lib.pkv_tree_evict(self._h, int(num_tokens), _ptr(out), len(out), C.byref(n)))
         return out[:n.value].copy()
 
+    def match_lock_batch(self, keys):
+        """match_prefix then inc_lock_ref of the last node, for every key in order, in one native
+        call.  Returns (list of matched value arrays, int64 array of last nodes)."""
+        n = len(keys)
+        off = np.zeros(n + 1, dtype=np.int64)
+        if n:
+            np.cumsum([len(k) for k in keys], out=off[1:])
+        flat = _i32(np.concatenate([np.asarray(k, dtype=np.int32) for k in keys])) if n and off[-1] else \
+            np.zeros(1, dtype=np.int32)
+        values = np.zeros(max(int(off[-1]), 1), dtype=np.int32)
+        matched = np.zeros(max(n, 1), dtype=np.int64)
+        last = np.zeros(max(n, 1), dtype=np.int64)
+        check("pkv_tree_match_lock_batch", lib.pkv_tree_match_lock_batch(self._h, _ptr(flat), _ptr(off), n, _ptr(values),
+                                                                         _ptr(matched), _ptr(last)))
+        ends = np.cumsum(matched[:n])
+        return [values[e - m:e] for e, m in zip(ends, matched[:n])], last[:n]
+
     def inc_lock_ref(self, node: int) -> int:
         d = C.c_int64(0)
         check("pkv_tree_inc_lock_ref", lib.pkv_tree_inc_lock_ref(self._h, int(node), C.byref(d)))

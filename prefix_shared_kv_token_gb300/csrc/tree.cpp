@@ -409,6 +409,27 @@ int pkv_tree_inc_lock_ref(pkv_tree *t, int64_t node, int64_t *delta) {
     return PKV_OK;
 }
 
+int pkv_tree_match_lock_batch(pkv_tree *t, const int32_t *keys, const int64_t *offsets, int32_t n,
+                              int32_t *values, int64_t *matched, int64_t *last_nodes) {
+    if (!t || n < 0 || (n > 0 && (!offsets || !values || !matched || !last_nodes))) return PKV_E_INVALID;
+    if (n > 0 && offsets[0] != 0) return PKV_E_INVALID;
+    for (int32_t i = 0; i < n; ++i)
+        if (offsets[i + 1] < offsets[i]) return PKV_E_INVALID;
+    if (n > 0 && offsets[n] > 0 && !keys) return PKV_E_INVALID;
+    std::vector<int32_t> v;
+    int64_t at = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        v.clear();
+        const int64_t node = t->match(keys + offsets[i], offsets[i + 1] - offsets[i], &v);
+        if (!v.empty()) std::memcpy(values + at, v.data(), sizeof(int32_t) * v.size());
+        at += (int64_t)v.size();
+        matched[i] = (int64_t)v.size();
+        last_nodes[i] = node;
+        t->inc_lock(node);
+    }
+    return PKV_OK;
+}
+
 int pkv_tree_dec_lock_ref(pkv_tree *t, int64_t node, int64_t *delta) {
     if (!t) return PKV_E_INVALID;
     if (!t->valid(node)) return PKV_E_NOTFOUND;

@@ -277,6 +277,7 @@ class PrefixCache:
         self.tree = RadixTree(page_size=self.page)
         self.alloc = Allocator(w.slot_perm if self.page == 1 else w.page_perm(self.page))
         self.private = {}   # paged pool: request id -> slots of its trailing partial block
+        self._tokens = {}   # request id -> its context tokens (the workload's, fixed)
         self.err = torch.zeros(64, dtype=torch.int32, device=device)
 
     # ---- slots of positions
@@ -369,21 +370,48 @@ class PrefixCache:
         w = self.w
         reqs = [r for r in (w.requests if requests is None else requests) if r.kind == kind]
         rows, last_nodes, seq, ext, new_all = [], [], [], [], []
+        toks_all = []
         for r in reqs:
-            toks = _ctx_tokens(w, r)
-            L, c = len(toks), len(toks) - r.n_new
-            vals, last = self.tree.match_prefix(toks[:c])
-            if self.page > 1:   # whole blocks from the tree, the partial one from the request
+            t = self._tokens.get(r.rid)
+            if t is None:
+                t = self._tokens[r.rid] = _ctx_tokens(w, r)
+            toks_all.append(t)
+        if self.page == 1:
+            # one native call matches and locks every request's cached part, in order; the new
+            # tokens' slots come from one FIFO allocation, split in request order (the same
+            # slots as one allocation per request)
+            cached = [len(t) - r.n_new for t, r in zip(toks_all, reqs)]
+            vals_all, last_all = self.tree.match_lock_batch([t[:c] for t, c in zip(toks_all, cached)])
+            for r, vals, c in zip(reqs, vals_all, cached):
+                if len(vals) != c:
+                    for n in last_all:
+                        self.tree.dec_lock_ref(int(n))
+                    raise RuntimeError(f"request {r.rid}: cached part not fully in the tree ({len(vals)} of {c})")
+            n_new = [r.n_new for r in reqs]
+            new_flat = self.alloc.alloc(int(sum(n_new)))
+            ends = np.cumsum(n_new)
+            for r, t, vals, last, e, n in zip(reqs, toks_all, vals_all, last_all, ends, n_new):
+                new = new_flat[e - n:e]
+                rows.append(np.concatenate([vals, new]).astype(np.int32))
+                last_nodes.append(int(last))
+                seq.append(len(t))
+                ext.append(n)
+                new_all.append(new)
+        else:
+            for r, toks in zip(reqs, toks_all):
+                L, c = len(toks), len(toks) - r.n_new
+                vals, last = self.tree.match_prefix(toks[:c])
+                # whole blocks from the tree, the partial one from the request
                 vals = np.concatenate([vals, self.private.get(r.rid, np.zeros(0, np.int32))]).astype(np.int32)
-            if len(vals) != c:
-                raise RuntimeError(f"request {r.rid}: cached part not fully in the tree ({len(vals)} of {c})")
-            self.tree.inc_lock_ref(last)
-            new = self._extend_slots(vals, r.n_new)
-            rows.append(np.concatenate([vals, new]).astype(np.int32))
-            last_nodes.append(last)
-            seq.append(L)
-            ext.append(r.n_new)
-            new_all.append(new)
+                if len(vals) != c:
+                    raise RuntimeError(f"request {r.rid}: cached part not fully in the tree ({len(vals)} of {c})")
+                self.tree.inc_lock_ref(last)
+                new = self._extend_slots(vals, r.n_new)
+                rows.append(np.concatenate([vals, new]).astype(np.int32))
+                last_nodes.append(last)
+                seq.append(L)
+                ext.append(r.n_new)
+                new_all.append(new)
         B = len(reqs)
         rt = self._table(rows, seq)
         seq = np.asarray(seq, dtype=np.int32)

@@ -218,3 +218,42 @@ def test_page_size_only_on_an_empty_tree():
     t.insert(list(range(20)), list(range(20)))
     assert _lib.lib.pkv_tree_set_page_size(t._h, 4) == -1   # holds nodes: refused
     assert t.match_prefix(list(range(20)))[0].tolist() == list(range(16))
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_match_lock_batch_equals_single_calls(seed):
+    # the batched match-and-lock leaves the same tree (splits, access times, hit counts,
+    # locks) and returns the same values and nodes as match_prefix + inc_lock_ref per key
+    rng = np.random.default_rng(seed)
+    base = [rng.integers(0, 6, size=int(rng.integers(5, 40))) for _ in range(12)]
+    trees = (RadixTree(), RadixTree())
+    slot = 0
+    for t in trees:
+        slot = 0
+        for k in base:
+            t.insert(k, np.arange(slot, slot + len(k), dtype=np.int32))
+            slot += len(k)
+    keys = []
+    for _ in range(30):   # prefixes that end inside nodes, past them, on nothing at all
+        k = base[int(rng.integers(0, len(base)))]
+        cut = int(rng.integers(0, len(k) + 1))
+        tail = rng.integers(0, 6, size=int(rng.integers(0, 4)))
+        keys.append(np.concatenate([k[:cut], tail]).astype(np.int32))
+    keys.append(np.zeros(0, np.int32))
+    single_v, single_n = [], []
+    for k in keys:
+        v, n = trees[0].match_prefix(k)
+        trees[0].inc_lock_ref(n)
+        single_v.append(v)
+        single_n.append(n)
+    batch_v, batch_n = trees[1].match_lock_batch(keys)
+    assert [n for n in batch_n.tolist()] == single_n
+    for a, b in zip(single_v, batch_v):
+        assert np.array_equal(a, b)
+    assert trees[0].dump() == trees[1].dump()
+    assert trees[0].sizes() == trees[1].sizes()
+    # the locks are real: unlocking every node returns both trees to the same evictable size
+    for t, nodes in zip(trees, (single_n, batch_n)):
+        for n in nodes:
+            t.dec_lock_ref(int(n))
+    assert trees[0].sizes() == trees[1].sizes() and trees[0].sizes()["protected"] == 0

@@ -100,6 +100,23 @@ uint64_t pkv_get_wait_limit_ns(void) { return pkv::wait_limit_ns(); }
 int pkv_check_out_cache_loc(const int32_t *out_cache_loc, int64_t n, int64_t num_slots, int64_t *bad) {
     if (bad) *bad = -1;
     if (n < 0 || num_slots <= 0 || (n > 0 && !out_cache_loc)) return PKV_E_INVALID;
+    if (n == 0) return PKV_OK;
+    // The first index, in call order, whose slot is out of range or was seen before: that is
+    // the smallest offending index.  A bitmap of the slots when it costs at most 16 bytes an
+    // entry (plus 64 KB), one pass; else (a huge pool, a short list) sorting the entries.
+    if (num_slots / 8 <= 16 * n + 65536) {
+        std::vector<uint64_t> seen((size_t)((num_slots + 63) / 64), 0ull);
+        for (int64_t i = 0; i < n; ++i) {
+            const int32_t s = out_cache_loc[i];
+            const uint64_t bit = 1ull << (s & 63);
+            if (s < 0 || (int64_t)s >= num_slots || (seen[(size_t)s >> 6] & bit)) {
+                if (bad) *bad = i;
+                return PKV_E_INVALID;
+            }
+            seen[(size_t)s >> 6] |= bit;
+        }
+        return PKV_OK;
+    }
     // (slot, index) pairs sorted by slot: a repeated slot sits next to its twin; the later
     // of the two occurrences (in call order) is the one reported
     std::vector<std::pair<int32_t, int64_t>> v;

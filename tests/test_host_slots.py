@@ -4,6 +4,7 @@ distinct free slots ("[SGLang] RadixAttention ...", "Eviction 전략": evicted s
 the allocator's free list), so a duplicate means a caller bug -- e.g. a slot released twice."""
 
 import numpy as np
+import pytest
 
 import prefix_shared_kv_token_gb300 as pkv
 
@@ -31,11 +32,19 @@ def test_out_of_range_slots_are_reported():
     assert pkv.check_out_cache_loc(np.array([3, 3, 20], np.int32), 16) == 1
 
 
-def test_matches_a_brute_force_scan():
+@pytest.mark.parametrize("pool", ["small", "huge"])
+def test_matches_a_brute_force_scan(pool):
+    # a small pool takes the one-pass bitmap, a huge one with a short list the sort
     rng = np.random.default_rng(1)
     for _ in range(200):
-        n, S = int(rng.integers(0, 40)), int(rng.integers(1, 30))
-        loc = rng.integers(-2, S + 2, size=n).astype(np.int32)
+        n = int(rng.integers(0, 40))
+        if pool == "small":
+            S = int(rng.integers(1, 30))
+            loc = rng.integers(-2, S + 2, size=n).astype(np.int32)
+        else:
+            S = (1 << 30) + int(rng.integers(0, 5))
+            near = rng.integers(-2, 30, size=n)           # low slots, repeats likely
+            loc = np.where(rng.random(n) < 0.2, S - 3 + rng.integers(0, 6, size=n), near).astype(np.int32)
         want, seen = -1, set()
         for i, s in enumerate(loc.tolist()):
             if s < 0 or s >= S or s in seen:

@@ -430,6 +430,15 @@ int pkv_tree_dec_lock_ref(pkv_tree *t, int64_t node, int64_t *delta);
 int pkv_tree_match_lock_batch(pkv_tree *t, const int32_t *keys, const int64_t *offsets, int32_t n,
                               int32_t *values, int64_t *matched, int64_t *last_nodes);
 
+/* A token pool's batch table in one call (host memory): row i of table ([n][stride] int32)
+ * gets request i's cached slots cached[ca_i .. ca_i + cached_len[i]) and then its new slots
+ * fresh[fa_i .. fa_i + fresh_len[i]), where ca_i and fa_i are the sums of cached_len and of
+ * fresh_len over the rows before i -- the req_to_token rows of the batch ([RC] "매칭": the
+ * matched values are the prefix's slots).  The rest of each row is left as it is.
+ * PKV_E_INVALID if a length is negative or a row would pass stride (nothing is written). */
+int pkv_fill_batch_table(const int32_t *cached, const int64_t *cached_len, const int32_t *fresh,
+                         const int64_t *fresh_len, int32_t n, int32_t *table, int64_t stride);
+
 int pkv_tree_sizes(pkv_tree *t, int64_t *evictable, int64_t *protected_size,
                    int64_t *total, int64_t *num_nodes);
 

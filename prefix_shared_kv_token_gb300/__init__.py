@@ -35,7 +35,7 @@ from ._lib import (PKV_BF16, PKV_FP8_E4M3, PkvBatch, PkvCascade, PkvError, PkvPl
 
 __all__ = ["Pool", "Batch", "Plan", "Cascade", "kv_store", "check_out_cache_loc", "plan_decode", "plan_extend",
            "plan_extend_ctx", "attn_decode", "attn_extend", "attn_extend_store", "attn_extend_ctx", "get_device_error", "get_noalloc_device_error", "set_kernel_events",
-           "set_wait_limit_ns", "get_wait_limit_ns",
+           "set_wait_limit_ns", "get_wait_limit_ns", "fill_batch_table",
            "RadixTree", "Allocator", "PkvError", "version"]
 
 
@@ -215,6 +215,18 @@ def kv_store(pool: Pool, k_new, v_new, out_cache_loc, workspace=None, stream=Non
                                            int(out_cache_loc.shape[0]), _ptr(workspace), _stream(stream)))
 
 
+def fill_batch_table(cached, cached_len, fresh, fresh_len, table) -> None:
+    """Row i of ``table`` (numpy int32 [n][stride], C-contiguous) = request i's cached slots,
+    then its new slots (flat arrays with per-row lengths); the rest of each row is untouched."""
+    assert table.dtype == np.int32 and table.flags["C_CONTIGUOUS"] and table.ndim == 2
+    c, f = _i32(cached) if len(cached) else np.zeros(1, np.int32), _i32(fresh) if len(fresh) else np.zeros(1, np.int32)
+    cl = np.ascontiguousarray(np.asarray(cached_len, dtype=np.int64))
+    fl = np.ascontiguousarray(np.asarray(fresh_len, dtype=np.int64))
+    assert len(cl) == len(fl) <= table.shape[0]
+    check("pkv_fill_batch_table", lib.pkv_fill_batch_table(_ptr(c), _ptr(cl), _ptr(f), _ptr(fl), len(cl), _ptr(table),
+                                                           table.shape[1]))
+
+
 def check_out_cache_loc(out_cache_loc, num_slots) -> int:
     """Host check of kv_store's slot list (numpy int32 [n]): -1 when every slot is in range
     and distinct, else the index of the first entry that is out of range or repeats a slot."""
@@ -376,20 +388,23 @@ class RadixTree:
         check("pkv_tree_evict", lib.pkv_tree_evict(self._h, int(num_tokens), _ptr(out), len(out), C.byref(n)))
         return out[:n.value].copy()
 
-    def match_lock_batch(self, keys):
+    def match_lock_batch(self, keys, flat: bool = False):
         """match_prefix then inc_lock_ref of the last node, for every key in order, in one native
-        call.  Returns (list of matched value arrays, int64 array of last nodes)."""
+        call.  Returns (list of matched value arrays, int64 array of last nodes), or with
+        ``flat`` (all matched values back to back, int64 matched lengths, last nodes)."""
         n = len(keys)
         off = np.zeros(n + 1, dtype=np.int64)
         if n:
             np.cumsum([len(k) for k in keys], out=off[1:])
-        flat = _i32(np.concatenate([np.asarray(k, dtype=np.int32) for k in keys])) if n and off[-1] else \
+        key_flat = _i32(np.concatenate([np.asarray(k, dtype=np.int32) for k in keys])) if n and off[-1] else \
             np.zeros(1, dtype=np.int32)
         values = np.zeros(max(int(off[-1]), 1), dtype=np.int32)
         matched = np.zeros(max(n, 1), dtype=np.int64)
         last = np.zeros(max(n, 1), dtype=np.int64)
-        check("pkv_tree_match_lock_batch", lib.pkv_tree_match_lock_batch(self._h, _ptr(flat), _ptr(off), n, _ptr(values),
+        check("pkv_tree_match_lock_batch", lib.pkv_tree_match_lock_batch(self._h, _ptr(key_flat), _ptr(off), n, _ptr(values),
                                                                          _ptr(matched), _ptr(last)))
+        if flat:
+            return values[:int(matched[:n].sum())], matched[:n], last[:n]
         ends = np.cumsum(matched[:n])
         return [values[e - m:e] for e, m in zip(ends, matched[:n])], last[:n]
 

@@ -98,6 +98,7 @@ SIGNATURES = {
     "pkv_tree_evict": (C.c_int, [_P, _I64, _P, _I64, _PI64]),
     "pkv_tree_inc_lock_ref": (C.c_int, [_P, _I64, _PI64]),
     "pkv_tree_match_lock_batch": (C.c_int, [_P, _P, _P, _I32, _P, _P, _P]),
+    "pkv_fill_batch_table": (C.c_int, [_P, _P, _P, _P, _I32, _P, _I64]),
     "pkv_tree_dec_lock_ref": (C.c_int, [_P, _I64, _PI64]),
     "pkv_tree_sizes": (C.c_int, [_P, _PI64, _PI64, _PI64, _PI64]),
     "pkv_tree_dump": (C.c_int, [_P, _P, _I64, _PI64]),

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstring>
 #include <atomic>
 #include <mutex>
 #include <utility>
@@ -139,6 +140,28 @@ int pkv_check_out_cache_loc(const int32_t *out_cache_loc, int64_t n, int64_t num
     if (first_bad < 0) return PKV_OK;
     if (bad) *bad = first_bad;
     return PKV_E_INVALID;
+}
+
+int pkv_fill_batch_table(const int32_t *cached, const int64_t *cached_len, const int32_t *fresh,
+                         const int64_t *fresh_len, int32_t n, int32_t *table, int64_t stride) {
+    if (n < 0 || stride < 0 || (n > 0 && (!cached_len || !fresh_len || !table))) return PKV_E_INVALID;
+    int64_t ca = 0, fa = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        if (cached_len[i] < 0 || fresh_len[i] < 0 || cached_len[i] + fresh_len[i] > stride) return PKV_E_INVALID;
+        ca += cached_len[i];
+        fa += fresh_len[i];
+    }
+    if ((ca > 0 && !cached) || (fa > 0 && !fresh)) return PKV_E_INVALID;
+    ca = fa = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        int32_t *row = table + (int64_t)i * stride;
+        if (cached_len[i] > 0) std::memcpy(row, cached + ca, sizeof(int32_t) * (size_t)cached_len[i]);
+        if (fresh_len[i] > 0)
+            std::memcpy(row + cached_len[i], fresh + fa, sizeof(int32_t) * (size_t)fresh_len[i]);
+        ca += cached_len[i];
+        fa += fresh_len[i];
+    }
+    return PKV_OK;
 }
 
 int pkv_get_device_error(void *workspace, void *stream, int32_t *raw) {

@@ -21,7 +21,7 @@ import numpy as np
 import torch
 
 from . import (Allocator, Batch, Pool, RadixTree, attn_decode, attn_extend, attn_extend_ctx, attn_extend_store,
-               check_out_cache_loc, kv_store, plan_decode, plan_extend, plan_extend_ctx)
+               check_out_cache_loc, fill_batch_table, kv_store, plan_decode, plan_extend, plan_extend_ctx)
 
 
 def _ctx_tokens(w, req):
@@ -376,27 +376,33 @@ class PrefixCache:
             if t is None:
                 t = self._tokens[r.rid] = _ctx_tokens(w, r)
             toks_all.append(t)
+        rt = None
         if self.page == 1:
             # one native call matches and locks every request's cached part, in order; the new
             # tokens' slots come from one FIFO allocation, split in request order (the same
-            # slots as one allocation per request)
-            cached = [len(t) - r.n_new for t, r in zip(toks_all, reqs)]
-            vals_all, last_all = self.tree.match_lock_batch([t[:c] for t, c in zip(toks_all, cached)])
-            for r, vals, c in zip(reqs, vals_all, cached):
-                if len(vals) != c:
-                    for n in last_all:
-                        self.tree.dec_lock_ref(int(n))
-                    raise RuntimeError(f"request {r.rid}: cached part not fully in the tree ({len(vals)} of {c})")
-            n_new = [r.n_new for r in reqs]
-            new_flat = self.alloc.alloc(int(sum(n_new)))
+            # slots as one allocation per request); one more fills the batch table, and each
+            # request's slot row is a view of its table row
+            cached = np.fromiter((len(t) - r.n_new for t, r in zip(toks_all, reqs)), dtype=np.int64,
+                                 count=len(reqs))
+            vals_flat, matched, last_all = self.tree.match_lock_batch(
+                [t[:c] for t, c in zip(toks_all, cached.tolist())], flat=True)
+            if not np.array_equal(matched, cached):
+                i = int(np.nonzero(matched != cached)[0][0])
+                for n in last_all:
+                    self.tree.dec_lock_ref(int(n))
+                raise RuntimeError(f"request {reqs[i].rid}: cached part not fully in the tree "
+                                   f"({int(matched[i])} of {int(cached[i])})")
+            n_new = np.fromiter((r.n_new for r in reqs), dtype=np.int64, count=len(reqs))
+            new_flat = self.alloc.alloc(int(n_new.sum()))
+            seq = (cached + n_new).tolist()
+            stride = max(16, ((max(seq) if seq else 1) + 15) // 16 * 16)
+            rt = np.zeros((max(len(reqs), 1), stride), dtype=np.int32)
+            fill_batch_table(vals_flat, matched, new_flat, n_new, rt)
             ends = np.cumsum(n_new)
-            for r, t, vals, last, e, n in zip(reqs, toks_all, vals_all, last_all, ends, n_new):
-                new = new_flat[e - n:e]
-                rows.append(np.concatenate([vals, new]).astype(np.int32))
-                last_nodes.append(int(last))
-                seq.append(len(t))
-                ext.append(n)
-                new_all.append(new)
+            rows = [rt[i, :L] for i, L in enumerate(seq)]
+            new_all = [new_flat[e - n:e] for e, n in zip(ends.tolist(), n_new.tolist())]
+            last_nodes = [int(n) for n in last_all]
+            ext = n_new.tolist()
         else:
             for r, toks in zip(reqs, toks_all):
                 L, c = len(toks), len(toks) - r.n_new
@@ -413,7 +419,8 @@ class PrefixCache:
                 ext.append(r.n_new)
                 new_all.append(new)
         B = len(reqs)
-        rt = self._table(rows, seq)
+        if rt is None:
+            rt = self._table(rows, seq)
         seq = np.asarray(seq, dtype=np.int32)
         ext = np.asarray(ext, dtype=np.int32)
         casc = self.tree.cascade(last_nodes, min_group) if (cascade and B > 1) else None
@@ -433,6 +440,8 @@ class PrefixCache:
         else:
             plan = plan_decode(seq, hq, hkv, d, casc, opts)
         loc_host = np.concatenate(new_all).astype(np.int32) if new_all else np.zeros(0, np.int32)
+        if self.page == 1:
+            loc_host = np.ascontiguousarray(new_flat, dtype=np.int32)
         if self.check_slots:
             bad = check_out_cache_loc(loc_host, self.pool.num_slots)
             if bad >= 0:

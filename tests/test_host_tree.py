@@ -257,3 +257,30 @@ def test_match_lock_batch_equals_single_calls(seed):
         for n in nodes:
             t.dec_lock_ref(int(n))
     assert trees[0].sizes() == trees[1].sizes() and trees[0].sizes()["protected"] == 0
+
+
+def test_fill_batch_table_matches_row_by_row_construction():
+    from prefix_shared_kv_token_gb300 import PkvError, fill_batch_table
+    rng = np.random.default_rng(5)
+    for _ in range(50):
+        n = int(rng.integers(0, 12))
+        cl = rng.integers(0, 30, size=n)
+        fl = rng.integers(0, 5, size=n)
+        cached = rng.integers(0, 1 << 20, size=int(cl.sum())).astype(np.int32)
+        fresh = rng.integers(0, 1 << 20, size=int(fl.sum())).astype(np.int32)
+        stride = int((cl + fl).max()) + int(rng.integers(0, 3)) if n else 4
+        table = np.full((max(n, 1), stride), -7, dtype=np.int32)
+        fill_batch_table(cached, cl, fresh, fl, table)
+        want = np.full_like(table, -7)
+        ca = fa = 0
+        for i in range(n):
+            want[i, :cl[i]] = cached[ca:ca + cl[i]]
+            want[i, cl[i]:cl[i] + fl[i]] = fresh[fa:fa + fl[i]]
+            ca += cl[i]
+            fa += fl[i]
+        assert np.array_equal(table, want)
+    # a row past the stride is refused and nothing is written
+    table = np.zeros((2, 4), dtype=np.int32)
+    with pytest.raises(PkvError):
+        fill_batch_table(np.arange(3, dtype=np.int32), [1, 2], np.arange(5, dtype=np.int32), [1, 4], table)
+    assert not table.any()
